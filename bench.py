@@ -1,0 +1,605 @@
+#!/usr/bin/env python3
+"""Benchmark of the SAW-INT4 hot path on one GB300 (per rank).
+
+Default workload (the Qwen3-4B-shaped latency case): 36 layers, 32 q-heads,
+8 kv-heads, head_dim 128, h = 128, page 16, batch 1, context 32768, K-only
+rotation.  One step = for every layer, quantize-append the new token's K/V
+into that layer's paged INT4 cache, then decode-attend over the 32768
+cached tokens.  The step is replayed as one CUDA graph (the 108 kernel
+launches of a step are captured once).
+
+Printed (rank 0, one JSON line): KV GB/s of the whole step (algorithmic
+bytes / step time), the decode kernel's HBM roofline fraction, the
+quantize-append throughput of a 131072-token prefill chunk, the end-to-end
+rate through the public API with host buffers, and the CPU oracle's rate.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl saw|reference]
+
+--impl reference times the CPU oracle (test infrastructure) on the host
+cores on a bounded sample of the same workload: this method has no
+installable reference implementation.  Under torchrun each rank runs an
+independent replica (the path has no exchange step): value = bytes of all
+ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode-attn KV GB/s & % HBM roofline; quantize-append tokens/s (1×GB300)"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_group(world: int):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("gloo")
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_over_ranks(seconds: float, units: float, world: int):
+    """(max time over ranks, sum of units over ranks).  Replicas only: no data
+    moves between ranks; this host-side reduction only aggregates timings."""
+    if world <= 1:
+        return seconds, units
+    t = torch.tensor([seconds], dtype=torch.float64)
+    u = torch.tensor([units], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ peaks, clocks
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (read-only)."""
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(io.StringIO(f.read())):
+                if len(r) >= 9:
+                    rows.append([x.strip() for x in r])
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        busy = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload
+
+def time_events(fn, iters: int, stream) -> list[float]:
+    """Per-iteration device time (ms) of fn() with CUDA events on `stream`."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+class LatencyCase:
+    """Qwen3-4B-shaped decode step: per layer a 1-token append + decode."""
+
+    def __init__(self, wl, device):
+        import bit_paged_kv_gb300 as saw
+        from bit_paged_kv_gb300 import workloads as W
+        self.saw, self.W, self.wl, self.dev = saw, W, wl, device
+        self.lens = W.seq_lens(wl)
+        self.L = int(self.lens.max())
+        self.bt_cpu, self.npages = W.page_tables(wl, self.lens)
+        self.bt = self.bt_cpu.to(device)
+        self.lens_d = self.lens.to(device)
+        B, Hq, Hkv, D, P = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
+        nb = saw.saw_cache_bytes(self.npages, P, Hkv, D)
+        self.kc = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(wl.num_layers)]
+        self.vc = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(wl.num_layers)]
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        # prefill every layer's cache with all but the last token of each sequence
+        for layer in range(wl.num_layers):
+            pre = [int(x) - 1 for x in self.lens.tolist()]
+            k = W.kv_rows(wl, layer, W.K, sum(pre), device)
+            v = W.kv_rows(wl, layer, W.V, sum(pre), device)
+            slots = W.prefill_slots(self.bt, pre, P)
+            saw.saw_quantize_append(k, v, slots, self.kc[layer], self.vc[layer], self.npages, P,
+                                    wl.rotate_k, wl.rotate_v, wl.block_h, dev_status=status)
+            del k, v
+        # per-step inputs: each layer's new token (the last one of each sequence) and q
+        self.slot = torch.cat([W.slots_for(self.bt, P, b, int(Lb) - 1, int(Lb))
+                               for b, Lb in enumerate(self.lens.tolist())])
+        self.knew = torch.stack([W.kv_rows(wl, l, W.K, 1, device, token_offset=self.L - 1)
+                                 for l in range(wl.num_layers)]).expand(-1, B, -1, -1).contiguous()
+        self.vnew = torch.stack([W.kv_rows(wl, l, W.V, 1, device, token_offset=self.L - 1)
+                                 for l in range(wl.num_layers)]).expand(-1, B, -1, -1).contiguous()
+        self.q = torch.stack([W.q_rows(wl, l, device) for l in range(wl.num_layers)])
+        self.out = torch.empty(wl.num_layers, B, Hq, D, dtype=torch.float32, device=device)
+        self.splits, self.pps = saw.saw_decode_plan(B, Hkv, P, self.L, 0)
+        wsb = saw.saw_decode_workspace_bytes(B, Hq, Hkv, D, P, self.L, 0)
+        self.ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
+        self.status = status
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+
+    def append(self, layer):
+        wl = self.wl
+        self.saw.saw_quantize_append(self.knew[layer], self.vnew[layer], self.slot,
+                                     self.kc[layer], self.vc[layer], self.npages, wl.page_size,
+                                     wl.rotate_k, wl.rotate_v, wl.block_h,
+                                     dev_status=self.status)
+
+    def decode(self, layer):
+        wl = self.wl
+        self.saw.saw_paged_decode_int4(self.q[layer], self.kc[layer], self.vc[layer], self.bt,
+                                       self.lens_d, self.L, wl.num_kv_heads, self.npages,
+                                       wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                                       self.out[layer], self.ws, dev_status=self.status)
+
+    def step(self):
+        for layer in range(self.wl.num_layers):
+            self.append(layer)
+            self.decode(layer)
+
+    def launches_per_step(self) -> int:
+        return self.wl.num_layers * (2 + (1 if self.splits > 1 else 0))
+
+    def step_bytes(self) -> int:
+        W, wl = self.W, self.wl
+        return wl.num_layers * (W.decode_bytes(wl, self.lens.tolist()) +
+                                W.append_bytes(wl, wl.num_seqs))
+
+    def decode_bytes(self) -> int:
+        return self.W.decode_bytes(self.wl, self.lens.tolist())
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm (sets kernel attributes outside capture)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def decode_kernel_times(case, stream, reps: int):
+    """Average device time of one decode call (split kernel + merge kernel),
+    from external event records captured around every layer's decode inside
+    a graph of the step; falls back to decode-only graph time / layers."""
+    nl = case.wl.num_layers
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)]
+    except TypeError:
+        evs = None
+    if evs is not None:
+        def fn():
+            s = torch.cuda.current_stream()
+            for layer in range(nl):
+                case.append(layer)
+                evs[layer][0].record(s)
+                case.decode(layer)
+                evs[layer][1].record(s)
+        try:
+            g = capture(fn, stream)
+            acc = []
+            for _ in range(reps):
+                g.replay()
+                torch.cuda.synchronize()
+                acc.extend(a.elapsed_time(b) for a, b in evs)
+            return statistics.mean(acc), "external events around each decode call in the step graph"
+        except Exception:
+            pass
+
+    def fn2():
+        for layer in range(nl):
+            case.decode(layer)
+    g = capture(fn2, stream)
+    t = time_events(g.replay, reps, stream)
+    return statistics.mean(t) / nl, "decode-only graph time / layers (includes launch gaps)"
+
+
+def append_chunk_measure(device, stream, iters: int = 20):
+    """Quantize-append of one 131072-token prefill chunk (8 kv-heads, K and V,
+    page 64), rotated (h = 128 and 64) and unrotated.  Inputs are 512 MB,
+    larger than L2."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    wl = W.LONG_PREFILL.variant(num_seqs=1)
+    T = wl.len_hi
+    lens = torch.tensor([T], dtype=torch.int32)
+    bt, npages = W.page_tables(wl, lens)
+    k = W.kv_rows(wl, 0, W.K, T, device)
+    v = W.kv_rows(wl, 0, W.V, T, device)
+    slots = W.prefill_slots(bt.to(device), [T], wl.page_size)
+    nb = saw.saw_cache_bytes(npages, wl.page_size, wl.num_kv_heads, wl.head_dim)
+    kc = torch.empty(nb, dtype=torch.uint8, device=device)
+    vc = torch.empty(nb, dtype=torch.uint8, device=device)
+    res = {}
+    nbytes = W.append_bytes(wl, T)
+    for name, rk, rv, h in (("rotated_h128", True, True, 128), ("rotated_h64", True, True, 64),
+                            ("unrotated", False, False, 128)):
+        def fn():
+            saw.saw_quantize_append(k, v, slots, kc, vc, npages, wl.page_size, rk, rv, h)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            t = statistics.median(time_events(fn, iters, stream))
+        res[name] = {"tokens_per_s": T / (t * 1e-3), "ms": t, "gbs": nbytes / (t * 1e-3) / 1e9}
+    return res, nbytes, T
+
+
+def cpu_oracle_decode_sample(case, layers, threads):
+    """Time the oracle (as it stands) on the step's work for `layers`:
+    append the new token, then decode every q-head over the layer's pages."""
+    import numpy as np
+
+    import oracle
+    wl = case.wl
+
+    def bits(t):
+        return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    hosts = []
+    for layer in layers:
+        hosts.append((case.kc[layer].cpu().numpy(), case.vc[layer].cpu().numpy(),
+                      bits(case.knew[layer]).reshape(wl.num_seqs, -1),
+                      bits(case.vnew[layer]).reshape(wl.num_seqs, -1), bits(case.q[layer])))
+    slots = case.slot.cpu().numpy()
+    bt = case.bt_cpu.numpy()
+    lens = case.lens.numpy()
+    t0 = time.perf_counter()
+    for kc, vc, kn, vn, q in hosts:
+        oracle.quantize_append(kn, vn, slots, wl.num_kv_heads, wl.head_dim, kc, vc, case.npages,
+                               wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h)
+        oracle.decode(q, kc, vc, bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                      case.npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                      threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = len(layers) * (case.W.decode_bytes(wl, case.lens.tolist()) +
+                            case.W.append_bytes(wl, wl.num_seqs))
+    return nbytes / dt / 1e9, dt
+
+
+# ------------------------------------------------------------------ arms
+
+def run_saw(args):
+    rank, world, local = dist_env()
+    init_group(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_paged_kv_gb300 import workloads as W
+
+    wl = W.QWEN3_4B_LATENCY
+    case = LatencyCase(wl, device)
+    stream = torch.cuda.Stream(device)
+    graph = capture(case.step, stream)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    clocks = sampler.stop()
+    barrier(world)
+    elapsed = start.elapsed_time(end) * 1e-3
+    step_bytes = case.step_bytes()
+    t_max, bytes_all = reduce_over_ranks(elapsed, step_bytes * args.steps, world)
+    value = bytes_all / t_max / 1e9
+    status = int(case.status.item())
+
+    # dominant kernel: the decode call, timed per launch inside a step graph
+    dec_ms, dec_how = decode_kernel_times(case, stream, reps=max(20, min(200, args.steps // 10)))
+    peak, peak_src = read_peaks()
+    achieved = case.decode_bytes() / (dec_ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    q_h = case.q.cpu().pin_memory()
+    k_h = case.knew.cpu().pin_memory()
+    v_h = case.vnew.cpu().pin_memory()
+    o_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+
+    def e2e_step():
+        case.q.copy_(q_h, non_blocking=True)
+        case.knew.copy_(k_h, non_blocking=True)
+        case.vnew.copy_(v_h, non_blocking=True)
+        graph.replay()
+        o_h.copy_(case.out, non_blocking=True)
+
+    e2e_iters = max(10, args.steps // 4)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(e2e_iters):
+            e2e_step()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    t_e2e, bytes_e2e = reduce_over_ranks(s2.elapsed_time(e2) * 1e-3, step_bytes * e2e_iters, world)
+    h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
+    d2h = o_h.numel() * 4
+
+    # quantize-append of a 131072-token prefill chunk
+    app, app_bytes, app_T = append_chunk_measure(device, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.host_threads()
+        layers = list(range(min(args.cpu_layers, wl.num_layers)))
+        gbs, dt = cpu_oracle_decode_sample(case, layers, threads)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{len(layers)} of 36 layers of the step (1-token append + fp64 decode "
+                         f"of all 32 q-heads over 32768 tokens), {dt:.1f} s wall"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4 KV (bf16 in, f32 rotation/softmax, f16 MMA f32 accumulate)",
+        "data": "synthetic",
+        "config": {
+            "workload": "qwen3-4b-latency: 36 layers, Hq 32, Hkv 8, head_dim 128, h 128, page 16, "
+                        "batch 1, context 32768, K-only rotation; step = per layer 1-token "
+                        "quantize-append + paged decode",
+            "l2": f"inputs larger than L2: 36 distinct layer caches, "
+                  f"{step_bytes / 1e9:.2f} GB read per step",
+            "execution": "one CUDA graph per step",
+            "decode_plan": {"splits": case.splits, "pages_per_split": case.pps},
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "saw_paged_decode_int4 (paged_decode_kernel<16> + combine_kernel)",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": None,
+            "bytes_per_launch": case.decode_bytes(),
+            "ms_per_launch": dec_ms,
+            "timing": dec_how,
+            "peak_source": peak_src,
+        },
+        "quantize_append": {
+            "workload": "131072-token prefill chunk, Hkv 8, head_dim 128, K and V, page 64",
+            "tokens_per_s": app["rotated_h128"]["tokens_per_s"],
+            "roofline": {"bound": "hbm", "achieved": app["rotated_h128"]["gbs"], "peak": peak,
+                         "unit": "GB/s", "frac": app["rotated_h128"]["gbs"] / peak,
+                         "bytes_per_launch": app_bytes},
+            "variants": app,
+            "rotation_overhead": app["rotated_h128"]["ms"] / app["unrotated"]["ms"] - 1.0,
+        },
+        "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "pinned host q/k/v copied in, graph step, output copied out, every step"},
+        "cpu_baseline": cpu,
+        "gpu_launches": case.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args):
+    """The CPU oracle on a bounded sample of the same workload per step."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from bit_paged_kv_gb300 import workloads as W
+    oracle.load()
+    wl = W.QWEN3_4B_LATENCY
+    lens = W.seq_lens(wl)
+    L = int(lens[0])
+    bt, npages = W.page_tables(wl, lens)
+    P, Hkv, D, G = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.group
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    # sample: layer 0, kv-head 0 and its G q-heads, full 32768-token context
+    k = W.kv_rows(wl, 0, W.K, L, "cpu")
+    v = W.kv_rows(wl, 0, W.V, L, "cpu")
+    slots = W.prefill_slots(bt, [L], P).numpy()
+    nb = oracle.cache_bytes(npages, P, Hkv, D)
+    kc, vc = np.zeros(nb, np.uint8), np.zeros(nb, np.uint8)
+    kb, vb = bits(k).reshape(L, -1), bits(v).reshape(L, -1)
+    threads = oracle.host_threads()
+    oracle.quantize_append(kb[:-1], vb[:-1], slots[:-1], Hkv, D, kc, vc, npages, P, wl.rotate_k,
+                           wl.rotate_v, wl.block_h, threads=threads)
+    q = bits(W.q_rows(wl, 0, "cpu"))
+    pairs = [(0, h) for h in range(G)]
+
+    def step():
+        oracle.quantize_append(kb[-1:], vb[-1:], slots[-1:], Hkv, D, kc, vc, npages, P,
+                               wl.rotate_k, wl.rotate_v, wl.block_h)
+        oracle.decode(q, kc, vc, bt.numpy(), lens.numpy(), wl.num_q_heads, Hkv, D, npages, P,
+                      wl.rotate_k, wl.rotate_v, wl.block_h, pairs=pairs, threads=min(threads, G))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    per_row = D // 2 + 4
+    # algorithmic bytes of the sample: one kv-head's K and V rows over the
+    # context, its block-table entries, G q rows in and out, one appended token
+    sample_bytes = (2 * per_row * L + 4 * -(-L // P) + G * D * (2 + 4)
+                    + W.append_bytes(wl, 1))
+    value = sample_bytes * args.steps / dt / 1e9
+    cores = min(threads, G)
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantizer",
+        "data": "synthetic",
+        "config": {"workload": "qwen3-4b-latency (same as the GPU arm)",
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: layer 0, kv-head 0 with its {G} q-heads over "
+                                   f"{L} tokens (1-token append + fp64 decode)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_profile(args):
+    """Small, fixed loops for ncu captures (no timing, no JSON):
+    decode: the latency case's decode over --profile-layers layer caches
+    (35.7 MB each, more than L2 in total), three passes;
+    append: three quantize-appends of the 131072-token chunk."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_paged_kv_gb300 import workloads as W
+    if args.profile == "decode":
+        wl = W.QWEN3_4B_LATENCY.variant(num_layers=args.profile_layers)
+        case = LatencyCase(wl, device)
+        for _ in range(3):
+            for layer in range(wl.num_layers):
+                case.decode(layer)
+        torch.cuda.synchronize()
+        assert int(case.status.item()) == 0
+    else:
+        append_chunk_measure(device, torch.cuda.current_stream(device), iters=1)
+    torch.cuda.synchronize()
+    print(f"profile {args.profile} done")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["saw", "reference"], default="saw")
+    ap.add_argument("--cpu-layers", type=int, default=12)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "append"], default=None,
+                    help="run a small fixed loop for an ncu capture instead of the benchmark")
+    ap.add_argument("--profile-layers", type=int, default=8)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_saw(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,25 @@
+"""SAW-INT4 hot path on GB300: rotate + token-wise INT4 quantize-append into a
+paged KV cache, and paged decode attention over that cache.
+
+The compute lives in the CUDA library built from `csrc/` (C ABI in
+`include/saw_int4.h`); this package is its thin Python binding, with the
+same names as the C entry points.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    SAW_ERR_CUDA,
+    SAW_ERR_DEVICE_INDEX,
+    SAW_ERR_DEVICE_TIMEOUT,
+    SAW_ERR_INVALID_ARG,
+    SAW_ERR_UNSUPPORTED,
+    SAW_OK,
+    SawError,
+    lib,
+    saw_cache_bytes,
+    saw_decode_plan,
+    saw_decode_workspace_bytes,
+    saw_paged_decode_int4,
+    saw_quantize_append,
+    saw_status_string,
+)

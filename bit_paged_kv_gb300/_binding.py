@@ -1,0 +1,142 @@
+"""Thin ctypes binding over the C ABI in include/saw_int4.h.
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and a nonzero status raises.  Every step of
+the hot path runs in the library's CUDA kernels; there is no fallback.  If
+the library has not been built this module raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libsaw_int4.so")
+
+SAW_OK = 0
+SAW_ERR_INVALID_ARG = 1
+SAW_ERR_UNSUPPORTED = 2
+SAW_ERR_CUDA = 3
+SAW_ERR_DEVICE_INDEX = 4
+SAW_ERR_DEVICE_TIMEOUT = 5
+
+EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_decode_plan",
+           "saw_decode_workspace_bytes", "saw_paged_decode_int4")
+
+_lib = None
+
+
+class SawError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {saw_status_string(status)} ({status})")
+        self.status = status
+
+
+def lib() -> C.CDLL:
+    """Load the in-tree CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"SAW-INT4 CUDA library not found at {LIB_PATH}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or `python bit_paged_kv_gb300/build.py`). There is no CPU fallback.")
+    L = C.CDLL(LIB_PATH)
+    P, i32, i64, sz, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
+    L.saw_status_string.restype = C.c_char_p
+    L.saw_status_string.argtypes = [i32]
+    L.saw_cache_bytes.restype = sz
+    L.saw_cache_bytes.argtypes = [i32, i32, i32, i32]
+    L.saw_quantize_append.restype = i32
+    L.saw_quantize_append.argtypes = [P, P, i64, i64, P, i32, i32, i32, P, P, i32, i32, i32, i32,
+                                      i32, P, P]
+    L.saw_decode_plan.restype = i32
+    L.saw_decode_plan.argtypes = [i32, i32, i32, i32, i32, P, P]
+    L.saw_decode_workspace_bytes.restype = sz
+    L.saw_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.saw_paged_decode_int4.restype = i32
+    L.saw_paged_decode_int4.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, i32, f32, P, P, sz, i32, P, P]
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor, stream):
+    if stream is not None:
+        return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return C.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _raise(rc: int, where: str) -> None:
+    if rc != SAW_OK:
+        raise SawError(rc, where)
+
+
+def saw_status_string(status: int) -> str:
+    return lib().saw_status_string(int(status)).decode()
+
+
+def saw_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().saw_cache_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def saw_quantize_append(k: torch.Tensor, v, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache, num_pages: int, page_size: int, rotate_k: bool, rotate_v: bool,
+                        block_h: int, dev_status=None, stream=None) -> None:
+    """k, v: bfloat16 [T, Hkv, D] (token dim may be strided); v may be None."""
+    T, hkv, d = k.shape
+    assert k.dtype == torch.bfloat16 and k.stride(2) == 1 and k.stride(1) == d
+    if v is not None:
+        assert v.dtype == torch.bfloat16 and v.shape == k.shape and v.stride(2) == 1 and v.stride(1) == d
+    assert slot_mapping.dtype == torch.int32 and slot_mapping.is_contiguous()
+    rc = lib().saw_quantize_append(
+        _ptr(k), _ptr(v), k.stride(0), v.stride(0) if v is not None else 0, _ptr(slot_mapping),
+        T, hkv, d, _ptr(k_cache), _ptr(v_cache) if v is not None else None, num_pages, page_size,
+        int(rotate_k), int(rotate_v), block_h, _ptr(dev_status), _stream(k, stream))
+    _raise(rc, "saw_quantize_append")
+
+
+def saw_decode_plan(num_seqs: int, num_kv_heads: int, page_size: int, max_seq_len: int,
+                    pages_per_split: int = 0):
+    s, p = C.c_int32(0), C.c_int32(0)
+    rc = lib().saw_decode_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split,
+                               C.byref(s), C.byref(p))
+    _raise(rc, "saw_decode_plan")
+    return s.value, p.value
+
+
+def saw_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                               head_dim: int, page_size: int, max_seq_len: int,
+                               pages_per_split: int = 0) -> int:
+    return int(lib().saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                page_size, max_seq_len, pages_per_split))
+
+
+def saw_paged_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                          num_kv_heads: int, num_pages: int, page_size: int, rotate_k: bool,
+                          rotate_v: bool, block_h: int, out: torch.Tensor, workspace=None,
+                          sm_scale: float = 0.0, pages_per_split: int = 0, dev_status=None,
+                          stream=None) -> None:
+    """q: bfloat16 [B, Hq, D] contiguous; out: float32 [B, Hq, D]."""
+    B, hq, d = q.shape
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, hq, d)
+    assert block_tables.dtype == torch.int32 and block_tables.is_contiguous()
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().saw_paged_decode_int4(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), B, max_seq_len, hq, num_kv_heads, d, num_pages, page_size,
+        int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out), _ptr(workspace),
+        ws_bytes, pages_per_split, _ptr(dev_status), _stream(q, stream))
+    _raise(rc, "saw_paged_decode_int4")

@@ -1,0 +1,220 @@
+// saw_api.cu -- the extern "C" entry points declared in include/saw_int4.h:
+// argument checks, the decode split plan, and kernel launches.  No state is
+// kept between calls and nothing is allocated.
+#include <cmath>
+#include <cstdint>
+
+#include "saw_int4.h"
+#include "saw_internal.h"
+
+namespace {
+
+using saw::kHeadDim;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+bool page_size_ok(int p) { return p == 16 || p == 32 || p == 64; }
+bool block_h_ok(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Split plan: enough (sequence, kv-head, split) CTAs to give every SM several
+// resident CTAs, without splits shorter than 256 tokens (each of the four
+// warps then still streams >= 4 pages of 16 tokens).
+int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int32_t max_seq_len,
+                  int32_t pages_per_split, int32_t* splits_out, int32_t* pps_out) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || !page_size_ok(page_size) || max_seq_len < 0 ||
+      pages_per_split < 0)
+    return SAW_ERR_INVALID_ARG;
+  const int64_t max_pages = ceil_div(max_seq_len, page_size);
+  int64_t pps;
+  if (max_pages == 0) {
+    pps = 1;
+  } else if (pages_per_split > 0) {
+    pps = pages_per_split;
+  } else {
+    const int64_t units = int64_t(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
+    const int sms = sm_count();
+    const int64_t target = 4LL * (sms > 0 ? sms : 148);
+    const int64_t min_pps = 256 / page_size;
+    int64_t splits = ceil_div(target, units);
+    const int64_t max_splits = ceil_div(max_pages, min_pps);
+    if (splits > max_splits) splits = max_splits;
+    if (splits < 1) splits = 1;
+    pps = ceil_div(max_pages, splits);
+  }
+  int64_t splits = max_pages == 0 ? 1 : ceil_div(max_pages, pps);
+  if (splits > 65535) return SAW_ERR_UNSUPPORTED;
+  *splits_out = int32_t(splits);
+  *pps_out = int32_t(pps);
+  return SAW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* saw_status_string(int32_t status) {
+  switch (status) {
+    case SAW_OK: return "SAW_OK";
+    case SAW_ERR_INVALID_ARG: return "SAW_ERR_INVALID_ARG";
+    case SAW_ERR_UNSUPPORTED: return "SAW_ERR_UNSUPPORTED";
+    case SAW_ERR_CUDA: return "SAW_ERR_CUDA";
+    case SAW_ERR_DEVICE_INDEX: return "SAW_ERR_DEVICE_INDEX";
+    case SAW_ERR_DEVICE_TIMEOUT: return "SAW_ERR_DEVICE_TIMEOUT";
+    default: return "SAW_ERR_UNKNOWN";
+  }
+}
+
+size_t saw_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                       int32_t head_dim) {
+  if (num_pages <= 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || (head_dim & 1))
+    return 0;
+  const size_t chunk = size_t(page_size) * size_t(head_dim / 2) + 4 * size_t(page_size);
+  return size_t(num_pages) * size_t(num_kv_heads) * chunk;
+}
+
+int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride,
+                            int64_t v_token_stride, const int32_t* slot_mapping,
+                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                            void* k_cache, void* v_cache, int32_t num_pages, int32_t page_size,
+                            int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                            int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_pages < 0) return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
+    return SAW_ERR_INVALID_ARG;
+  const bool has_v = v != nullptr;
+  if (rotate_k || (has_v && rotate_v)) {
+    if (!pow2(block_h) || block_h > head_dim || head_dim % block_h) return SAW_ERR_INVALID_ARG;
+    if (!block_h_ok(block_h)) return SAW_ERR_UNSUPPORTED;
+  }
+  if (int64_t(num_tokens) * num_kv_heads > INT32_MAX / 2) return SAW_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return SAW_OK;
+  if (!k || !slot_mapping || !k_cache || (has_v && !v_cache)) return SAW_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(k_cache) || (has_v && (!aligned16(v) || !aligned16(v_cache))))
+    return SAW_ERR_INVALID_ARG;
+  if (k_token_stride < int64_t(num_kv_heads) * head_dim || (k_token_stride & 7))
+    return SAW_ERR_INVALID_ARG;
+  if (has_v && (v_token_stride < int64_t(num_kv_heads) * head_dim || (v_token_stride & 7)))
+    return SAW_ERR_INVALID_ARG;
+
+  saw::AppendParams p{};
+  p.src[0] = static_cast<const uint16_t*>(k);
+  p.src[1] = static_cast<const uint16_t*>(v);
+  p.stride[0] = k_token_stride;
+  p.stride[1] = has_v ? v_token_stride : 0;
+  p.cache[0] = static_cast<uint8_t*>(k_cache);
+  p.cache[1] = static_cast<uint8_t*>(v_cache);
+  p.rotate[0] = rotate_k;
+  p.rotate[1] = has_v ? rotate_v : 0;
+  p.slot_mapping = slot_mapping;
+  p.dev_status = dev_status;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.page_size = page_size;
+  p.block_h = block_h;
+  p.num_slots = int64_t(num_pages) * page_size;
+  p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
+  cudaError_t err =
+      saw::launch_quantize_append(p, has_v ? 2 : 1, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size,
+                        int32_t max_seq_len, int32_t pages_per_split, int32_t* num_splits,
+                        int32_t* pages_per_split_out) {
+  if (!num_splits || !pages_per_split_out) return SAW_ERR_INVALID_ARG;
+  return make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, num_splits,
+                   pages_per_split_out);
+}
+
+size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t page_size, int32_t max_seq_len,
+                                  int32_t pages_per_split) {
+  if (head_dim != kHeadDim || num_q_heads <= 0) return 0;
+  int32_t splits = 0, pps = 0;
+  if (make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, &splits, &pps) !=
+      SAW_OK)
+    return 0;
+  if (splits <= 1) return 0;
+  const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
+  return rows * size_t(head_dim) * 4 + rows * 2 * 4;
+}
+
+int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                              int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                              void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                              int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || max_seq_len < 0)
+    return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > saw::kMaxGroup) return SAW_ERR_UNSUPPORTED;
+  if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
+    return SAW_ERR_INVALID_ARG;
+  if (rotate_k || rotate_v) {
+    if (!pow2(block_h) || block_h > head_dim || head_dim % block_h) return SAW_ERR_INVALID_ARG;
+    if (!block_h_ok(block_h)) return SAW_ERR_UNSUPPORTED;
+  }
+  if (!(sm_scale >= 0.0f) || std::isinf(sm_scale)) return SAW_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return SAW_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return SAW_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+    return SAW_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
+    return SAW_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * page_size < int64_t(max_seq_len)) return SAW_ERR_INVALID_ARG;
+
+  int32_t splits = 0, pps = 0;
+  int32_t rc = make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split,
+                         &splits, &pps);
+  if (rc != SAW_OK) return rc;
+  const size_t need = saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 page_size, max_seq_len, pages_per_split);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return SAW_ERR_INVALID_ARG;
+
+  saw::DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = need > 0 ? static_cast<float*>(workspace) + rows * head_dim : nullptr;
+  p.dev_status = dev_status;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.max_seq_len = max_seq_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.num_pages = num_pages;
+  p.page_size = page_size;
+  p.rotate_k = rotate_k;
+  p.rotate_v = rotate_v;
+  p.block_h = block_h;
+  p.pages_per_split = pps;
+  p.num_splits = splits;
+  p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
+  const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
+  p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// saw_internal.h -- kernel parameter blocks and launchers (library-internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace saw {
+
+constexpr int kHeadDim = 128;       // the one head size this build supports
+constexpr int kMaxGroup = 8;        // q-heads per kv-head served by one CTA (MMA N = 8)
+constexpr int kDecodeWarps = 4;     // warps per decode CTA
+
+__host__ __device__ constexpr int chunk_bytes(int page_size) {
+  return page_size * (kHeadDim / 2) + 4 * page_size;
+}
+
+// ---------------------------------------------------------------- append
+
+struct AppendParams {
+  const uint16_t* src[2];       // K, V bfloat16 bits [T][Hkv][D] with token stride
+  int64_t stride[2];            // token stride in elements
+  uint8_t* cache[2];            // K, V caches
+  int32_t rotate[2];
+  const int32_t* slot_mapping;  // [T]
+  int32_t* dev_status;
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t block_h;
+  int64_t num_slots;            // num_pages * page_size
+  float c_h;                    // binary32(1/sqrt(block_h))
+};
+
+cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode
+
+struct DecodeParams {
+  const uint16_t* q;            // [B][Hq][D] bfloat16 bits
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* seq_lens;      // [B]
+  float* out;                   // [B][Hq][D]
+  float* part_o;                // [B][Hq][num_splits][D]
+  float* part_ml;               // [B][Hq][num_splits][2]
+  int32_t* dev_status;
+  int32_t max_blocks;
+  int32_t num_seqs;
+  int32_t max_seq_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;                // num_q_heads / num_kv_heads
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t rotate_k;
+  int32_t rotate_v;
+  int32_t block_h;
+  int32_t pages_per_split;
+  int32_t num_splits;
+  float c_h;                    // 1/sqrt(block_h)
+  float q_scale;                // sm_scale * log2(e)
+};
+
+cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace saw

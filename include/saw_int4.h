@@ -1,0 +1,185 @@
+/*
+ * saw_int4.h -- C ABI of the SAW-INT4 hot path on GB300 (sm_103a).
+ *
+ * Two operations, from the pages on SAW-INT4 (Jia et al., 2026):
+ *
+ *  1. saw_quantize_append: each new token's K/V vector of head_dim values
+ *     per kv-head is rotated by a block-diagonal Hadamard transform (blocks
+ *     of h), quantized token-wise to INT4 with its own scale, and appended
+ *     into a paged KV cache without touching any other token.
+ *     youngju.dev, "INT4 KV-cache quantization" (English transcription),
+ *     "Why Naive INT4 Breaks", "The Rotation Trick -- Block-Diagonal
+ *     Hadamard" and the fused-kernel diagram in "The System Is the Design --
+ *     A Fused Kernel"; gist.science, "SAW-INT4: System-Aware 4-Bit KV-Cache
+ *     Quantization for Real-World LLM Serving", s.2 "Metodologia" (token-wise
+ *     quantization, Block-Diagonal Rotation, fused kernel) and s.4 (h = 128,
+ *     rotation of K only).
+ *
+ *  2. saw_paged_decode_int4: decode attention of one query token per
+ *     sequence over that INT4 cache, with dequantization fused into the
+ *     attention kernel (gist.science s.2 point 3, fusion into decoding).
+ *     q is rotated once (q.k = Hq.Hk because H is orthogonal), and the output
+ *     is rotated back when V was rotated.
+ *
+ * Readings taken where the pages are silent: Sylvester ordering of H, the
+ * 1/sqrt(h) scale applied after an ascending-stride butterfly, one binary16
+ * (scale, zero) pair per (token, kv-head) from the rotated row's min/max
+ * (zero rounded toward -inf, scale toward +inf), round-half-even codes 0..15,
+ * two codes per byte (even index in the low nibble), and the page layout
+ * below.  Each is stated with the function it governs.
+ *
+ * Common rules for every entry point:
+ *  - All buffers are owned by the caller.  The library allocates nothing and
+ *    keeps no state between calls; every call is thread-safe.
+ *  - Pointers marked "device" must be device memory of the current device.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously on it.  The return value reports argument
+ *    checks and launch errors only.
+ *  - `dev_status` is an optional device int32 (may be NULL).  A kernel that
+ *    meets a bad index or a wait that runs out writes a nonzero
+ *    saw_status code into it (the first one wins); it never traps.  The
+ *    caller zeroes it and reads it after the stream has finished.
+ */
+#ifndef SAW_INT4_H
+#define SAW_INT4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum saw_status {
+  SAW_OK = 0,
+  SAW_ERR_INVALID_ARG = 1,    /* a null pointer, a bad size, a misaligned buffer */
+  SAW_ERR_UNSUPPORTED = 2,    /* a shape this build has no kernel for */
+  SAW_ERR_CUDA = 3,           /* a CUDA runtime error at launch */
+  SAW_ERR_DEVICE_INDEX = 4,   /* device-side: a slot, page id or length out of range (skipped) */
+  SAW_ERR_DEVICE_TIMEOUT = 5  /* device-side: a bounded wait on a copy ran out */
+} saw_status;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* saw_status_string(int32_t status);
+
+/*
+ * Bytes of one cache tensor (K or V of one layer):
+ *   [num_pages][num_kv_heads][chunk],  chunk = page_size*head_dim/2 + 4*page_size.
+ * Inside a chunk: token offset o's packed codes at o*head_dim/2 (byte j holds
+ * code 2j in the low nibble and 2j+1 in the high nibble), then, from
+ * page_size*head_dim/2, one 4-byte word per offset: binary16 scale, binary16
+ * zero, little-endian.  A row dequantizes as code*scale + zero.  The layout
+ * is a reading: the pages require only a paged, token-wise layout.
+ * Returns 0 for a negative or zero argument.
+ */
+size_t saw_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                       int32_t head_dim);
+
+/*
+ * Rotate, quantize and append num_tokens tokens of K (and V) into the paged
+ * caches (youngju.dev "The System Is the Design -- A Fused Kernel";
+ * gist.science s.2 and s.3 point 3).
+ *
+ * k, v          device bfloat16 [num_tokens][num_kv_heads][head_dim], rows of
+ *               a token contiguous; token stride k_token_stride /
+ *               v_token_stride elements (>= num_kv_heads*head_dim, multiple
+ *               of 8).  v may be NULL: K only (v_cache is then ignored).
+ * slot_mapping  device int32 [num_tokens]: slot = page*page_size + offset.
+ *               -1 marks padding and is skipped; any other value outside
+ *               [0, num_pages*page_size) is skipped and reported through
+ *               dev_status as SAW_ERR_DEVICE_INDEX.
+ * k_cache, v_cache  device, saw_cache_bytes() each, 16-byte aligned.
+ * rotate_k, rotate_v  0 or 1: apply the block-diagonal Hadamard rotation
+ *               before quantizing.  The gist.science page (s.4) reports that
+ *               rotating K only matches rotating both.
+ * block_h       rotation block size h: 16, 32, 64 or 128, dividing head_dim
+ *               (ignored when neither tensor is rotated).
+ *
+ * Per row, exactly: widen to binary32; if rotated, an in-place butterfly per
+ * h-block with strides 1, 2, ..., h/2 (each a+b, a-b rounded to nearest),
+ * then multiply by binary32(1/sqrt(h)); mn/mx over the row; zero =
+ * binary16 round-down(mn), scale = binary16 round-up((mx - zero)/15), both
+ * saturating at +-65504 and writing zero as +0; r = 1/scale (0 if scale is
+ * 0); code = clamp(round-half-even((y - zero)*r), 0, 15).  Each operation is
+ * one binary32 round-to-nearest step, so the bytes are fully determined.
+ * Inputs are expected finite; non-finite inputs give unspecified codes.
+ *
+ * Supported: head_dim 128; page_size 16, 32 or 64; num_kv_heads >= 1.
+ * Rows whose slot is written by two tokens of the same call race.
+ */
+int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride,
+                            int64_t v_token_stride, const int32_t* slot_mapping,
+                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                            void* k_cache, void* v_cache, int32_t num_pages, int32_t page_size,
+                            int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * How many splits of the context the decode will use, and how many pages
+ * each split covers, for these sizes on the current device
+ * (pages_per_split = 0 picks them from the SM count; > 0 forces it).
+ * Writes *num_splits and *pages_per_split_out; returns a saw_status.
+ */
+int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size,
+                        int32_t max_seq_len, int32_t pages_per_split, int32_t* num_splits,
+                        int32_t* pages_per_split_out);
+
+/*
+ * Workspace bytes saw_paged_decode_int4 needs for these sizes with the same
+ * pages_per_split argument, on the current device (0 when the plan has one
+ * split, which writes the output directly).  Returns 0 on bad arguments.
+ */
+size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t page_size, int32_t max_seq_len,
+                                  int32_t pages_per_split);
+
+/*
+ * Decode attention for one query token per sequence over the INT4 pages
+ * (gist.science s.2 point 3: the rotation and dequantization live inside
+ * the decode kernel; youngju.dev "The Rotation Trick": H is orthogonal, so
+ * attention can run in the rotated domain).
+ *
+ * q             device bfloat16 [num_seqs][num_q_heads][head_dim].
+ * k_cache, v_cache  device caches written by saw_quantize_append with the
+ *               same num_kv_heads, head_dim, page_size, rotate_* and block_h
+ *               (the caller's contract; a mismatch gives wrong numbers).
+ * block_tables  device int32 [num_seqs][max_blocks_per_seq]: logical page i
+ *               of a sequence -> physical page id.  Ids outside
+ *               [0, num_pages) are skipped and reported as
+ *               SAW_ERR_DEVICE_INDEX.
+ * seq_lens      device int32 [num_seqs]: tokens to attend over (including a
+ *               token just appended).  0 gives a zero output row.  A value
+ *               below 0 or above max_seq_len is reported as
+ *               SAW_ERR_DEVICE_INDEX and treated as 0.
+ * max_seq_len   host upper bound on seq_lens; fixes the split plan.
+ *               max_blocks_per_seq must be >= ceil(max_seq_len / page_size).
+ * num_q_heads   a multiple of num_kv_heads with at most 8 q-heads per
+ *               kv-head; q-head j reads kv-head j / (num_q_heads/num_kv_heads).
+ * sm_scale      softmax scale on q.k; 0 means 1/sqrt(head_dim).
+ * out           device float32 [num_seqs][num_q_heads][head_dim].
+ * workspace     device, >= saw_decode_workspace_bytes(...) bytes, 16-byte
+ *               aligned (may be NULL when that is 0).
+ * pages_per_split  0 = automatic; > 0 forces the split size (tests).
+ *
+ * Computes, per (sequence, q-head): q' = (1/sqrt(h)) H q if K was rotated;
+ * t_j = sm_scale * q'.(code_j*s_j + z_j); p = softmax(t); o' = sum_j p_j
+ * (code_j*s_j + z_j) over V; o = (1/sqrt(h)) H o' if V was rotated.  The
+ * GQA group of a kv-head is served by one pass over its pages.  Arithmetic:
+ * q' and p*s in binary16 on the tensor cores with binary32 accumulation,
+ * softmax in binary32; results match a float64 evaluation to about 1e-3 of
+ * the output's largest magnitude.
+ */
+int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                              int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                              void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                              int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAW_INT4_H */

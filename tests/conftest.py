@@ -40,3 +40,14 @@ def read_golden(name):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+def pytest_terminal_summary(terminalreporter):
+    try:
+        from gpu_helpers import ERRORS
+    except Exception:
+        return
+    if ERRORS:
+        worst = max(e for _, e in ERRORS)
+        terminalreporter.write_line(
+            f"attention comparisons: {len(ERRORS)}, worst relative error {worst:.3e}")

@@ -1,0 +1,146 @@
+"""C-ABI library checks that need no GPU.
+
+The library must load, export every function include/saw_int4.h declares,
+and reject bad arguments on the host before anything is launched.  Every
+call below carries exactly one invalid argument that the host checks catch,
+so no kernel is ever launched with these made-up pointers.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import bit_paged_kv_gb300 as saw
+from bit_paged_kv_gb300 import build as saw_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "saw_int4.h")
+
+A = 0x10000   # a 16-byte-aligned made-up address (never dereferenced)
+B = 0x20000
+MIS = 0x10008  # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def L():
+    saw_build.build()
+    return saw.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(saw_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) == set(saw.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+    # the binding module exposes the same names
+    for n in names:
+        assert callable(getattr(saw, n))
+
+
+def test_status_strings(L):
+    for code, name in [(0, "SAW_OK"), (1, "SAW_ERR_INVALID_ARG"), (2, "SAW_ERR_UNSUPPORTED"),
+                       (3, "SAW_ERR_CUDA"), (4, "SAW_ERR_DEVICE_INDEX"),
+                       (5, "SAW_ERR_DEVICE_TIMEOUT"), (99, "SAW_ERR_UNKNOWN")]:
+        assert saw.saw_status_string(code) == name
+
+
+def test_cache_bytes(L):
+    assert saw.saw_cache_bytes(1, 16, 1, 128) == 16 * 64 + 16 * 4 == 1088
+    assert saw.saw_cache_bytes(2048, 16, 8, 128) == 2048 * 8 * 1088
+    assert saw.saw_cache_bytes(10, 64, 8, 128) == 10 * 8 * 4352
+    assert saw.saw_cache_bytes(0, 16, 8, 128) == 0
+    assert saw.saw_cache_bytes(4, 16, -1, 128) == 0
+
+
+def _append(L, **kw):
+    a = dict(k=A, v=B, ks=1024, vs=1024, slots=A, T=4, hkv=8, d=128, kc=A, vc=B, pages=4, P=16,
+             rk=1, rv=1, h=128, status=None, stream=None)
+    a.update(kw)
+    return L.saw_quantize_append(a["k"], a["v"], a["ks"], a["vs"], a["slots"], a["T"], a["hkv"],
+                                 a["d"], a["kc"], a["vc"], a["pages"], a["P"], a["rk"], a["rv"],
+                                 a["h"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
+    (dict(P=8), saw.SAW_ERR_UNSUPPORTED),
+    (dict(h=3), saw.SAW_ERR_INVALID_ARG),
+    (dict(h=256), saw.SAW_ERR_INVALID_ARG),
+    (dict(h=8), saw.SAW_ERR_UNSUPPORTED),
+    (dict(rk=2), saw.SAW_ERR_INVALID_ARG),
+    (dict(k=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(slots=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(vc=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(k=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(ks=1000), saw.SAW_ERR_INVALID_ARG),
+    (dict(vs=1020), saw.SAW_ERR_INVALID_ARG),
+    (dict(T=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(hkv=0), saw.SAW_ERR_INVALID_ARG),
+    (dict(T=0), saw.SAW_OK),  # nothing to do: returns before any launch
+])
+def test_append_rejects_before_launch(L, kw, expect):
+    assert _append(L, **kw) == expect
+
+
+def _decode(L, **kw):
+    a = dict(q=A, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128, pages=8,
+             P=16, rk=1, rv=1, h=128, scale=0.0, out=A, ws=B, wsb=1 << 20, pps=0, status=None,
+             stream=None)
+    a.update(kw)
+    return L.saw_paged_decode_int4(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"], a["B"],
+                                   a["maxlen"], a["hq"], a["hkv"], a["d"], a["pages"], a["P"],
+                                   a["rk"], a["rv"], a["h"], a["scale"], a["out"], a["ws"],
+                                   a["wsb"], a["pps"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=256), saw.SAW_ERR_UNSUPPORTED),
+    (dict(P=128), saw.SAW_ERR_UNSUPPORTED),
+    (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
+    (dict(hq=72), saw.SAW_ERR_UNSUPPORTED),        # 9 q-heads per kv-head
+    (dict(h=48), saw.SAW_ERR_INVALID_ARG),
+    (dict(rv=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(scale=-1.0), saw.SAW_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), saw.SAW_ERR_INVALID_ARG),
+    (dict(q=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(bt=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(sl=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(out=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(out=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(mb=3), saw.SAW_ERR_INVALID_ARG),           # 3 * 16 < 64 tokens
+    (dict(pps=1, ws=None), saw.SAW_ERR_INVALID_ARG),  # 4 splits need a workspace
+    (dict(pps=1, wsb=16), saw.SAW_ERR_INVALID_ARG),
+    (dict(pps=1, ws=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(B=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(B=0), saw.SAW_OK),
+])
+def test_decode_rejects_before_launch(L, kw, expect):
+    assert _decode(L, **kw) == expect
+
+
+def test_plan_and_workspace(L):
+    # forced split size: 4 pages of 16 tokens -> ceil(1000/16)=63 pages -> 16 splits
+    s, pps = saw.saw_decode_plan(2, 8, 16, 1000, 4)
+    assert (s, pps) == (16, 4)
+    ws = saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 1000, 4)
+    assert ws == 2 * 32 * 16 * (128 + 2) * 4
+    # one split -> no workspace
+    assert saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 64, 64) == 0
+    # automatic plan: splits never shorter than 256 tokens, and cover the context
+    s, pps = saw.saw_decode_plan(1, 8, 16, 32768, 0)
+    assert pps * 16 >= 256 and s * pps * 16 >= 32768
+    s, pps = saw.saw_decode_plan(256, 8, 16, 8192, 0)
+    assert s * pps * 16 >= 8192
+    assert saw.saw_decode_plan(1, 8, 64, 0, 0) == (1, 1)
+    with pytest.raises(saw.SawError):
+        saw.saw_decode_plan(1, 8, 12, 100, 0)

@@ -1,0 +1,134 @@
+"""GPU parity of the paged INT4 decode attention (through the C-ABI) against
+the oracle's float64 attention on the same cache bytes.
+
+Bar: max |o_gpu - o_ref| / max |o_ref| <= 2e-3.  Pages: gist.science s.2
+point 3 (dequantization fused into decoding); youngju.dev "The Rotation
+Trick" (q.k = Hq.Hk, output rotated back)."""
+import numpy as np
+import pytest
+import torch
+
+import bit_paged_kv_gb300 as saw
+from bit_paged_kv_gb300 import workloads as W
+from gpu_helpers import (ATTN_TOL, fill_layer, gpu_append, gpu_decode, new_caches,
+                         oracle_decode, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(wl, lens, spare=5):
+    lens = torch.tensor(lens, dtype=torch.int32)
+    bt, npages = W.page_tables(wl, lens, spare_pages=spare)
+    kc, vc, _, _, _ = fill_layer(wl, 0, lens, bt, npages)
+    q = W.q_rows(wl, 0, "cuda", num_seqs=len(lens))
+    return lens, bt, npages, kc, vc, q
+
+
+def _check(wl, lens, bt, npages, kc, vc, q, pps=0, pairs=None, max_seq_len=None):
+    out, st = gpu_decode(q, kc, vc, bt.cuda(), lens.cuda(), wl.num_kv_heads, npages,
+                         wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                         max_seq_len=max_seq_len, pages_per_split=pps)
+    assert st == 0
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
+                        wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h, pairs=pairs)
+    got = out.cpu().numpy().reshape(-1, wl.head_dim)
+    if pairs is not None:
+        got = np.stack([out[b, h].cpu().numpy() for b, h in pairs])
+    assert np.all(np.isfinite(got))
+    err = rel_err(got, ref)
+    assert err <= ATTN_TOL, f"relative error {err:.3e}"
+    return err
+
+
+@pytest.mark.parametrize("pps", [0, 1, 3, 100])
+def test_tiny_full(pps):
+    """Config 'tiny' in full: 4 seqs x 256 tokens, GQA 2, K and V rotated."""
+    wl = W.TINY
+    lens, bt, npages, kc, vc, q = _setup(wl, W.seq_lens(wl).tolist())
+    _check(wl, lens, bt, npages, kc, vc, q, pps=pps)
+
+
+EDGE_LENS = [0, 1, 15, 16, 17, 33, 255, 700]
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("rot", [(1, 1), (1, 0), (0, 0), (0, 1)])
+def test_edge_lengths_groups_rotations(group, rot):
+    wl = W.TINY.variant(num_kv_heads=2, num_q_heads=2 * group, rotate_k=bool(rot[0]),
+                        rotate_v=bool(rot[1]), shuffle_pages=True, dist="student_t", nu=4)
+    lens, bt, npages, kc, vc, q = _setup(wl, EDGE_LENS)
+    _check(wl, lens, bt, npages, kc, vc, q, pps=0)
+    _check(wl, lens, bt, npages, kc, vc, q, pps=2)
+
+
+@pytest.mark.parametrize("P", [32, 64])
+@pytest.mark.parametrize("h", [128, 64, 16])
+def test_page_sizes_and_blocks(P, h):
+    wl = W.TINY.variant(page_size=P, block_h=h, num_q_heads=8, num_kv_heads=2,
+                        shuffle_pages=True)
+    lens, bt, npages, kc, vc, q = _setup(wl, [1, P - 1, P, P + 1, 5 * P + 3, 1000])
+    _check(wl, lens, bt, npages, kc, vc, q, pps=0)
+    _check(wl, lens, bt, npages, kc, vc, q, pps=1)
+
+
+def test_max_seq_len_bound_and_lengths_below_it():
+    """A plan made for a larger max_seq_len than any sequence uses."""
+    wl = W.TINY.variant(shuffle_pages=True)
+    lens, bt, npages, kc, vc, q = _setup(wl, [40, 300, 7, 256])
+    bt_wide = torch.full((bt.shape[0], 200), -1, dtype=torch.int32)
+    bt_wide[:, :bt.shape[1]] = bt
+    _check(wl, lens, bt_wide, npages, kc, vc, q, pps=0, max_seq_len=200 * 16)
+
+
+def test_bad_page_and_bad_length_are_reported():
+    wl = W.TINY
+    lens, bt, npages, kc, vc, q = _setup(wl, [64, 64])
+    bt_bad = bt.clone()
+    bt_bad[0, 1] = npages + 10
+    out, st = gpu_decode(q, kc, vc, bt_bad.cuda(), lens.cuda(), wl.num_kv_heads, npages,
+                         wl.page_size, True, True, 128)
+    assert st == saw.SAW_ERR_DEVICE_INDEX
+    assert torch.all(torch.isfinite(out[1]))
+    lens_bad = torch.tensor([64, 5000], dtype=torch.int32)
+    out, st = gpu_decode(q, kc, vc, bt.cuda(), lens_bad.cuda(), wl.num_kv_heads, npages,
+                         wl.page_size, True, True, 128, max_seq_len=64)
+    assert st == saw.SAW_ERR_DEVICE_INDEX
+    assert torch.all(out[1] == 0)
+
+
+def test_explicit_sm_scale():
+    wl = W.TINY
+    lens, bt, npages, kc, vc, q = _setup(wl, [100, 31])
+    out, st = gpu_decode(q, kc, vc, bt.cuda(), lens.cuda(), wl.num_kv_heads, npages,
+                         wl.page_size, True, True, 128, sm_scale=0.3)
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads,
+                        npages, wl.page_size, True, True, 128, sm_scale=0.3)
+    assert st == 0
+    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) <= ATTN_TOL
+
+
+def test_rotation_mismatch_is_detectable():
+    """Decoding with rotation flags that differ from the append's gives a
+    clearly wrong answer (the caller's contract)."""
+    wl = W.TINY
+    lens, bt, npages, kc, vc, q = _setup(wl, [256])
+    good = _check(wl, lens, bt, npages, kc, vc, q)
+    out, _ = gpu_decode(q, kc, vc, bt.cuda(), lens.cuda(), wl.num_kv_heads, npages,
+                        wl.page_size, True, False, 128)
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
+                        wl.page_size, True, True, 128)
+    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) > 50 * max(good, 1e-5)
+
+
+def test_decode_after_single_token_append():
+    """The decode step: append one token per sequence, then attend including it."""
+    wl = W.TINY.variant(num_seqs=3)
+    lens0 = [31, 64, 100]
+    lens, bt, npages, kc, vc, q = _setup(wl, [L + 1 for L in lens0], spare=2)
+    # overwrite the last token of every sequence through a one-token append
+    knew = torch.randn(3, wl.num_kv_heads, 128, device="cuda").to(torch.bfloat16) * 3
+    vnew = torch.randn(3, wl.num_kv_heads, 128, device="cuda").to(torch.bfloat16) * 3
+    slots = torch.stack([W.slots_for(bt, wl.page_size, b, L, L + 1)[0]
+                         for b, L in enumerate(lens0)]).to(torch.int32).cuda()
+    gpu_append(knew, vnew, slots, npages, wl.page_size, True, True, 128, kc=kc, vc=vc)
+    _check(wl, lens, bt, npages, kc, vc, q)
