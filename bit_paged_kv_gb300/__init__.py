@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     saw_decode_plan,
     saw_decode_workspace_bytes,
     saw_paged_decode_int4,
+    saw_paged_decode_int4_noalloc,
     saw_quantize_append,
     saw_status_string,
 )

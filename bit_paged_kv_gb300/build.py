@@ -23,7 +23,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
 # The append kernel's bytes are defined by separately rounded binary32 steps;
 # it uses explicit _rn intrinsics and is also compiled with contraction off.
 EXTRA = {"quantize_append.cu": ["-fmad=false"]}
-SOURCES = ["saw_api.cu", "quantize_append.cu", "paged_decode.cu"]
+SOURCES = ["saw_api.cu", "quantize_append.cu", "paged_decode.cu", "decode_static_scratch.cu"]
 
 
 def _nvcc() -> str:

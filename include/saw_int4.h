@@ -178,6 +178,40 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
                               void* workspace, size_t workspace_bytes, int32_t pages_per_split,
                               int32_t* dev_status, void* stream);
 
+/*
+ * saw_paged_decode_int4_noalloc -- the same decode as saw_paged_decode_int4
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a deployment convenience of this library.
+ *
+ * Who needs it: a plugin or custom op whose host framework owns every device
+ * allocation, code running while a CUDA graph is captured (no allocation is
+ * allowed then), or a latency-critical loop that cannot afford
+ * cudaMalloc/cudaFree's device synchronisation.  The split-K scratch comes
+ * from a fixed 4 MiB array in device memory declared by the library itself;
+ * the caller passes only inputs and outputs (arguments as in
+ * saw_paged_decode_int4, without the workspace).
+ *
+ *  - Limit: the plan's scratch (saw_decode_workspace_bytes) must be at most
+ *    4 MiB; a larger plan returns SAW_ERR_UNSUPPORTED before any launch
+ *    (use saw_paged_decode_int4, or a larger pages_per_split).
+ *  - Memory: every GPU that loads the library holds the 4 MiB until the
+ *    process exits.  No cudaMalloc/cudaFree is ever called.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Sharing: all calls on a device share the array, so calls whose kernels
+ *    may overlap on the GPU (different streams without ordering) race.
+ *    Nothing in it needs to start at zero.
+ */
+int32_t saw_paged_decode_int4_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t max_seq_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
+                                      int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                                      int32_t block_h, float sm_scale, float* out,
+                                      int32_t pages_per_split, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
