@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     lib,
     saw_cache_bytes,
     saw_decode_plan,
+    saw_decode_step,
     saw_decode_workspace_bytes,
     saw_paged_decode_int4,
     saw_paged_decode_int4_noalloc,

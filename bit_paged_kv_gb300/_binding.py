@@ -23,7 +23,8 @@ SAW_ERR_DEVICE_INDEX = 4
 SAW_ERR_DEVICE_TIMEOUT = 5
 
 EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_decode_plan",
-           "saw_decode_workspace_bytes", "saw_paged_decode_int4", "saw_paged_decode_int4_noalloc")
+           "saw_decode_workspace_bytes", "saw_paged_decode_int4", "saw_decode_step",
+           "saw_paged_decode_int4_noalloc")
 
 _lib = None
 
@@ -60,6 +61,9 @@ def lib() -> C.CDLL:
     L.saw_paged_decode_int4.restype = i32
     L.saw_paged_decode_int4.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, i32, f32, P, P, sz, i32, P, P]
+    L.saw_decode_step.restype = i32
+    L.saw_decode_step.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                  i32, i32, f32, P, P, sz, i32, P, P]
     L.saw_paged_decode_int4_noalloc.restype = i32
     L.saw_paged_decode_int4_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
                                                 i32, i32, i32, i32, f32, P, i32, P, P]
@@ -130,7 +134,9 @@ def saw_paged_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           rotate_v: bool, block_h: int, out: torch.Tensor, workspace=None,
                           sm_scale: float = 0.0, pages_per_split: int = 0, dev_status=None,
                           stream=None) -> None:
-    """q: bfloat16 [B, Hq, D] contiguous; out: float32 [B, Hq, D]."""
+    """q: bfloat16 [B, Hq, D] contiguous; out: float32 [B, Hq, D].  workspace:
+    saw_decode_workspace_bytes() bytes, zero-filled before its first use
+    (torch.zeros); each call leaves it ready for the next."""
     B, hq, d = q.shape
     assert q.dtype == torch.bfloat16 and q.is_contiguous()
     assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, hq, d)
@@ -143,6 +149,30 @@ def saw_paged_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out), _ptr(workspace),
         ws_bytes, pages_per_split, _ptr(dev_status), _stream(q, stream))
     _raise(rc, "saw_paged_decode_int4")
+
+
+def saw_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                    seq_lens: torch.Tensor, max_seq_len: int, num_kv_heads: int, num_pages: int,
+                    page_size: int, rotate_k: bool, rotate_v: bool, block_h: int,
+                    out: torch.Tensor, workspace=None, sm_scale: float = 0.0,
+                    pages_per_split: int = 0, dev_status=None, stream=None) -> None:
+    """One fused decode step: append k_new/v_new (bfloat16 [B, Hkv, D]) at
+    position seq_lens[b] - 1 of each sequence, then attend (one launch)."""
+    B, hq, d = q.shape
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    for t in (k_new, v_new):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous() and tuple(t.shape) == (B, num_kv_heads, d)
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, hq, d)
+    assert block_tables.dtype == torch.int32 and block_tables.is_contiguous()
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().saw_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), B, max_seq_len, hq, num_kv_heads, d, num_pages,
+        page_size, int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out),
+        _ptr(workspace), ws_bytes, pages_per_split, _ptr(dev_status), _stream(q, stream))
+    _raise(rc, "saw_decode_step")
 
 
 def saw_paged_decode_int4_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

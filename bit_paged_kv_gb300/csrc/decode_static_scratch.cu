@@ -63,8 +63,14 @@ extern "C" int32_t saw_paged_decode_int4_noalloc(
     const int32_t rc = scratch_for_current_device(&scratch);
     if (rc != SAW_OK) return rc;
   }
-  // Nothing in the scratch has to start at zero: every split partial that
-  // the merge reads is written earlier in the same call.
+  // The merge counts finished splits in the first words of the scratch;
+  // they must start at zero, so clear them (the split partials need no
+  // clearing: every partial the merge reads is written earlier in the call).
+  if (need > 0) {
+    const size_t tb = saw::decode_ticket_bytes(num_seqs, num_kv_heads);
+    if (cudaMemsetAsync(scratch, 0, tb, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SAW_ERR_CUDA;
+  }
   return saw_paged_decode_int4(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                                num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim,
                                num_pages, page_size, rotate_k, rotate_v, block_h, sm_scale, out,

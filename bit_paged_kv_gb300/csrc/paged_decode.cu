@@ -1,5 +1,6 @@
-// paged_decode.cu -- K2/K3: split-K decode attention over the INT4 paged
-// cache (SAW-INT4), with dequantization fused into the attention loop.
+// paged_decode.cu -- K2: split-K decode attention over the INT4 paged cache
+// (SAW-INT4), with dequantization fused into the attention loop and the
+// split merge done by the last split to finish.
 //
 // Pages: gist.science "SAW-INT4: System-Aware 4-Bit KV-Cache Quantization
 // for Real-World LLM Serving", s.2 point 3 (rotation and quantization fused
@@ -8,28 +9,32 @@
 // orthogonal, undoable rotation, so q.k = (Hq).(Hk) and o = H^-1 o'.
 //
 // Design (sm_103a):
-//  * One CTA per (split of the context, kv-head, sequence); 4 warps.  The
-//    whole GQA group of the kv-head is served by the CTA, so each page chunk
-//    is read from HBM once.
-//  * Each warp streams its own pages (pages w, w+4, ... of the split) through
-//    a private ring of shared-memory stages filled by the bulk-copy engine
-//    (cp.async.bulk + mbarrier complete_tx).  One K chunk and one V chunk per
-//    page; the chunk carries the page's codes and (scale, zero) words.
+//  * One 16-warp CTA per (split of the context, kv-head, sequence), one CTA
+//    per SM.  The whole GQA group of the kv-head is served by the CTA, so
+//    each page is read from HBM once, and q is rotated once per CTA.
+//  * The split is consumed in 32-token steps; warp w takes steps w, w+16, ...
+//    through a private two-stage shared-memory ring filled by the bulk-copy
+//    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds the step's
+//    K and V codes and their (scale, zero) words: two 16-token pages, or 32
+//    rows of a larger page (codes and metadata copied separately).
 //  * Scores: S = K~ q' on the tensor cores (mma.m16n8k16, binary16 in,
-//    binary32 accumulate), 16 tokens on M, the <= 8 q-heads on N, the head
-//    dimension on K.  K~ are the raw codes 0..15, exact in binary16,
-//    converted in registers with the 0x6400 exponent trick; the per-token
-//    scale and zero are applied afterwards: t = s*(K~.q') + z*sum(q').
+//    binary32 accumulate), 16 tokens on M, q-heads on N, the head dimension
+//    on K.  K~ are the raw codes 0..15, exact in binary16, converted in
+//    registers with the 0x6400 exponent trick; the per-token scale and zero
+//    are applied afterwards: t = s*(K~.q') + z*sum(q').
 //  * Output: O'^T += V~^T (p*s) on the tensor cores, dims on M, tokens on K,
 //    heads on N, plus sum_j p_j z_j on the CUDA cores.  p*s is moved from the
 //    score fragment to the B-operand layout with four warp shuffles.
 //  * Online softmax in base 2 per head; sm_scale*log2(e) scales the binary32
-//    score after the MMA, so an unrotated q enters the MMA exactly.
-//  * Splits write (m, l, numerator) partials; K3 merges them, normalizes and
+//    score after the MMA, so an unrotated q enters the MMA exactly; the
+//    accumulators are rescaled only when a running max grows.
+//  * Splits write (m, l, numerator) partials and take a ticket; the last
+//    split of a (sequence, kv-head) to finish merges them, normalizes and
 //    applies the inverse rotation to V's output.  With one split the CTA
-//    finishes the row itself.
+//    finishes the row itself.  No CTA waits for another.
 #include "saw_device.cuh"
 #include "saw_int4.h"
+#include "saw_quant_row.cuh"
 
 namespace saw {
 namespace {
@@ -38,23 +43,46 @@ constexpr int kWarps = kDecodeWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kRedStride = kHeadDim + 4;  // padded row of the cross-warp reduction
+constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
+constexpr int kStepTok = 32;              // tokens per step (one softmax update)
+constexpr int kTiles = kStepTok / 16;     // 16-token MMA tiles per step
+constexpr int kStages = 2;
+constexpr int kCodeRow = kHeadDim / 2;    // code bytes per token
 
+// Stage layout for a 32-token step.  Page size 16: [K chunk | V chunk] of
+// page 0, then of page 1 (each chunk = 16 code rows, then 16 meta words).
+// Page size >= 32: [K codes 32 rows | K meta 32 words | V codes | V meta].
 template <int P>
 struct Cfg {
   static constexpr int kChunk = chunk_bytes(P);
-  static constexpr int kStage = 2 * kChunk;  // K chunk, then V chunk
-  static constexpr int kStages = (P == 16) ? 4 : (P == 32) ? 3 : 2;
-  static constexpr int kTiles = P / 16;
+  static constexpr int kPagesPerStep = (P == 16) ? 2 : 1;
+  static constexpr int kStepsPerPage = (P == 16) ? 1 : P / kStepTok;
+  static constexpr int kStage = 2 * (kStepTok * kCodeRow + kStepTok * 4);  // 4352 bytes
+  // byte offset of K's code row / meta word `row` of tile tt in a stage; V's
+  // are at the same offsets from vbase
+  __device__ static constexpr int kcode(int tt, int row) {
+    return (P == 16) ? tt * 2 * chunk_bytes(16) + row * kCodeRow : (tt * 16 + row) * kCodeRow;
+  }
+  __device__ static constexpr int kmeta(int tt, int row) {
+    return (P == 16) ? tt * 2 * chunk_bytes(16) + 16 * kCodeRow + row * 4
+                     : kStepTok * kCodeRow + (tt * 16 + row) * 4;
+  }
+  __device__ static constexpr int vbase() {
+    return (P == 16) ? chunk_bytes(16) : kStepTok * kCodeRow + kStepTok * 4;
+  }
   static constexpr int kRing = kWarps * kStages * kStage;
+  // after the main loop the ring is reused: cross-warp reduction, then rows
   static constexpr int kRed = kWarps * kMaxGroup * kRedStride * 4 + 3 * kWarps * kMaxGroup * 4;
-  static_assert(kRed <= kRing, "reduction scratch must fit in the ring");
-  // dynamic shared memory layout
+  static constexpr int kOffQ = (kRed + 15) / 16 * 16;                          // f32 [8][128]
+  static_assert(kOffQ + kMaxGroup * kHeadDim * 4 <= kRing, "epilogue scratch must fit the ring");
   static constexpr int kOffBars = kRing;
-  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;
-  static constexpr int kOffQ = (kOffOk + kWarps * kStages * 4 + 15) / 16 * 16;  // float [8][128]
-  static constexpr int kOffQh = kOffQ + kMaxGroup * kHeadDim * 4;   // half [2][8][128]: hi, lo
-  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;         // float [8]
-  static constexpr int kSmem = kOffQsum + kMaxGroup * 4;
+  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][2][2]
+  static constexpr int kOffIds = kOffOk + kWarps * kStages * 2 * 4;           // int [16][kIdCap]
+  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8][128]
+  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [8]
+  static constexpr int kOffFlag = kOffQsum + kMaxGroup * 4;                   // int
+  static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (64 code bytes, meta)
+  static constexpr int kSmem = kOffNew + 2 * (kCodeRow + 16);
 };
 
 // In-place butterfly over each h-block of nvec vectors of 128 floats in shared
@@ -92,15 +120,30 @@ __device__ __forceinline__ uint32_t hfma_hi(uint32_t x) {
 
 constexpr uint32_t kMagic = 0x64006400u;  // binary16 1024.0 in both halves
 
-template <int P>
-__global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kernel(const DecodeParams p) {
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
+}
+
+// PACKED (group <= 4): the MMA's 8 columns carry the hi parts of the (up to)
+// 4 heads in columns 0-3 and the lo parts in columns 4-7, both for q' in the
+// score product and for p*s in the output product; lanes c and c^2 of an
+// MMA quad then hold the two halves of the same heads and are summed with one
+// shuffle.  WIDE (group 5..8): all 8 columns are heads; the score product
+// runs twice (q' hi, then lo) and p*s is one binary16 value.
+template <int P, bool PACKED, bool APPEND>
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeParams p) {
   using C = Cfg<P>;
+  pdl_wait_then_release();
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + C::kOffOk);
   float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
   __half* qh = reinterpret_cast<__half*>(smem + C::kOffQh);
   float* qsum = reinterpret_cast<float*>(smem + C::kOffQsum);
+  int* flag = reinterpret_cast<int*>(smem + C::kOffFlag);
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -124,54 +167,127 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
   const bool direct = (p.num_splits == 1);
 
   if (p_begin >= p_end) {
-    // nothing to attend over: a direct launch still owes the output row
-    if (direct) {
+    // nothing to attend over here; an empty sequence still owes a zero row
+    if (split == 0 && n_pages == 0) {
       for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
         p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = 0.0f;
     }
     return;
   }
 
-  // ---- per-warp page stream: barriers and the first copies go out first,
-  // so HBM latency overlaps the q prologue below
-  const int my_first = p_begin + warp;
-  const int n_my = (my_first < p_end) ? (p_end - my_first + kWarps - 1) / kWarps : 0;
-  uint8_t* ring = smem + warp * C::kStages * C::kStage;
-  uint64_t* wbars = bars + warp * C::kStages;
-  int32_t* wok = stage_ok + warp * C::kStages;
+  // ---- this warp's steps: step j covers tokens [p_begin*P + 32j, +32);
+  // warp w takes steps w, w+16, ...
+  const int n_steps = ((p_end - p_begin) * P + kStepTok - 1) / kStepTok;
+  const int n_my = (warp < n_steps) ? (n_steps - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* ring = smem + warp * kStages * C::kStage;
+  uint64_t* wbars = bars + warp * kStages;
+  int32_t* wok = stage_ok + warp * kStages * 2;
   const int32_t* btab = p.block_tables + int64_t(seq) * p.max_blocks;
 
+  // physical page id of page q of this warp's step i (-1: none or invalid)
+  auto page_id = [&](int i, int q) {
+    const int j = warp + i * kWarps;
+    const int lp = p_begin + ((P == 16) ? 2 * j + q : j / C::kStepsPerPage);
+    int id = -1;
+    if (lp < p_end) {
+      id = btab[lp];
+      if (id < 0 || id >= p.num_pages) {
+        report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+        id = -1;
+      }
+    }
+    return id;
+  };
+  // the warp's page ids, fetched once instead of one dependent global load
+  // in front of every copy
+  int32_t* wids = reinterpret_cast<int32_t*>(smem + C::kOffIds) + warp * kIdCap;
+  for (int e = lane; e < n_my * C::kPagesPerStep && e < kIdCap; e += 32)
+    wids[e] = page_id(e / C::kPagesPerStep, e % C::kPagesPerStep);
+  __syncwarp();
+
   auto issue = [&](int i) {  // lane 0 only
-    const int lp = my_first + i * kWarps;
-    const int s = i % C::kStages;
-    const int pid = btab[lp];
-    if (pid >= 0 && pid < p.num_pages) {
-      wok[s] = 1;
-      mbar_arrive_expect_tx(&wbars[s], 2 * C::kChunk);
-      const int64_t off = (int64_t(pid) * p.num_kv_heads + kvh) * C::kChunk;
-      bulk_g2s(ring + s * C::kStage, p.k_cache + off, C::kChunk, &wbars[s]);
-      bulk_g2s(ring + s * C::kStage + C::kChunk, p.v_cache + off, C::kChunk, &wbars[s]);
-    } else {
-      wok[s] = 0;
-      report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+    const int s = i % kStages;
+    uint8_t* st = ring + s * C::kStage;
+    uint32_t bytes = 0;
+    int pid[C::kPagesPerStep];
+#pragma unroll
+    for (int q = 0; q < C::kPagesPerStep; ++q) {
+      const int e = i * C::kPagesPerStep + q;
+      pid[q] = (e < kIdCap) ? wids[e] : page_id(i, q);
+      wok[s * 2 + q] = (pid[q] >= 0);
+      if (pid[q] >= 0) bytes += (P == 16) ? 2 * C::kChunk : C::kStage;
+    }
+    if (bytes == 0) {
       mbar_arrive(&wbars[s]);
+      return;
+    }
+    mbar_arrive_expect_tx(&wbars[s], bytes);
+#pragma unroll
+    for (int q = 0; q < C::kPagesPerStep; ++q) {
+      if (pid[q] < 0) continue;
+      const int64_t off = (int64_t(pid[q]) * p.num_kv_heads + kvh) * C::kChunk;
+      if (P == 16) {
+        bulk_g2s(st + q * 2 * C::kChunk, p.k_cache + off, C::kChunk, &wbars[s]);
+        bulk_g2s(st + q * 2 * C::kChunk + C::kChunk, p.v_cache + off, C::kChunk, &wbars[s]);
+      } else {
+        const int part = (warp + i * kWarps) % C::kStepsPerPage;
+        const int64_t codes = off + part * (kStepTok * kCodeRow);
+        const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
+        bulk_g2s(st, p.k_cache + codes, kStepTok * kCodeRow, &wbars[s]);
+        bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, &wbars[s]);
+        bulk_g2s(st + C::vbase(), p.v_cache + codes, kStepTok * kCodeRow, &wbars[s]);
+        bulk_g2s(st + C::vbase() + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4,
+                 &wbars[s]);
+      }
     }
   };
 
   if (lane == 0) {
-    for (int i = 0; i < C::kStages; ++i) mbar_init(&wbars[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&wbars[i], 1);
     mbar_fence_init();
-    for (int i = 0; i < C::kStages && i < n_my; ++i) issue(i);
+    for (int i = 0; i < kStages && i < n_my; ++i) issue(i);
   }
   __syncwarp();
 
+  // ---- decode step: the CTA whose split holds the new token (position L-1)
+  // quantizes its K and V rows for this kv-head (the same warp quantizer as
+  // the append kernels, so the bytes match), writes them into the cache, and
+  // keeps them to patch its own copy of that page below.
+  uint8_t* newrow = smem + C::kOffNew;
+  const int new_tok = L - 1;
+  const bool owner = APPEND && new_tok >= 0 && new_tok / P >= p_begin && new_tok / P < p_end;
+  if (owner && warp >= kWarps - 2) {
+    const int tensor = warp - (kWarps - 2);
+    const uint16_t* src = (tensor == 0 ? p.k_new + int64_t(seq) * p.k_new_stride
+                                       : p.v_new + int64_t(seq) * p.v_new_stride) +
+                          int64_t(kvh) * kHeadDim;
+    const bool rot = (tensor == 0 ? p.rotate_k : p.rotate_v) != 0;
+    uint32_t meta;
+    const uint16_t codes = warp_quantize_row(src, rot, p.block_h, p.c_h, lane, &meta);
+    uint8_t* nr = newrow + tensor * (kCodeRow + 16);
+    reinterpret_cast<uint16_t*>(nr)[lane] = codes;
+    if (lane == 0) *reinterpret_cast<uint32_t*>(nr + kCodeRow) = meta;
+    const int pid = btab[new_tok / P];
+    if (pid >= 0 && pid < p.num_pages) {
+      const int off = new_tok % P;
+      uint8_t* chunk = (tensor == 0 ? p.k_cache_w : p.v_cache_w) +
+                       (int64_t(pid) * p.num_kv_heads + kvh) * C::kChunk;
+      reinterpret_cast<uint16_t*>(chunk + off * kCodeRow)[lane] = codes;
+      if (lane == 0) *reinterpret_cast<uint32_t*>(chunk + P * kCodeRow + 4 * off) = meta;
+    }
+  }
+  // the step (and its row) that holds the new token, for the patch
+  const int new_local = new_tok - p_begin * P;
+  const int new_step = owner ? new_local / kStepTok : -1;
+
   // ---- q' = (1/sqrt h) H q for the group's heads, as binary16 hi + lo parts
-  // (q' = hi + lo to ~22 bits; zeros beyond G).  Warp w rotates heads w and
-  // w + 4, lane l holding elements 4l..4l+3; sm_scale*log2(e) is applied to
-  // the binary32 score, so an unrotated q enters the MMA exactly.
+  // (q' = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8 rotates head h,
+  // lane l holding elements 4l..4l+3; sm_scale*log2(e) is applied to the
+  // binary32 score, so an unrotated q enters the MMA exactly.
   __half* qh_hi = qh;
   __half* qh_lo = qh + kMaxGroup * kHeadDim;
-  for (int h = warp; h < kMaxGroup; h += kWarps) {
+  if (warp < kMaxGroup) {
+    const int h = warp;
     float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (h < G) {
       const uint2 raw = *reinterpret_cast<const uint2*>(
@@ -182,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
       x[3] = bf16_hi(raw.y);
       if (p.rotate_k) {
         const int hb = p.block_h;
-        float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
+        const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
         if (hb > 2) {
           x[0] = a0 + a2; x[1] = a1 + a3; x[2] = a0 - a2; x[3] = a1 - a3;
         } else {
@@ -217,23 +333,32 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
   __syncthreads();
 
   // B fragments of q' for the score MMA (k-step t uses word 4c + t/2 of a
-  // token's codes: bytes (0,2) for even t, (1,3) for odd t).
-  uint32_t bq[8][2], bl[8][2];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int base = 8 * (4 * c + t / 2) + ((t & 1) ? 2 : 0);
-    const __half* rh = qh_hi + g * kHeadDim;
+  // token's codes: bytes (0,2) for even t, (1,3) for odd t).  Column g:
+  // PACKED -> hi of head g (g < 4) or lo of head g - 4; WIDE -> head g.
+  uint32_t bq[8][2];
+  uint32_t bl[PACKED ? 1 : 8][2];
+  {
+    const __half* rh = PACKED ? ((g < 4) ? qh_hi + g * kHeadDim : qh_lo + (g - 4) * kHeadDim)
+                              : qh_hi + g * kHeadDim;
     const __half* rl = qh_lo + g * kHeadDim;
-    __half2 v0 = __halves2half2(rh[base], rh[base + 4]);
-    __half2 v1 = __halves2half2(rh[base + 1], rh[base + 5]);
-    __half2 w0 = __halves2half2(rl[base], rl[base + 4]);
-    __half2 w1 = __halves2half2(rl[base + 1], rl[base + 5]);
-    bq[t][0] = *reinterpret_cast<uint32_t*>(&v0);
-    bq[t][1] = *reinterpret_cast<uint32_t*>(&v1);
-    bl[t][0] = *reinterpret_cast<uint32_t*>(&w0);
-    bl[t][1] = *reinterpret_cast<uint32_t*>(&w1);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int base = 8 * (4 * c + t / 2) + ((t & 1) ? 2 : 0);
+      __half2 v0 = __halves2half2(rh[base], rh[base + 4]);
+      __half2 v1 = __halves2half2(rh[base + 1], rh[base + 5]);
+      bq[t][0] = *reinterpret_cast<uint32_t*>(&v0);
+      bq[t][1] = *reinterpret_cast<uint32_t*>(&v1);
+      if (!PACKED) {
+        __half2 w0 = __halves2half2(rl[base], rl[base + 4]);
+        __half2 w1 = __halves2half2(rl[base + 1], rl[base + 5]);
+        bl[PACKED ? 0 : t][0] = *reinterpret_cast<uint32_t*>(&w0);
+        bl[PACKED ? 0 : t][1] = *reinterpret_cast<uint32_t*>(&w1);
+      }
+    }
   }
-  const float qsum0 = qsum[2 * c] * p.q_scale, qsum1 = qsum[2 * c + 1] * p.q_scale;
+  // this thread's two heads
+  const int hb = PACKED ? 2 * (c & 1) : 2 * c;
+  const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
 
   float acc[8][4];
 #pragma unroll
@@ -245,63 +370,84 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
   int waited = 0;
 
   for (int i = 0; i < n_my; ++i) {
-    const int s = i % C::kStages;
-    const bool ok = mbar_wait_bounded(&wbars[s], (i / C::kStages) & 1);
+    const int s = i % kStages;
+    const bool ok = mbar_wait_bounded(&wbars[s], (i / kStages) & 1);
     if (!__all_sync(kFull, ok)) {
       failed = true;
       break;
     }
     waited = i + 1;
-    const uint8_t* kst = ring + s * C::kStage;
-    const uint8_t* vst = kst + C::kChunk;
-    const bool page_ok = wok[s] != 0;
-    const int tok_base = (my_first + i * kWarps) * P;
+    const uint8_t* st = ring + s * C::kStage;
+    const int tok0 = p_begin * P + (warp + i * kWarps) * kStepTok;
+    if (APPEND && warp + i * kWarps == new_step) {
+      // replace the copied row of the new token by its freshly quantized one
+      const int r = new_local % kStepTok, tt = r / 16, row = r % 16;
+      uint8_t* w = ring + s * C::kStage;
+      if (lane < 16) {
+        const int tensor = lane >> 3, part = lane & 7;  // 8 x 8 bytes per tensor
+        const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
+        uint8_t* dst = w + (tensor ? C::vbase() : 0) + C::kcode(tt, row);
+        reinterpret_cast<uint2*>(dst)[part] = reinterpret_cast<const uint2*>(nr)[part];
+      } else if (lane < 18) {
+        const int tensor = lane - 16;
+        const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
+        *reinterpret_cast<uint32_t*>(w + (tensor ? C::vbase() : 0) + C::kmeta(tt, row)) =
+            *reinterpret_cast<const uint32_t*>(nr + kCodeRow);
+      }
+      __syncwarp();
+    }
 
-    // ---- scores for every 16-token tile of the page
-    float sc[C::kTiles][4];
+    // ---- scores of both 16-token tiles of the step
+    float sc[kTiles][4];
 #pragma unroll
-    for (int tt = 0; tt < C::kTiles; ++tt) {
-      const uint8_t* krow = kst + (16 * tt + g) * (kHeadDim / 2) + 16 * c;
+    for (int tt = 0; tt < kTiles; ++tt) {
+      const bool pok = wok[s * 2 + ((P == 16) ? tt : 0)] != 0;
+      const uint8_t* krow = st + C::kcode(tt, g) + 16 * c;
       const uint4 ka = *reinterpret_cast<const uint4*>(krow);
-      const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * (kHeadDim / 2));
+      const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow);
       const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w};
       const uint32_t kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+      // two independent accumulator chains (even / odd byte pairs)
       float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float e2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          const uint32_t ya = hb ? (kaw[w] >> 8) : kaw[w];
-          const uint32_t yb = hb ? (kbw[w] >> 8) : kbw[w];
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t ya = hh ? (kaw[w] >> 8) : kaw[w];
+          const uint32_t yb = hh ? (kbw[w] >> 8) : kbw[w];
           uint32_t a[4];
           a[0] = hsub_1024(and_or(ya, 0x000F000Fu, kMagic));
           a[1] = hsub_1024(and_or(yb, 0x000F000Fu, kMagic));
           a[2] = hfma_hi(and_or(ya, 0x00F000F0u, kMagic));
           a[3] = hfma_hi(and_or(yb, 0x00F000F0u, kMagic));
-          mma_16816(d, a, bq[2 * w + hb][0], bq[2 * w + hb][1]);
-          mma_16816(d, a, bl[2 * w + hb][0], bl[2 * w + hb][1]);
+          float (&dst)[4] = hh ? e2 : d;
+          mma_16816(dst, a, bq[2 * w + hh][0], bq[2 * w + hh][1]);
+          if (!PACKED) mma_16816(dst, a, bl[PACKED ? 0 : 2 * w + hh][0], bl[PACKED ? 0 : 2 * w + hh][1]);
         }
       }
-      const uint32_t mk0 =
-          *reinterpret_cast<const uint32_t*>(kst + P * (kHeadDim / 2) + (16 * tt + g) * 4);
-      const uint32_t mk1 =
-          *reinterpret_cast<const uint32_t*>(kst + P * (kHeadDim / 2) + (16 * tt + g + 8) * 4);
-      const float sk0 = __half2float(__ushort_as_half(uint16_t(mk0 & 0xFFFF))) * p.q_scale;
-      const float zk0 = __half2float(__ushort_as_half(uint16_t(mk0 >> 16)));
-      const float sk1 = __half2float(__ushort_as_half(uint16_t(mk1 & 0xFFFF))) * p.q_scale;
-      const float zk1 = __half2float(__ushort_as_half(uint16_t(mk1 >> 16)));
-      const bool v0 = page_ok && (tok_base + 16 * tt + g) < L;
-      const bool v1 = page_ok && (tok_base + 16 * tt + g + 8) < L;
-      sc[tt][0] = v0 ? fmaf(sk0, d[0], zk0 * qsum0) : -INFINITY;
-      sc[tt][1] = v0 ? fmaf(sk0, d[1], zk0 * qsum1) : -INFINITY;
-      sc[tt][2] = v1 ? fmaf(sk1, d[2], zk1 * qsum0) : -INFINITY;
-      sc[tt][3] = v1 ? fmaf(sk1, d[3], zk1 * qsum1) : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[j] += e2[j];
+      if (PACKED) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j] += __shfl_xor_sync(kFull, d[j], 2);
+      }
+      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(tt, g));
+      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(tt, g + 8));
+      const float sk0 = half_lo(mk0) * p.q_scale, zk0 = half_hi(mk0);
+      const float sk1 = half_lo(mk1) * p.q_scale, zk1 = half_hi(mk1);
+      const bool v0 = pok && (tok0 + 16 * tt + g) < L;
+      const bool v1 = pok && (tok0 + 16 * tt + g + 8) < L;
+      sc[tt][0] = v0 ? fmaf(sk0, d[0], zk0 * qsA) : -INFINITY;
+      sc[tt][1] = v0 ? fmaf(sk0, d[1], zk0 * qsB) : -INFINITY;
+      sc[tt][2] = v1 ? fmaf(sk1, d[2], zk1 * qsA) : -INFINITY;
+      sc[tt][3] = v1 ? fmaf(sk1, d[3], zk1 * qsB) : -INFINITY;
     }
 
-    // ---- online softmax update (per head 2c, 2c+1)
+    // ---- online softmax: rescale only when a running max grows
     float mloc0 = -INFINITY, mloc1 = -INFINITY;
 #pragma unroll
-    for (int tt = 0; tt < C::kTiles; ++tt) {
+    for (int tt = 0; tt < kTiles; ++tt) {
       mloc0 = fmaxf(mloc0, fmaxf(sc[tt][0], sc[tt][2]));
       mloc1 = fmaxf(mloc1, fmaxf(sc[tt][1], sc[tt][3]));
     }
@@ -310,46 +456,55 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
       mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
       mloc1 = fmaxf(mloc1, __shfl_xor_sync(kFull, mloc1, x));
     }
-    const float mn0 = fmaxf(m_run[0], mloc0), mn1 = fmaxf(m_run[1], mloc1);
-    const float mu0 = (mn0 == -INFINITY) ? 0.0f : mn0;
-    const float mu1 = (mn1 == -INFINITY) ? 0.0f : mn1;
-    const float al0 = ex2(m_run[0] - mu0), al1 = ex2(m_run[1] - mu1);
-    m_run[0] = mn0;
-    m_run[1] = mn1;
-    l_run[0] *= al0;
-    l_run[1] *= al1;
-    z_run[0] *= al0;
-    z_run[1] *= al1;
+    if (__any_sync(kFull, (mloc0 > m_run[0]) || (mloc1 > m_run[1]))) {
+      const float mn0 = fmaxf(m_run[0], mloc0), mn1 = fmaxf(m_run[1], mloc1);
+      const float al0 = ex2(m_run[0] - ((mn0 == -INFINITY) ? 0.0f : mn0));
+      const float al1 = ex2(m_run[1] - ((mn1 == -INFINITY) ? 0.0f : mn1));
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+      l_run[0] *= al0;
+      l_run[1] *= al1;
+      z_run[0] *= al0;
+      z_run[1] *= al1;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      acc[k][0] *= al0;
-      acc[k][1] *= al1;
-      acc[k][2] *= al0;
-      acc[k][3] *= al1;
+      for (int k = 0; k < 8; ++k) {
+        acc[k][0] *= al0;
+        acc[k][1] *= al1;
+        acc[k][2] *= al0;
+        acc[k][3] *= al1;
+      }
     }
+    const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
+    const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
 
     // ---- probabilities, V terms, and the PV product per tile
 #pragma unroll
-    for (int tt = 0; tt < C::kTiles; ++tt) {
+    for (int tt = 0; tt < kTiles; ++tt) {
+      const bool pok = wok[s * 2 + ((P == 16) ? tt : 0)] != 0;
+      const uint8_t* vst = st + C::vbase();
       const float p0 = ex2(sc[tt][0] - mu0), p1 = ex2(sc[tt][1] - mu1);
       const float p2 = ex2(sc[tt][2] - mu0), p3 = ex2(sc[tt][3] - mu1);
-      const uint32_t mv0 =
-          *reinterpret_cast<const uint32_t*>(vst + P * (kHeadDim / 2) + (16 * tt + g) * 4);
-      const uint32_t mv1 =
-          *reinterpret_cast<const uint32_t*>(vst + P * (kHeadDim / 2) + (16 * tt + g + 8) * 4);
-      const bool v0 = page_ok && (tok_base + 16 * tt + g) < L;
-      const bool v1 = page_ok && (tok_base + 16 * tt + g + 8) < L;
-      const float sv0 = v0 ? __half2float(__ushort_as_half(uint16_t(mv0 & 0xFFFF))) : 0.0f;
-      const float zv0 = v0 ? __half2float(__ushort_as_half(uint16_t(mv0 >> 16))) : 0.0f;
-      const float sv1 = v1 ? __half2float(__ushort_as_half(uint16_t(mv1 & 0xFFFF))) : 0.0f;
-      const float zv1 = v1 ? __half2float(__ushort_as_half(uint16_t(mv1 >> 16))) : 0.0f;
+      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(tt, g));
+      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(tt, g + 8));
+      const bool v0 = pok && (tok0 + 16 * tt + g) < L;
+      const bool v1 = pok && (tok0 + 16 * tt + g + 8) < L;
+      const float sv0 = v0 ? half_lo(mv0) : 0.0f, zv0 = v0 ? half_hi(mv0) : 0.0f;
+      const float sv1 = v1 ? half_lo(mv1) : 0.0f, zv1 = v1 ? half_hi(mv1) : 0.0f;
       l_run[0] += p0 + p2;
       l_run[1] += p1 + p3;
       z_run[0] += p0 * zv0 + p2 * zv1;
       z_run[1] += p1 * zv0 + p3 * zv1;
-      // (p*s) for head 2c / 2c+1 over tokens (g, g+8) -> B layout for head g
-      const uint32_t X = pack_half2(p0 * sv0, p2 * sv1);
-      const uint32_t Y = pack_half2(p1 * sv0, p3 * sv1);
+      // (p*s) for this thread's columns over tokens (g, g+8); PACKED lanes
+      // c >= 2 carry the binary16 remainder (lo part)
+      float ps0 = p0 * sv0, ps1 = p1 * sv0, ps2 = p2 * sv1, ps3 = p3 * sv1;
+      if (PACKED && c >= 2) {
+        ps0 -= __half2float(__float2half_rn(ps0));
+        ps1 -= __half2float(__float2half_rn(ps1));
+        ps2 -= __half2float(__float2half_rn(ps2));
+        ps3 -= __half2float(__float2half_rn(ps3));
+      }
+      const uint32_t X = pack_half2(ps0, ps2);
+      const uint32_t Y = pack_half2(ps1, ps3);
       const int src0 = 8 * c + (g >> 1);
       const uint32_t xa = __shfl_sync(kFull, X, src0);
       const uint32_t ya = __shfl_sync(kFull, Y, src0);
@@ -360,17 +515,17 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
       const uint32_t b0 = prmt(va, vb, 0x5410u);
       const uint32_t b1 = prmt(va, vb, 0x7632u);
 
-      const uint8_t* vrow = vst + (16 * tt) * (kHeadDim / 2) + 8 * g;
-      const uint2 r0 = *reinterpret_cast<const uint2*>(vrow + (2 * c) * (kHeadDim / 2));
-      const uint2 r1 = *reinterpret_cast<const uint2*>(vrow + (2 * c + 1) * (kHeadDim / 2));
-      const uint2 r2 = *reinterpret_cast<const uint2*>(vrow + (2 * c + 8) * (kHeadDim / 2));
-      const uint2 r3 = *reinterpret_cast<const uint2*>(vrow + (2 * c + 9) * (kHeadDim / 2));
+      const uint8_t* vrow = vst + C::kcode(tt, 0) + 8 * g;
+      const uint2 r0w = *reinterpret_cast<const uint2*>(vrow + (2 * c) * kCodeRow);
+      const uint2 r1w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 1) * kCodeRow);
+      const uint2 r2w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 8) * kCodeRow);
+      const uint2 r3w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 9) * kCodeRow);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t w0 = (k < 4) ? r0.x : r0.y;
-        const uint32_t w1 = (k < 4) ? r1.x : r1.y;
-        const uint32_t w2 = (k < 4) ? r2.x : r2.y;
-        const uint32_t w3 = (k < 4) ? r3.x : r3.y;
+        const uint32_t w0 = (k < 4) ? r0w.x : r0w.y;
+        const uint32_t w1 = (k < 4) ? r1w.x : r1w.y;
+        const uint32_t w2 = (k < 4) ? r2w.x : r2w.y;
+        const uint32_t w3 = (k < 4) ? r3w.x : r3w.y;
         const uint32_t sel = uint32_t(k & 3) | (uint32_t((k & 3) + 4) << 8);
         const uint32_t x01 = prmt(w0, w1, sel);
         const uint32_t x23 = prmt(w2, w3, sel);
@@ -384,17 +539,18 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
     }
 
     __syncwarp();
-    if (lane == 0 && i + C::kStages < n_my) issue(i + C::kStages);
+    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
   }
 
   if (failed) {
     if (lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
     // let this warp's copies in flight land before the CTA's memory is reused
-    for (int i = waited; i < n_my && i < waited + C::kStages; ++i)
-      (void)mbar_wait_bounded(&wbars[i % C::kStages], (i / C::kStages) & 1);
+    for (int i = waited; i < n_my && i < waited + kStages; ++i)
+      (void)mbar_wait_bounded(&wbars[i % kStages], (i / kStages) & 1);
   }
 
-  // ---- cross-thread reductions of l and the z term (lanes sharing c)
+  // ---- cross-thread reductions of l and the z term (lanes sharing c), and
+  // of the hi/lo column halves in PACKED mode
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
     l_run[0] += __shfl_xor_sync(kFull, l_run[0], x);
@@ -402,22 +558,29 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
     z_run[0] += __shfl_xor_sync(kFull, z_run[0], x);
     z_run[1] += __shfl_xor_sync(kFull, z_run[1], x);
   }
-  __syncthreads();  // every warp is done with its ring: reuse it
-
-  float* red_acc = reinterpret_cast<float*>(smem);                     // [4][8][132]
-  float* red_m = red_acc + kWarps * kMaxGroup * kRedStride;           // [4][8]
-  float* red_l = red_m + kWarps * kMaxGroup;
-  float* red_z = red_l + kWarps * kMaxGroup;
-  if (g == 0) {
+  if (PACKED) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      red_m[warp * kMaxGroup + 2 * c + hh] = m_run[hh];
-      red_l[warp * kMaxGroup + 2 * c + hh] = l_run[hh];
-      red_z[warp * kMaxGroup + 2 * c + hh] = z_run[hh];
+    for (int k = 0; k < 8; ++k) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[k][j] += __shfl_xor_sync(kFull, acc[k][j], 2);
     }
   }
-  {
-    float* base0 = red_acc + (warp * kMaxGroup + 2 * c) * kRedStride;
+  __syncthreads();  // every warp is done with its ring: reuse it
+
+  float* red_acc = reinterpret_cast<float*>(smem);                     // [16][8][132]
+  float* red_m = red_acc + kWarps * kMaxGroup * kRedStride;           // [16][8]
+  float* red_l = red_m + kWarps * kMaxGroup;
+  float* red_z = red_l + kWarps * kMaxGroup;
+  if (!PACKED || c < 2) {
+    if (g == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        red_m[warp * kMaxGroup + hb + hh] = m_run[hh];
+        red_l[warp * kMaxGroup + hb + hh] = l_run[hh];
+        red_z[warp * kMaxGroup + hb + hh] = z_run[hh];
+      }
+    }
+    float* base0 = red_acc + (warp * kMaxGroup + hb) * kRedStride;
     float* base1 = base0 + kRedStride;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -429,16 +592,15 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
   }
   __syncthreads();
 
-  // ---- merge the warps: thread = output dimension
-  const int dd = tid;  // kThreads == kHeadDim
-  for (int h = 0; h < G; ++h) {
+  // ---- merge the warps: one (head, dim) per thread
+  const int nw = min(kWarps, n_steps);  // warps that saw any step
+  for (int idx = tid; idx < G * kHeadDim; idx += kThreads) {
+    const int h = idx / kHeadDim, dd = idx - h * kHeadDim;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kMaxGroup + h]);
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w * kMaxGroup + h]);
     const float Mu = (M == -INFINITY) ? 0.0f : M;
     float num = 0.0f, den = 0.0f, zz = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       const float f = ex2(red_m[w * kMaxGroup + h] - Mu);
       num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * f;
       den += red_l[w * kMaxGroup + h] * f;
@@ -456,86 +618,110 @@ __global__ void __launch_bounds__(kThreads, (P == 64) ? 3 : 4) paged_decode_kern
       }
     }
   }
-  if (direct) {
+
+  if (!direct) {
+    // ---- the last split of this (sequence, kv-head) to finish merges them
+    // all: one launch covers the decode, and no CTA ever waits for another.
+    __threadfence();  // this CTA's partials are visible before its ticket
     __syncthreads();
-    if (p.rotate_v) smem_fwht(qs, G, p.block_h);
-    const float post = p.rotate_v ? p.c_h : 1.0f;
-    for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
-      p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = qs[idx] * post;
+    const int ns = (n_pages + p.pages_per_split - 1) / p.pages_per_split;
+    if (tid == 0) {
+      uint32_t* ticket = p.tickets + (int64_t(seq) * p.num_kv_heads + kvh);
+      const uint32_t done = atomicAdd(ticket, 1u) + 1u;
+      *flag = (done == uint32_t(ns));
+      if (done >= uint32_t(ns)) {
+        if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
+        *ticket = 0u;  // every split has counted: ready for the next call
+      }
+    }
+    __syncthreads();
+    if (*flag == 0) return;
+    __threadfence();
+    // item = (head, 4 dims); four threads per item share the splits, so each
+    // thread has only a few loads in flight and one round of L2 latency
+    for (int base = 0; base < G * 32 * 4; base += kThreads) {
+      const int t = base + tid;
+      const int item = t >> 2, part = t & 3;
+      const bool active = item < G * 32;
+      const int h = active ? item >> 5 : 0, ch = item & 31;
+      const int64_t row0 = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits;
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row0;
+      const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kHeadDim) + ch;
+      float M = -INFINITY;
+      if (active)
+        for (int sp = part; sp < ns; sp += 4) M = fmaxf(M, __ldcg(&ml[sp]).x);
+      M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
+      M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
+      const float Mu = (M == -INFINITY) ? 0.0f : M;
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float den = 0.0f;
+      if (active) {
+#pragma unroll 8
+        for (int sp = part; sp < ns; sp += 4) {
+          const float2 v = __ldcg(&ml[sp]);
+          const float4 o = __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]);
+          const float f = ex2(v.x - Mu);
+          den += v.y * f;
+          a.x += o.x * f;
+          a.y += o.y * f;
+          a.z += o.z * f;
+          a.w += o.w * f;
+        }
+      }
+#pragma unroll
+      for (int x = 1; x <= 2; x <<= 1) {
+        den += __shfl_xor_sync(kFull, den, x);
+        a.x += __shfl_xor_sync(kFull, a.x, x);
+        a.y += __shfl_xor_sync(kFull, a.y, x);
+        a.z += __shfl_xor_sync(kFull, a.z, x);
+        a.w += __shfl_xor_sync(kFull, a.w, x);
+      }
+      if (active && part == 0) {
+        const float inv = (den > 0.0f) ? 1.0f / den : 0.0f;
+        float* dst = qs + h * kHeadDim + 4 * ch;
+        dst[0] = a.x * inv;
+        dst[1] = a.y * inv;
+        dst[2] = a.z * inv;
+        dst[3] = a.w * inv;
+      }
+    }
   }
+  __syncthreads();
+  if (p.rotate_v) smem_fwht(qs, G, p.block_h);
+  const float post = p.rotate_v ? p.c_h : 1.0f;
+  for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
+    p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = qs[idx] * post;
 }
 
-// K3: merge the split partials of one (sequence, q-head), normalise, and
-// rotate V's output back.  Warp w folds splits w, w+4, ... with lane l owning
-// dims 4l..4l+3 (coalesced float4 reads), then the four warps are summed.
-__global__ void __launch_bounds__(kHeadDim) combine_kernel(const DecodeParams p) {
-  __shared__ float red[kWarps][kHeadDim];
-  __shared__ float wmax[kWarps], wden[kWarps];
-  __shared__ float buf[kHeadDim];
-  const int hq = blockIdx.x;
-  const int seq = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  int L = p.seq_lens[seq];
-  if (L < 0 || L > p.max_seq_len) L = 0;
-  const int n_pages = (L + p.page_size - 1) / p.page_size;
-  const int ns = (n_pages + p.pages_per_split - 1) / p.pages_per_split;
-  const int64_t row0 = (int64_t(seq) * p.num_q_heads + hq) * p.num_splits;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row0;
-
-  float m = -INFINITY;
-  for (int s = tid; s < ns; s += kHeadDim) m = fmaxf(m, ml[s].x);
-#pragma unroll
-  for (int x = 16; x >= 1; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
-  if (lane == 0) wmax[warp] = m;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-  const float Mu = (M == -INFINITY) ? 0.0f : M;
-
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  float den = 0.0f;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kHeadDim) + lane;
-#pragma unroll 4
-  for (int s = warp; s < ns; s += kWarps) {
-    const float2 v = ml[s];
-    const float4 o = po[int64_t(s) * (kHeadDim / 4)];
-    const float f = ex2(v.x - Mu);
-    den += v.y * f;
-    acc.x += o.x * f;
-    acc.y += o.y * f;
-    acc.z += o.z * f;
-    acc.w += o.w * f;
-  }
-  red[warp][4 * lane + 0] = acc.x;
-  red[warp][4 * lane + 1] = acc.y;
-  red[warp][4 * lane + 2] = acc.z;
-  red[warp][4 * lane + 3] = acc.w;
-  if (lane == 0) wden[warp] = den;
-  __syncthreads();
-  const float num = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
-  const float dsum = wden[0] + wden[1] + wden[2] + wden[3];
-  float val = (ns > 0 && dsum > 0.0f) ? num / dsum : 0.0f;
-  if (p.rotate_v) {
-    buf[tid] = val;
-    __syncthreads();
-    smem_fwht(buf, 1, p.block_h);
-    val = buf[tid] * p.c_h;
-  }
-  p.out[(int64_t(seq) * p.num_q_heads + hq) * kHeadDim + tid] = val;
+// Launched with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; it waits for it (griddepcontrol)
+// before reading anything.
+template <int P, bool PACKED, bool APPEND>
+cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
+  using C = Cfg<P>;
+  auto kernel = paged_decode_kernel<P, PACKED, APPEND>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.num_kv_heads, p.num_seqs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <int P>
-cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
-  using C = Cfg<P>;
-  cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<P>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  if (err != cudaSuccess) return err;
-  dim3 grid(p.num_splits, p.num_kv_heads, p.num_seqs);
-  paged_decode_kernel<P><<<grid, kThreads, C::kSmem, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess || p.num_splits == 1) return err;
-  combine_kernel<<<dim3(p.num_q_heads, p.num_seqs), kHeadDim, 0, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_page(const DecodeParams& p, cudaStream_t stream) {
+  const bool packed = p.group <= kMaxGroup / 2;
+  if (p.append)
+    return packed ? launch_p<P, true, true>(p, stream) : launch_p<P, false, true>(p, stream);
+  return packed ? launch_p<P, true, false>(p, stream) : launch_p<P, false, false>(p, stream);
 }
 
 }  // namespace
@@ -543,9 +729,9 @@ cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
 cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.num_seqs == 0) return cudaSuccess;
   switch (p.page_size) {
-    case 16: return launch_p<16>(p, stream);
-    case 32: return launch_p<32>(p, stream);
-    case 64: return launch_p<64>(p, stream);
+    case 16: return launch_page<16>(p, stream);
+    case 32: return launch_page<32>(p, stream);
+    case 64: return launch_page<64>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -9,36 +9,21 @@
 // include/saw_int4.h; each binary32 step below is one explicit
 // round-to-nearest intrinsic so that no contraction changes a bit.
 //
-// Mapping: one CTA quantizes 128 consecutive (token, kv-head) rows of one
-// tensor (K or V, blockIdx.y).  Warps first stream the 32 KB tile from HBM
+// Mapping (bulk appends): one CTA quantizes 128 consecutive (token, kv-head)
+// rows of one tensor (K or V, blockIdx.y).  Warps first stream the 32 KB tile from HBM
 // with coalesced 16-byte loads into XOR-swizzled shared memory; then each
 // thread owns one row: 128 binary32 values in registers, the butterfly runs
 // without any shuffle, min/max reduce as a tree, and the 64 code bytes plus
 // the 4-byte (scale, zero) word are stored into the page slot.
 #include "saw_device.cuh"
 #include "saw_int4.h"
+#include "saw_quant_row.cuh"
 
 namespace saw {
 namespace {
 
 constexpr int kRows = 128;       // rows per CTA, one per thread
 constexpr int kRowBytes = kHeadDim * 2;
-
-__device__ __forceinline__ uint16_t f16_round_down_sat(float x) {
-  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
-  const uint16_t b = __half_as_ushort(__float2half_rd(x));
-  return (b & 0x7FFFu) ? b : uint16_t(0);  // any zero is stored as +0
-}
-
-__device__ __forceinline__ uint16_t f16_round_up_sat(float x) {
-  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
-  const uint16_t b = __half_as_ushort(__float2half_ru(x));
-  return (b & 0x7FFFu) ? b : uint16_t(0);
-}
-
-__device__ __forceinline__ float f16_bits_to_f32(uint16_t b) {
-  return __half2float(__ushort_as_half(b));
-}
 
 // In-register butterfly over each H-block of the row, strides 1, 2, ..., H/2,
 // then one multiply by c = binary32(1/sqrt(H)).
@@ -111,6 +96,7 @@ template <int H>
 __global__ void __launch_bounds__(kRows) quantize_append_kernel(const AppendParams p) {
   __shared__ __align__(16) uint8_t tile[kRows * kRowBytes];
 
+  pdl_wait_then_release();
   const int tensor = blockIdx.y;
   const uint16_t* __restrict__ src = p.src[tensor];
   const int64_t stride = p.stride[tensor];
@@ -180,22 +166,91 @@ __global__ void __launch_bounds__(kRows) quantize_append_kernel(const AppendPara
   *reinterpret_cast<uint32_t*>(chunk + P * (kHeadDim / 2) + 4 * off) = meta;
 }
 
+// Small appends (a decode step appends one token: Hkv rows per tensor): one
+// warp per row, lane l holding elements 4l..4l+3.  The butterfly is the same
+// ascending-stride sequence of (a+b, a-b) steps as the row kernel -- strides
+// 1 and 2 inside a lane, the rest across lanes with shuffles -- so every value,
+// and therefore every stored byte, is identical.
+constexpr int kWarpRowsPerCta = 4;
+
+template <int H>
+__global__ void __launch_bounds__(32 * kWarpRowsPerCta) quantize_append_warp_kernel(
+    const AppendParams p) {
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31;
+  const int hkv = p.num_kv_heads;
+  const int rows_per_tensor = p.num_tokens * hkv;
+  const int gw = blockIdx.x * kWarpRowsPerCta + (threadIdx.x >> 5);
+  const int tensor = gw / rows_per_tensor;
+  const int row = gw - tensor * rows_per_tensor;
+  if (tensor >= p.num_tensors) return;
+  const int t = row / hkv;
+  const int hd = row - t * hkv;
+  const int32_t slot = p.slot_mapping[t];
+  if (slot == -1) return;
+  if (slot < 0 || int64_t(slot) >= p.num_slots) {
+    if (lane == 0) report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+    return;
+  }
+  uint32_t meta;
+  const uint16_t codes = warp_quantize_row(
+      p.src[tensor] + int64_t(t) * p.stride[tensor] + int64_t(hd) * kHeadDim, p.rotate[tensor] != 0,
+      H, p.c_h, lane, &meta);
+  const int P = p.page_size;
+  const int page = slot / P;
+  const int off = slot - page * P;
+  uint8_t* chunk = p.cache[tensor] + (int64_t(page) * hkv + hd) * int64_t(P * (kHeadDim / 2 + 4));
+  reinterpret_cast<uint16_t*>(chunk + off * (kHeadDim / 2))[lane] = codes;
+  if (lane == 0) *reinterpret_cast<uint32_t*>(chunk + P * (kHeadDim / 2) + 4 * off) = meta;
+}
+
 }  // namespace
+
+// Rows up to which the warp-per-row kernel is used (small appends).
+constexpr int kWarpPathMaxRows = 4096;
+
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, int threads, cudaStream_t stream, const AppendParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream) {
   const int num_rows = p.num_tokens * p.num_kv_heads;
   if (num_rows == 0) return cudaSuccess;
-  dim3 grid((num_rows + kRows - 1) / kRows, num_tensors);
   const bool any_rot = p.rotate[0] || (num_tensors > 1 && p.rotate[1]);
   const int h = any_rot ? p.block_h : kHeadDim;
+  if (num_rows <= kWarpPathMaxRows) {
+    // one warp per (tensor, row): K rows first, then V rows
+    AppendParams q = p;
+    q.num_tensors = num_tensors;
+    const dim3 grid((num_rows * num_tensors + kWarpRowsPerCta - 1) / kWarpRowsPerCta);
+    const int nt = 32 * kWarpRowsPerCta;
+    switch (h) {
+      case 16: return launch_pdl(quantize_append_warp_kernel<16>, grid, nt, stream, q);
+      case 32: return launch_pdl(quantize_append_warp_kernel<32>, grid, nt, stream, q);
+      case 64: return launch_pdl(quantize_append_warp_kernel<64>, grid, nt, stream, q);
+      case 128: return launch_pdl(quantize_append_warp_kernel<128>, grid, nt, stream, q);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  dim3 grid((num_rows + kRows - 1) / kRows, num_tensors);
   switch (h) {
-    case 16: quantize_append_kernel<16><<<grid, kRows, 0, stream>>>(p); break;
-    case 32: quantize_append_kernel<32><<<grid, kRows, 0, stream>>>(p); break;
-    case 64: quantize_append_kernel<64><<<grid, kRows, 0, stream>>>(p); break;
-    case 128: quantize_append_kernel<128><<<grid, kRows, 0, stream>>>(p); break;
+    case 16: return launch_pdl(quantize_append_kernel<16>, grid, kRows, stream, p);
+    case 32: return launch_pdl(quantize_append_kernel<32>, grid, kRows, stream, p);
+    case 64: return launch_pdl(quantize_append_kernel<64>, grid, kRows, stream, p);
+    case 128: return launch_pdl(quantize_append_kernel<128>, grid, kRows, stream, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace saw

@@ -1,6 +1,7 @@
 // saw_api.cu -- the extern "C" entry points declared in include/saw_int4.h:
 // argument checks, the decode split plan, and kernel launches.  No state is
 // kept between calls and nothing is allocated.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -25,9 +26,12 @@ int sm_count() {
   return n;
 }
 
-// Split plan: enough (sequence, kv-head, split) CTAs to give every SM several
-// resident CTAs, without splits shorter than 256 tokens (each of the four
-// warps then still streams >= 4 pages of 16 tokens).
+// Split plan.  A decode CTA has 16 warps and fills one SM; a split should
+// give each warp at least two 32-token steps (1024 tokens per split).  Among
+// the split counts allowed, take the one whose CTA count (sequences x
+// kv-heads x splits) wastes the least of its last wave of SMs, preferring
+// fewer splits (a smaller merge) unless more splits fill the waves clearly
+// better.
 int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int32_t max_seq_len,
                   int32_t pages_per_split, int32_t* splits_out, int32_t* pps_out) {
   if (num_seqs < 0 || num_kv_heads <= 0 || !page_size_ok(page_size) || max_seq_len < 0 ||
@@ -41,14 +45,23 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
     pps = pages_per_split;
   } else {
     const int64_t units = int64_t(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
-    const int sms = sm_count();
-    const int64_t target = 4LL * (sms > 0 ? sms : 148);
-    const int64_t min_pps = 256 / page_size;
-    int64_t splits = ceil_div(target, units);
-    const int64_t max_splits = ceil_div(max_pages, min_pps);
-    if (splits > max_splits) splits = max_splits;
-    if (splits < 1) splits = 1;
-    pps = ceil_div(max_pages, splits);
+    const int sms_raw = sm_count();
+    const int64_t sms = sms_raw > 0 ? sms_raw : 148;
+    const int64_t min_pps = ceil_div(1024, page_size);
+    const int64_t max_splits = std::min<int64_t>(64, ceil_div(max_pages, min_pps));
+    int64_t best = 1;
+    double best_q = 1e30;
+    for (int64_t s = 1; s <= max_splits; ++s) {
+      const int64_t n = units * s;
+      const double q = double(ceil_div(n, sms) * sms) / double(n);  // >= 1; 1 = full waves
+      if (q < best_q - 0.02) {
+        best = s;
+        best_q = q;
+      }
+    }
+    pps = ceil_div(max_pages, best);
+    const int64_t step = page_size >= 32 ? 1 : 32 / page_size;  // pages per decode step
+    pps = ceil_div(pps, step) * step;
   }
   int64_t splits = max_pages == 0 ? 1 : ceil_div(max_pages, pps);
   if (splits > 65535) return SAW_ERR_UNSUPPORTED;
@@ -119,6 +132,7 @@ int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride
   p.dev_status = dev_status;
   p.num_tokens = num_tokens;
   p.num_kv_heads = num_kv_heads;
+  p.num_tensors = has_v ? 2 : 1;
   p.page_size = page_size;
   p.block_h = block_h;
   p.num_slots = int64_t(num_pages) * page_size;
@@ -146,17 +160,23 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
     return 0;
   if (splits <= 1) return 0;
   const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
-  return rows * size_t(head_dim) * 4 + rows * 2 * 4;
+  return saw::decode_ticket_bytes(num_seqs, num_kv_heads) + rows * size_t(head_dim) * 4 +
+         rows * 2 * 4;
 }
 
-int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
-                              const int32_t* block_tables, int32_t max_blocks_per_seq,
-                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
-                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                              int32_t num_pages, int32_t page_size, int32_t rotate_k,
-                              int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
-                              void* workspace, size_t workspace_bytes, int32_t pages_per_split,
-                              int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the decode entry points; fills the kernel parameters.
+int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                       int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                       int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                       void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                       int32_t* dev_status) {
   if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || max_seq_len < 0)
     return SAW_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
@@ -186,7 +206,6 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return SAW_ERR_INVALID_ARG;
 
-  saw::DecodeParams p{};
   p.q = static_cast<const uint16_t*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
   p.v_cache = static_cast<const uint8_t*>(v_cache);
@@ -194,8 +213,12 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
   p.seq_lens = seq_lens;
   p.out = out;
   const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = need > 0 ? static_cast<float*>(workspace) + rows * head_dim : nullptr;
+  if (need > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.tickets = reinterpret_cast<uint32_t*>(ws);
+    p.part_o = reinterpret_cast<float*>(ws + saw::decode_ticket_bytes(num_seqs, num_kv_heads));
+    p.part_ml = p.part_o + rows * head_dim;
+  }
   p.dev_status = dev_status;
   p.max_blocks = max_blocks_per_seq;
   p.num_seqs = num_seqs;
@@ -213,6 +236,56 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  return SAW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                              int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                              void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                              int32_t* dev_status, void* stream) {
+  saw::DecodeParams p{};
+  const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
+                                    head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+                                    sm_scale, out, workspace, workspace_bytes, pages_per_split,
+                                    dev_status);
+  if (rc != SAW_OK || num_seqs == 0) return rc;
+  cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                        int32_t block_h, float sm_scale, float* out, void* workspace,
+                        size_t workspace_bytes, int32_t pages_per_split, int32_t* dev_status,
+                        void* stream) {
+  saw::DecodeParams p{};
+  const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
+                                    head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+                                    sm_scale, out, workspace, workspace_bytes, pages_per_split,
+                                    dev_status);
+  if (rc != SAW_OK) return rc;
+  if (num_seqs == 0) return SAW_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SAW_ERR_INVALID_ARG;
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_new_stride = int64_t(num_kv_heads) * head_dim;
+  p.v_new_stride = int64_t(num_kv_heads) * head_dim;
+  p.k_cache_w = static_cast<uint8_t*>(k_cache);
+  p.v_cache_w = static_cast<uint8_t*>(v_cache);
+  p.append = 1;
   cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }

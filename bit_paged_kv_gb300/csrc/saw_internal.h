@@ -8,7 +8,7 @@ namespace saw {
 
 constexpr int kHeadDim = 128;       // the one head size this build supports
 constexpr int kMaxGroup = 8;        // q-heads per kv-head served by one CTA (MMA N = 8)
-constexpr int kDecodeWarps = 4;     // warps per decode CTA
+constexpr int kDecodeWarps = 16;    // warps per decode CTA (one CTA per SM)
 
 __host__ __device__ constexpr int chunk_bytes(int page_size) {
   return page_size * (kHeadDim / 2) + 4 * page_size;
@@ -25,6 +25,7 @@ struct AppendParams {
   int32_t* dev_status;
   int32_t num_tokens;
   int32_t num_kv_heads;
+  int32_t num_tensors;          // 2 = K and V, 1 = K only
   int32_t page_size;
   int32_t block_h;
   int64_t num_slots;            // num_pages * page_size
@@ -44,6 +45,17 @@ struct DecodeParams {
   float* out;                   // [B][Hq][D]
   float* part_o;                // [B][Hq][num_splits][D]
   float* part_ml;               // [B][Hq][num_splits][2]
+  uint32_t* tickets;            // [B][Hkv] finished-split counters, zero between calls
+  // decode step only: the new token's K and V rows, bfloat16 [B][Hkv][D]
+  // with a per-sequence stride, quantized and appended at position
+  // seq_len - 1 before attending
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t k_new_stride;
+  int64_t v_new_stride;
+  uint8_t* k_cache_w;           // writable views of the caches (decode step)
+  uint8_t* v_cache_w;
+  int32_t append;               // 1: decode step (append, then attend)
   int32_t* dev_status;
   int32_t max_blocks;
   int32_t num_seqs;
@@ -63,5 +75,11 @@ struct DecodeParams {
 };
 
 cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Split-K workspace layout: ticket words first (rounded to 16 bytes), then the
+// numerators [B][Hq][splits][D], then (m, l) pairs [B][Hq][splits][2].
+inline size_t decode_ticket_bytes(int num_seqs, int num_kv_heads) {
+  return (size_t(num_seqs) * size_t(num_kv_heads) * 4 + 15) / 16 * 16;
+}
 
 }  // namespace saw

@@ -128,6 +128,10 @@ int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_siz
  * Workspace bytes saw_paged_decode_int4 needs for these sizes with the same
  * pages_per_split argument, on the current device (0 when the plan has one
  * split, which writes the output directly).  Returns 0 on bad arguments.
+ * The workspace holds the split partials and, first, one counter word per
+ * (sequence, kv-head) that the merge uses: zero-fill a new workspace once
+ * (e.g. cudaMemset) before its first use; every call leaves those words at
+ * zero again.
  */
 size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t page_size, int32_t max_seq_len,
@@ -158,7 +162,11 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  * sm_scale      softmax scale on q.k; 0 means 1/sqrt(head_dim).
  * out           device float32 [num_seqs][num_q_heads][head_dim].
  * workspace     device, >= saw_decode_workspace_bytes(...) bytes, 16-byte
- *               aligned (may be NULL when that is 0).
+ *               aligned (may be NULL when that is 0), zero-filled before its
+ *               first use (calls leave it reusable).  The last split to
+ *               finish for a (sequence, kv-head) merges the partials, so one
+ *               launch covers the whole decode.  Calls sharing a workspace
+ *               must be ordered (one stream).
  * pages_per_split  0 = automatic; > 0 forces the split size (tests).
  *
  * Computes, per (sequence, q-head): q' = (1/sqrt(h)) H q if K was rotated;
@@ -177,6 +185,33 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
                               int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
                               void* workspace, size_t workspace_bytes, int32_t pages_per_split,
                               int32_t* dev_status, void* stream);
+
+/*
+ * One decode step of a layer, fused into one launch: for every sequence b,
+ * quantize-append the new token's K and V rows at position seq_lens[b] - 1
+ * (slot = block_tables[b][(L-1)/page_size]*page_size + (L-1)%page_size),
+ * then attend over all seq_lens[b] tokens -- the per-token path of the
+ * fused-kernel diagram in youngju.dev "The System Is the Design -- A Fused
+ * Kernel" (rotate, quantize, append to the paged block) followed by the
+ * decode of gist.science s.2 point 3.
+ *
+ * k_new, v_new  device bfloat16 [num_seqs][num_kv_heads][head_dim],
+ *               contiguous, 16-byte aligned: the new token of each sequence.
+ * k_cache, v_cache  written (the new rows) and read.
+ * seq_lens      lengths INCLUDING the new token (>= 1).  A length of 0
+ *               appends nothing and gives a zero output row.
+ * Other arguments as saw_paged_decode_int4.  The appended bytes equal those
+ * of saw_quantize_append on the same row, and the output equals
+ * saw_quantize_append followed by saw_paged_decode_int4.
+ */
+int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                        int32_t block_h, float sm_scale, float* out, void* workspace,
+                        size_t workspace_bytes, int32_t pages_per_split, int32_t* dev_status,
+                        void* stream);
 
 /*
  * saw_paged_decode_int4_noalloc -- the same decode as saw_paged_decode_int4
@@ -201,7 +236,8 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
  *    before any stream capture.
  *  - Sharing: all calls on a device share the array, so calls whose kernels
  *    may overlap on the GPU (different streams without ordering) race.
- *    Nothing in it needs to start at zero.
+ *    Each call first clears the merge's counter words in it
+ *    (cudaMemsetAsync on `stream`); the rest needs no clearing.
  */
 int32_t saw_paged_decode_int4_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -68,7 +68,7 @@ def gpu_decode(q, kc, vc, bt, lens, num_kv_heads, num_pages, P, rotate_k, rotate
         max_seq_len = max(int(x) for x in lens.tolist()) if B else 0
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
     wsb = saw.saw_decode_workspace_bytes(B, Hq, num_kv_heads, D, P, max_seq_len, pages_per_split)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     saw.saw_paged_decode_int4(q, kc, vc, bt, lens, max_seq_len, num_kv_heads, num_pages, P,
                               rotate_k, rotate_v, h, out, ws, sm_scale=sm_scale,

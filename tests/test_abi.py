@@ -133,7 +133,8 @@ def test_plan_and_workspace(L):
     s, pps = saw.saw_decode_plan(2, 8, 16, 1000, 4)
     assert (s, pps) == (16, 4)
     ws = saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 1000, 4)
-    assert ws == 2 * 32 * 16 * (128 + 2) * 4
+    # one counter word per (sequence, kv-head), rounded to 16 bytes, then partials
+    assert ws == 64 + 2 * 32 * 16 * (128 + 2) * 4
     # one split -> no workspace
     assert saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 64, 64) == 0
     # automatic plan: splits never shorter than 256 tokens, and cover the context
@@ -144,3 +145,28 @@ def test_plan_and_workspace(L):
     assert saw.saw_decode_plan(1, 8, 64, 0, 0) == (1, 1)
     with pytest.raises(saw.SawError):
         saw.saw_decode_plan(1, 8, 12, 100, 0)
+
+
+def _step(L, **kw):
+    a = dict(q=A, kn=B, vn=A, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128,
+             pages=8, P=16, rk=1, rv=0, h=128, scale=0.0, out=A, ws=B, wsb=1 << 20, pps=0,
+             status=None, stream=None)
+    a.update(kw)
+    return L.saw_decode_step(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["mb"],
+                             a["sl"], a["B"], a["maxlen"], a["hq"], a["hkv"], a["d"], a["pages"],
+                             a["P"], a["rk"], a["rv"], a["h"], a["scale"], a["out"], a["ws"],
+                             a["wsb"], a["pps"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(kn=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(vn=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(kn=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
+    (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
+    (dict(mb=3), saw.SAW_ERR_INVALID_ARG),
+    (dict(B=0), saw.SAW_OK),
+])
+def test_decode_step_rejects_before_launch(L, kw, expect):
+    assert _step(L, **kw) == expect

@@ -79,10 +79,12 @@ def test_k_only_and_bad_slots():
     assert_bytes_equal(kc, kr, "K cache")
 
 
-def test_special_rows():
+@pytest.mark.parametrize("repeat", [1, 1024], ids=["warp-per-row", "row-per-thread"])
+def test_special_rows(repeat):
     """Constant rows, all-zero rows with negative zeros, one-hot rows, and
     magnitudes at the edges of binary16 (subnormal zero-points, saturating
-    scales)."""
+    scales).  Few rows take the warp-per-row kernel; tiled to 9216 rows they
+    take the row-per-thread kernel."""
     D, hkv = 128, 1
     rows = []
     rows.append(torch.full((D,), 1.5))
@@ -99,13 +101,14 @@ def test_special_rows():
     rows.append(torch.linspace(-0.5, 0.5, D) + 300.0)  # large bias, tiny spread
     g = torch.Generator().manual_seed(0)
     rows.append(torch.randn(D, generator=g) * 1e-3)
-    x = torch.stack(rows).to(torch.bfloat16).view(-1, hkv, D)
+    x = torch.stack(rows).to(torch.bfloat16).view(-1, hkv, D).repeat(repeat, 1, 1)
     T = x.shape[0]
     slots = torch.arange(T, dtype=torch.int32)
+    pages = -(-T // 16)
     for rot in (0, 1):
         k = x.cuda()
-        kc, vc, st = gpu_append(k, k, slots.cuda(), 1, 16, rot, rot, 128)
-        kr, vr, bad = oracle_append(x, x, slots, 1, 16, rot, rot, 128)
+        kc, vc, st = gpu_append(k, k, slots.cuda(), pages, 16, rot, rot, 128)
+        kr, vr, bad = oracle_append(x, x, slots, pages, 16, rot, rot, 128)
         assert st == 0
         assert_bytes_equal(kc, kr, f"K cache rot={rot}")
         assert_bytes_equal(vc, vr, f"V cache rot={rot}")
@@ -135,3 +138,19 @@ def test_empty_append_is_a_no_op():
     saw.saw_quantize_append(k, None, s, kc, None, 1, 16, True, False, 128)
     torch.cuda.synchronize()
     assert torch.all(kc == 7)
+
+
+@pytest.mark.parametrize("T", [1, 3, 511, 512, 513, 3000])
+def test_both_kernels_across_the_size_switch(T):
+    """Appends just below, at and above the warp-per-row size limit (4096 rows)
+    with 8 kv-heads: every size must give the oracle's bytes."""
+    wl = W.TINY.variant(num_kv_heads=8, dist="student_t", nu=3)
+    k, v = _inputs(wl, T)
+    num_pages = -(-T // 16) + 2
+    slots = torch.randperm(num_pages * 16, generator=torch.Generator().manual_seed(T))[:T]
+    slots = slots.to(torch.int32)
+    kc, vc, st = gpu_append(k, v, slots.cuda(), num_pages, 16, True, False, 128)
+    kr, vr, bad = oracle_append(k, v, slots, num_pages, 16, True, False, 128)
+    assert st == 0 and bad == 0
+    assert_bytes_equal(kc, kr, "K cache")
+    assert_bytes_equal(vc, vr, "V cache")

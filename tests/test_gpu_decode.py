@@ -132,3 +132,74 @@ def test_decode_after_single_token_append():
                          for b, L in enumerate(lens0)]).to(torch.int32).cuda()
     gpu_append(knew, vnew, slots, npages, wl.page_size, True, True, 128, kc=kc, vc=vc)
     _check(wl, lens, bt, npages, kc, vc, q)
+
+
+def test_workspace_reuse_across_calls_and_plans():
+    """One zero-filled workspace serves many calls with different split plans:
+    the merge's counters are back at zero after every call."""
+    wl = W.TINY.variant(shuffle_pages=True)
+    lens, bt, npages, kc, vc, q = _setup(wl, [300, 47, 128, 256])
+    B, Hq, D = q.shape
+    Lmax = int(lens.max())
+    wsb = max(saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, p)
+              for p in (1, 2, 3))
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
+                        wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h)
+    for pps in (1, 2, 3, 1, 3):
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        saw.saw_paged_decode_int4(q, kc, vc, bt.cuda(), lens.cuda(), Lmax, wl.num_kv_heads,
+                                  npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                                  out, ws, pages_per_split=pps, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) <= ATTN_TOL
+    n_tickets = B * wl.num_kv_heads
+    assert torch.all(ws[:4 * n_tickets].view(torch.int32) == 0)
+
+
+@pytest.mark.parametrize("P,group,pps", [(16, 4, 0), (16, 4, 2), (16, 1, 3), (16, 8, 1),
+                                        (32, 4, 1), (64, 2, 1), (64, 8, 0)])
+def test_fused_decode_step(P, group, pps):
+    """saw_decode_step = append the new token at seq_len - 1, then attend, in
+    one launch: cache bytes equal the oracle's append, attention the oracle's."""
+    from gpu_helpers import new_caches, oracle_append
+    wl = W.TINY.variant(page_size=P, num_q_heads=2 * group, num_kv_heads=2, shuffle_pages=True,
+                        rotate_v=False, dist="student_t", nu=4)
+    lens_l = [1, 17, 16, P + 1, 300, 31, 0]
+    lens = torch.tensor(lens_l, dtype=torch.int32)
+    bt, npages = W.page_tables(wl, lens, spare_pages=3)
+    # prefill all but the last token, with the append kernel
+    kc, vc, k_pre, v_pre, slots_pre = fill_layer(wl, 0, lens, bt, npages,
+                                                 upto=lambda n: max(n - 1, 0))
+    B, D = len(lens_l), 128
+    knew = (torch.randn(B, wl.num_kv_heads, D, device="cuda") * 2).to(torch.bfloat16)
+    vnew = (torch.randn(B, wl.num_kv_heads, D, device="cuda") * 2).to(torch.bfloat16)
+    q = W.q_rows(wl, 0, "cuda", num_seqs=B)
+    Lmax = int(lens.max())
+    out = torch.full((B, wl.num_q_heads, D), float("nan"), dtype=torch.float32, device="cuda")
+    wsb = saw.saw_decode_workspace_bytes(B, wl.num_q_heads, wl.num_kv_heads, D, P, Lmax, pps)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    saw.saw_decode_step(q, knew, vnew, kc, vc, bt.cuda(), lens.cuda(), Lmax, wl.num_kv_heads,
+                        npages, P, wl.rotate_k, wl.rotate_v, wl.block_h, out, ws,
+                        pages_per_split=pps, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # oracle: same prefill, then append the new token of each non-empty sequence
+    kr, vr, _ = oracle_append(k_pre, v_pre, slots_pre.cpu(), npages, P, wl.rotate_k, wl.rotate_v,
+                              wl.block_h)
+    keep = [b for b in range(B) if lens_l[b] > 0]
+    slots_new = torch.tensor([int(bt[b, (lens_l[b] - 1) // P]) * P + (lens_l[b] - 1) % P
+                              for b in keep], dtype=torch.int32)
+    oracle_append(knew[keep], vnew[keep], slots_new, npages, P, wl.rotate_k, wl.rotate_v,
+                  wl.block_h, kc=kr, vc=vr)
+    from gpu_helpers import assert_bytes_equal
+    assert_bytes_equal(kc, kr, "K cache after the step")
+    assert_bytes_equal(vc, vr, "V cache after the step")
+    ref = oracle_decode(q, kr, vr, bt, lens, wl.num_kv_heads, npages, P, wl.rotate_k, wl.rotate_v,
+                        wl.block_h)
+    got = out.cpu().numpy().reshape(-1, D)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, ref) <= ATTN_TOL
