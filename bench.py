@@ -224,7 +224,7 @@ class LatencyCase:
                                  self.kc[layer], self.vc[layer], self.bt, self.lens_d, self.L,
                                  wl.num_kv_heads, self.npages, wl.page_size, wl.rotate_k,
                                  wl.rotate_v, wl.block_h, self.out[layer], self.ws,
-                                 dev_status=self.status)
+                                 flags=self.saw.SAW_STEP_EARLY_PAGES, dev_status=self.status)
 
     def step(self):
         for layer in range(self.wl.num_layers):

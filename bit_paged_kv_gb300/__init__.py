@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     SAW_ERR_INVALID_ARG,
     SAW_ERR_UNSUPPORTED,
     SAW_OK,
+    SAW_STEP_EARLY_PAGES,
     SawError,
     lib,
     saw_cache_bytes,

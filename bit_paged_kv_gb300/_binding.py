@@ -21,6 +21,7 @@ SAW_ERR_UNSUPPORTED = 2
 SAW_ERR_CUDA = 3
 SAW_ERR_DEVICE_INDEX = 4
 SAW_ERR_DEVICE_TIMEOUT = 5
+SAW_STEP_EARLY_PAGES = 1
 
 EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_decode_plan",
            "saw_decode_workspace_bytes", "saw_paged_decode_int4", "saw_decode_step",
@@ -63,7 +64,7 @@ def lib() -> C.CDLL:
                                         i32, i32, i32, f32, P, P, sz, i32, P, P]
     L.saw_decode_step.restype = i32
     L.saw_decode_step.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, i32,
-                                  i32, i32, f32, P, P, sz, i32, P, P]
+                                  i32, i32, f32, P, P, sz, i32, i32, P, P]
     L.saw_paged_decode_int4_noalloc.restype = i32
     L.saw_paged_decode_int4_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
                                                 i32, i32, i32, i32, f32, P, i32, P, P]
@@ -156,9 +157,11 @@ def saw_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     seq_lens: torch.Tensor, max_seq_len: int, num_kv_heads: int, num_pages: int,
                     page_size: int, rotate_k: bool, rotate_v: bool, block_h: int,
                     out: torch.Tensor, workspace=None, sm_scale: float = 0.0,
-                    pages_per_split: int = 0, dev_status=None, stream=None) -> None:
+                    pages_per_split: int = 0, flags: int = 0, dev_status=None,
+                    stream=None) -> None:
     """One fused decode step: append k_new/v_new (bfloat16 [B, Hkv, D]) at
-    position seq_lens[b] - 1 of each sequence, then attend (one launch)."""
+    position seq_lens[b] - 1 of each sequence, then attend (one launch).
+    flags=SAW_STEP_EARLY_PAGES: see include/saw_int4.h."""
     B, hq, d = q.shape
     assert q.dtype == torch.bfloat16 and q.is_contiguous()
     for t in (k_new, v_new):
@@ -171,7 +174,8 @@ def saw_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), B, max_seq_len, hq, num_kv_heads, d, num_pages,
         page_size, int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out),
-        _ptr(workspace), ws_bytes, pages_per_split, _ptr(dev_status), _stream(q, stream))
+        _ptr(workspace), ws_bytes, pages_per_split, int(flags), _ptr(dev_status),
+        _stream(q, stream))
     _raise(rc, "saw_decode_step")
 
 

@@ -44,40 +44,34 @@ constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kRedStride = kHeadDim + 4;  // padded row of the cross-warp reduction
 constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
-constexpr int kStepTok = 32;              // tokens per step (one softmax update)
-constexpr int kTiles = kStepTok / 16;     // 16-token MMA tiles per step
-constexpr int kStages = 2;
+constexpr int kStepTok = 16;              // tokens per step (one MMA tile, one softmax update)
+constexpr int kStages = 4;
 constexpr int kCodeRow = kHeadDim / 2;    // code bytes per token
 
-// Stage layout for a 32-token step.  Page size 16: [K chunk | V chunk] of
-// page 0, then of page 1 (each chunk = 16 code rows, then 16 meta words).
-// Page size >= 32: [K codes 32 rows | K meta 32 words | V codes | V meta].
+// Stage layout for a 16-token step, the same for every page size:
+// [K codes 16 rows | K meta 16 words | V codes 16 rows | V meta 16 words].
+// A 16-token page is exactly [K chunk | V chunk]; larger pages are copied
+// as 16-row slices of their code and meta regions.
 template <int P>
 struct Cfg {
   static constexpr int kChunk = chunk_bytes(P);
-  static constexpr int kPagesPerStep = (P == 16) ? 2 : 1;
-  static constexpr int kStepsPerPage = (P == 16) ? 1 : P / kStepTok;
-  static constexpr int kStage = 2 * (kStepTok * kCodeRow + kStepTok * 4);  // 4352 bytes
-  // byte offset of K's code row / meta word `row` of tile tt in a stage; V's
-  // are at the same offsets from vbase
-  __device__ static constexpr int kcode(int tt, int row) {
-    return (P == 16) ? tt * 2 * chunk_bytes(16) + row * kCodeRow : (tt * 16 + row) * kCodeRow;
-  }
-  __device__ static constexpr int kmeta(int tt, int row) {
-    return (P == 16) ? tt * 2 * chunk_bytes(16) + 16 * kCodeRow + row * 4
-                     : kStepTok * kCodeRow + (tt * 16 + row) * 4;
-  }
-  __device__ static constexpr int vbase() {
-    return (P == 16) ? chunk_bytes(16) : kStepTok * kCodeRow + kStepTok * 4;
-  }
+  static constexpr int kStepsPerPage = P / kStepTok;
+  static constexpr int kHalf = kStepTok * kCodeRow + kStepTok * 4;  // 1088: one tensor
+  static constexpr int kStage = 2 * kHalf;                          // 2176
+  // byte offset of K's code row / meta word `row` in a stage; V's are at the
+  // same offsets from kHalf
+  __device__ static constexpr int kcode(int row) { return row * kCodeRow; }
+  __device__ static constexpr int kmeta(int row) { return kStepTok * kCodeRow + row * 4; }
   static constexpr int kRing = kWarps * kStages * kStage;
   // after the main loop the ring is reused: cross-warp reduction, then rows
-  static constexpr int kRed = kWarps * kMaxGroup * kRedStride * 4 + 3 * kWarps * kMaxGroup * 4;
+  // red_acc [16][8][132], red_m / red_l / red_z / weights [16][8], per-head
+  // totals [3][8]
+  static constexpr int kRed = (kWarps * kMaxGroup * kRedStride + 4 * kWarps * kMaxGroup + 3 * kMaxGroup) * 4;
   static constexpr int kOffQ = (kRed + 15) / 16 * 16;                          // f32 [8][128]
   static_assert(kOffQ + kMaxGroup * kHeadDim * 4 <= kRing, "epilogue scratch must fit the ring");
   static constexpr int kOffBars = kRing;
-  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][2][2]
-  static constexpr int kOffIds = kOffOk + kWarps * kStages * 2 * 4;           // int [16][kIdCap]
+  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][4]
+  static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [16][kIdCap]
   static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8][128]
   static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [8]
   static constexpr int kOffFlag = kOffQsum + kMaxGroup * 4;                   // int
@@ -136,7 +130,12 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
 template <int P, bool PACKED, bool APPEND>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeParams p) {
   using C = Cfg<P>;
-  pdl_wait_then_release();
+  // Wait for the previous kernel in the stream before reading anything --
+  // unless the caller declared that it writes neither the tables nor the
+  // pages: then the page copies start first and the wait comes just before q
+  // and the new token are read (and before anything is written).
+  const bool early = p.early_pages != 0;
+  if (!early) pdl_wait_then_release();
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + C::kOffOk);
@@ -169,76 +168,60 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   if (p_begin >= p_end) {
     // nothing to attend over here; an empty sequence still owes a zero row
     if (split == 0 && n_pages == 0) {
+      if (early) pdl_wait_then_release();
       for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
         p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = 0.0f;
     }
     return;
   }
 
-  // ---- this warp's steps: step j covers tokens [p_begin*P + 32j, +32);
+  // ---- this warp's steps: step j covers tokens [p_begin*P + 16j, +16);
   // warp w takes steps w, w+16, ...
-  const int n_steps = ((p_end - p_begin) * P + kStepTok - 1) / kStepTok;
+  const int n_steps = (p_end - p_begin) * C::kStepsPerPage;
   const int n_my = (warp < n_steps) ? (n_steps - warp + kWarps - 1) / kWarps : 0;
   uint8_t* ring = smem + warp * kStages * C::kStage;
   uint64_t* wbars = bars + warp * kStages;
-  int32_t* wok = stage_ok + warp * kStages * 2;
+  int32_t* wok = stage_ok + warp * kStages;
   const int32_t* btab = p.block_tables + int64_t(seq) * p.max_blocks;
 
-  // physical page id of page q of this warp's step i (-1: none or invalid)
-  auto page_id = [&](int i, int q) {
-    const int j = warp + i * kWarps;
-    const int lp = p_begin + ((P == 16) ? 2 * j + q : j / C::kStepsPerPage);
-    int id = -1;
-    if (lp < p_end) {
-      id = btab[lp];
-      if (id < 0 || id >= p.num_pages) {
-        report(p.dev_status, SAW_ERR_DEVICE_INDEX);
-        id = -1;
-      }
+  // physical page id of this warp's step i (-1: invalid)
+  auto page_id = [&](int i) {
+    const int lp = p_begin + (warp + i * kWarps) / C::kStepsPerPage;
+    int id = btab[lp];
+    if (id < 0 || id >= p.num_pages) {
+      report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+      id = -1;
     }
     return id;
   };
   // the warp's page ids, fetched once instead of one dependent global load
   // in front of every copy
   int32_t* wids = reinterpret_cast<int32_t*>(smem + C::kOffIds) + warp * kIdCap;
-  for (int e = lane; e < n_my * C::kPagesPerStep && e < kIdCap; e += 32)
-    wids[e] = page_id(e / C::kPagesPerStep, e % C::kPagesPerStep);
+  for (int e = lane; e < n_my && e < kIdCap; e += 32) wids[e] = page_id(e);
   __syncwarp();
 
   auto issue = [&](int i) {  // lane 0 only
     const int s = i % kStages;
     uint8_t* st = ring + s * C::kStage;
-    uint32_t bytes = 0;
-    int pid[C::kPagesPerStep];
-#pragma unroll
-    for (int q = 0; q < C::kPagesPerStep; ++q) {
-      const int e = i * C::kPagesPerStep + q;
-      pid[q] = (e < kIdCap) ? wids[e] : page_id(i, q);
-      wok[s * 2 + q] = (pid[q] >= 0);
-      if (pid[q] >= 0) bytes += (P == 16) ? 2 * C::kChunk : C::kStage;
-    }
-    if (bytes == 0) {
+    const int pid = (i < kIdCap) ? wids[i] : page_id(i);
+    wok[s] = (pid >= 0);
+    if (pid < 0) {
       mbar_arrive(&wbars[s]);
       return;
     }
-    mbar_arrive_expect_tx(&wbars[s], bytes);
-#pragma unroll
-    for (int q = 0; q < C::kPagesPerStep; ++q) {
-      if (pid[q] < 0) continue;
-      const int64_t off = (int64_t(pid[q]) * p.num_kv_heads + kvh) * C::kChunk;
-      if (P == 16) {
-        bulk_g2s(st + q * 2 * C::kChunk, p.k_cache + off, C::kChunk, &wbars[s]);
-        bulk_g2s(st + q * 2 * C::kChunk + C::kChunk, p.v_cache + off, C::kChunk, &wbars[s]);
-      } else {
-        const int part = (warp + i * kWarps) % C::kStepsPerPage;
-        const int64_t codes = off + part * (kStepTok * kCodeRow);
-        const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
-        bulk_g2s(st, p.k_cache + codes, kStepTok * kCodeRow, &wbars[s]);
-        bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, &wbars[s]);
-        bulk_g2s(st + C::vbase(), p.v_cache + codes, kStepTok * kCodeRow, &wbars[s]);
-        bulk_g2s(st + C::vbase() + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4,
-                 &wbars[s]);
-      }
+    mbar_arrive_expect_tx(&wbars[s], C::kStage);
+    const int64_t off = (int64_t(pid) * p.num_kv_heads + kvh) * C::kChunk;
+    if (P == 16) {
+      bulk_g2s(st, p.k_cache + off, C::kChunk, &wbars[s]);
+      bulk_g2s(st + C::kHalf, p.v_cache + off, C::kChunk, &wbars[s]);
+    } else {
+      const int part = (warp + i * kWarps) % C::kStepsPerPage;
+      const int64_t codes = off + part * (kStepTok * kCodeRow);
+      const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
+      bulk_g2s(st, p.k_cache + codes, kStepTok * kCodeRow, &wbars[s]);
+      bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, &wbars[s]);
+      bulk_g2s(st + C::kHalf, p.v_cache + codes, kStepTok * kCodeRow, &wbars[s]);
+      bulk_g2s(st + C::kHalf + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4, &wbars[s]);
     }
   };
 
@@ -247,15 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     mbar_fence_init();
     for (int i = 0; i < kStages && i < n_my; ++i) issue(i);
   }
-  __syncwarp();
-
-  // ---- decode step: the CTA whose split holds the new token (position L-1)
-  // quantizes its K and V rows for this kv-head (the same warp quantizer as
-  // the append kernels, so the bytes match), writes them into the cache, and
-  // keeps them to patch its own copy of that page below.
-  uint8_t* newrow = smem + C::kOffNew;
+  // decode step: the page that receives the new token (position L-1)
   const int new_tok = L - 1;
   const bool owner = APPEND && new_tok >= 0 && new_tok / P >= p_begin && new_tok / P < p_end;
+  const int new_pid = owner ? btab[new_tok / P] : -1;
+  __syncwarp();
+  if (early) pdl_wait_then_release();
+
+  // ---- decode step: the CTA whose split holds the new token quantizes its
+  // K and V rows for this kv-head (the same warp quantizer as the append
+  // kernels, so the bytes match), writes them into the cache, and keeps them
+  // to patch its own copy of that page below.
+  uint8_t* newrow = smem + C::kOffNew;
   if (owner && warp >= kWarps - 2) {
     const int tensor = warp - (kWarps - 2);
     const uint16_t* src = (tensor == 0 ? p.k_new + int64_t(seq) * p.k_new_stride
@@ -267,11 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     uint8_t* nr = newrow + tensor * (kCodeRow + 16);
     reinterpret_cast<uint16_t*>(nr)[lane] = codes;
     if (lane == 0) *reinterpret_cast<uint32_t*>(nr + kCodeRow) = meta;
-    const int pid = btab[new_tok / P];
-    if (pid >= 0 && pid < p.num_pages) {
+    if (new_pid >= 0 && new_pid < p.num_pages) {
       const int off = new_tok % P;
       uint8_t* chunk = (tensor == 0 ? p.k_cache_w : p.v_cache_w) +
-                       (int64_t(pid) * p.num_kv_heads + kvh) * C::kChunk;
+                       (int64_t(new_pid) * p.num_kv_heads + kvh) * C::kChunk;
       reinterpret_cast<uint16_t*>(chunk + off * kCodeRow)[lane] = codes;
       if (lane == 0) *reinterpret_cast<uint32_t*>(chunk + P * kCodeRow + 4 * off) = meta;
     }
@@ -280,10 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   const int new_local = new_tok - p_begin * P;
   const int new_step = owner ? new_local / kStepTok : -1;
 
-  // ---- q' = (1/sqrt h) H q for the group's heads, as binary16 hi + lo parts
-  // (q' = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8 rotates head h,
-  // lane l holding elements 4l..4l+3; sm_scale*log2(e) is applied to the
-  // binary32 score, so an unrotated q enters the MMA exactly.
+  // ---- b = 4 q', q' = (1/sqrt h) H q for the group's heads, as binary16 hi
+  // + lo parts (b = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8
+  // rotates head h, lane l holding elements 4l..4l+3.  sm_scale*log2(e) is
+  // applied to the binary32 score, so an unrotated q enters the MMA exactly
+  // (4 q is exact in binary16).
   __half* qh_hi = qh;
   __half* qh_lo = qh + kMaxGroup * kHeadDim;
   if (warp < kMaxGroup) {
@@ -316,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] *= p.c_h;
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] *= 4.0f;
     }
     float part = 0.0f;
 #pragma unroll
@@ -356,9 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       }
     }
   }
-  // this thread's two heads
+  // this thread's two heads.  The codes enter the score MMA as 1024 + 16 n
+  // (one LOP3 per two codes, no subtraction), so with b = 4 q' the MMA gives
+  // acc = 1024 sum(b) + 64 (n . q').  The constant is removed in binary32
+  // together with the zero term:  t = sm'*(s (n.q') + z sum(q'))
+  //   = (sm' s / 64) acc + (sm' sum(b) / 4) (z - 64 s).
   const int hb = PACKED ? 2 * (c & 1) : 2 * c;
-  const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
+  const float qsA = qsum[hb] * (0.25f * p.q_scale), qsB = qsum[hb + 1] * (0.25f * p.q_scale);
+  const float sk_scale = p.q_scale * (1.0f / 64.0f);
 
   float acc[8][4];
 #pragma unroll
@@ -381,28 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     const int tok0 = p_begin * P + (warp + i * kWarps) * kStepTok;
     if (APPEND && warp + i * kWarps == new_step) {
       // replace the copied row of the new token by its freshly quantized one
-      const int r = new_local % kStepTok, tt = r / 16, row = r % 16;
+      const int row = new_local % kStepTok;
       uint8_t* w = ring + s * C::kStage;
       if (lane < 16) {
         const int tensor = lane >> 3, part = lane & 7;  // 8 x 8 bytes per tensor
         const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
-        uint8_t* dst = w + (tensor ? C::vbase() : 0) + C::kcode(tt, row);
+        uint8_t* dst = w + (tensor ? C::kHalf : 0) + C::kcode(row);
         reinterpret_cast<uint2*>(dst)[part] = reinterpret_cast<const uint2*>(nr)[part];
       } else if (lane < 18) {
         const int tensor = lane - 16;
         const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
-        *reinterpret_cast<uint32_t*>(w + (tensor ? C::vbase() : 0) + C::kmeta(tt, row)) =
+        *reinterpret_cast<uint32_t*>(w + (tensor ? C::kHalf : 0) + C::kmeta(row)) =
             *reinterpret_cast<const uint32_t*>(nr + kCodeRow);
       }
       __syncwarp();
     }
+    const bool pok = wok[s] != 0;
+    const bool v0 = pok && (tok0 + g) < L;
+    const bool v1 = pok && (tok0 + g + 8) < L;
 
-    // ---- scores of both 16-token tiles of the step
-    float sc[kTiles][4];
-#pragma unroll
-    for (int tt = 0; tt < kTiles; ++tt) {
-      const bool pok = wok[s * 2 + ((P == 16) ? tt : 0)] != 0;
-      const uint8_t* krow = st + C::kcode(tt, g) + 16 * c;
+    // ---- scores of the 16 tokens
+    float sc[4];
+    {
+      const uint8_t* krow = st + C::kcode(g) + 16 * c;
       const uint4 ka = *reinterpret_cast<const uint4*>(krow);
       const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow);
       const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w};
@@ -414,13 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       for (int w = 0; w < 4; ++w) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t ya = hh ? (kaw[w] >> 8) : kaw[w];
-          const uint32_t yb = hh ? (kbw[w] >> 8) : kbw[w];
+          // every nibble moved to bits 4-7 / 20-23 of its binary16 half:
+          // low nibbles of bytes (0,2) by << 4, of bytes (1,3) by >> 4;
+          // high nibbles of bytes (1,3) by >> 8
+          const uint32_t wa = kaw[w], wb = kbw[w];
           uint32_t a[4];
-          a[0] = hsub_1024(and_or(ya, 0x000F000Fu, kMagic));
-          a[1] = hsub_1024(and_or(yb, 0x000F000Fu, kMagic));
-          a[2] = hfma_hi(and_or(ya, 0x00F000F0u, kMagic));
-          a[3] = hfma_hi(and_or(yb, 0x00F000F0u, kMagic));
+          a[0] = and_or(hh ? (wa >> 4) : (wa << 4), 0x00F000F0u, kMagic);
+          a[1] = and_or(hh ? (wb >> 4) : (wb << 4), 0x00F000F0u, kMagic);
+          a[2] = and_or(hh ? (wa >> 8) : wa, 0x00F000F0u, kMagic);
+          a[3] = and_or(hh ? (wb >> 8) : wb, 0x00F000F0u, kMagic);
           float (&dst)[4] = hh ? e2 : d;
           mma_16816(dst, a, bq[2 * w + hh][0], bq[2 * w + hh][1]);
           if (!PACKED) mma_16816(dst, a, bl[PACKED ? 0 : 2 * w + hh][0], bl[PACKED ? 0 : 2 * w + hh][1]);
@@ -432,25 +428,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
 #pragma unroll
         for (int j = 0; j < 4; ++j) d[j] += __shfl_xor_sync(kFull, d[j], 2);
       }
-      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(tt, g));
-      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(tt, g + 8));
-      const float sk0 = half_lo(mk0) * p.q_scale, zk0 = half_hi(mk0);
-      const float sk1 = half_lo(mk1) * p.q_scale, zk1 = half_hi(mk1);
-      const bool v0 = pok && (tok0 + 16 * tt + g) < L;
-      const bool v1 = pok && (tok0 + 16 * tt + g + 8) < L;
-      sc[tt][0] = v0 ? fmaf(sk0, d[0], zk0 * qsA) : -INFINITY;
-      sc[tt][1] = v0 ? fmaf(sk0, d[1], zk0 * qsB) : -INFINITY;
-      sc[tt][2] = v1 ? fmaf(sk1, d[2], zk1 * qsA) : -INFINITY;
-      sc[tt][3] = v1 ? fmaf(sk1, d[3], zk1 * qsB) : -INFINITY;
+      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g));
+      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8));
+      const float sk0 = half_lo(mk0) * sk_scale, zk0 = fmaf(-64.0f, half_lo(mk0), half_hi(mk0));
+      const float sk1 = half_lo(mk1) * sk_scale, zk1 = fmaf(-64.0f, half_lo(mk1), half_hi(mk1));
+      sc[0] = v0 ? fmaf(sk0, d[0], zk0 * qsA) : -INFINITY;
+      sc[1] = v0 ? fmaf(sk0, d[1], zk0 * qsB) : -INFINITY;
+      sc[2] = v1 ? fmaf(sk1, d[2], zk1 * qsA) : -INFINITY;
+      sc[3] = v1 ? fmaf(sk1, d[3], zk1 * qsB) : -INFINITY;
     }
 
     // ---- online softmax: rescale only when a running max grows
-    float mloc0 = -INFINITY, mloc1 = -INFINITY;
-#pragma unroll
-    for (int tt = 0; tt < kTiles; ++tt) {
-      mloc0 = fmaxf(mloc0, fmaxf(sc[tt][0], sc[tt][2]));
-      mloc1 = fmaxf(mloc1, fmaxf(sc[tt][1], sc[tt][3]));
-    }
+    float mloc0 = fmaxf(sc[0], sc[2]), mloc1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
     for (int x = 4; x < 32; x <<= 1) {
       mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
@@ -477,17 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
     const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
 
-    // ---- probabilities, V terms, and the PV product per tile
-#pragma unroll
-    for (int tt = 0; tt < kTiles; ++tt) {
-      const bool pok = wok[s * 2 + ((P == 16) ? tt : 0)] != 0;
-      const uint8_t* vst = st + C::vbase();
-      const float p0 = ex2(sc[tt][0] - mu0), p1 = ex2(sc[tt][1] - mu1);
-      const float p2 = ex2(sc[tt][2] - mu0), p3 = ex2(sc[tt][3] - mu1);
-      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(tt, g));
-      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(tt, g + 8));
-      const bool v0 = pok && (tok0 + 16 * tt + g) < L;
-      const bool v1 = pok && (tok0 + 16 * tt + g + 8) < L;
+    // ---- probabilities, V terms, and the PV product
+    {
+      const uint8_t* vst = st + C::kHalf;
+      const float p0 = ex2(sc[0] - mu0), p1 = ex2(sc[1] - mu1);
+      const float p2 = ex2(sc[2] - mu0), p3 = ex2(sc[3] - mu1);
+      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g));
+      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8));
       const float sv0 = v0 ? half_lo(mv0) : 0.0f, zv0 = v0 ? half_hi(mv0) : 0.0f;
       const float sv1 = v1 ? half_lo(mv1) : 0.0f, zv1 = v1 ? half_hi(mv1) : 0.0f;
       l_run[0] += p0 + p2;
@@ -515,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       const uint32_t b0 = prmt(va, vb, 0x5410u);
       const uint32_t b1 = prmt(va, vb, 0x7632u);
 
-      const uint8_t* vrow = vst + C::kcode(tt, 0) + 8 * g;
+      const uint8_t* vrow = vst + C::kcode(0) + 8 * g;
       const uint2 r0w = *reinterpret_cast<const uint2*>(vrow + (2 * c) * kCodeRow);
       const uint2 r1w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 1) * kCodeRow);
       const uint2 r2w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 8) * kCodeRow);
@@ -571,6 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   float* red_m = red_acc + kWarps * kMaxGroup * kRedStride;           // [16][8]
   float* red_l = red_m + kWarps * kMaxGroup;
   float* red_z = red_l + kWarps * kMaxGroup;
+  float* wgt = red_z + kWarps * kMaxGroup;                            // [16][8]
+  float* tot = wgt + kWarps * kMaxGroup;                              // den, zz, M [3][8]
   if (!PACKED || c < 2) {
     if (g == 0) {
 #pragma unroll
@@ -592,21 +579,40 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   }
   __syncthreads();
 
-  // ---- merge the warps: one (head, dim) per thread
+  // ---- merge the warps.  Weights 2^(m_w - M) per (head, warp): thread
+  // 16h + w of warps 0-3, reduced over the 16 warps with shuffles inside
+  // each half-warp; then one (head, dim) per thread.
   const int nw = min(kWarps, n_steps);  // warps that saw any step
+  if (tid < kMaxGroup * kWarps) {
+    const int h = tid >> 4, w = tid & 15;
+    const bool in = h < G && w < nw;
+    const float m = in ? red_m[w * kMaxGroup + h] : -INFINITY;
+    float M = m;
+#pragma unroll
+    for (int x = 1; x < 16; x <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+    const float Mu = (M == -INFINITY) ? 0.0f : M;
+    const float f = in ? ex2(m - Mu) : 0.0f;
+    float den = in ? red_l[w * kMaxGroup + h] * f : 0.0f;
+    float zz = in ? red_z[w * kMaxGroup + h] * f : 0.0f;
+#pragma unroll
+    for (int x = 1; x < 16; x <<= 1) {
+      den += __shfl_xor_sync(kFull, den, x);
+      zz += __shfl_xor_sync(kFull, zz, x);
+    }
+    wgt[w * kMaxGroup + h] = f;
+    if (w == 0) {
+      tot[h] = den;
+      tot[kMaxGroup + h] = zz;
+      tot[2 * kMaxGroup + h] = M;
+    }
+  }
+  __syncthreads();
   for (int idx = tid; idx < G * kHeadDim; idx += kThreads) {
     const int h = idx / kHeadDim, dd = idx - h * kHeadDim;
-    float M = -INFINITY;
-    for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w * kMaxGroup + h]);
-    const float Mu = (M == -INFINITY) ? 0.0f : M;
-    float num = 0.0f, den = 0.0f, zz = 0.0f;
-    for (int w = 0; w < nw; ++w) {
-      const float f = ex2(red_m[w * kMaxGroup + h] - Mu);
-      num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * f;
-      den += red_l[w * kMaxGroup + h] * f;
-      zz += red_z[w * kMaxGroup + h] * f;
-    }
-    num += zz;
+    float num = tot[kMaxGroup + h];
+    for (int w = 0; w < nw; ++w)
+      num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * wgt[w * kMaxGroup + h];
+    const float den = tot[h], M = tot[2 * kMaxGroup + h];
     if (direct) {
       qs[h * kHeadDim + dd] = (den > 0.0f) ? num / den : 0.0f;
     } else {
@@ -622,12 +628,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   if (!direct) {
     // ---- the last split of this (sequence, kv-head) to finish merges them
     // all: one launch covers the decode, and no CTA ever waits for another.
-    __threadfence();  // this CTA's partials are visible before its ticket
     __syncthreads();
     const int ns = (n_pages + p.pages_per_split - 1) / p.pages_per_split;
     if (tid == 0) {
+      // release (cumulative over the CTA barrier above): this CTA's partials
+      // are visible before its ticket; acquire: the other splits' partials
+      // are read after it
       uint32_t* ticket = p.tickets + (int64_t(seq) * p.num_kv_heads + kvh);
-      const uint32_t done = atomicAdd(ticket, 1u) + 1u;
+      uint32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(ticket)
+                   : "memory");
+      const uint32_t done = prev + 1u;
       *flag = (done == uint32_t(ns));
       if (done >= uint32_t(ns)) {
         if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
@@ -636,9 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     }
     __syncthreads();
     if (*flag == 0) return;
-    __threadfence();
-    // item = (head, 4 dims); four threads per item share the splits, so each
-    // thread has only a few loads in flight and one round of L2 latency
+    // item = (head, 4 dims); four threads per item share the splits.  Every
+    // load is issued before any is used (one round of L2 latency); thread 0's
+    // fences around the ticket order them after the other splits' writes.
+    constexpr int kMaxSplitsPerThread = 8;
     for (int base = 0; base < G * 32 * 4; base += kThreads) {
       const int t = base + tid;
       const int item = t >> 2, part = t & 3;
@@ -648,33 +662,52 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row0;
       const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kHeadDim) + ch;
       float M = -INFINITY;
-      if (active)
-        for (int sp = part; sp < ns; sp += 4) M = fmaxf(M, __ldcg(&ml[sp]).x);
-      M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
-      M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
-      const float Mu = (M == -INFINITY) ? 0.0f : M;
       float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       float den = 0.0f;
-      if (active) {
-#pragma unroll 8
-        for (int sp = part; sp < ns; sp += 4) {
-          const float2 v = __ldcg(&ml[sp]);
-          const float4 o = __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]);
-          const float f = ex2(v.x - Mu);
-          den += v.y * f;
-          a.x += o.x * f;
-          a.y += o.y * f;
-          a.z += o.z * f;
-          a.w += o.w * f;
+      for (int sp0 = part; sp0 < ns; sp0 += 4 * kMaxSplitsPerThread) {
+        float2 v[kMaxSplitsPerThread];
+        float4 o[kMaxSplitsPerThread];
+#pragma unroll
+        for (int u = 0; u < kMaxSplitsPerThread; ++u) {
+          const int sp = sp0 + 4 * u;
+          const bool in = active && sp < ns;
+          v[u] = in ? __ldcg(&ml[sp]) : make_float2(-INFINITY, 0.0f);
+          o[u] = in ? __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
+        float Mb = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kMaxSplitsPerThread; ++u) Mb = fmaxf(Mb, v[u].x);
+        const float Mn = fmaxf(M, Mb);
+        const float Mu = (Mn == -INFINITY) ? 0.0f : Mn;
+        const float al = ex2(M - Mu);
+        a.x *= al; a.y *= al; a.z *= al; a.w *= al; den *= al;
+#pragma unroll
+        for (int u = 0; u < kMaxSplitsPerThread; ++u) {
+          const float f = ex2(v[u].x - Mu);
+          den += v[u].y * f;
+          a.x += o[u].x * f;
+          a.y += o[u].y * f;
+          a.z += o[u].z * f;
+          a.w += o[u].w * f;
+        }
+        M = Mn;
       }
+      // combine the four parts of the item
 #pragma unroll
       for (int x = 1; x <= 2; x <<= 1) {
-        den += __shfl_xor_sync(kFull, den, x);
-        a.x += __shfl_xor_sync(kFull, a.x, x);
-        a.y += __shfl_xor_sync(kFull, a.y, x);
-        a.z += __shfl_xor_sync(kFull, a.z, x);
-        a.w += __shfl_xor_sync(kFull, a.w, x);
+        const float Mo = __shfl_xor_sync(kFull, M, x);
+        const float Mn = fmaxf(M, Mo);
+        const float Mu = (Mn == -INFINITY) ? 0.0f : Mn;
+        const float fs = ex2(M - Mu), fo = ex2(Mo - Mu);
+        const float dn = __shfl_xor_sync(kFull, den, x);
+        const float ox = __shfl_xor_sync(kFull, a.x, x), oy = __shfl_xor_sync(kFull, a.y, x);
+        const float oz = __shfl_xor_sync(kFull, a.z, x), ow = __shfl_xor_sync(kFull, a.w, x);
+        den = den * fs + dn * fo;
+        a.x = a.x * fs + ox * fo;
+        a.y = a.y * fs + oy * fo;
+        a.z = a.z * fs + oz * fo;
+        a.w = a.w * fs + ow * fo;
+        M = Mn;
       }
       if (active && part == 0) {
         const float inv = (den > 0.0f) ? 1.0f / den : 0.0f;

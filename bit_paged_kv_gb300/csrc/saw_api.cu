@@ -60,8 +60,6 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
       }
     }
     pps = ceil_div(max_pages, best);
-    const int64_t step = page_size >= 32 ? 1 : 32 / page_size;  // pages per decode step
-    pps = ceil_div(pps, step) * step;
   }
   int64_t splits = max_pages == 0 ? 1 : ceil_div(max_pages, pps);
   if (splits > 65535) return SAW_ERR_UNSUPPORTED;
@@ -268,9 +266,10 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
                         int32_t block_h, float sm_scale, float* out, void* workspace,
-                        size_t workspace_bytes, int32_t pages_per_split, int32_t* dev_status,
-                        void* stream) {
+                        size_t workspace_bytes, int32_t pages_per_split, int32_t flags,
+                        int32_t* dev_status, void* stream) {
   saw::DecodeParams p{};
+  if (flags & ~int32_t(SAW_STEP_EARLY_PAGES)) return SAW_ERR_INVALID_ARG;
   const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                     seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
                                     head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
@@ -286,6 +285,7 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
   p.k_cache_w = static_cast<uint8_t*>(k_cache);
   p.v_cache_w = static_cast<uint8_t*>(v_cache);
   p.append = 1;
+  p.early_pages = (flags & SAW_STEP_EARLY_PAGES) ? 1 : 0;
   cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }

@@ -56,6 +56,7 @@ struct DecodeParams {
   uint8_t* k_cache_w;           // writable views of the caches (decode step)
   uint8_t* v_cache_w;
   int32_t append;               // 1: decode step (append, then attend)
+  int32_t early_pages;          // 1: tables and pages may be read before the previous kernel ends
   int32_t* dev_status;
   int32_t max_blocks;
   int32_t num_seqs;

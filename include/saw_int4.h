@@ -200,18 +200,25 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
  * k_cache, v_cache  written (the new rows) and read.
  * seq_lens      lengths INCLUDING the new token (>= 1).  A length of 0
  *               appends nothing and gives a zero output row.
+ * flags         0, or SAW_STEP_EARLY_PAGES: the caller guarantees that the
+ *               kernel issued just before this call on `stream` writes none
+ *               of block_tables, seq_lens, k_cache and v_cache.  The kernel
+ *               may then read them and start its page copies while that
+ *               kernel finishes (programmatic dependent launch); it still
+ *               waits for it before reading q, k_new, v_new or writing.
  * Other arguments as saw_paged_decode_int4.  The appended bytes equal those
  * of saw_quantize_append on the same row, and the output equals
  * saw_quantize_append followed by saw_paged_decode_int4.
  */
+#define SAW_STEP_EARLY_PAGES 1
 int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
                         void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
                         const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
                         int32_t block_h, float sm_scale, float* out, void* workspace,
-                        size_t workspace_bytes, int32_t pages_per_split, int32_t* dev_status,
-                        void* stream);
+                        size_t workspace_bytes, int32_t pages_per_split, int32_t flags,
+                        int32_t* dev_status, void* stream);
 
 /*
  * saw_paged_decode_int4_noalloc -- the same decode as saw_paged_decode_int4

@@ -150,12 +150,12 @@ def test_plan_and_workspace(L):
 def _step(L, **kw):
     a = dict(q=A, kn=B, vn=A, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128,
              pages=8, P=16, rk=1, rv=0, h=128, scale=0.0, out=A, ws=B, wsb=1 << 20, pps=0,
-             status=None, stream=None)
+             flags=0, status=None, stream=None)
     a.update(kw)
     return L.saw_decode_step(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["mb"],
                              a["sl"], a["B"], a["maxlen"], a["hq"], a["hkv"], a["d"], a["pages"],
                              a["P"], a["rk"], a["rv"], a["h"], a["scale"], a["out"], a["ws"],
-                             a["wsb"], a["pps"], a["status"], a["stream"])
+                             a["wsb"], a["pps"], a["flags"], a["status"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -166,6 +166,7 @@ def _step(L, **kw):
     (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
     (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
     (dict(mb=3), saw.SAW_ERR_INVALID_ARG),
+    (dict(flags=2), saw.SAW_ERR_INVALID_ARG),
     (dict(B=0), saw.SAW_OK),
 ])
 def test_decode_step_rejects_before_launch(L, kw, expect):

@@ -43,8 +43,8 @@ def _decode_parity(wl, layer, lens, bt, npages, kc, vc, kr, vr, pairs):
                         wl.rotate_v, wl.block_h, pairs=pairs)
     got = out.cpu().numpy()[[b for b, _ in pairs], [h for _, h in pairs]]
     assert np.all(np.isfinite(got))
-    err = rel_err(got, ref)
-    row_err = max(rel_err(got[i], ref[i]) for i in range(len(pairs)))
+    err = rel_err(got, ref, f"{wl.name}-L{layer}-rk{int(wl.rotate_k)}rv{int(wl.rotate_v)}-h{wl.block_h}")
+    row_err = max(rel_err(got[i], ref[i], "row") for i in range(len(pairs)))
     print(f"{wl.name} layer {layer}: rel err {err:.3e} (worst row {row_err:.3e})")
     assert err <= ATTN_TOL, f"{wl.name} layer {layer}: relative error {err:.3e}"
 

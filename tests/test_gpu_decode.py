@@ -35,7 +35,7 @@ def _check(wl, lens, bt, npages, kc, vc, q, pps=0, pairs=None, max_seq_len=None)
     if pairs is not None:
         got = np.stack([out[b, h].cpu().numpy() for b, h in pairs])
     assert np.all(np.isfinite(got))
-    err = rel_err(got, ref)
+    err = rel_err(got, ref, f"{wl.name}-G{wl.group}-P{wl.page_size}-h{wl.block_h}-pps{pps}")
     assert err <= ATTN_TOL, f"relative error {err:.3e}"
     return err
 
@@ -117,7 +117,7 @@ def test_rotation_mismatch_is_detectable():
                         wl.page_size, True, False, 128)
     ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
                         wl.page_size, True, True, 128)
-    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) > 50 * max(good, 1e-5)
+    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref, "mismatch") > 50 * max(good, 1e-5)
 
 
 def test_decode_after_single_token_append():
@@ -159,9 +159,10 @@ def test_workspace_reuse_across_calls_and_plans():
     assert torch.all(ws[:4 * n_tickets].view(torch.int32) == 0)
 
 
-@pytest.mark.parametrize("P,group,pps", [(16, 4, 0), (16, 4, 2), (16, 1, 3), (16, 8, 1),
-                                        (32, 4, 1), (64, 2, 1), (64, 8, 0)])
-def test_fused_decode_step(P, group, pps):
+@pytest.mark.parametrize("P,group,pps,flags", [(16, 4, 0, 0), (16, 4, 2, 1), (16, 1, 3, 0),
+                                              (16, 8, 1, 1), (32, 4, 1, 0), (64, 2, 1, 1),
+                                              (64, 8, 0, 0)])
+def test_fused_decode_step(P, group, pps, flags):
     """saw_decode_step = append the new token at seq_len - 1, then attend, in
     one launch: cache bytes equal the oracle's append, attention the oracle's."""
     from gpu_helpers import new_caches, oracle_append
@@ -184,7 +185,7 @@ def test_fused_decode_step(P, group, pps):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     saw.saw_decode_step(q, knew, vnew, kc, vc, bt.cuda(), lens.cuda(), Lmax, wl.num_kv_heads,
                         npages, P, wl.rotate_k, wl.rotate_v, wl.block_h, out, ws,
-                        pages_per_split=pps, dev_status=st)
+                        pages_per_split=pps, flags=flags, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     # oracle: same prefill, then append the new token of each non-empty sequence
@@ -202,4 +203,4 @@ def test_fused_decode_step(P, group, pps):
                         wl.block_h)
     got = out.cpu().numpy().reshape(-1, D)
     assert np.all(np.isfinite(got))
-    assert rel_err(got, ref) <= ATTN_TOL
+    assert rel_err(got, ref, f"step-P{P}-G{group}-pps{pps}") <= ATTN_TOL
