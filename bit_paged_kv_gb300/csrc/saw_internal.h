@@ -30,6 +30,11 @@ struct AppendParams {
   int32_t block_h;
   int64_t num_slots;            // num_pages * page_size
   float c_h;                    // binary32(1/sqrt(block_h))
+  // set by the launcher: row / num_kv_heads = (row * hkv_mul) >> hkv_shift
+  // for rows below 2^31, and page_size = 1 << page_shift
+  uint32_t hkv_mul;
+  uint32_t hkv_shift;
+  int32_t page_shift;
 };
 
 cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream);

@@ -37,14 +37,17 @@ def test_tiny_all_tokens(rotate_k, rotate_v, h):
     assert_bytes_equal(vc, vr, "V cache")
 
 
+@pytest.mark.parametrize("size", ["warp", "tiled"])
 @pytest.mark.parametrize("P", [16, 32, 64])
 @pytest.mark.parametrize("hkv", [1, 3, 8])
-def test_ragged_strided_shuffled(P, hkv):
+def test_ragged_strided_shuffled(P, hkv, size):
     """Row counts that are not a multiple of the CTA tile, a strided token
-    dimension, scattered slots and padding entries."""
+    dimension, scattered slots and padding entries -- on the warp-per-row
+    kernel (77 tokens) and on the tiled kernel (above 4096 rows, with a
+    ragged last tile)."""
     wl = W.TINY.variant(num_kv_heads=hkv, page_size=P, dist="student_t", nu=3)
-    T = 77
-    num_pages = 9
+    T = 77 if size == "warp" else 4096 // hkv + 333
+    num_pages = -(-T // P) + 5
     g = torch.Generator().manual_seed(P * 10 + hkv)
     slots = torch.randperm(num_pages * P, generator=g)[:T].to(torch.int32)
     slots[[3, 40, 76]] = -1
@@ -64,9 +67,13 @@ def test_ragged_strided_shuffled(P, hkv):
     assert_bytes_equal(vc, vr, "V cache")
 
 
-def test_k_only_and_bad_slots():
+@pytest.mark.parametrize("T", [40, 5000], ids=["warp", "tiled"])
+def test_k_only_and_bad_slots(T):
+    """K only; a slot one past the end and a negative slot are reported and
+    skipped, padding (-1) is skipped silently, every other row is stored."""
     wl = W.TINY
-    T, num_pages, P = 40, 4, 16
+    P = 16
+    num_pages = -(-T // P)
     k, _ = _inputs(wl, T)
     slots = torch.arange(T, dtype=torch.int32)
     slots[5] = num_pages * P       # one past the end
@@ -138,6 +145,24 @@ def test_empty_append_is_a_no_op():
     saw.saw_quantize_append(k, None, s, kc, None, 1, 16, True, False, 128)
     torch.cuda.synchronize()
     assert torch.all(kc == 7)
+
+
+@pytest.mark.parametrize("h", [16, 32, 64, 128])
+@pytest.mark.parametrize("rotate_k,rotate_v", [(1, 1), (1, 0), (0, 1)])
+def test_tiled_block_sizes(h, rotate_k, rotate_v):
+    """Every block size on the tiled kernel (3000 tokens x 2 kv-heads, a
+    ragged last tile), with each tensor rotated or not."""
+    wl = W.TINY.variant(dist="student_t", nu=4)
+    T = 3000
+    k, v = _inputs(wl, T)
+    num_pages = -(-T // 16) + 1
+    slots = torch.randperm(num_pages * 16, generator=torch.Generator().manual_seed(h))[:T]
+    slots = slots.to(torch.int32)
+    kc, vc, st = gpu_append(k, v, slots.cuda(), num_pages, 16, rotate_k, rotate_v, h)
+    kr, vr, bad = oracle_append(k, v, slots, num_pages, 16, rotate_k, rotate_v, h)
+    assert st == 0 and bad == 0
+    assert_bytes_equal(kc, kr, "K cache")
+    assert_bytes_equal(vc, vr, "V cache")
 
 
 @pytest.mark.parametrize("T", [1, 3, 511, 512, 513, 3000])
