@@ -9,15 +9,18 @@
 // include/saw_int4.h; each binary32 step below is one explicit
 // round-to-nearest intrinsic so that no contraction changes a bit.
 //
-// Mapping (bulk appends): a persistent kernel, a few 128-thread CTAs per SM.
-// A tile is 128 consecutive (token, kv-head) rows of one tensor (K or V),
-// 32 KB of bfloat16.  Each CTA walks its tiles with two shared-memory
-// buffers: every thread issues 16-byte asynchronous copies of the next tile
-// into an XOR-swizzled layout while the current tile is being quantized, so
-// HBM reads overlap the arithmetic.  Then each thread owns one row: 128
-// binary32 values in registers, the butterfly runs two lanes at a time with
-// packed f32x2 adds, min/max reduce three at a time, and the 64 code bytes
-// plus the 4-byte (scale, zero) word are stored into the page slot.
+// Mapping (bulk appends): a persistent kernel, two 256-thread CTAs per SM,
+// each warp an independent worker.  A tile is 16 consecutive (token,
+// kv-head) rows of one tensor (K or V), 4 KB of bfloat16.  Each warp walks
+// its tiles through a private ring of three shared-memory buffers: its
+// lanes issue 16-byte asynchronous copies of the tile two ahead into a
+// swizzled layout while the current tile is being quantized, so HBM reads
+// overlap the arithmetic, and no CTA-wide barrier is needed.  Two
+// neighbouring threads own one row, 64 binary32 values each: butterfly
+// strides up to 32 stay inside a thread (two lanes per packed f32x2
+// instruction), stride 64 is one shuffle with the partner, min/max reduce
+// three at a time, and each thread stores its 32 code bytes; the (scale,
+// zero) word goes to the page's metadata run.
 #include <algorithm>
 
 #include "saw_device.cuh"
@@ -27,10 +30,14 @@
 namespace saw {
 namespace {
 
-constexpr int kTileRows = 128;  // rows per tile, one per thread
+constexpr int kTileRows = 16;                      // rows per warp tile (two threads per row)
+constexpr int kHalfRow = kHeadDim / 2;             // elements per thread
 constexpr int kRowBytes = kHeadDim * 2;
-constexpr int kTileBytes = kTileRows * kRowBytes;  // 32 KB
-constexpr int kTileCtasPerSm = 3;
+constexpr int kTileBytes = kTileRows * kRowBytes;  // 4 KB
+constexpr int kTileStages = 3;                     // tiles in flight per warp
+constexpr int kTileWarps = 8;                      // warps per CTA
+constexpr int kTileThreads = 32 * kTileWarps;
+constexpr int kTileCtasPerSm = 2;
 
 // ------------------------------------------------------------ PTX pieces
 
@@ -75,174 +82,227 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Codes of two elements when no clamp is needed (0 <= (y - z) * r <= 15 +
-// a few ulp): v = RN(RN(y - z) * r) as in the scalar rule (two lanes per
-// instruction), then v + 1.5 * 2^23 rounds to the nearest integer with ties
-// to even in the low mantissa bits, so byte 0 of each result is the code
-// (high bits 0x4B40....).  The magic add is a scalar RN add: it must round
-// the already-rounded product, never be fused with the multiply.
-__device__ __forceinline__ void codes2(float y0, float y1, float z, float r, uint32_t& t0,
-                                       uint32_t& t1) {
-  float v0, v1;
-  asm("{\n\t.reg .b64 y, zz, rr;\n\t"
-      "mov.b64 y, {%2, %3};\n\tmov.b64 zz, {%4, %4};\n\tmov.b64 rr, {%5, %5};\n\t"
-      "sub.rn.f32x2 y, y, zz;\n\tmul.rn.f32x2 y, y, rr;\n\t"
-      "mov.b64 {%0, %1}, y;\n\t}"
-      : "=f"(v0), "=f"(v1)
-      : "f"(y0), "f"(y1), "f"(z), "f"(r));
-  t0 = __float_as_uint(__fadd_rn(v0, 12582912.0f));
-  t1 = __float_as_uint(__fadd_rn(v1, 12582912.0f));
-}
-
 // q = n / d for 0 <= n < 2^31 with a host-computed multiplier (m, sh):
 // m = ceil(2^sh / d), sh = 31 + ceil(log2 d), exact on that range.
 __device__ __forceinline__ uint32_t div_rows(uint32_t n, uint32_t m, uint32_t sh) {
   return uint32_t((uint64_t(n) * m) >> sh);
 }
 
-// ------------------------------------------------------------ one row
+// ------------------------------------------------------------ half row
+//
+// Two neighbouring threads share a row.  Writing G0..G3 for its four
+// 32-element quarters, the lower thread (h = 0) holds G0 in local elements
+// 0..31 and G1 in 32..63; the upper thread (h = 1) holds G3 in 0..31 and G2
+// in 32..63.  Strides up to 16 stay inside a quarter.  Stride 32 pairs local
+// j with local 32 + j in both threads, and stride 64 pairs the lower
+// thread's local j (G0) with the upper thread's local 32 + j (G2), and the
+// upper thread's local j (G3) with the lower thread's 32 + j (G1): one
+// shuffle of local 32 + j covers both.  In both steps the thread whose pair
+// members sit in swapped roles computes the same two RN sums through
+// x' = RN(sg * x + y), y' = RN(-sg * y + x) with sg = +-1 (exact products).
+// After a stride-64 step the lower thread's local 32..63 hold G2 and the
+// upper thread's hold G1.
 
-// In-register butterfly over each H-block of the row, strides 1, 2, ..., H/2
-// (stride 1 scalar, the rest two pairs per instruction), then one multiply
-// by c = binary32(1/sqrt(H)).
+// (x0, x1) and (y0, y1) <- RN(sg * x + y) and RN(-sg * y + x).
+__device__ __forceinline__ void bfly2_signed(float& x0, float& x1, float& y0, float& y1,
+                                             float sg) {
+  asm("{\n\t.reg .b64 x, y, p, m, a, b;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "mov.b64 p, {%4, %4};\n\tmov.b64 m, {%5, %5};\n\t"
+      "fma.rn.f32x2 a, x, p, y;\n\tfma.rn.f32x2 b, y, m, x;\n\t"
+      "mov.b64 {%0, %1}, a;\n\tmov.b64 {%2, %3}, b;\n\t}"
+      : "+f"(x0), "+f"(x1), "+f"(y0), "+f"(y1)
+      : "f"(sg), "f"(-sg));
+}
+
+// Butterfly of the row's H-blocks (strides 1, 2, ..., H/2 in ascending
+// order, every step an RN add or subtract), then one multiply by
+// c = binary32(1/sqrt(H)).
 template <int H>
-__device__ __forceinline__ void rotate_row(float (&u)[kHeadDim], float c) {
+__device__ __forceinline__ void rotate_half(float (&u)[kHalfRow], float c, int h) {
 #pragma unroll
-  for (int i = 0; i < kHeadDim; i += 2) {
+  for (int i = 0; i < kHalfRow; i += 2) {
     const float a = u[i], b = u[i + 1];
     u[i] = __fadd_rn(a, b);
     u[i + 1] = __fsub_rn(a, b);
   }
 #pragma unroll
-  for (int len = 2; len < H; len *= 2) {
+  for (int len = 2; len < (H < 32 ? H : 32); len *= 2) {
 #pragma unroll
-    for (int i = 0; i < kHeadDim; i += 2) {
+    for (int i = 0; i < kHalfRow; i += 2) {
       if ((i & len) == 0) bfly2(u[i], u[i + 1], u[i + len], u[i + len + 1]);
     }
   }
+  const float sg = h ? -1.0f : 1.0f;
+  if (H >= 64) {
 #pragma unroll
-  for (int i = 0; i < kHeadDim; i += 2) mul2(u[i], u[i + 1], c);
+    for (int j = 0; j < 32; j += 2) bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sg);
+  }
+  if (H == 128) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float o0 = __shfl_xor_sync(0xFFFFFFFFu, u[32 + j], 1);
+      const float o1 = __shfl_xor_sync(0xFFFFFFFFu, u[33 + j], 1);
+      u[32 + j] = o0;
+      u[33 + j] = o1;
+      bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sg);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kHalfRow; i += 2) mul2(u[i], u[i + 1], c);
 }
 
-// Row min and max, three at a time (exact: no rounding involved).
-__device__ __forceinline__ void row_min_max(const float (&u)[kHeadDim], float& mn, float& mx) {
-  float lo[43], hi[43];
+// Min and max of the whole row: 64 values here, three at a time (exact),
+// then the partner's.
+__device__ __forceinline__ void half_min_max(const float (&u)[kHalfRow], float& mn, float& mx) {
+  float lo[22], hi[22];
 #pragma unroll
-  for (int i = 0; i < 42; ++i) {
+  for (int i = 0; i < 21; ++i) {
     lo[i] = min3(u[3 * i], u[3 * i + 1], u[3 * i + 2]);
     hi[i] = max3(u[3 * i], u[3 * i + 1], u[3 * i + 2]);
   }
-  lo[42] = fminf(u[126], u[127]);
-  hi[42] = fmaxf(u[126], u[127]);
+  lo[21] = u[63];
+  hi[21] = u[63];
 #pragma unroll
-  for (int i = 0; i < 14; ++i) {
+  for (int i = 0; i < 7; ++i) {
     lo[i] = min3(lo[3 * i], lo[3 * i + 1], lo[3 * i + 2]);
     hi[i] = max3(hi[3 * i], hi[3 * i + 1], hi[3 * i + 2]);
   }
-  lo[14] = lo[42];
-  hi[14] = hi[42];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) {
-    lo[i] = min3(lo[3 * i], lo[3 * i + 1], lo[3 * i + 2]);
-    hi[i] = max3(hi[3 * i], hi[3 * i + 1], hi[3 * i + 2]);
-  }
-  mn = fminf(min3(lo[0], lo[1], lo[2]), fminf(lo[3], lo[4]));
-  mx = fmaxf(max3(hi[0], hi[1], hi[2]), fmaxf(hi[3], hi[4]));
+  lo[7] = lo[21];
+  hi[7] = hi[21];
+  mn = fminf(min3(lo[0], lo[1], lo[2]), min3(lo[3], lo[4], fminf(lo[5], fminf(lo[6], lo[7]))));
+  mx = fmaxf(max3(hi[0], hi[1], hi[2]), max3(hi[3], hi[4], fmaxf(hi[5], fmaxf(hi[6], hi[7]))));
+  mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
 }
 
-// Quantize the row and store its 64 code bytes (two codes per byte, even
-// index in the low nibble) at dst; returns (scale | zero << 16).
-__device__ __forceinline__ uint32_t quantize_store(const float (&u)[kHeadDim], uint4* dst) {
-  float mn, mx;
-  row_min_max(u, mn, mx);
-  const uint16_t zb = f16_round_down_sat(mn);
-  const float z = f16_bits_to_f32(zb);
-  const float step = __fdiv_rn(__fsub_rn(mx, z), 15.0f);
-  const uint16_t sb = f16_round_up_sat(step);
-  const float s = f16_bits_to_f32(sb);
-  const float r = (s == 0.0f) ? 0.0f : __frcp_rn(s);
-  // No clamp can bite when z <= every element (min not below -65504) and
-  // the scale did not saturate: then 0 <= y - z <= max - z and
-  // r <= (1 + 2^-24) / s with s >= (max - z) / 15 (1 - 2^-24), so
-  // (y - z) * r stays below 15.5.
-  const bool fast = (mn >= -65504.0f) && (step <= 65504.0f);
+// Codes of this thread's 64 elements, packed two per byte (even local index
+// in the low nibble): words 0..3 hold local 0..31, words 4..7 local 32..63.
+//
+// Fast path (no clamp can bite, see the caller): with r24 = r * 2^-24 (exact),
+// RN((y - z) * r24) = RN((y - z) * r) * 2^-24 whenever the result is normal,
+// and below that the code is 0 either way.  Binary16 spaces its subnormals
+// 2^-24 apart, so the RN conversion to binary16 of that value rounds
+// (y - z) * r to the nearest integer with ties to even, and the code is the
+// binary16 bit pattern itself.
+__device__ __forceinline__ void quantize_half(const float (&u)[kHalfRow], float z, float r,
+                                              bool fast, uint32_t (&word)[8]) {
+  if (fast) {
+    const float r24 = __fmul_rn(r, 5.9604644775390625e-08f);  // 2^-24
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t word[4];
+    for (int w = 0; w < 8; ++w) {
+      uint32_t d[4];
 #pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) {
-      const int w = 4 * j + w4;
-      if (fast) {
-        uint32_t t[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          codes2(u[8 * w + 2 * e], u[8 * w + 2 * e + 1], z, r, t[2 * e], t[2 * e + 1]);
-        const uint32_t even = prmt(prmt(t[0], t[2], 0x0040u), prmt(t[4], t[6], 0x0040u), 0x5410u);
-        const uint32_t odd = prmt(prmt(t[1], t[3], 0x0040u), prmt(t[5], t[7], 0x0040u), 0x5410u);
-        word[w4] = even | (odd << 4);
-      } else {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float v = __fmul_rn(__fsub_rn(u[8 * w + k], z), r);
-          int q = __float2int_rn(v);  // round half to even
-          q = min(max(q, 0), 15);
-          acc |= uint32_t(q) << (4 * k);
-        }
-        word[w4] = acc;
+      for (int e = 0; e < 4; ++e) {
+        float v0 = u[8 * w + 2 * e], v1 = u[8 * w + 2 * e + 1];
+        asm("{\n\t.reg .b64 y, zz, rr;\n\t"
+            "mov.b64 y, {%0, %1};\n\tmov.b64 zz, {%2, %2};\n\tmov.b64 rr, {%3, %3};\n\t"
+            "sub.rn.f32x2 y, y, zz;\n\tmul.rn.f32x2 y, y, rr;\n\t"
+            "mov.b64 {%0, %1}, y;\n\t}"
+            : "+f"(v0), "+f"(v1)
+            : "f"(z), "f"(r24));
+        const __half2 hv = __floats2half2_rn(v0, v1);  // .x (low half) = code of v0
+        d[e] = *reinterpret_cast<const uint32_t*>(&hv);
       }
+      // d[e] = c(2e) | c(2e+1) << 16
+      const uint32_t x = prmt(d[0], d[1], 0x6240u);  // c0 c2 c1 c3
+      const uint32_t y = prmt(d[2], d[3], 0x6240u);  // c4 c6 c5 c7
+      const uint32_t even = prmt(x, y, 0x5410u);     // c0 c2 c4 c6
+      const uint32_t odd = prmt(x, y, 0x7632u);      // c1 c3 c5 c7
+      word[w] = even | (odd << 4);
     }
-    dst[j] = make_uint4(word[0], word[1], word[2], word[3]);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float v = __fmul_rn(__fsub_rn(u[8 * w + k], z), r);
+        int q = __float2int_rn(v);  // round half to even
+        q = min(max(q, 0), 15);
+        acc |= uint32_t(q) << (4 * k);
+      }
+      word[w] = acc;
+    }
   }
-  return uint32_t(sb) | (uint32_t(zb) << 16);
 }
 
 // ------------------------------------------------------------ tiled kernel
 
-// Tiles 0 .. tiles_per_tensor-1 are K rows, the rest V rows.
+// Chunk c (16 bytes: elements 8c .. 8c+7) of tile row r sits in 16-byte slot
+// c ^ (r & 3) of the row's 256 bytes: the copy (16 consecutive chunks of a
+// row per half-warp) and the reads (rows r..r+3, both halves, chunks
+// j and 8 + (j ^ 4) per phase) both hit 8 distinct bank groups.
+__device__ __forceinline__ int chunk_slot(int r, int c) { return c ^ (r & 3); }
+
+// Tiles 0 .. tiles_per_tensor-1 are K rows, the rest V rows.  Each warp is
+// an independent worker with its own ring of kTileStages tiles: no CTA-wide
+// barrier, so a warp waiting for its data never holds up the others.
 template <int H>
-__global__ void __launch_bounds__(kTileRows, kTileCtasPerSm)
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     quantize_append_tiled_kernel(const AppendParams p, int tiles_per_tensor, int num_tiles) {
-  extern __shared__ __align__(128) uint8_t tiles[];  // two tiles
+  extern __shared__ __align__(128) uint8_t ring_all[];
 
   pdl_wait_then_release();
-  const int tid = threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* ring = ring_all + warp * (kTileStages * kTileBytes);
   const int hkv = p.num_kv_heads;
   const int num_rows = p.num_tokens * hkv;
 
-  // Copies of one tile: 16 per thread, 16 threads per 256-byte row; chunk c
-  // of row r lands at 16 * (c ^ (r & 15)) so that the row-per-thread reads
-  // below hit distinct banks.
+  // Copies of one tile: 8 per lane, 16 lanes per 256-byte row.
   auto issue = [&](int tile, uint8_t* buf) {
     const int tensor = tile >= tiles_per_tensor ? 1 : 0;
     const int row0 = (tile - tensor * tiles_per_tensor) * kTileRows;
     const uint16_t* __restrict__ src = tensor ? p.src[1] : p.src[0];
     const int64_t stride = tensor ? p.stride[1] : p.stride[0];
-    const int ch = tid & 15;
+    const int ch = lane & 15;
+    const bool full = row0 + kTileRows <= num_rows;
+    if (full && stride == int64_t(hkv) * kHeadDim) {
+      // contiguous rows: row i of the tile starts 128 elements after row i-1
+      const uint16_t* g = src + int64_t(row0) * kHeadDim + ch * 8;
 #pragma unroll
-    for (int it = 0; it < kTileRows / 8; ++it) {
-      const int r = it * 8 + (tid >> 4);
-      const int row = row0 + r;
-      if (row < num_rows) {
-        const uint32_t t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
-        const uint32_t hd = uint32_t(row) - t * uint32_t(hkv);
-        cp_async16(buf + r * kRowBytes + ((ch ^ (r & 15)) << 4),
-                   src + int64_t(t) * stride + hd * kHeadDim + ch * 8);
+      for (int it = 0; it < kTileRows / 2; ++it) {
+        const int r = it * 2 + (lane >> 4);
+        cp_async16(buf + r * kRowBytes + (chunk_slot(r, ch) << 4), g + r * kHeadDim);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < kTileRows / 2; ++it) {
+        const int r = it * 2 + (lane >> 4);
+        const int row = row0 + r;
+        if (row < num_rows) {
+          const uint32_t t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
+          const uint32_t hd = uint32_t(row) - t * uint32_t(hkv);
+          cp_async16(buf + r * kRowBytes + (chunk_slot(r, ch) << 4),
+                     src + int64_t(t) * stride + hd * kHeadDim + ch * 8);
+        }
       }
     }
   };
 
-  int tile = blockIdx.x;
-  if (tile < num_tiles) issue(tile, tiles);
-  cp_async_commit();
-  for (int k = 0; tile < num_tiles; ++k, tile += gridDim.x) {
-    uint8_t* buf = tiles + (k & 1) * kTileBytes;
-    const int nxt = tile + gridDim.x;
-    if (nxt < num_tiles) issue(nxt, tiles + ((k + 1) & 1) * kTileBytes);
+  const int r = lane >> 1;  // this thread's row in the tile
+  const int h = lane & 1;   // and its half
+  const int step = int(gridDim.x) * kTileWarps;
+  int tile = int(blockIdx.x) * kTileWarps + warp;
+#pragma unroll
+  for (int s = 0; s < kTileStages - 1; ++s) {
+    const int pre = tile + s * step;
+    if (pre < num_tiles) issue(pre, ring + s * kTileBytes);
     cp_async_commit();
+  }
+  int cur = 0;                  // ring slot of the current tile
+  int ahead = kTileStages - 1;  // ring slot of the tile issued next
+  for (; tile < num_tiles; tile += step) {
+    uint8_t* buf = ring + cur * kTileBytes;
+    const int nxt = tile + (kTileStages - 1) * step;
+    if (nxt < num_tiles) issue(nxt, ring + ahead * kTileBytes);
+    cp_async_commit();
+    cur = (cur + 1 == kTileStages) ? 0 : cur + 1;
+    ahead = (ahead + 1 == kTileStages) ? 0 : ahead + 1;
 
     const int tensor = tile >= tiles_per_tensor ? 1 : 0;
-    const int row = (tile - tensor * tiles_per_tensor) * kTileRows + tid;
+    const int row = (tile - tensor * tiles_per_tensor) * kTileRows + r;
     const bool live = row < num_rows;
     uint32_t t = 0, hd = 0;
     int32_t slot = -1;
@@ -251,40 +311,70 @@ __global__ void __launch_bounds__(kTileRows, kTileCtasPerSm)
       hd = uint32_t(row) - t * uint32_t(hkv);
       slot = __ldg(p.slot_mapping + t);
     }
-    cp_async_wait<1>();  // this thread's copies of the current tile landed
-    __syncthreads();     // ... and everyone's
+    cp_async_wait<kTileStages - 1>();  // this lane's copies of the current tile landed
+    __syncwarp();                      // ... and the whole warp's
+
+    // Every thread computes (rows past the end or without a slot on stale
+    // data) so that the pair shuffles run converged; only stores are guarded.
+    float u[kHalfRow];
+    {
+      // local chunk j of thread h: chunk j (h = 0), chunk 8 + (j ^ 4) (h = 1)
+      const uint8_t* rowp = buf + r * kRowBytes + h * (kRowBytes / 2);
+      const int x = (r & 3) ^ (h << 2);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((j ^ x) << 4));
+        u[8 * j + 0] = bf16_lo(w.x);
+        u[8 * j + 1] = bf16_hi(w.x);
+        u[8 * j + 2] = bf16_lo(w.y);
+        u[8 * j + 3] = bf16_hi(w.y);
+        u[8 * j + 4] = bf16_lo(w.z);
+        u[8 * j + 5] = bf16_hi(w.z);
+        u[8 * j + 6] = bf16_lo(w.w);
+        u[8 * j + 7] = bf16_hi(w.w);
+      }
+    }
+    const bool rot = tensor ? p.rotate[1] != 0 : p.rotate[0] != 0;
+    if (rot) rotate_half<H>(u, p.c_h, h);
+    float mn, mx;
+    half_min_max(u, mn, mx);
+    const uint16_t zb = f16_round_down_sat(mn);
+    const float z = f16_bits_to_f32(zb);
+    const float step = __fdiv_rn(__fsub_rn(mx, z), 15.0f);
+    const uint16_t sb = f16_round_up_sat(step);
+    const float sv = f16_bits_to_f32(sb);
+    const float rcp = (sv == 0.0f) ? 0.0f : __frcp_rn(sv);
+    // No clamp can bite when z <= every element (min not below -65504) and
+    // the scale did not saturate: then 0 <= y - z <= max - z and
+    // r <= (1 + 2^-24) / s with s >= (max - z) / 15 (1 - 2^-24), so
+    // (y - z) * r stays below 15.5.
+    const bool fast = (mn >= -65504.0f) && (step <= 65504.0f);
+    uint32_t word[8];
+    quantize_half(u, z, rcp, fast, word);
 
     if (live && slot != -1) {
       if (slot < 0 || int64_t(slot) >= p.num_slots) {
-        report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+        if (h == 0) report(p.dev_status, SAW_ERR_DEVICE_INDEX);
       } else {
-        float u[kHeadDim];
-        const int r = tid;
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint4 w =
-              *reinterpret_cast<const uint4*>(buf + r * kRowBytes + ((ch ^ (r & 15)) << 4));
-          u[8 * ch + 0] = bf16_lo(w.x);
-          u[8 * ch + 1] = bf16_hi(w.x);
-          u[8 * ch + 2] = bf16_lo(w.y);
-          u[8 * ch + 3] = bf16_hi(w.y);
-          u[8 * ch + 4] = bf16_lo(w.z);
-          u[8 * ch + 5] = bf16_hi(w.z);
-          u[8 * ch + 6] = bf16_lo(w.w);
-          u[8 * ch + 7] = bf16_hi(w.w);
-        }
-        if (tensor ? p.rotate[1] : p.rotate[0]) rotate_row<H>(u, p.c_h);
         const int P = p.page_size;
         const int page = slot >> p.page_shift;
         const int off = slot & (P - 1);
         uint8_t* chunk = (tensor ? p.cache[1] : p.cache[0]) +
                          (int64_t(page) * hkv + hd) * int64_t(chunk_bytes(P));
-        const uint32_t meta =
-            quantize_store(u, reinterpret_cast<uint4*>(chunk + off * (kHeadDim / 2)));
-        *reinterpret_cast<uint32_t*>(chunk + P * (kHeadDim / 2) + 4 * off) = meta;
+        // local quarter 0 is G0 (h = 0) or G3 (h = 1); local quarter 1 is G1 /
+        // G2, or G2 / G1 after a stride-64 step; quarter g = code bytes 16g..
+        uint8_t* codes = chunk + off * (kHeadDim / 2);
+        const bool swapped = rot && H == kHeadDim;
+        const int q1 = h ? (swapped ? 1 : 2) : (swapped ? 2 : 1);
+        *reinterpret_cast<uint4*>(codes + (h ? 48 : 0)) =
+            make_uint4(word[0], word[1], word[2], word[3]);
+        *reinterpret_cast<uint4*>(codes + 16 * q1) = make_uint4(word[4], word[5], word[6], word[7]);
+        if (h == 0)
+          *reinterpret_cast<uint32_t*>(chunk + P * (kHeadDim / 2) + 4 * off) =
+              uint32_t(sb) | (uint32_t(zb) << 16);
       }
     }
-    __syncthreads();  // the buffer is refilled by the next-but-one issue
+    __syncwarp();  // the buffer is refilled by a later issue
   }
   cp_async_wait<0>();
 }
@@ -354,12 +444,13 @@ template <typename K>
 cudaError_t launch_tiled(K kernel, dim3 grid, cudaStream_t stream, const AppendParams& p,
                          int tiles_per_tensor, int num_tiles) {
   cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileBytes);
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTileWarps * kTileStages * kTileBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kTileRows);
-  cfg.dynamicSmemBytes = 2 * kTileBytes;
+  cfg.blockDim = dim3(kTileThreads);
+  cfg.dynamicSmemBytes = kTileWarps * kTileStages * kTileBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -394,7 +485,7 @@ cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaS
   if (e != cudaSuccess) return e;
   const int tiles_per_tensor = (num_rows + kTileRows - 1) / kTileRows;
   const int num_tiles = tiles_per_tensor * num_tensors;
-  const dim3 grid(std::min(num_tiles, sms * kTileCtasPerSm));
+  const dim3 grid(std::min((num_tiles + kTileWarps - 1) / kTileWarps, sms * kTileCtasPerSm));
   AppendParams q = p;
   q.num_tensors = num_tensors;
   int lg = 0;
