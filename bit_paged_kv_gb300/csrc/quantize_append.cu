@@ -63,12 +63,20 @@ __device__ __forceinline__ void bfly2(float& a0, float& a1, float& b0, float& b1
       : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
 }
 
-__device__ __forceinline__ void mul2(float& a0, float& a1, float c) {
-  asm("{\n\t.reg .b64 x, k;\n\t"
-      "mov.b64 x, {%0, %1};\n\tmov.b64 k, {%2, %2};\n\t"
-      "mul.rn.f32x2 x, x, k;\n\tmov.b64 {%0, %1}, x;\n\t}"
+// {a, b} as one 64-bit register pair, for the packed instructions' operands
+// that are the same for a whole row (built once, not per instruction).
+__device__ __forceinline__ uint64_t pair(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// (a0, a1) <- RN((a0, a1) * k)
+__device__ __forceinline__ void mul2(float& a0, float& a1, uint64_t k) {
+  asm("{\n\t.reg .b64 x;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmul.rn.f32x2 x, x, %2;\n\tmov.b64 {%0, %1}, x;\n\t}"
       : "+f"(a0), "+f"(a1)
-      : "f"(c));
+      : "l"(k));
 }
 
 __device__ __forceinline__ float min3(float a, float b, float c) {
@@ -103,28 +111,33 @@ __device__ __forceinline__ uint32_t div_rows(uint32_t n, uint32_t m, uint32_t sh
 // After a stride-64 step the lower thread's local 32..63 hold G2 and the
 // upper thread's hold G1.
 
-// (x0, x1) and (y0, y1) <- RN(sg * x + y) and RN(-sg * y + x).
+// (x0, x1) and (y0, y1) <- RN(sg * x + y) and RN(-sg * y + x), with
+// p = {sg, sg} and m = {-sg, -sg}.
 __device__ __forceinline__ void bfly2_signed(float& x0, float& x1, float& y0, float& y1,
-                                             float sg) {
-  asm("{\n\t.reg .b64 x, y, p, m, a, b;\n\t"
+                                             uint64_t p, uint64_t m) {
+  asm("{\n\t.reg .b64 x, y, a, b;\n\t"
       "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
-      "mov.b64 p, {%4, %4};\n\tmov.b64 m, {%5, %5};\n\t"
-      "fma.rn.f32x2 a, x, p, y;\n\tfma.rn.f32x2 b, y, m, x;\n\t"
+      "fma.rn.f32x2 a, x, %4, y;\n\tfma.rn.f32x2 b, y, %5, x;\n\t"
       "mov.b64 {%0, %1}, a;\n\tmov.b64 {%2, %3}, b;\n\t}"
       : "+f"(x0), "+f"(x1), "+f"(y0), "+f"(y1)
-      : "f"(sg), "f"(-sg));
+      : "l"(p), "l"(m));
 }
 
 // Butterfly of the row's H-blocks (strides 1, 2, ..., H/2 in ascending
 // order, every step an RN add or subtract), then one multiply by
-// c = binary32(1/sqrt(H)).
+// c = binary32(1/sqrt(H)).  The stride-1 step reads the bfloat16 pairs
+// straight from the loaded words: a mixed-precision add takes the even
+// element as bfloat16 (exact widening) and the odd one as binary32.
 template <int H>
-__device__ __forceinline__ void rotate_half(float (&u)[kHalfRow], float c, int h) {
+__device__ __forceinline__ void rotate_half(const uint32_t (&wd)[kHalfRow / 2],
+                                            float (&u)[kHalfRow], float c, int h) {
 #pragma unroll
-  for (int i = 0; i < kHalfRow; i += 2) {
-    const float a = u[i], b = u[i + 1];
-    u[i] = __fadd_rn(a, b);
-    u[i + 1] = __fsub_rn(a, b);
+  for (int i = 0; i < kHalfRow / 2; ++i) {
+    const float odd = bf16_hi(wd[i]);
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tsub.rn.f32.bf16 %1, lo, %3;\n\t}"
+        : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
+        : "r"(wd[i]), "f"(odd));
   }
 #pragma unroll
   for (int len = 2; len < (H < 32 ? H : 32); len *= 2) {
@@ -134,9 +147,10 @@ __device__ __forceinline__ void rotate_half(float (&u)[kHalfRow], float c, int h
     }
   }
   const float sg = h ? -1.0f : 1.0f;
+  const uint64_t sp = pair(sg, sg), sm = pair(-sg, -sg);
   if (H >= 64) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sg);
+    for (int j = 0; j < 32; j += 2) bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sp, sm);
   }
   if (H == 128) {
 #pragma unroll
@@ -145,11 +159,12 @@ __device__ __forceinline__ void rotate_half(float (&u)[kHalfRow], float c, int h
       const float o1 = __shfl_xor_sync(0xFFFFFFFFu, u[33 + j], 1);
       u[32 + j] = o0;
       u[33 + j] = o1;
-      bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sg);
+      bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sp, sm);
     }
   }
+  const uint64_t cc = pair(c, c);
 #pragma unroll
-  for (int i = 0; i < kHalfRow; i += 2) mul2(u[i], u[i + 1], c);
+  for (int i = 0; i < kHalfRow; i += 2) mul2(u[i], u[i + 1], cc);
 }
 
 // Min and max of the whole row: 64 values here, three at a time (exact),
@@ -189,27 +204,37 @@ __device__ __forceinline__ void quantize_half(const float (&u)[kHalfRow], float 
                                               bool fast, uint32_t (&word)[8]) {
   if (fast) {
     const float r24 = __fmul_rn(r, 5.9604644775390625e-08f);  // 2^-24
+    const uint64_t zz = pair(z, z), rr = pair(r24, r24);
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        v[e] = u[8 * w + e];
+        v[e + 1] = u[8 * w + e + 1];
+        asm("{\n\t.reg .b64 y;\n\t"
+            "mov.b64 y, {%0, %1};\n\t"
+            "sub.rn.f32x2 y, y, %2;\n\tmul.rn.f32x2 y, y, %3;\n\t"
+            "mov.b64 {%0, %1}, y;\n\t}"
+            : "+f"(v[e]), "+f"(v[e + 1])
+            : "l"(zz), "l"(rr));
+      }
+      // binary16 pairs (low half first): d[k] = c(a) | c(b) << 16 for
+      // (a, b) = (0, 2), (1, 3), (4, 6), (5, 7)
       uint32_t d[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v0 = u[8 * w + 2 * e], v1 = u[8 * w + 2 * e + 1];
-        asm("{\n\t.reg .b64 y, zz, rr;\n\t"
-            "mov.b64 y, {%0, %1};\n\tmov.b64 zz, {%2, %2};\n\tmov.b64 rr, {%3, %3};\n\t"
-            "sub.rn.f32x2 y, y, zz;\n\tmul.rn.f32x2 y, y, rr;\n\t"
-            "mov.b64 {%0, %1}, y;\n\t}"
-            : "+f"(v0), "+f"(v1)
-            : "f"(z), "f"(r24));
-        const __half2 hv = __floats2half2_rn(v0, v1);  // .x (low half) = code of v0
-        d[e] = *reinterpret_cast<const uint32_t*>(&hv);
+      for (int k = 0; k < 4; ++k) {
+        const int a = (k & 1) + 4 * (k >> 1);
+        const __half2 hv = __floats2half2_rn(v[a], v[a + 2]);
+        d[k] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      // d[e] = c(2e) | c(2e+1) << 16
-      const uint32_t x = prmt(d[0], d[1], 0x6240u);  // c0 c2 c1 c3
-      const uint32_t y = prmt(d[2], d[3], 0x6240u);  // c4 c6 c5 c7
-      const uint32_t even = prmt(x, y, 0x5410u);     // c0 c2 c4 c6
-      const uint32_t odd = prmt(x, y, 0x7632u);      // c1 c3 c5 c7
-      word[w] = even | (odd << 4);
+      // bytes 0 and 2 of x: (c0 c1), (c2 c3); of y: (c4 c5), (c6 c7).  A code
+      // of -0 (y = -0, z = +0) converts to 0x8000: its sign bit stays in the
+      // discarded bytes 1 and 3 of d[0], d[2], and is masked off after the
+      // shift for d[1], d[3].
+      const uint32_t x = d[0] | ((d[1] << 4) & 0x00F000F0u);
+      const uint32_t y = d[2] | ((d[3] << 4) & 0x00F000F0u);
+      word[w] = prmt(x, y, 0x6420u);
     }
   } else {
 #pragma unroll
@@ -316,7 +341,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
 
     // Every thread computes (rows past the end or without a slot on stale
     // data) so that the pair shuffles run converged; only stores are guarded.
-    float u[kHalfRow];
+    uint32_t wd[kHalfRow / 2];  // this thread's 64 bfloat16 values, in pairs
     {
       // local chunk j of thread h: chunk j (h = 0), chunk 8 + (j ^ 4) (h = 1)
       const uint8_t* rowp = buf + r * kRowBytes + h * (kRowBytes / 2);
@@ -324,18 +349,23 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((j ^ x) << 4));
-        u[8 * j + 0] = bf16_lo(w.x);
-        u[8 * j + 1] = bf16_hi(w.x);
-        u[8 * j + 2] = bf16_lo(w.y);
-        u[8 * j + 3] = bf16_hi(w.y);
-        u[8 * j + 4] = bf16_lo(w.z);
-        u[8 * j + 5] = bf16_hi(w.z);
-        u[8 * j + 6] = bf16_lo(w.w);
-        u[8 * j + 7] = bf16_hi(w.w);
+        wd[4 * j + 0] = w.x;
+        wd[4 * j + 1] = w.y;
+        wd[4 * j + 2] = w.z;
+        wd[4 * j + 3] = w.w;
       }
     }
+    float u[kHalfRow];
     const bool rot = tensor ? p.rotate[1] != 0 : p.rotate[0] != 0;
-    if (rot) rotate_half<H>(u, p.c_h, h);
+    if (rot) {
+      rotate_half<H>(wd, u, p.c_h, h);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kHalfRow / 2; ++i) {
+        u[2 * i] = bf16_lo(wd[i]);
+        u[2 * i + 1] = bf16_hi(wd[i]);
+      }
+    }
     float mn, mx;
     half_min_max(u, mn, mx);
     const uint16_t zb = f16_round_down_sat(mn);
