@@ -12,16 +12,18 @@
 //  * One 16-warp CTA per (split of the context, kv-head, sequence), one CTA
 //    per SM.  The whole GQA group of the kv-head is served by the CTA, so
 //    each page is read from HBM once, and q is rotated once per CTA.
-//  * The split is consumed in 32-token steps; warp w takes steps w, w+16, ...
-//    through a private two-stage shared-memory ring filled by the bulk-copy
-//    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds the step's
-//    K and V codes and their (scale, zero) words: two 16-token pages, or 32
-//    rows of a larger page (codes and metadata copied separately).
+//  * The split is cut into 16-token tiles; warp w takes tiles w, w+16, ...
+//    through a private four-stage shared-memory ring filled by the bulk-copy
+//    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds one tile's
+//    K and V codes and their (scale, zero) words: a whole 16-token page, or
+//    16 rows of a larger page (codes and metadata copied separately).  A warp
+//    consumes its tiles two at a time; the two share one softmax update.
 //  * Scores: S = K~ q' on the tensor cores (mma.m16n8k16, binary16 in,
 //    binary32 accumulate), 16 tokens on M, q-heads on N, the head dimension
-//    on K.  K~ are the raw codes 0..15, exact in binary16, converted in
-//    registers with the 0x6400 exponent trick; the per-token scale and zero
-//    are applied afterwards: t = s*(K~.q') + z*sum(q').
+//    on K.  K~ are the raw codes, masked in place into binary16 subnormals
+//    (n * 2^-24 or n * 2^-20, exact); q' carries the matching power of two.
+//    The per-token scale and zero are applied afterwards:
+//    t = s*(K~.q') + z*sum(q').
 //  * Output: O'^T += V~^T (p*s) on the tensor cores, dims on M, tokens on K,
 //    heads on N, plus sum_j p_j z_j on the CUDA cores.  p*s is moved from the
 //    score fragment to the B-operand layout with four warp shuffles.
@@ -32,6 +34,8 @@
 //    split of a (sequence, kv-head) to finish merges them, normalizes and
 //    applies the inverse rotation to V's output.  With one split the CTA
 //    finishes the row itself.  No CTA waits for another.
+#include <type_traits>
+
 #include "saw_device.cuh"
 #include "saw_int4.h"
 #include "saw_quant_row.cuh"
@@ -73,8 +77,8 @@ struct Cfg {
   static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][4]
   static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [16][kIdCap]
   static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8][128]
-  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [8]
-  static constexpr int kOffFlag = kOffQsum + kMaxGroup * 4;                   // int
+  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [2][8]
+  static constexpr int kOffFlag = kOffQsum + 2 * kMaxGroup * 4;               // int
   static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (64 code bytes, meta)
   static constexpr int kSmem = kOffNew + 2 * (kCodeRow + 16);
 };
@@ -99,20 +103,11 @@ __device__ void smem_fwht(float* buf, int nvec, int h) {
   }
 }
 
-__device__ __forceinline__ uint32_t hsub_1024(uint32_t x) {
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  h = __hsub2(h, __half2half2(__ushort_as_half(0x6400)));
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// (1024 + 16 n) / 16 - 64 = n, exact in binary16
-__device__ __forceinline__ uint32_t hfma_hi(uint32_t x) {
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  h = __hfma2(h, __half2half2(__ushort_as_half(0x2C00)), __half2half2(__ushort_as_half(0xD400)));
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-constexpr uint32_t kMagic = 0x64006400u;  // binary16 1024.0 in both halves
+// Codes enter the MMAs as binary16 subnormals: a nibble n masked in place at
+// bits 0-3 of a half is n * 2^-24, at bits 4-7 it is n * 2^-20 -- exact, with
+// no offset to remove.  The other operand carries the matching power of two.
+constexpr uint32_t kLoNib = 0x000F000Fu;  // bits 0-3 of both halves
+constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 
 __device__ __forceinline__ float half_lo(uint32_t w) {
   return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
@@ -265,11 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   const int new_local = new_tok - p_begin * P;
   const int new_step = owner ? new_local / kStepTok : -1;
 
-  // ---- b = 4 q', q' = (1/sqrt h) H q for the group's heads, as binary16 hi
-  // + lo parts (b = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8
-  // rotates head h, lane l holding elements 4l..4l+3.  sm_scale*log2(e) is
-  // applied to the binary32 score, so an unrotated q enters the MMA exactly
-  // (4 q is exact in binary16).
+  // ---- b = 2^S q', q' = (1/sqrt h) H q for the group's heads, as binary16
+  // hi + lo parts (b = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8
+  // rotates head h, lane l holding elements 4l..4l+3.  S is per head, the
+  // largest with |b| < 2^14, and odd elements get 2^(S-4): they meet the
+  // high nibbles (n * 2^-20) and even ones the low nibbles (n * 2^-24), so
+  // every product is n q' 2^(S-24).  sm_scale*log2(e) is applied to the
+  // binary32 score, so an unrotated q enters the MMA exactly.
   __half* qh_hi = qh;
   __half* qh_lo = qh + kMaxGroup * kHeadDim;
   if (warp < kMaxGroup) {
@@ -302,21 +299,30 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] *= p.c_h;
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] *= 4.0f;
     }
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int x2 = 16; x2 >= 1; x2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, x2));
+    int ex;
+    frexpf(amax, &ex);                       // amax < 2^ex (ex = 0 for amax = 0)
+    const int S = min(max(14 - ex, -100), 100);
     float part = 0.0f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const __half hi = __float2half_rn(x[e]);
-      const __half lo = __float2half_rn(x[e] - __half2float(hi));
+      const int se = (e & 1) ? S - 4 : S;
+      const float y = ldexpf(x[e], se);
+      const __half hi = __float2half_rn(y);
+      const __half lo = __float2half_rn(y - __half2float(hi));
       qh_hi[h * kHeadDim + 4 * lane + e] = hi;
       qh_lo[h * kHeadDim + 4 * lane + e] = lo;
-      part += __half2float(hi) + __half2float(lo);
+      part += ldexpf(__half2float(hi) + __half2float(lo), -se);
     }
 #pragma unroll
     for (int x2 = 16; x2 >= 1; x2 >>= 1) part += __shfl_xor_sync(kFull, part, x2);
-    if (lane == 0) qsum[h] = part;
+    if (lane == 0) {
+      qsum[h] = part;
+      qsum[kMaxGroup + h] = ldexpf(1.0f, 24 - S);
+    }
   }
   __syncthreads();
 
@@ -344,14 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       }
     }
   }
-  // this thread's two heads.  The codes enter the score MMA as 1024 + 16 n
-  // (one LOP3 per two codes, no subtraction), so with b = 4 q' the MMA gives
-  // acc = 1024 sum(b) + 64 (n . q').  The constant is removed in binary32
-  // together with the zero term:  t = sm'*(s (n.q') + z sum(q'))
-  //   = (sm' s / 64) acc + (sm' sum(b) / 4) (z - 64 s).
+  // this thread's two heads: the MMA gives acc = 2^(S-24) (n . q'), so the
+  // base-2 logit t = sm'*(s (n.q') + z sum(q')) = (sm' 2^(24-S) s) acc +
+  // (sm' sum(q')) z.
   const int hb = PACKED ? 2 * (c & 1) : 2 * c;
-  const float qsA = qsum[hb] * (0.25f * p.q_scale), qsB = qsum[hb + 1] * (0.25f * p.q_scale);
-  const float sk_scale = p.q_scale * (1.0f / 64.0f);
+  const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
+  const float skA = qsum[kMaxGroup + hb] * p.q_scale, skB = qsum[kMaxGroup + hb + 1] * p.q_scale;
 
   float acc[8][4];
 #pragma unroll
@@ -360,42 +364,52 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   float l_run[2] = {0.0f, 0.0f};
   float z_run[2] = {0.0f, 0.0f};
   bool failed = false;
-  int waited = 0;
+  int waited = 0;  // first of this warp's tiles not yet consumed
 
-  for (int i = 0; i < n_my; ++i) {
-    const int s = i % kStages;
-    const bool ok = mbar_wait_bounded(&wbars[s], (i / kStages) & 1);
-    if (!__all_sync(kFull, ok)) {
-      failed = true;
-      break;
-    }
-    waited = i + 1;
-    const uint8_t* st = ring + s * C::kStage;
-    const int tok0 = p_begin * P + (warp + i * kWarps) * kStepTok;
-    if (APPEND && warp + i * kWarps == new_step) {
-      // replace the copied row of the new token by its freshly quantized one
-      const int row = new_local % kStepTok;
-      uint8_t* w = ring + s * C::kStage;
-      if (lane < 16) {
-        const int tensor = lane >> 3, part = lane & 7;  // 8 x 8 bytes per tensor
-        const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
-        uint8_t* dst = w + (tensor ? C::kHalf : 0) + C::kcode(row);
-        reinterpret_cast<uint2*>(dst)[part] = reinterpret_cast<const uint2*>(nr)[part];
-      } else if (lane < 18) {
-        const int tensor = lane - 16;
-        const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
-        *reinterpret_cast<uint32_t*>(w + (tensor ? C::kHalf : 0) + C::kmeta(row)) =
-            *reinterpret_cast<const uint32_t*>(nr + kCodeRow);
+  // One step consumes NT consecutive tiles of this warp (i, i+1, ...): the
+  // tiles' score products and PV products are independent, and they share
+  // one max reduction and one rescale of the online softmax.
+  auto step = [&](auto ntc, int i) -> bool {
+    constexpr int NT = decltype(ntc)::value;
+    waited = i;
+    bool ok = true;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      ok = mbar_wait_bounded(&wbars[(i + t) % kStages], ((i + t) / kStages) & 1) && ok;
+    if (!__all_sync(kFull, ok)) return false;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (APPEND && warp + (i + t) * kWarps == new_step) {
+        // replace the copied row of the new token by its freshly quantized one
+        const int row = new_local % kStepTok;
+        uint8_t* w = ring + ((i + t) % kStages) * C::kStage;
+        if (lane < 16) {
+          const int tensor = lane >> 3, part = lane & 7;  // 8 x 8 bytes per tensor
+          const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
+          uint8_t* dst = w + (tensor ? C::kHalf : 0) + C::kcode(row);
+          reinterpret_cast<uint2*>(dst)[part] = reinterpret_cast<const uint2*>(nr)[part];
+        } else if (lane < 18) {
+          const int tensor = lane - 16;
+          const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
+          *reinterpret_cast<uint32_t*>(w + (tensor ? C::kHalf : 0) + C::kmeta(row)) =
+              *reinterpret_cast<const uint32_t*>(nr + kCodeRow);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
-    const bool pok = wok[s] != 0;
-    const bool v0 = pok && (tok0 + g) < L;
-    const bool v1 = pok && (tok0 + g + 8) < L;
 
-    // ---- scores of the 16 tokens
-    float sc[4];
-    {
+    // ---- scores of the NT x 16 tokens
+    float sc[NT][4];
+    bool v0[NT], v1[NT], full[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int s_ = (i + t) % kStages;
+      const uint8_t* st = ring + s_ * C::kStage;
+      const int tok0 = p_begin * P + (warp + (i + t) * kWarps) * kStepTok;
+      const bool pok = wok[s_] != 0;
+      v0[t] = pok && (tok0 + g) < L;
+      v1[t] = pok && (tok0 + g + 8) < L;
+      full[t] = pok && tok0 + kStepTok <= L;  // warp-uniform
       const uint8_t* krow = st + C::kcode(g) + 16 * c;
       const uint4 ka = *reinterpret_cast<const uint4*>(krow);
       const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow);
@@ -408,15 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       for (int w = 0; w < 4; ++w) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          // every nibble moved to bits 4-7 / 20-23 of its binary16 half:
-          // low nibbles of bytes (0,2) by << 4, of bytes (1,3) by >> 4;
-          // high nibbles of bytes (1,3) by >> 8
-          const uint32_t wa = kaw[w], wb = kbw[w];
+          // bytes (0,2) in place, bytes (1,3) moved down by 8: low nibbles
+          // for columns 2c, 2c+1, high nibbles for 2c+8, 2c+9
+          const uint32_t wa = hh ? (kaw[w] >> 8) : kaw[w];
+          const uint32_t wb = hh ? (kbw[w] >> 8) : kbw[w];
           uint32_t a[4];
-          a[0] = and_or(hh ? (wa >> 4) : (wa << 4), 0x00F000F0u, kMagic);
-          a[1] = and_or(hh ? (wb >> 4) : (wb << 4), 0x00F000F0u, kMagic);
-          a[2] = and_or(hh ? (wa >> 8) : wa, 0x00F000F0u, kMagic);
-          a[3] = and_or(hh ? (wb >> 8) : wb, 0x00F000F0u, kMagic);
+          a[0] = wa & kLoNib;
+          a[1] = wb & kLoNib;
+          a[2] = wa & kHiNib;
+          a[3] = wb & kHiNib;
           float (&dst)[4] = hh ? e2 : d;
           mma_16816(dst, a, bq[2 * w + hh][0], bq[2 * w + hh][1]);
           if (!PACKED) mma_16816(dst, a, bl[PACKED ? 0 : 2 * w + hh][0], bl[PACKED ? 0 : 2 * w + hh][1]);
@@ -430,16 +444,27 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       }
       const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g));
       const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8));
-      const float sk0 = half_lo(mk0) * sk_scale, zk0 = fmaf(-64.0f, half_lo(mk0), half_hi(mk0));
-      const float sk1 = half_lo(mk1) * sk_scale, zk1 = fmaf(-64.0f, half_lo(mk1), half_hi(mk1));
-      sc[0] = v0 ? fmaf(sk0, d[0], zk0 * qsA) : -INFINITY;
-      sc[1] = v0 ? fmaf(sk0, d[1], zk0 * qsB) : -INFINITY;
-      sc[2] = v1 ? fmaf(sk1, d[2], zk1 * qsA) : -INFINITY;
-      sc[3] = v1 ? fmaf(sk1, d[3], zk1 * qsB) : -INFINITY;
+      const float s0 = half_lo(mk0), z0 = half_hi(mk0);
+      const float s1 = half_lo(mk1), z1 = half_hi(mk1);
+      sc[t][0] = fmaf(s0 * skA, d[0], z0 * qsA);
+      sc[t][1] = fmaf(s0 * skB, d[1], z0 * qsB);
+      sc[t][2] = fmaf(s1 * skA, d[2], z1 * qsA);
+      sc[t][3] = fmaf(s1 * skB, d[3], z1 * qsB);
+      if (!full[t]) {  // the tile holding the end of the sequence, or a bad page
+        sc[t][0] = v0[t] ? sc[t][0] : -INFINITY;
+        sc[t][1] = v0[t] ? sc[t][1] : -INFINITY;
+        sc[t][2] = v1[t] ? sc[t][2] : -INFINITY;
+        sc[t][3] = v1[t] ? sc[t][3] : -INFINITY;
+      }
     }
 
     // ---- online softmax: rescale only when a running max grows
-    float mloc0 = fmaxf(sc[0], sc[2]), mloc1 = fmaxf(sc[1], sc[3]);
+    float mloc0 = fmaxf(sc[0][0], sc[0][2]), mloc1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+    for (int t = 1; t < NT; ++t) {
+      mloc0 = fmaxf(mloc0, fmaxf(sc[t][0], sc[t][2]));
+      mloc1 = fmaxf(mloc1, fmaxf(sc[t][1], sc[t][3]));
+    }
 #pragma unroll
     for (int x = 4; x < 32; x <<= 1) {
       mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
@@ -466,28 +491,30 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
     const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
 
-    // ---- probabilities, V terms, and the PV product
-    {
-      const uint8_t* vst = st + C::kHalf;
-      const float p0 = ex2(sc[0] - mu0), p1 = ex2(sc[1] - mu1);
-      const float p2 = ex2(sc[2] - mu0), p3 = ex2(sc[3] - mu1);
+    // ---- probabilities, V terms, and the PV products
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* vst = ring + ((i + t) % kStages) * C::kStage + C::kHalf;
+      const float p0 = ex2(sc[t][0] - mu0), p1 = ex2(sc[t][1] - mu1);
+      const float p2 = ex2(sc[t][2] - mu0), p3 = ex2(sc[t][3] - mu1);
       const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g));
       const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8));
-      const float sv0 = v0 ? half_lo(mv0) : 0.0f, zv0 = v0 ? half_hi(mv0) : 0.0f;
-      const float sv1 = v1 ? half_lo(mv1) : 0.0f, zv1 = v1 ? half_hi(mv1) : 0.0f;
+      float sv0 = half_lo(mv0), zv0 = half_hi(mv0);
+      float sv1 = half_lo(mv1), zv1 = half_hi(mv1);
+      if (!full[t]) {  // rows past the end may hold anything, even inf
+        sv0 = v0[t] ? sv0 : 0.0f;
+        zv0 = v0[t] ? zv0 : 0.0f;
+        sv1 = v1[t] ? sv1 : 0.0f;
+        zv1 = v1[t] ? zv1 : 0.0f;
+      }
       l_run[0] += p0 + p2;
       l_run[1] += p1 + p3;
       z_run[0] += p0 * zv0 + p2 * zv1;
       z_run[1] += p1 * zv0 + p3 * zv1;
-      // (p*s) for this thread's columns over tokens (g, g+8); PACKED lanes
-      // c >= 2 carry the binary16 remainder (lo part)
-      float ps0 = p0 * sv0, ps1 = p1 * sv0, ps2 = p2 * sv1, ps3 = p3 * sv1;
-      if (PACKED && c >= 2) {
-        ps0 -= __half2float(__float2half_rn(ps0));
-        ps1 -= __half2float(__float2half_rn(ps1));
-        ps2 -= __half2float(__float2half_rn(ps2));
-        ps3 -= __half2float(__float2half_rn(ps3));
-      }
+      // (p*s) for this thread's columns over tokens (g, g+8) as binary16.
+      // PACKED: lanes c >= 2 repeat the heads of lanes c - 2, so output
+      // columns 4-7 duplicate 0-3 and are never read.
+      const float ps0 = p0 * sv0, ps1 = p1 * sv0, ps2 = p2 * sv1, ps3 = p3 * sv1;
       const uint32_t X = pack_half2(ps0, ps2);
       const uint32_t Y = pack_half2(ps1, ps3);
       const int src0 = 8 * c + (g >> 1);
@@ -515,16 +542,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
         const uint32_t x01 = prmt(w0, w1, sel);
         const uint32_t x23 = prmt(w2, w3, sel);
         uint32_t a[4];
-        a[0] = hsub_1024(and_or(x01, 0x000F000Fu, kMagic));
-        a[1] = hfma_hi(and_or(x01, 0x00F000F0u, kMagic));
-        a[2] = hsub_1024(and_or(x23, 0x000F000Fu, kMagic));
-        a[3] = hfma_hi(and_or(x23, 0x00F000F0u, kMagic));
+        a[0] = x01 & kLoNib;  // dims of rows g: n * 2^-24
+        a[1] = x01 & kHiNib;  // dims of rows g + 8: n * 2^-20
+        a[2] = x23 & kLoNib;
+        a[3] = x23 & kHiNib;
         mma_16816(acc[k], a, b0, b1);
       }
     }
 
     __syncwarp();
-    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        if (i + t + kStages < n_my) issue(i + t + kStages);
+    }
+    return true;
+  };
+
+  {
+    int i = 0;
+    for (; i + 1 < n_my; i += 2) {
+      if (!step(std::integral_constant<int, 2>{}, i)) {
+        failed = true;
+        break;
+      }
+    }
+    if (!failed && i < n_my && !step(std::integral_constant<int, 1>{}, i)) failed = true;
   }
 
   if (failed) {
@@ -534,8 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       (void)mbar_wait_bounded(&wbars[i % kStages], (i / kStages) & 1);
   }
 
-  // ---- cross-thread reductions of l and the z term (lanes sharing c), and
-  // of the hi/lo column halves in PACKED mode
+  // ---- cross-thread reductions of l and the z term (lanes sharing c)
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
     l_run[0] += __shfl_xor_sync(kFull, l_run[0], x);
@@ -543,12 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
     z_run[0] += __shfl_xor_sync(kFull, z_run[0], x);
     z_run[1] += __shfl_xor_sync(kFull, z_run[1], x);
   }
-  if (PACKED) {
+  // output rows g (even dims) carried n * 2^-24, rows g + 8 (odd) n * 2^-20
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[k][j] += __shfl_xor_sync(kFull, acc[k][j], 2);
-    }
+  for (int k = 0; k < 8; ++k) {
+    acc[k][0] *= 16777216.0f;
+    acc[k][1] *= 16777216.0f;
+    acc[k][2] *= 1048576.0f;
+    acc[k][3] *= 1048576.0f;
   }
   __syncthreads();  // every warp is done with its ring: reuse it
 

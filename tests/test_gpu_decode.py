@@ -104,7 +104,7 @@ def test_explicit_sm_scale():
     ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads,
                         npages, wl.page_size, True, True, 128, sm_scale=0.3)
     assert st == 0
-    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) <= ATTN_TOL
+    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref, "tiny-sm_scale-0.3") <= ATTN_TOL
 
 
 def test_rotation_mismatch_is_detectable():
@@ -154,7 +154,7 @@ def test_workspace_reuse_across_calls_and_plans():
                                   out, ws, pages_per_split=pps, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        assert rel_err(out.cpu().numpy().reshape(-1, 128), ref) <= ATTN_TOL
+        assert rel_err(out.cpu().numpy().reshape(-1, 128), ref, f"tiny-ws-reuse-pps{pps}") <= ATTN_TOL
     n_tickets = B * wl.num_kv_heads
     assert torch.all(ws[:4 * n_tickets].view(torch.int32) == 0)
 

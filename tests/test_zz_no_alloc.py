@@ -65,7 +65,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         assert rc == saw.SAW_OK and st2 == 0
         g, r = got.cpu().numpy(), ref.cpu().numpy()
         assert np.all(np.isfinite(g))
-        assert rel_err(g.reshape(-1, 128), r.reshape(-1, 128)) <= ATTN_TOL
+        assert rel_err(g.reshape(-1, 128), r.reshape(-1, 128), "noalloc-vs-decode") <= ATTN_TOL
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
