@@ -319,6 +319,83 @@ def append_chunk_measure(device, stream, iters: int = 20):
     return res, nbytes, T
 
 
+def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
+    """One layer's K and V caches holding every token of every sequence,
+    written by the library's quantize-append (seeded synthetic rows)."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    P = wl.page_size
+    lens_l = [int(x) for x in lens.tolist()]
+    total = sum(lens_l)
+    nb = saw.saw_cache_bytes(npages, P, wl.num_kv_heads, wl.head_dim)
+    kc = torch.empty(nb, dtype=torch.uint8, device=device)
+    vc = torch.empty(nb, dtype=torch.uint8, device=device)
+    slots = W.prefill_slots(bt.to(device), lens_l, P)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    for a in range(0, total, chunk_tokens):
+        b = min(total, a + chunk_tokens)
+        k = W.kv_rows(wl, layer, W.K, b - a, device, token_offset=a)
+        v = W.kv_rows(wl, layer, W.V, b - a, device, token_offset=a)
+        saw.saw_quantize_append(k, v, slots[a:b], kc, vc, npages, P, wl.rotate_k, wl.rotate_v,
+                                wl.block_h, dev_status=status)
+        del k, v
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return kc, vc
+
+
+def decode_config_measure(device, stream, layers: int = 2, reps: int = 10):
+    """Decode-only throughput of the bandwidth-bound workloads (Qwen3-8B
+    concurrent, Qwen3-32B high concurrency in its three rotation variants,
+    long context at h 128 and 64): `layers` distinct layer caches (each
+    larger than L2) decoded in turn, CUDA events around reps passes."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    c32 = W.QWEN3_32B_HIGH_CONCURRENCY
+    cases = [("qwen3-8b-concurrent", W.QWEN3_8B_CONCURRENT),
+             ("qwen3-32b-high-concurrency k+v", c32),
+             ("qwen3-32b-high-concurrency k-only", c32.variant(rotate_k=True, rotate_v=False)),
+             ("qwen3-32b-high-concurrency unrotated", c32.variant(rotate_k=False, rotate_v=False)),
+             ("long-131072 h128", W.LONG_PREFILL),
+             ("long-131072 h64", W.LONG_PREFILL.variant(block_h=64))]
+    res = {}
+    for name, wl in cases:
+        lens = W.seq_lens(wl)
+        bt, npages = W.page_tables(wl, lens)
+        btd, lensd = bt.to(device), lens.to(device)
+        B, Hq, D = wl.num_seqs, wl.num_q_heads, wl.head_dim
+        Lmax = int(lens.max())
+        caches = [fill_caches(wl, l, lens, bt, npages, device) for l in range(layers)]
+        qs = [W.q_rows(wl, l, device) for l in range(layers)]
+        wsb = saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, 0)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def one_pass():
+            for l in range(layers):
+                saw.saw_paged_decode_int4(qs[l], caches[l][0], caches[l][1], btd, lensd, Lmax,
+                                          wl.num_kv_heads, npages, wl.page_size, wl.rotate_k,
+                                          wl.rotate_v, wl.block_h, out, ws, dev_status=status)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                one_pass()
+            t = statistics.median(time_events(one_pass, reps, stream)) / layers
+        assert int(status.item()) == 0
+        nbytes = W.decode_bytes(wl, lens.tolist())
+        splits, pps = saw.saw_decode_plan(B, wl.num_kv_heads, wl.page_size, Lmax, 0)
+        res[name] = {"ms_per_layer": t, "gbs": nbytes / (t * 1e-3) / 1e9,
+                     "bytes_per_layer": nbytes, "splits": splits, "pages_per_split": pps,
+                     "seqs": B, "tokens": int(lens.sum())}
+        del caches, qs, ws, out
+        torch.cuda.empty_cache()
+    a = res["qwen3-32b-high-concurrency k+v"]["ms_per_layer"]
+    k1 = res["qwen3-32b-high-concurrency k-only"]["ms_per_layer"]
+    u = res["qwen3-32b-high-concurrency unrotated"]["ms_per_layer"]
+    overhead = {"k+v_vs_unrotated": a / u - 1.0, "k-only_vs_unrotated": k1 / u - 1.0}
+    return res, overhead
+
+
 def cpu_oracle_decode_sample(case, layers, threads):
     """Time the oracle (as it stands) on the step's work for `layers`:
     append the new token, then decode every q-head over the layer's pages."""
@@ -432,6 +509,8 @@ def run_saw(args):
 
     # quantize-append of a 131072-token prefill chunk
     app, app_bytes, app_T = append_chunk_measure(device, stream)
+    # decode alone on the bandwidth-bound workloads
+    dec_cfg, dec_rot = (None, None) if args.no_decode_configs else decode_config_measure(device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -492,6 +571,13 @@ def run_saw(args):
                          "bytes_per_launch": app_bytes},
             "variants": app,
             "rotation_overhead": app["rotated_h128"]["ms"] / app["unrotated"]["ms"] - 1.0,
+        },
+        "decode_configs": None if dec_cfg is None else {
+            "what": "saw_paged_decode_int4 alone, automatic split plan, distinct layer caches "
+                    "decoded in turn (each larger than L2); GB/s = algorithmic bytes / time",
+            "peak": peak,
+            "results": {k: dict(v, frac=v["gbs"] / peak) for k, v in dec_cfg.items()},
+            "rotation_overhead": dec_rot,
         },
         "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -603,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["saw", "reference"], default="saw")
     ap.add_argument("--cpu-layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode-configs", action="store_true",
+                    help="skip the decode-only measurements of the other workloads")
     ap.add_argument("--profile", choices=["decode", "append"], default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)

@@ -106,6 +106,12 @@ __device__ void smem_fwht(float* buf, int nvec, int h) {
 // Codes enter the MMAs as binary16 subnormals: a nibble n masked in place at
 // bits 0-3 of a half is n * 2^-24, at bits 4-7 it is n * 2^-20 -- exact, with
 // no offset to remove.  The other operand carries the matching power of two.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 constexpr uint32_t kLoNib = 0x000F000Fu;  // bits 0-3 of both halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 
@@ -577,6 +583,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       (void)mbar_wait_bounded(&wbars[i % kStages], (i / kStages) & 1);
   }
 
+  // ---- merge protocol, part 1: with several splits, count this one as
+  // arrived.  From here on it finishes without waiting for anyone, which is
+  // what lets the last arrival wait for the others' partials below.  The
+  // returned count is needed only after the CTA's own reduction, so the
+  // round trip overlaps it.
+  const int ns = (n_pages + p.pages_per_split - 1) / p.pages_per_split;  // splits with pages
+  uint32_t* tk = p.tickets + 2 * (int64_t(seq) * p.num_kv_heads + kvh);  // {arrived, published}
+  uint32_t arrived = 0;
+  if (!direct && tid == 0)
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(tk) : "memory");
+
   // ---- cross-thread reductions of l and the z term (lanes sharing c)
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
@@ -649,52 +666,68 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       tot[2 * kMaxGroup + h] = M;
     }
   }
+  if (!direct && tid == 0) {
+    // merge protocol, part 2: the split whose arrival completes the count
+    // merges; every other split publishes its partial
+    const uint32_t done = arrived + 1u;
+    if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
+    *flag = (done == uint32_t(ns));
+  }
   __syncthreads();
+  const bool last = !direct && *flag != 0;
   for (int idx = tid; idx < G * kHeadDim; idx += kThreads) {
     const int h = idx / kHeadDim, dd = idx - h * kHeadDim;
     float num = tot[kMaxGroup + h];
-    for (int w = 0; w < nw; ++w)
-      num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * wgt[w * kMaxGroup + h];
-    const float den = tot[h], M = tot[2 * kMaxGroup + h];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (w < nw) num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * wgt[w * kMaxGroup + h];
     if (direct) {
+      const float den = tot[h];
       qs[h * kHeadDim + dd] = (den > 0.0f) ? num / den : 0.0f;
+    } else if (last) {
+      qs[h * kHeadDim + dd] = num;  // this split's partial stays here; den, M in tot
     } else {
       const int64_t row = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits + split;
       p.part_o[row * kHeadDim + dd] = num;
       if (dd == 0) {
-        p.part_ml[2 * row] = M;
-        p.part_ml[2 * row + 1] = den;
+        p.part_ml[2 * row] = tot[2 * kMaxGroup + h];
+        p.part_ml[2 * row + 1] = tot[h];
       }
     }
   }
 
   if (!direct) {
-    // ---- the last split of this (sequence, kv-head) to finish merges them
-    // all: one launch covers the decode, and no CTA ever waits for another.
     __syncthreads();
-    const int ns = (n_pages + p.pages_per_split - 1) / p.pages_per_split;
+    if (!last) {
+      // publish: release (cumulative over the barrier above) orders this
+      // CTA's partials before the count the merging split waits for
+      if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(tk + 1) : "memory");
+      return;
+    }
+    // ---- the last split to arrive: wait (bounded) until every other split
+    // has published, then merge all partials, its own from shared memory
     if (tid == 0) {
-      // release (cumulative over the CTA barrier above): this CTA's partials
-      // are visible before its ticket; acquire: the other splits' partials
-      // are read after it
-      uint32_t* ticket = p.tickets + (int64_t(seq) * p.num_kv_heads + kvh);
-      uint32_t prev;
-      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(ticket)
-                   : "memory");
-      const uint32_t done = prev + 1u;
-      *flag = (done == uint32_t(ns));
-      if (done >= uint32_t(ns)) {
-        if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
-        *ticket = 0u;  // every split has counted: ready for the next call
+      const uint32_t want = uint32_t(ns - 1);
+      bool ok = ld_acquire_u32(tk + 1) == want;
+      if (!ok) {
+        const long long t0 = clock64();
+        while (!(ok = (ld_acquire_u32(tk + 1) == want))) {
+          if (clock64() - t0 > kWaitLimitCycles) break;
+          __nanosleep(32);
+        }
       }
+      if (ok) {
+        tk[0] = 0u;  // every split has counted and published: ready for the next call
+        tk[1] = 0u;
+      } else {
+        report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+      }
+      *flag = ok ? 1 : 0;
     }
     __syncthreads();
-    if (*flag == 0) return;
+    const bool merge_ok = *flag != 0;
     // item = (head, 4 dims); four threads per item share the splits.  Every
-    // load is issued before any is used (one round of L2 latency); thread 0's
-    // fences around the ticket order them after the other splits' writes.
+    // load is issued before any is used (one round of L2 latency).
     constexpr int kMaxSplitsPerThread = 8;
     for (int base = 0; base < G * 32 * 4; base += kThreads) {
       const int t = base + tid;
@@ -704,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       const int64_t row0 = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits;
       const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row0;
       const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kHeadDim) + ch;
+      const float4* own = reinterpret_cast<const float4*>(qs + h * kHeadDim) + ch;
       float M = -INFINITY;
       float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       float den = 0.0f;
@@ -713,9 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
 #pragma unroll
         for (int u = 0; u < kMaxSplitsPerThread; ++u) {
           const int sp = sp0 + 4 * u;
-          const bool in = active && sp < ns;
-          v[u] = in ? __ldcg(&ml[sp]) : make_float2(-INFINITY, 0.0f);
-          o[u] = in ? __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          const bool mine = sp == split;
+          const bool in = active && sp < ns && (mine || merge_ok);
+          v[u] = !in ? make_float2(-INFINITY, 0.0f)
+                     : mine ? make_float2(tot[2 * kMaxGroup + h], tot[h]) : __ldcg(&ml[sp]);
+          o[u] = !in ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                     : mine ? *own : __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]);
         }
         float Mb = -INFINITY;
 #pragma unroll

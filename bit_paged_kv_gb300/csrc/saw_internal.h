@@ -50,7 +50,7 @@ struct DecodeParams {
   float* out;                   // [B][Hq][D]
   float* part_o;                // [B][Hq][num_splits][D]
   float* part_ml;               // [B][Hq][num_splits][2]
-  uint32_t* tickets;            // [B][Hkv] finished-split counters, zero between calls
+  uint32_t* tickets;            // [B][Hkv][2] split counters (arrived, published), zero between calls
   // decode step only: the new token's K and V rows, bfloat16 [B][Hkv][D]
   // with a per-sequence stride, quantized and appended at position
   // seq_len - 1 before attending
@@ -82,10 +82,11 @@ struct DecodeParams {
 
 cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream);
 
-// Split-K workspace layout: ticket words first (rounded to 16 bytes), then the
-// numerators [B][Hq][splits][D], then (m, l) pairs [B][Hq][splits][2].
+// Split-K workspace layout: the merge's counter words first, two per
+// (sequence, kv-head), rounded to 16 bytes; then the numerators
+// [B][Hq][splits][D], then (m, l) pairs [B][Hq][splits][2].
 inline size_t decode_ticket_bytes(int num_seqs, int num_kv_heads) {
-  return (size_t(num_seqs) * size_t(num_kv_heads) * 4 + 15) / 16 * 16;
+  return (size_t(num_seqs) * size_t(num_kv_heads) * 8 + 15) / 16 * 16;
 }
 
 }  // namespace saw

@@ -128,7 +128,7 @@ int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_siz
  * Workspace bytes saw_paged_decode_int4 needs for these sizes with the same
  * pages_per_split argument, on the current device (0 when the plan has one
  * split, which writes the output directly).  Returns 0 on bad arguments.
- * The workspace holds the split partials and, first, one counter word per
+ * The workspace holds the split partials and, first, two counter words per
  * (sequence, kv-head) that the merge uses: zero-fill a new workspace once
  * (e.g. cudaMemset) before its first use; every call leaves those words at
  * zero again.

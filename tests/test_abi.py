@@ -133,8 +133,8 @@ def test_plan_and_workspace(L):
     s, pps = saw.saw_decode_plan(2, 8, 16, 1000, 4)
     assert (s, pps) == (16, 4)
     ws = saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 1000, 4)
-    # one counter word per (sequence, kv-head), rounded to 16 bytes, then partials
-    assert ws == 64 + 2 * 32 * 16 * (128 + 2) * 4
+    # two counter words per (sequence, kv-head), rounded to 16 bytes, then partials
+    assert ws == 2 * 8 * 8 + 2 * 32 * 16 * (128 + 2) * 4
     # one split -> no workspace
     assert saw.saw_decode_workspace_bytes(2, 32, 8, 128, 16, 64, 64) == 0
     # automatic plan: splits never shorter than 256 tokens, and cover the context

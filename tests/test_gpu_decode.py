@@ -155,8 +155,8 @@ def test_workspace_reuse_across_calls_and_plans():
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         assert rel_err(out.cpu().numpy().reshape(-1, 128), ref, f"tiny-ws-reuse-pps{pps}") <= ATTN_TOL
-    n_tickets = B * wl.num_kv_heads
-    assert torch.all(ws[:4 * n_tickets].view(torch.int32) == 0)
+    n_counters = 2 * B * wl.num_kv_heads
+    assert torch.all(ws[:4 * n_counters].view(torch.int32) == 0)
 
 
 @pytest.mark.parametrize("P,group,pps,flags", [(16, 4, 0, 0), (16, 4, 2, 1), (16, 1, 3, 0),
