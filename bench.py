@@ -45,6 +45,31 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
 
+# ------------------------------------------------------------------ ncu traffic record
+
+DECODE_SOURCES = ["paged_decode.cu", "saw_device.cuh", "saw_internal.h", "saw_quant_row.cuh"]
+
+
+def decode_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    record (profiles/dram_traffic.txt), or None when the kernel's sources
+    have changed since that capture."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "bit_paged_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as fh:
+            for line in fh:
+                parts = line.split()
+                if len(parts) == 4 and not line.startswith("#") and parts[2] == h.hexdigest():
+                    return int(parts[3]), "ncu capture in profiles/paged_decode_qwen3-4b-latency.md"
+    except OSError:
+        pass
+    return None, "no ncu capture of the current kernel sources"
+
+
 # ------------------------------------------------------------------ ranks
 
 def dist_env():
@@ -478,6 +503,7 @@ def run_saw(args):
     iso_ms, iso_how = decode_kernel_times(case, stream, reps=max(20, min(200, args.steps // 10)))
     peak, peak_src = read_peaks()
     achieved = case.layer_bytes() / (dec_ms * 1e-3) / 1e9
+    traffic, traffic_src = decode_traffic()
 
     # end to end through the public API with host buffers
     q_h = case.q.cpu().pin_memory()
@@ -555,7 +581,8 @@ def run_saw(args):
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_source": traffic_src,
             "bytes_per_launch": case.layer_bytes(),
             "ms_per_launch": dec_ms,
             "timing": dec_how,

@@ -204,3 +204,44 @@ def test_fused_decode_step(P, group, pps, flags):
     got = out.cpu().numpy().reshape(-1, D)
     assert np.all(np.isfinite(got))
     assert rel_err(got, ref, f"step-P{P}-G{group}-pps{pps}") <= ATTN_TOL
+
+
+def test_merge_wait_times_out_and_reports():
+    """Failure detection without a fault: the 'published' counter words of a
+    workspace are set to a value no call reaches, so the merging split's
+    bounded wait runs out (about a second).  The call returns, reports
+    SAW_ERR_DEVICE_TIMEOUT, writes finite numbers, and a clean workspace
+    works again afterwards on the same context."""
+    import time
+    wl = W.TINY
+    lens, bt, npages, kc, vc, q = _setup(wl, [256, 200])
+    B, Hq, D = q.shape
+    Lmax = int(lens.max())
+    pps = 2
+    splits, _ = saw.saw_decode_plan(B, wl.num_kv_heads, wl.page_size, Lmax, pps)
+    assert splits > 1
+    wsb = saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, pps)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    counters = ws[:8 * B * wl.num_kv_heads].view(torch.int32).view(-1, 2)
+    counters[:, 1] = 0x40000000  # 'published': never equals a split count
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    saw.saw_paged_decode_int4(q, kc, vc, bt.cuda(), lens.cuda(), Lmax, wl.num_kv_heads, npages,
+                              wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h, out, ws,
+                              pages_per_split=pps, dev_status=st)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30.0
+    assert int(st.item()) == saw.SAW_ERR_DEVICE_TIMEOUT
+    assert torch.all(torch.isfinite(out))
+    # the context is still usable: a clean workspace gives the right answer
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
+                        wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h)
+    ws.zero_()
+    st.zero_()
+    saw.saw_paged_decode_int4(q, kc, vc, bt.cuda(), lens.cuda(), Lmax, wl.num_kv_heads, npages,
+                              wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h, out, ws,
+                              pages_per_split=pps, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert rel_err(out.cpu().numpy().reshape(-1, 128), ref, "tiny-after-timeout") <= ATTN_TOL
