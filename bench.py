@@ -369,7 +369,7 @@ def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
     return kc, vc
 
 
-def decode_config_measure(device, stream, layers: int = 2, reps: int = 10):
+def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=None):
     """Decode-only throughput of the bandwidth-bound workloads (Qwen3-8B
     concurrent, Qwen3-32B high concurrency in its three rotation variants,
     long context at h 128 and 64): `layers` distinct layer caches (each
@@ -383,6 +383,8 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10):
              ("qwen3-32b-high-concurrency unrotated", c32.variant(rotate_k=False, rotate_v=False)),
              ("long-131072 h128", W.LONG_PREFILL),
              ("long-131072 h64", W.LONG_PREFILL.variant(block_h=64))]
+    if only is not None:
+        cases = [(n, w) for n, w in cases if n in only]
     res = {}
     for name, wl in cases:
         lens = W.seq_lens(wl)
@@ -414,6 +416,8 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10):
                      "seqs": B, "tokens": int(lens.sum())}
         del caches, qs, ws, out
         torch.cuda.empty_cache()
+    if only is not None:
+        return res, None
     a = res["qwen3-32b-high-concurrency k+v"]["ms_per_layer"]
     k1 = res["qwen3-32b-high-concurrency k-only"]["ms_per_layer"]
     u = res["qwen3-32b-high-concurrency unrotated"]["ms_per_layer"]

@@ -76,7 +76,7 @@ struct Cfg {
   static constexpr int kOffBars = kRing;
   static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][4]
   static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [16][kIdCap]
-  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8][128]
+  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8 t][32 lanes][4]
   static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [2][8]
   static constexpr int kOffFlag = kOffQsum + 2 * kMaxGroup * 4;               // int
   static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (64 code bytes, meta)
@@ -235,6 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   const int new_tok = L - 1;
   const bool owner = APPEND && new_tok >= 0 && new_tok / P >= p_begin && new_tok / P < p_end;
   const int new_pid = owner ? btab[new_tok / P] : -1;
+  if (early && lane < 2) {
+    // warm L2 with the rows read right after the wait (a prefetch only
+    // hints the cache, which stays coherent with the previous kernel's
+    // writes, so it may run before the wait)
+    const uint16_t* row = nullptr;
+    if (warp < G) row = p.q + (int64_t(seq) * p.num_q_heads + hq0 + warp) * kHeadDim;
+    if (owner && warp == kWarps - 2) row = p.k_new + int64_t(seq) * p.k_new_stride + int64_t(kvh) * kHeadDim;
+    if (owner && warp == kWarps - 1) row = p.v_new + int64_t(seq) * p.v_new_stride + int64_t(kvh) * kHeadDim;
+    if (row) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + lane * 64));
+  }
   __syncwarp();
   if (early) pdl_wait_then_release();
 
@@ -273,8 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   // high nibbles (n * 2^-20) and even ones the low nibbles (n * 2^-24), so
   // every product is n q' 2^(S-24).  sm_scale*log2(e) is applied to the
   // binary32 score, so an unrotated q enters the MMA exactly.
-  __half* qh_hi = qh;
-  __half* qh_lo = qh + kMaxGroup * kHeadDim;
+  // q' is stored in the B-fragment order of the score MMA: buffer 0 holds,
+  // for k-step t and lane (g, c), the four binary16 values of that lane's
+  // two fragment registers (PACKED: column g = hi of head g for g < 4, lo
+  // of head g - 4 otherwise; WIDE: hi of head g); buffer 1 (WIDE) the lo
+  // parts.  Each lane then loads its fragments with conflict-free 8-byte
+  // reads.  Element d of a head sits at k-step 2((d >> 3) & 3) + ((d >> 1) & 1),
+  // thread-in-group c = d >> 5, register d & 1, half (d >> 2) & 1.
   if (warp < kMaxGroup) {
     const int h = warp;
     float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -319,8 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       const float y = ldexpf(x[e], se);
       const __half hi = __float2half_rn(y);
       const __half lo = __float2half_rn(y - __half2float(hi));
-      qh_hi[h * kHeadDim + 4 * lane + e] = hi;
-      qh_lo[h * kHeadDim + 4 * lane + e] = lo;
+      const int d = 4 * lane + e;
+      const int t = 2 * ((d >> 3) & 3) + ((d >> 1) & 1);
+      const int w2 = (d & 1) * 2 + ((d >> 2) & 1);
+      const int c_ = d >> 5;
+      if (PACKED) {
+        if (h < kMaxGroup / 2) {
+          qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
+          qh[(t * 32 + (h + 4) * 4 + c_) * 4 + w2] = lo;
+        }
+      } else {
+        qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
+        qh[8 * 32 * 4 + (t * 32 + h * 4 + c_) * 4 + w2] = lo;
+      }
       part += ldexpf(__half2float(hi) + __half2float(lo), -se);
     }
 #pragma unroll
@@ -338,21 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   uint32_t bq[8][2];
   uint32_t bl[PACKED ? 1 : 8][2];
   {
-    const __half* rh = PACKED ? ((g < 4) ? qh_hi + g * kHeadDim : qh_lo + (g - 4) * kHeadDim)
-                              : qh_hi + g * kHeadDim;
-    const __half* rl = qh_lo + g * kHeadDim;
+    const uint2* qf = reinterpret_cast<const uint2*>(qh);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int base = 8 * (4 * c + t / 2) + ((t & 1) ? 2 : 0);
-      __half2 v0 = __halves2half2(rh[base], rh[base + 4]);
-      __half2 v1 = __halves2half2(rh[base + 1], rh[base + 5]);
-      bq[t][0] = *reinterpret_cast<uint32_t*>(&v0);
-      bq[t][1] = *reinterpret_cast<uint32_t*>(&v1);
+      const uint2 v = qf[t * 32 + lane];
+      bq[t][0] = v.x;
+      bq[t][1] = v.y;
       if (!PACKED) {
-        __half2 w0 = __halves2half2(rl[base], rl[base + 4]);
-        __half2 w1 = __halves2half2(rl[base + 1], rl[base + 5]);
-        bl[PACKED ? 0 : t][0] = *reinterpret_cast<uint32_t*>(&w0);
-        bl[PACKED ? 0 : t][1] = *reinterpret_cast<uint32_t*>(&w1);
+        const uint2 u = qf[8 * 32 + t * 32 + lane];
+        bl[PACKED ? 0 : t][0] = u.x;
+        bl[PACKED ? 0 : t][1] = u.y;
       }
     }
   }
