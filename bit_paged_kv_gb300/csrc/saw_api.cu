@@ -59,6 +59,14 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
         best_q = q;
       }
     }
+    // One wave: leave two SMs per (sequence, kv-head) free.  Back-to-back
+    // launches overlap (programmatic dependent launch), and the previous
+    // launch's merging splits still hold one SM per unit while the next
+    // launch starts; its splits should not queue behind them.
+    if (units * best <= sms && best > 1) {
+      const int64_t fit = (sms - 2 * units) / units;
+      if (fit >= 1 && fit < best) best = fit;
+    }
     pps = ceil_div(max_pages, best);
   }
   int64_t splits = max_pages == 0 ? 1 : ceil_div(max_pages, pps);
