@@ -544,21 +544,24 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
       const float ps0 = p0 * sv0, ps1 = p1 * sv0, ps2 = p2 * sv1, ps3 = p3 * sv1;
       const uint32_t X = pack_half2(ps0, ps2);
       const uint32_t Y = pack_half2(ps1, ps3);
-      const int src0 = 8 * c + (g >> 1);
+      // PV k-columns (2c, 2c+1, 2c+8, 2c+9) carry tokens (c, c+4, c+8, c+12):
+      // any order works when A and B agree, and this one puts the four V
+      // rows a lane group reads 64 bytes apart (2-way bank conflicts, not 4)
+      const int src0 = 4 * c + (g >> 1);
       const uint32_t xa = __shfl_sync(kFull, X, src0);
       const uint32_t ya = __shfl_sync(kFull, Y, src0);
-      const uint32_t xb = __shfl_sync(kFull, X, src0 + 4);
-      const uint32_t yb = __shfl_sync(kFull, Y, src0 + 4);
-      const uint32_t va = (g & 1) ? ya : xa;  // tokens (2c, 2c+8)
-      const uint32_t vb = (g & 1) ? yb : xb;  // tokens (2c+1, 2c+9)
+      const uint32_t xb = __shfl_sync(kFull, X, src0 + 16);
+      const uint32_t yb = __shfl_sync(kFull, Y, src0 + 16);
+      const uint32_t va = (g & 1) ? ya : xa;  // tokens (c, c+8)
+      const uint32_t vb = (g & 1) ? yb : xb;  // tokens (c+4, c+12)
       const uint32_t b0 = prmt(va, vb, 0x5410u);
       const uint32_t b1 = prmt(va, vb, 0x7632u);
 
       const uint8_t* vrow = vst + C::kcode(0) + 8 * g;
-      const uint2 r0w = *reinterpret_cast<const uint2*>(vrow + (2 * c) * kCodeRow);
-      const uint2 r1w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 1) * kCodeRow);
-      const uint2 r2w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 8) * kCodeRow);
-      const uint2 r3w = *reinterpret_cast<const uint2*>(vrow + (2 * c + 9) * kCodeRow);
+      const uint2 r0w = *reinterpret_cast<const uint2*>(vrow + c * kCodeRow);
+      const uint2 r1w = *reinterpret_cast<const uint2*>(vrow + (c + 4) * kCodeRow);
+      const uint2 r2w = *reinterpret_cast<const uint2*>(vrow + (c + 8) * kCodeRow);
+      const uint2 r3w = *reinterpret_cast<const uint2*>(vrow + (c + 12) * kCodeRow);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t w0 = (k < 4) ? r0w.x : r0w.y;
