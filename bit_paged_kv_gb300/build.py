@@ -20,10 +20,15 @@ LIB = os.path.join(OUT_DIR, "libsaw_int4.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-# The append kernel's bytes are defined by separately rounded binary32 steps;
-# it uses explicit _rn intrinsics and is also compiled with contraction off.
-EXTRA = {"quantize_append.cu": ["-fmad=false"]}
-SOURCES = ["saw_api.cu", "quantize_append.cu", "paged_decode.cu", "decode_static_scratch.cu"]
+# (source, object, extra flags).  The append kernel's bytes are defined by
+# separately rounded binary32 steps; it uses explicit _rn intrinsics and is
+# also compiled with contraction off.  The decode kernel is built once per CTA
+# shape.
+UNITS = [("saw_api.cu", "saw_api.o", []),
+         ("quantize_append.cu", "quantize_append.o", ["-fmad=false"]),
+         ("paged_decode.cu", "paged_decode_w16.o", ["-DSAW_DECODE_WARPS=16"]),
+         ("paged_decode.cu", "paged_decode_w8.o", ["-DSAW_DECODE_WARPS=8"]),
+         ("decode_static_scratch.cu", "decode_static_scratch.o", [])]
 
 
 def _nvcc() -> str:
@@ -46,9 +51,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             return LIB
     nvcc = _nvcc()
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *COMMON, *EXTRA.get(src, []), "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(unit) -> str:
+        src, obj_name, extra = unit
+        obj = os.path.join(OUT_DIR, obj_name)
+        cmd = [nvcc, *ARCH, *COMMON, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,8 +64,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stderr.write(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    with ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+        objs = list(ex.map(compile_one, UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:

@@ -9,10 +9,12 @@
 // orthogonal, undoable rotation, so q.k = (Hq).(Hk) and o = H^-1 o'.
 //
 // Design (sm_103a):
-//  * One 16-warp CTA per (split of the context, kv-head, sequence), one CTA
-//    per SM.  The whole GQA group of the kv-head is served by the CTA, so
-//    each page is read from HBM once, and q is rotated once per CTA.
-//  * The split is cut into 16-token tiles; warp w takes tiles w, w+16, ...
+//  * One CTA per (split of the context, kv-head, sequence): 16 warps, one
+//    CTA per SM, or 8 warps, two CTAs per SM (this file is compiled once per
+//    shape; the host plan picks one).  The whole GQA group of the kv-head is
+//    served by the CTA, so each page is read from HBM once, and q is rotated
+//    once per CTA.
+//  * The split is cut into 16-token tiles; warp w of W takes tiles w, w+W, ...
 //    through a private four-stage shared-memory ring filled by the bulk-copy
 //    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds one tile's
 //    K and V codes and their (scale, zero) words: a whole 16-token page, or
@@ -43,7 +45,12 @@
 namespace saw {
 namespace {
 
-constexpr int kWarps = kDecodeWarps;
+#ifndef SAW_DECODE_WARPS
+#define SAW_DECODE_WARPS 16
+#endif
+constexpr int kWarps = SAW_DECODE_WARPS;              // this object's CTA shape
+constexpr int kCtasPerSm = kWarps == 16 ? 1 : 2;      // 128 registers per thread either way
+static_assert(kWarps == 16 || kWarps == 8, "decode CTAs have 16 or 8 warps");
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kRedStride = kHeadDim + 4;  // padded row of the cross-warp reduction
@@ -129,7 +136,7 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
 // shuffle.  WIDE (group 5..8): all 8 columns are heads; the score product
 // runs twice (q' hi, then lo) and p*s is one binary16 value.
 template <int P, bool PACKED, bool APPEND>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(const DecodeParams p) {
   using C = Cfg<P>;
   // Wait for the previous kernel in the stream before reading anything --
   // unless the caller declared that it writes neither the tables nor the
@@ -668,18 +675,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecodeP
   // each half-warp; then one (head, dim) per thread.
   const int nw = min(kWarps, n_steps);  // warps that saw any step
   if (tid < kMaxGroup * kWarps) {
-    const int h = tid >> 4, w = tid & 15;
+    const int h = tid / kWarps, w = tid % kWarps;
     const bool in = h < G && w < nw;
     const float m = in ? red_m[w * kMaxGroup + h] : -INFINITY;
     float M = m;
 #pragma unroll
-    for (int x = 1; x < 16; x <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+    for (int x = 1; x < kWarps; x <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
     const float Mu = (M == -INFINITY) ? 0.0f : M;
     const float f = in ? ex2(m - Mu) : 0.0f;
     float den = in ? red_l[w * kMaxGroup + h] * f : 0.0f;
     float zz = in ? red_z[w * kMaxGroup + h] * f : 0.0f;
 #pragma unroll
-    for (int x = 1; x < 16; x <<= 1) {
+    for (int x = 1; x < kWarps; x <<= 1) {
       den += __shfl_xor_sync(kFull, den, x);
       zz += __shfl_xor_sync(kFull, zz, x);
     }
@@ -863,7 +870,10 @@ cudaError_t launch_page(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
+#define SAW_CAT2(a, b) a##b
+#define SAW_CAT(a, b) SAW_CAT2(a, b)
+cudaError_t SAW_CAT(launch_paged_decode_w, SAW_DECODE_WARPS)(const DecodeParams& p,
+                                                             cudaStream_t stream) {
   if (p.num_seqs == 0) return cudaSuccess;
   switch (p.page_size) {
     case 16: return launch_page<16>(p, stream);

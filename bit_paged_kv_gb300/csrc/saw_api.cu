@@ -26,53 +26,85 @@ int sm_count() {
   return n;
 }
 
-// Split plan.  A decode CTA has 16 warps and fills one SM; a split should
-// give each warp at least two 32-token steps (1024 tokens per split).  Among
-// the split counts allowed, take the one whose CTA count (sequences x
-// kv-heads x splits) wastes the least of its last wave of SMs, preferring
-// fewer splits (a smaller merge) unless more splits fill the waves clearly
-// better.
+// Split plan.  A split should give every warp several 16-token tiles (at
+// least 1024 tokens per split).  Among the split counts allowed, take the one
+// whose CTA count (sequences x kv-heads x splits) wastes the least of its
+// last wave, preferring fewer splits (a smaller merge) unless more splits
+// fill the waves clearly better.
+// Split search for a grid with `slots` resident CTAs: the split count with
+// the least wave quantisation, then, in a one-wave grid, two slots per
+// (sequence, kv-head) left free.  Back-to-back launches overlap
+// (programmatic dependent launch), and the previous launch's merging splits
+// still hold one slot per unit while the next starts; its splits should not
+// queue behind them.
+int64_t best_splits(int64_t units, int64_t slots, int64_t max_splits) {
+  int64_t best = 1;
+  double best_q = 1e30;
+  for (int64_t s = 1; s <= max_splits; ++s) {
+    const int64_t n = units * s;
+    const double q = double(ceil_div(n, slots) * slots) / double(n);  // >= 1; 1 = full waves
+    if (q < best_q - 0.02) {
+      best = s;
+      best_q = q;
+    }
+  }
+  if (units * best <= slots && best > 1) {
+    const int64_t fit = (slots - 2 * units) / units;
+    if (fit >= 1 && fit < best) best = fit;
+  }
+  return best;
+}
+
+// The split plan and the CTA shape.  16-warp CTAs (one per SM) serve grids of
+// one wave and long splits; grids of several waves of short splits use 8-warp
+// CTAs, two per SM, so that one CTA's prologue and merge overlap the other's
+// streaming.
 int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int32_t max_seq_len,
-                  int32_t pages_per_split, int32_t* splits_out, int32_t* pps_out) {
+                  int32_t pages_per_split, int32_t* splits_out, int32_t* pps_out,
+                  int32_t* warps_out = nullptr) {
   if (num_seqs < 0 || num_kv_heads <= 0 || !page_size_ok(page_size) || max_seq_len < 0 ||
       pages_per_split < 0)
     return SAW_ERR_INVALID_ARG;
   const int64_t max_pages = ceil_div(max_seq_len, page_size);
-  int64_t pps;
+  const int64_t units = int64_t(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
+  const int sms_raw = sm_count();
+  const int64_t sms = sms_raw > 0 ? sms_raw : 148;
+  auto shape_for = [&](int64_t splits, int64_t pps) -> int32_t {
+    const bool one_wave = units * splits <= sms;
+    const bool long_splits = pps * page_size > saw::kLongSplitTokens;
+    return (one_wave || long_splits) ? 16 : 8;
+  };
+  int64_t pps, splits;
+  int32_t warps;
   if (max_pages == 0) {
     pps = 1;
+    splits = 1;
+    warps = 16;
   } else if (pages_per_split > 0) {
     pps = pages_per_split;
+    splits = ceil_div(max_pages, pps);
+    warps = shape_for(splits, pps);
   } else {
-    const int64_t units = int64_t(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
-    const int sms_raw = sm_count();
-    const int64_t sms = sms_raw > 0 ? sms_raw : 148;
     const int64_t min_pps = ceil_div(1024, page_size);
     const int64_t max_splits = std::min<int64_t>(64, ceil_div(max_pages, min_pps));
-    int64_t best = 1;
-    double best_q = 1e30;
-    for (int64_t s = 1; s <= max_splits; ++s) {
-      const int64_t n = units * s;
-      const double q = double(ceil_div(n, sms) * sms) / double(n);  // >= 1; 1 = full waves
-      if (q < best_q - 0.02) {
-        best = s;
-        best_q = q;
-      }
+    int64_t s16 = best_splits(units, sms, max_splits);
+    int64_t p16 = ceil_div(max_pages, s16);
+    s16 = ceil_div(max_pages, p16);
+    if (shape_for(s16, p16) == 16) {
+      pps = p16;
+      splits = s16;
+      warps = 16;
+    } else {
+      const int64_t s8 = best_splits(units, 2 * sms, max_splits);
+      pps = ceil_div(max_pages, s8);
+      splits = ceil_div(max_pages, pps);
+      warps = 8;
     }
-    // One wave: leave two SMs per (sequence, kv-head) free.  Back-to-back
-    // launches overlap (programmatic dependent launch), and the previous
-    // launch's merging splits still hold one SM per unit while the next
-    // launch starts; its splits should not queue behind them.
-    if (units * best <= sms && best > 1) {
-      const int64_t fit = (sms - 2 * units) / units;
-      if (fit >= 1 && fit < best) best = fit;
-    }
-    pps = ceil_div(max_pages, best);
   }
-  int64_t splits = max_pages == 0 ? 1 : ceil_div(max_pages, pps);
   if (splits > 65535) return SAW_ERR_UNSUPPORTED;
   *splits_out = int32_t(splits);
   *pps_out = int32_t(pps);
+  if (warps_out) *warps_out = warps;
   return SAW_OK;
 }
 
@@ -203,9 +235,9 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
     return SAW_ERR_INVALID_ARG;
   if (int64_t(max_blocks_per_seq) * page_size < int64_t(max_seq_len)) return SAW_ERR_INVALID_ARG;
 
-  int32_t splits = 0, pps = 0;
+  int32_t splits = 0, pps = 0, warps = 16;
   int32_t rc = make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split,
-                         &splits, &pps);
+                         &splits, &pps, &warps);
   if (rc != SAW_OK) return rc;
   const size_t need = saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  page_size, max_seq_len, pages_per_split);
@@ -239,6 +271,7 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.block_h = block_h;
   p.pages_per_split = pps;
   p.num_splits = splits;
+  p.warps = warps;
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)

@@ -8,7 +8,11 @@ namespace saw {
 
 constexpr int kHeadDim = 128;       // the one head size this build supports
 constexpr int kMaxGroup = 8;        // q-heads per kv-head served by one CTA (MMA N = 8)
-constexpr int kDecodeWarps = 16;    // warps per decode CTA (one CTA per SM)
+// Decode CTA shapes: 16 warps, one CTA per SM (one-wave grids and long
+// splits), or 8 warps, two CTAs per SM (many short splits: one CTA's prologue
+// and merge overlap the other's streaming).  Splits of more than this many
+// tokens count as long.
+constexpr int kLongSplitTokens = 8192;
 
 __host__ __device__ constexpr int chunk_bytes(int page_size) {
   return page_size * (kHeadDim / 2) + 4 * page_size;
@@ -78,9 +82,15 @@ struct DecodeParams {
   int32_t num_splits;
   float c_h;                    // 1/sqrt(block_h)
   float q_scale;                // sm_scale * log2(e)
+  int32_t warps;                // CTA shape: 16 (one per SM) or 8 (two per SM)
 };
 
-cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream);
+// One launcher per CTA shape (paged_decode.cu compiled once per shape).
+cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
+inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
+  return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
+}
 
 // Split-K workspace layout: the merge's counter words first, two per
 // (sequence, kv-head), rounded to 16 bytes; then the numerators

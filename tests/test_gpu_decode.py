@@ -51,6 +51,21 @@ def test_tiny_full(pps):
 EDGE_LENS = [0, 1, 15, 16, 17, 33, 255, 700]
 
 
+@pytest.mark.parametrize("group", [1, 4, 8])
+@pytest.mark.parametrize("P", [16, 32, 64])
+def test_many_sequences_eight_warp_ctas(group, P):
+    """100 sequences x 2 kv-heads of short, mixed lengths: a grid of several
+    waves of short splits, which the plan serves with 8-warp CTAs, two per SM
+    (automatic plan and a forced split size)."""
+    wl = W.TINY.variant(num_kv_heads=2, num_q_heads=2 * group, page_size=P, shuffle_pages=True,
+                        dist="student_t", nu=4)
+    g = torch.Generator().manual_seed(7 * P + group)
+    lens_l = EDGE_LENS + torch.randint(1, 700, (92,), generator=g).tolist()
+    lens, bt, npages, kc, vc, q = _setup(wl, lens_l)
+    for pps in (0, 2):
+        _check(wl, lens, bt, npages, kc, vc, q, pps=pps)
+
+
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
 @pytest.mark.parametrize("rot", [(1, 1), (1, 0), (0, 0), (0, 1)])
 def test_edge_lengths_groups_rotations(group, rot):
@@ -159,16 +174,21 @@ def test_workspace_reuse_across_calls_and_plans():
     assert torch.all(ws[:4 * n_counters].view(torch.int32) == 0)
 
 
-@pytest.mark.parametrize("P,group,pps,flags", [(16, 4, 0, 0), (16, 4, 2, 1), (16, 1, 3, 0),
-                                              (16, 8, 1, 1), (32, 4, 1, 0), (64, 2, 1, 1),
-                                              (64, 8, 0, 0)])
-def test_fused_decode_step(P, group, pps, flags):
+@pytest.mark.parametrize("P,group,pps,flags,many", [
+    (16, 4, 0, 0, False), (16, 4, 2, 1, False), (16, 1, 3, 0, False), (16, 8, 1, 1, False),
+    (32, 4, 1, 0, False), (64, 2, 1, 1, False), (64, 8, 0, 0, False),
+    (16, 4, 0, 1, True), (16, 8, 2, 0, True), (64, 1, 0, 1, True)])
+def test_fused_decode_step(P, group, pps, flags, many):
     """saw_decode_step = append the new token at seq_len - 1, then attend, in
-    one launch: cache bytes equal the oracle's append, attention the oracle's."""
+    one launch: cache bytes equal the oracle's append, attention the oracle's.
+    many = 100 sequences: several waves of short splits, 8-warp CTAs."""
     from gpu_helpers import new_caches, oracle_append
     wl = W.TINY.variant(page_size=P, num_q_heads=2 * group, num_kv_heads=2, shuffle_pages=True,
                         rotate_v=False, dist="student_t", nu=4)
     lens_l = [1, 17, 16, P + 1, 300, 31, 0]
+    if many:
+        g = torch.Generator().manual_seed(P + group)
+        lens_l = lens_l + torch.randint(1, 400, (93,), generator=g).tolist()
     lens = torch.tensor(lens_l, dtype=torch.int32)
     bt, npages = W.page_tables(wl, lens, spare_pages=3)
     # prefill all but the last token, with the append kernel
@@ -203,7 +223,7 @@ def test_fused_decode_step(P, group, pps, flags):
                         wl.block_h)
     got = out.cpu().numpy().reshape(-1, D)
     assert np.all(np.isfinite(got))
-    assert rel_err(got, ref, f"step-P{P}-G{group}-pps{pps}") <= ATTN_TOL
+    assert rel_err(got, ref, f"step-P{P}-G{group}-pps{pps}{'-many' if many else ''}") <= ATTN_TOL
 
 
 def test_merge_wait_times_out_and_reports():
