@@ -53,7 +53,10 @@ constexpr int kCtasPerSm = kWarps == 16 ? 1 : 2;      // 128 registers per threa
 static_assert(kWarps == 16 || kWarps == 8, "decode CTAs have 16 or 8 warps");
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kRedStride = kHeadDim + 4;  // padded row of the cross-warp reduction
+constexpr int kRedStride = kHeadDim + 8;  // padded row of the cross-warp reduction
+// dim d of a reduction row sits at d + d / 16: the stores (lane group g
+// writes dims 16g + ..) and the per-dim reads are then free of bank conflicts
+__device__ __forceinline__ int red_col(int d) { return d + (d >> 4); }
 constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
 constexpr int kStepTok = 16;              // tokens per step (one MMA tile, one softmax update)
 constexpr int kStages = 4;
@@ -662,10 +665,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     float* base1 = base0 + kRedStride;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      base0[16 * g + 2 * k] = acc[k][0];
-      base1[16 * g + 2 * k] = acc[k][1];
-      base0[16 * g + 2 * k + 1] = acc[k][2];
-      base1[16 * g + 2 * k + 1] = acc[k][3];
+      base0[red_col(16 * g + 2 * k)] = acc[k][0];
+      base1[red_col(16 * g + 2 * k)] = acc[k][1];
+      base0[red_col(16 * g + 2 * k + 1)] = acc[k][2];
+      base1[red_col(16 * g + 2 * k + 1)] = acc[k][3];
     }
   }
   __syncthreads();
@@ -711,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     float num = tot[kMaxGroup + h];
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
-      if (w < nw) num += red_acc[(w * kMaxGroup + h) * kRedStride + dd] * wgt[w * kMaxGroup + h];
+      if (w < nw) num += red_acc[(w * kMaxGroup + h) * kRedStride + red_col(dd)] * wgt[w * kMaxGroup + h];
     if (direct) {
       const float den = tot[h];
       qs[h * kHeadDim + dd] = (den > 0.0f) ? num / den : 0.0f;
