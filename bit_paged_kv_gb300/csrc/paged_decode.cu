@@ -700,15 +700,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       tot[2 * kMaxGroup + h] = M;
     }
   }
-  if (!direct && tid == 0) {
-    // merge protocol, part 2: the split whose arrival completes the count
-    // merges; every other split publishes its partial
-    const uint32_t done = arrived + 1u;
-    if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
-    *flag = (done == uint32_t(ns));
-  }
   __syncthreads();
-  const bool last = !direct && *flag != 0;
   for (int idx = tid; idx < G * kHeadDim; idx += kThreads) {
     const int h = idx / kHeadDim, dd = idx - h * kHeadDim;
     float num = tot[kMaxGroup + h];
@@ -718,9 +710,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     if (direct) {
       const float den = tot[h];
       qs[h * kHeadDim + dd] = (den > 0.0f) ? num / den : 0.0f;
-    } else if (last) {
-      qs[h * kHeadDim + dd] = num;  // this split's partial stays here; den, M in tot
     } else {
+      // publish the partial, and keep it here in case this split merges
+      // (den and M stay in tot)
+      qs[h * kHeadDim + dd] = num;
       const int64_t row = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits + split;
       p.part_o[row * kHeadDim + dd] = num;
       if (dd == 0) {
@@ -731,7 +724,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   }
 
   if (!direct) {
+    if (tid == 0) {
+      // merge protocol, part 2: the split whose arrival completed the count
+      // merges; every other split publishes its partial.  The count's round
+      // trip has been overlapping the reduction above.
+      const uint32_t done = arrived + 1u;
+      if (done > uint32_t(ns)) report(p.dev_status, SAW_ERR_DEVICE_INDEX);  // not zero-filled
+      *flag = (done == uint32_t(ns));
+    }
     __syncthreads();
+    const bool last = *flag != 0;
     if (!last) {
       // publish: release (cumulative over the barrier above) orders this
       // CTA's partials before the count the merging split waits for
@@ -756,10 +758,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       } else {
         report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
       }
-      *flag = ok ? 1 : 0;
+      flag[1] = ok ? 1 : 0;  // a word of its own: flag[0] may still be read
     }
     __syncthreads();
-    const bool merge_ok = *flag != 0;
+    const bool merge_ok = flag[1] != 0;
     // item = (head, 4 dims); four threads per item share the splits.  Every
     // load is issued before any is used (one round of L2 latency).
     constexpr int kMaxSplitsPerThread = 8;
