@@ -53,6 +53,9 @@ def load() -> C.CDLL:
                                          i32, i32, i32]),
         "oracle_decode_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f64,
                                     P]),
+        "oracle_bf16_cache_bytes": (i64, [i32, i32, i32, i32]),
+        "oracle_bf16_append": (i64, [P, P, i64, i64, P, i32, i32, i32, i32, P, P, i32, i32]),
+        "oracle_decode_bf16_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -245,6 +248,75 @@ def decode(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
                                    page_size, int(rotate_k), int(rotate_v), block_h,
                                    float(sm_scale), _ptr(o))
         _check(rc, "decode_one")
+        out[i] = o
+
+    if threads <= 1 or len(pairs) <= 1:
+        for i in range(len(pairs)):
+            run(i)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(run, range(len(pairs))))
+    return out
+
+
+# ---------------------------------------------------------------- BF16 baseline
+
+def bf16_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load().oracle_bf16_cache_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def bf16_append(k_bits, v_bits, slot_mapping, num_kv_heads: int, head_dim: int,
+                k_cache: np.ndarray, v_cache, num_pages: int, page_size: int) -> int:
+    """Copy every token's bf16 rows into its slot of the BF16 caches (uint16
+    arrays) in place; returns the number of out-of-range slots skipped."""
+    k = np.ascontiguousarray(np.asarray(k_bits, dtype=np.uint16))
+    T = k.shape[0]
+    if T == 0:
+        return 0
+    k2 = k.reshape(T, -1)
+    v2 = None
+    if v_bits is not None:
+        v2 = np.ascontiguousarray(np.asarray(v_bits, dtype=np.uint16)).reshape(T, -1)
+    slots = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int32))
+    assert slots.shape == (T,)
+    assert k_cache.dtype == np.uint16 and k_cache.flags["C_CONTIGUOUS"]
+    rc = load().oracle_bf16_append(_ptr(k2), _ptr(v2) if v2 is not None else None, k2.shape[1],
+                                   v2.shape[1] if v2 is not None else 0, _ptr(slots), 0, T,
+                                   num_kv_heads, head_dim, _ptr(k_cache),
+                                   _ptr(v_cache) if v2 is not None else None, num_pages,
+                                   page_size)
+    _check(rc, "bf16_append")
+    return int(rc)
+
+
+def decode_bf16(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
+                num_kv_heads: int, head_dim: int, num_pages: int, page_size: int,
+                sm_scale: float | None = None, pairs=None, threads: int = 1) -> np.ndarray:
+    """fp64 decode attention over BF16 pages for the (seq, q_head) pairs given
+    (default: all); same q-head -> kv-head map as `decode`."""
+    q = np.ascontiguousarray(np.asarray(q_bits, dtype=np.uint16))
+    B = q.shape[0]
+    q = q.reshape(B, num_q_heads, head_dim)
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    G = num_q_heads // num_kv_heads
+    if sm_scale is None or sm_scale == 0.0:
+        sm_scale = 1.0 / np.sqrt(head_dim)
+    if pairs is None:
+        pairs = [(b, hq) for b in range(B) for hq in range(num_q_heads)]
+    pairs = list(pairs)
+    out = np.zeros((len(pairs), head_dim), dtype=np.float64)
+    lib = load()
+
+    def run(i):
+        b, hq = pairs[i]
+        qrow = np.ascontiguousarray(q[b, hq])
+        row = np.ascontiguousarray(bt[b]) if bt.ndim == 2 and bt.shape[1] > 0 else np.zeros(1, np.int32)
+        o = np.zeros(head_dim, dtype=np.float64)
+        rc = lib.oracle_decode_bf16_one(_ptr(qrow), _ptr(k_cache), _ptr(v_cache), _ptr(row),
+                                        int(sl[b]), hq // G, num_kv_heads, head_dim, num_pages,
+                                        page_size, float(sm_scale), _ptr(o))
+        _check(rc, "decode_bf16_one")
         out[i] = o
 
     if threads <= 1 or len(pairs) <= 1:

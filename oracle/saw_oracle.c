@@ -449,3 +449,88 @@ done:
   free(t);
   return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* BF16 paged cache: the unquantized baseline ([IT] s.4 compares the   */
+/* throughput of INT4 + rotation against a BF16 KV cache)              */
+/* ------------------------------------------------------------------ */
+/*
+ * Layout (ours; the pages name only "BF16"): per layer and tensor,
+ * [num_pages][Hkv][P][D] bfloat16, token `off` of page `page` for kv-head
+ * `head` at element ((page * Hkv + head) * P + off) * D.
+ */
+int64_t oracle_bf16_cache_bytes(int32_t num_pages, int32_t P, int32_t Hkv, int32_t D) {
+  if (num_pages < 0 || P <= 0 || Hkv <= 0 || D <= 0) return 0;
+  return (int64_t)num_pages * Hkv * P * D * 2;
+}
+
+/* Copy the rows of tokens [t_begin, t_end) into their slots (slot -1 is
+ * padding and skipped; other out-of-range slots are skipped and counted).
+ * Returns the count of bad slots. */
+int64_t oracle_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_stride,
+                           int64_t v_stride, const int32_t* slot_mapping, int32_t t_begin,
+                           int32_t t_end, int32_t Hkv, int32_t D, uint16_t* k_cache,
+                           uint16_t* v_cache, int32_t num_pages, int32_t P) {
+  if (!k || !slot_mapping || !k_cache || (v && !v_cache) || Hkv <= 0 || D <= 0 || P <= 0)
+    return ORACLE_EINVAL;
+  int64_t bad = 0;
+  const int64_t num_slots = (int64_t)num_pages * P;
+  for (int32_t t = t_begin; t < t_end; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) {
+      ++bad;
+      continue;
+    }
+    const int64_t page = slot / P, off = slot % P;
+    for (int32_t hd = 0; hd < Hkv; ++hd) {
+      const int64_t dst = ((page * Hkv + hd) * P + off) * D;
+      memcpy(k_cache + dst, k + (int64_t)t * k_stride + (int64_t)hd * D, sizeof(uint16_t) * D);
+      if (v)
+        memcpy(v_cache + dst, v + (int64_t)t * v_stride + (int64_t)hd * D, sizeof(uint16_t) * D);
+    }
+  }
+  return bad;
+}
+
+/* Attention output of one query row over the first seq_len tokens of its
+ * BF16 pages, in double: t_j = sm_scale * (q . k_j), p = softmax(t),
+ * o = sum_j p_j v_j.  seq_len == 0 gives zeros; ORACLE_EPAGE for a page id
+ * outside [0, num_pages). */
+int32_t oracle_decode_bf16_one(const uint16_t* q_bf16, const uint16_t* k_cache,
+                               const uint16_t* v_cache, const int32_t* block_table_row,
+                               int32_t seq_len, int32_t kv_head, int32_t Hkv, int32_t D,
+                               int32_t num_pages, int32_t P, double sm_scale, double* out) {
+  if (!q_bf16 || !k_cache || !v_cache || !out || (seq_len > 0 && !block_table_row) || D <= 0 ||
+      P <= 0 || seq_len < 0 || kv_head < 0 || kv_head >= Hkv)
+    return ORACLE_EINVAL;
+  for (int32_t i = 0; i < D; ++i) out[i] = 0.0;
+  if (seq_len == 0) return ORACLE_OK;
+  double* t = (double*)malloc(sizeof(double) * (size_t)seq_len);
+  if (!t) return ORACLE_ENOMEM;
+  for (int32_t j = 0; j < seq_len; ++j) {
+    const int64_t page = block_table_row[j / P];
+    if (page < 0 || page >= num_pages) {
+      free(t);
+      return ORACLE_EPAGE;
+    }
+    const uint16_t* kr = k_cache + ((page * Hkv + kv_head) * P + j % P) * D;
+    double dot = 0.0;
+    for (int32_t i = 0; i < D; ++i) dot += (double)bf16_to_f32(q_bf16[i]) * bf16_to_f32(kr[i]);
+    t[j] = sm_scale * dot;
+  }
+  double m = t[0];
+  for (int32_t j = 1; j < seq_len; ++j)
+    if (t[j] > m) m = t[j];
+  double l = 0.0;
+  for (int32_t j = 0; j < seq_len; ++j) {
+    const double p = exp(t[j] - m);
+    l += p;
+    const int64_t page = block_table_row[j / P];
+    const uint16_t* vr = v_cache + ((page * Hkv + kv_head) * P + j % P) * D;
+    for (int32_t i = 0; i < D; ++i) out[i] += p * bf16_to_f32(vr[i]);
+  }
+  for (int32_t i = 0; i < D; ++i) out[i] /= l;
+  free(t);
+  return ORACLE_OK;
+}
