@@ -17,10 +17,14 @@ from ._binding import (  # noqa: F401
     SAW_STEP_EARLY_PAGES,
     SawError,
     lib,
+    saw_bf16_append,
+    saw_bf16_cache_bytes,
     saw_cache_bytes,
+    saw_decode_bf16_workspace_bytes,
     saw_decode_plan,
     saw_decode_step,
     saw_decode_workspace_bytes,
+    saw_paged_decode_bf16,
     saw_paged_decode_int4,
     saw_paged_decode_int4_noalloc,
     saw_quantize_append,

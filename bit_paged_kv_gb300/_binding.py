@@ -25,7 +25,8 @@ SAW_STEP_EARLY_PAGES = 1
 
 EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_decode_plan",
            "saw_decode_workspace_bytes", "saw_paged_decode_int4", "saw_decode_step",
-           "saw_paged_decode_int4_noalloc")
+           "saw_paged_decode_int4_noalloc", "saw_bf16_cache_bytes", "saw_bf16_append",
+           "saw_decode_bf16_workspace_bytes", "saw_paged_decode_bf16")
 
 _lib = None
 
@@ -68,6 +69,15 @@ def lib() -> C.CDLL:
     L.saw_paged_decode_int4_noalloc.restype = i32
     L.saw_paged_decode_int4_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
                                                 i32, i32, i32, i32, f32, P, i32, P, P]
+    L.saw_bf16_cache_bytes.restype = sz
+    L.saw_bf16_cache_bytes.argtypes = [i32, i32, i32, i32]
+    L.saw_bf16_append.restype = i32
+    L.saw_bf16_append.argtypes = [P, P, i64, i64, P, i32, i32, i32, P, P, i32, i32, P, P]
+    L.saw_decode_bf16_workspace_bytes.restype = sz
+    L.saw_decode_bf16_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.saw_paged_decode_bf16.restype = i32
+    L.saw_paged_decode_bf16.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                        P, P, sz, P, P]
     _lib = L
     return L
 
@@ -200,3 +210,51 @@ def saw_paged_decode_int4_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cach
         int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out), pages_per_split,
         _ptr(dev_status), _stream(q, stream))
     _raise(rc, "saw_paged_decode_int4_noalloc")
+
+
+def saw_bf16_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().saw_bf16_cache_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def saw_bf16_append(k: torch.Tensor, v, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache, num_pages: int, page_size: int, dev_status=None,
+                    stream=None) -> None:
+    """k, v: bfloat16 [T, Hkv, D] (token dim may be strided); v may be None."""
+    T, hkv, d = k.shape
+    assert k.dtype == torch.bfloat16 and k.stride(2) == 1 and k.stride(1) == d
+    if v is not None:
+        assert v.dtype == torch.bfloat16 and v.shape == k.shape and v.stride(2) == 1 and v.stride(1) == d
+    assert slot_mapping.dtype == torch.int32 and slot_mapping.is_contiguous()
+    rc = lib().saw_bf16_append(
+        _ptr(k), _ptr(v), k.stride(0), v.stride(0) if v is not None else 0, _ptr(slot_mapping),
+        T, hkv, d, _ptr(k_cache), _ptr(v_cache) if v is not None else None, num_pages,
+        page_size, _ptr(dev_status), _stream(k, stream))
+    _raise(rc, "saw_bf16_append")
+
+
+def saw_decode_bf16_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                    head_dim: int, page_size: int, max_seq_len: int) -> int:
+    return int(lib().saw_decode_bf16_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                     head_dim, page_size, max_seq_len))
+
+
+def saw_paged_decode_bf16(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                          num_kv_heads: int, num_pages: int, page_size: int, out: torch.Tensor,
+                          workspace=None, sm_scale: float = 0.0, dev_status=None,
+                          stream=None) -> None:
+    """Decode over the BF16 cache.  q: bfloat16 [B, Hq, D]; out: float32
+    [B, Hq, D]; workspace: saw_decode_bf16_workspace_bytes() bytes, zero-filled
+    before its first use."""
+    B, hq, d = q.shape
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, hq, d)
+    assert block_tables.dtype == torch.int32 and block_tables.is_contiguous()
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().saw_paged_decode_bf16(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), B, max_seq_len, hq, num_kv_heads, d, num_pages, page_size,
+        float(sm_scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
+        _stream(q, stream))
+    _raise(rc, "saw_paged_decode_bf16")

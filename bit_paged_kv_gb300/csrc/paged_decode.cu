@@ -116,12 +116,6 @@ __device__ void smem_fwht(float* buf, int nvec, int h) {
 // Codes enter the MMAs as binary16 subnormals: a nibble n masked in place at
 // bits 0-3 of a half is n * 2^-24, at bits 4-7 it is n * 2^-20 -- exact, with
 // no offset to remove.  The other operand carries the matching power of two.
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-  return v;
-}
-
 constexpr uint32_t kLoNib = 0x000F000Fu;  // bits 0-3 of both halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 

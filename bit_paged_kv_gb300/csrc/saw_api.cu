@@ -108,6 +108,28 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
   return SAW_OK;
 }
 
+// Split plan of the BF16 baseline: one 8-warp CTA per SM, at least 1024
+// tokens per split, the split count with the least wave quantisation.
+int32_t make_plan_bf16(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size,
+                       int32_t max_seq_len, int32_t* splits_out, int32_t* pps_out) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || !page_size_ok(page_size) || max_seq_len < 0)
+    return SAW_ERR_INVALID_ARG;
+  const int64_t max_pages = ceil_div(max_seq_len, page_size);
+  int64_t pps = 1, splits = 1;
+  if (max_pages > 0) {
+    const int64_t units = int64_t(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
+    const int sms_raw = sm_count();
+    const int64_t sms = sms_raw > 0 ? sms_raw : 148;
+    const int64_t max_splits = std::min<int64_t>(64, ceil_div(max_pages, ceil_div(1024, page_size)));
+    const int64_t best = best_splits(units, sms, max_splits);
+    pps = ceil_div(max_pages, best);
+    splits = ceil_div(max_pages, pps);
+  }
+  *splits_out = int32_t(splits);
+  *pps_out = int32_t(pps);
+  return SAW_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -328,6 +350,110 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
   p.append = 1;
   p.early_pages = (flags & SAW_STEP_EARLY_PAGES) ? 1 : 0;
   cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+
+// ---------------------------------------------------------------- BF16 baseline
+
+size_t saw_bf16_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                            int32_t head_dim) {
+  if (num_pages < 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return size_t(num_pages) * size_t(num_kv_heads) * size_t(page_size) * size_t(head_dim) * 2;
+}
+
+int32_t saw_bf16_append(const void* k, const void* v, int64_t k_token_stride,
+                        int64_t v_token_stride, const int32_t* slot_mapping, int32_t num_tokens,
+                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                        int32_t num_pages, int32_t page_size, int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_pages < 0) return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (int64_t(num_tokens) * num_kv_heads > INT32_MAX / 2) return SAW_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return SAW_OK;
+  const bool has_v = v != nullptr;
+  if (!k || !slot_mapping || !k_cache || (has_v && !v_cache)) return SAW_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(k_cache) || (has_v && (!aligned16(v) || !aligned16(v_cache))))
+    return SAW_ERR_INVALID_ARG;
+  if (k_token_stride < int64_t(num_kv_heads) * head_dim || (k_token_stride & 7))
+    return SAW_ERR_INVALID_ARG;
+  if (has_v && (v_token_stride < int64_t(num_kv_heads) * head_dim || (v_token_stride & 7)))
+    return SAW_ERR_INVALID_ARG;
+  const cudaError_t err = saw::launch_bf16_append(
+      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), k_token_stride,
+      has_v ? v_token_stride : 0, slot_mapping, num_tokens, num_kv_heads,
+      static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
+      int64_t(num_pages) * page_size, page_size, dev_status, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+size_t saw_decode_bf16_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                       int32_t max_seq_len) {
+  if (head_dim != kHeadDim || num_q_heads <= 0) return 0;
+  int32_t splits = 0, pps = 0;
+  if (make_plan_bf16(num_seqs, num_kv_heads, page_size, max_seq_len, &splits, &pps) != SAW_OK)
+    return 0;
+  if (splits <= 1) return 0;
+  const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
+  return saw::decode_ticket_bytes(num_seqs, num_kv_heads) + rows * size_t(head_dim) * 4 +
+         rows * 2 * 4;
+}
+
+int32_t saw_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, int32_t page_size, float sm_scale, float* out,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || max_seq_len < 0)
+    return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > saw::kMaxGroup) return SAW_ERR_UNSUPPORTED;
+  if (!(sm_scale >= 0.0f) || std::isinf(sm_scale)) return SAW_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return SAW_ERR_UNSUPPORTED;
+  if (int64_t(num_pages) * num_kv_heads * page_size > INT32_MAX) return SAW_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return SAW_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return SAW_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
+    return SAW_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * page_size < int64_t(max_seq_len)) return SAW_ERR_INVALID_ARG;
+  int32_t splits = 0, pps = 0;
+  int32_t rc = make_plan_bf16(num_seqs, num_kv_heads, page_size, max_seq_len, &splits, &pps);
+  if (rc != SAW_OK) return rc;
+  const size_t need = saw_decode_bf16_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                      head_dim, page_size, max_seq_len);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return SAW_ERR_INVALID_ARG;
+  saw::DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  if (need > 0) {
+    const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.tickets = reinterpret_cast<uint32_t*>(ws);
+    p.part_o = reinterpret_cast<float*>(ws + saw::decode_ticket_bytes(num_seqs, num_kv_heads));
+    p.part_ml = p.part_o + rows * head_dim;
+  }
+  p.dev_status = dev_status;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.max_seq_len = max_seq_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.num_pages = num_pages;
+  p.page_size = page_size;
+  p.pages_per_split = pps;
+  p.num_splits = splits;
+  const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
+  p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  const cudaError_t err = saw::launch_paged_decode_bf16(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 

@@ -68,6 +68,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// A GPU-scope acquire load (pairs with a release by another CTA).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 // 1-D bulk copy global -> shared through the copy engine, completing on an
 // mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -88,6 +88,12 @@ struct DecodeParams {
 // One launcher per CTA shape (paged_decode.cu compiled once per shape).
 cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
+// BF16 baseline (paged_decode_bf16.cu)
+cudaError_t launch_paged_decode_bf16(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_stride,
+                               int64_t v_stride, const int32_t* slots, int num_tokens, int hkv,
+                               uint16_t* kc, uint16_t* vc, int64_t num_slots, int P,
+                               int32_t* dev_status, cudaStream_t stream);
 inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
   return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
 }

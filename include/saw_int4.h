@@ -255,6 +255,63 @@ int32_t saw_paged_decode_int4_noalloc(const void* q, const void* k_cache, const 
                                       int32_t block_h, float sm_scale, float* out,
                                       int32_t pages_per_split, int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * BF16 baseline.  gist.science "SAW-INT4: System-Aware 4-Bit KV-Cache
+ * Quantization for Real-World LLM Serving", s.4 measures SAW-INT4's serving
+ * throughput against an unquantized BF16 KV cache.  These two calls are that
+ * baseline at the kernel level: the same paging and split-K decode, over a
+ * cache of bfloat16 rows, so that INT4 and BF16 can be timed side by side.
+ *
+ * Cache layout, per layer and tensor (K and V separately):
+ *   [num_pages][num_kv_heads][page_size][head_dim] bfloat16, rows of 256 B
+ *   (head_dim 128).  Token t of a sequence lives in page block_tables[b][t /
+ *   page_size], row t % page_size.  Owned by the caller; 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of one BF16 cache tensor; 0 for a nonpositive size. */
+size_t saw_bf16_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                            int32_t head_dim);
+
+/*
+ * saw_bf16_append -- copy the bfloat16 rows k[t][h][:] (and v, if not NULL)
+ * to slot slot_mapping[t] of the BF16 cache, unchanged.  Argument meaning,
+ * strides (in elements, multiples of 8), the -1 padding slot and the
+ * out-of-range rule (skipped, SAW_ERR_DEVICE_INDEX in *dev_status) are those
+ * of saw_quantize_append.  head_dim must be 128 and page_size 16, 32 or 64
+ * (else SAW_ERR_UNSUPPORTED).  Asynchronous on `stream`.
+ */
+int32_t saw_bf16_append(const void* k, const void* v, int64_t k_token_stride,
+                        int64_t v_token_stride, const int32_t* slot_mapping, int32_t num_tokens,
+                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                        int32_t num_pages, int32_t page_size, int32_t* dev_status, void* stream);
+
+/*
+ * Bytes of device workspace saw_paged_decode_bf16 needs for this shape (its
+ * own split plan: one CTA per SM, at least 1024 tokens per split); 0 if it
+ * needs none or the shape is invalid.  Zero-fill it before its first use;
+ * each call leaves it ready for the next.
+ */
+size_t saw_decode_bf16_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                       int32_t max_seq_len);
+
+/*
+ * saw_paged_decode_bf16 -- out[b][h][:] = softmax(sm_scale * K_b q_bh) V_b
+ * over the seq_lens[b] cached tokens of kv-head h / (num_q_heads /
+ * num_kv_heads), K and V read from the BF16 cache (no rotation, no
+ * quantization).  q: bfloat16 [num_seqs][num_q_heads][128]; out: float32,
+ * same shape.  Other arguments, sequences of length 0 (output zero), the
+ * device-side index and timeout reports, and the return codes are those of
+ * saw_paged_decode_int4.  Asynchronous on `stream`.
+ */
+int32_t saw_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, int32_t page_size, float sm_scale, float* out,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

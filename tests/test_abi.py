@@ -171,3 +171,79 @@ def _step(L, **kw):
 ])
 def test_decode_step_rejects_before_launch(L, kw, expect):
     assert _step(L, **kw) == expect
+
+
+def test_bf16_cache_bytes(L):
+    assert saw.saw_bf16_cache_bytes(1, 16, 1, 128) == 16 * 128 * 2
+    assert saw.saw_bf16_cache_bytes(10, 64, 8, 128) == 10 * 8 * 64 * 256
+    assert saw.saw_bf16_cache_bytes(0, 16, 8, 128) == 0
+    assert saw.saw_bf16_cache_bytes(4, 16, -1, 128) == 0
+
+
+def _bf16_append(L, **kw):
+    a = dict(k=A, v=B, ks=1024, vs=1024, slots=A, T=4, hkv=8, d=128, kc=A, vc=B, pages=8, P=16,
+             status=None, stream=None)
+    a.update(kw)
+    return L.saw_bf16_append(a["k"], a["v"], a["ks"], a["vs"], a["slots"], a["T"], a["hkv"],
+                             a["d"], a["kc"], a["vc"], a["pages"], a["P"], a["status"],
+                             a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
+    (dict(P=8), saw.SAW_ERR_UNSUPPORTED),
+    (dict(T=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(hkv=0), saw.SAW_ERR_INVALID_ARG),
+    (dict(k=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(slots=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(vc=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(k=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(ks=1000), saw.SAW_ERR_INVALID_ARG),     # shorter than Hkv * D
+    (dict(vs=1028), saw.SAW_ERR_INVALID_ARG),     # not a multiple of 8
+    (dict(T=0), saw.SAW_OK),
+])
+def test_bf16_append_rejects_before_launch(L, kw, expect):
+    assert _bf16_append(L, **kw) == expect
+
+
+def _bf16_decode(L, **kw):
+    a = dict(q=A, kc=A, vc=B, bt=A, mb=512, sl=B, B=2, maxlen=8192, hq=32, hkv=8, d=128,
+             pages=1024, P=16, scale=0.0, out=A, ws=B, wsb=1 << 24, status=None, stream=None)
+    a.update(kw)
+    return L.saw_paged_decode_bf16(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"], a["B"],
+                                   a["maxlen"], a["hq"], a["hkv"], a["d"], a["pages"], a["P"],
+                                   a["scale"], a["out"], a["ws"], a["wsb"], a["status"],
+                                   a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=256), saw.SAW_ERR_UNSUPPORTED),
+    (dict(P=128), saw.SAW_ERR_UNSUPPORTED),
+    (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
+    (dict(hq=72), saw.SAW_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), saw.SAW_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), saw.SAW_ERR_INVALID_ARG),
+    (dict(q=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(out=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(vc=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(mb=511), saw.SAW_ERR_INVALID_ARG),         # 511 * 16 < 8192 tokens
+    (dict(ws=None), saw.SAW_ERR_INVALID_ARG),        # several splits need a workspace
+    (dict(wsb=16), saw.SAW_ERR_INVALID_ARG),
+    (dict(ws=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(B=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(B=0), saw.SAW_OK),
+])
+def test_bf16_decode_rejects_before_launch(L, kw, expect):
+    assert _bf16_decode(L, **kw) == expect
+
+
+def test_bf16_workspace(L):
+    # several splits at 8192 tokens: counters + partials per (seq, q-head, split)
+    ws = saw.saw_decode_bf16_workspace_bytes(2, 32, 8, 128, 16, 8192)
+    assert ws > 0 and (ws - 2 * 8 * 8) % (2 * 32 * (128 + 2) * 4) == 0
+    splits = (ws - 2 * 8 * 8) // (2 * 32 * (128 + 2) * 4)
+    assert 2 <= splits <= 8   # at least 1024 tokens per split
+    # one split (short context) needs none
+    assert saw.saw_decode_bf16_workspace_bytes(2, 32, 8, 128, 16, 512) == 0
+    assert saw.saw_decode_bf16_workspace_bytes(2, 32, 8, 64, 16, 8192) == 0
