@@ -398,6 +398,7 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=
         ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
         status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()  # the zero fills ran on the default stream
 
         def one_pass():
             for l in range(layers):
@@ -425,9 +426,95 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=
     return res, overhead
 
 
-def cpu_oracle_decode_sample(case, layers, threads):
+def fill_caches_bf16(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
+    """One layer's BF16 K and V caches holding every token of every sequence
+    (the same seeded rows as fill_caches), written by saw_bf16_append."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    P = wl.page_size
+    lens_l = [int(x) for x in lens.tolist()]
+    total = sum(lens_l)
+    n = saw.saw_bf16_cache_bytes(npages, P, wl.num_kv_heads, wl.head_dim) // 2
+    kc = torch.empty(n, dtype=torch.int16, device=device)
+    vc = torch.empty(n, dtype=torch.int16, device=device)
+    slots = W.prefill_slots(bt.to(device), lens_l, P)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    for a in range(0, total, chunk_tokens):
+        b = min(total, a + chunk_tokens)
+        k = W.kv_rows(wl, layer, W.K, b - a, device, token_offset=a)
+        v = W.kv_rows(wl, layer, W.V, b - a, device, token_offset=a)
+        saw.saw_bf16_append(k, v, slots[a:b], kc, vc, npages, P, dev_status=status)
+        del k, v
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return kc, vc
+
+
+def concurrency_sweep(device, stream, batches=(1, 4, 16, 64, 128, 256), reps=10,
+                      min_pool=600_000_000):
+    """INT4 (rotated, saw_paged_decode_int4) against BF16 (saw_paged_decode_bf16)
+    decode attention on the qwen3-8b-concurrent shape (Hq 32, Hkv 8, page 16,
+    lengths uniform in [2048, 16384]) at 1..256 concurrent sequences.  Each
+    side decodes enough copies of its layer cache in turn (at least 600 MB,
+    2..64 copies) that every pass reads from HBM, not L2."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    base = W.QWEN3_8B_CONCURRENT
+    rows = []
+    for B in batches:
+        wl = base.variant(num_seqs=B)
+        lens = W.seq_lens(wl)
+        bt, npages = W.page_tables(wl, lens)
+        btd, lensd = bt.to(device), lens.to(device)
+        Hq, Hkv, D, P = wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
+        Lmax = int(lens.max())
+        q = W.q_rows(wl, 0, device)
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        row = {"seqs": B, "tokens": int(lens.sum())}
+        for kind in ("int4", "bf16"):
+            if kind == "int4":
+                kc, vc = fill_caches(wl, 0, lens, bt, npages, device, chunk_tokens=1 << 20)
+                wsb = saw.saw_decode_workspace_bytes(B, Hq, Hkv, D, P, Lmax, 0)
+                nbytes = W.decode_bytes(wl, lens.tolist())
+            else:
+                kc, vc = fill_caches_bf16(wl, 0, lens, bt, npages, device, chunk_tokens=1 << 20)
+                wsb = saw.saw_decode_bf16_workspace_bytes(B, Hq, Hkv, D, P, Lmax)
+                nbytes = W.decode_bytes_bf16(wl, lens.tolist())
+            cache_bytes = 2 * kc.numel() * kc.element_size()
+            copies = max(2, min(64, -(-min_pool // cache_bytes)))
+            pool = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(copies - 1)]
+            ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
+            torch.cuda.synchronize()  # the zero fill and the clones ran on the default stream
+
+            def one_pass():
+                for k_, v_ in pool:
+                    if kind == "int4":
+                        saw.saw_paged_decode_int4(q, k_, v_, btd, lensd, Lmax, Hkv, npages, P,
+                                                  wl.rotate_k, wl.rotate_v, wl.block_h, out, ws,
+                                                  dev_status=status)
+                    else:
+                        saw.saw_paged_decode_bf16(q, k_, v_, btd, lensd, Lmax, Hkv, npages, P,
+                                                  out, ws, dev_status=status)
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    one_pass()
+                t = statistics.median(time_events(one_pass, reps, stream)) / copies
+            assert int(status.item()) == 0
+            row[kind] = {"ms_per_layer": t, "gbs": nbytes / (t * 1e-3) / 1e9,
+                         "bytes_per_layer": nbytes, "copies": copies,
+                         "decode_tokens_per_s_36_layers": B / (36 * t * 1e-3)}
+            del pool, kc, vc, ws
+            torch.cuda.empty_cache()
+        row["int4_speedup"] = row["bf16"]["ms_per_layer"] / row["int4"]["ms_per_layer"]
+        rows.append(row)
+    return rows
+
+
+def cpu_oracle_decode_sample(case, layers, threads, min_seconds=10.0, max_passes=40):
     """Time the oracle (as it stands) on the step's work for `layers`:
-    append the new token, then decode every q-head over the layer's pages."""
+    append the new token, then decode every q-head over the layer's pages;
+    whole passes over the layers are repeated until min_seconds have gone."""
     import numpy as np
 
     import oracle
@@ -444,17 +531,23 @@ def cpu_oracle_decode_sample(case, layers, threads):
     slots = case.slot.cpu().numpy()
     bt = case.bt_cpu.numpy()
     lens = case.lens.numpy()
+    passes = 0
     t0 = time.perf_counter()
-    for kc, vc, kn, vn, q in hosts:
-        oracle.quantize_append(kn, vn, slots, wl.num_kv_heads, wl.head_dim, kc, vc, case.npages,
-                               wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h)
-        oracle.decode(q, kc, vc, bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                      case.npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
-                      threads=threads)
-    dt = time.perf_counter() - t0
-    nbytes = len(layers) * (case.W.decode_bytes(wl, case.lens.tolist()) +
-                            case.W.append_bytes(wl, wl.num_seqs))
-    return nbytes / dt / 1e9, dt
+    while True:  # whole passes over the layers until min_seconds (re-appending is idempotent)
+        for kc, vc, kn, vn, q in hosts:
+            oracle.quantize_append(kn, vn, slots, wl.num_kv_heads, wl.head_dim, kc, vc,
+                                   case.npages, wl.page_size, wl.rotate_k, wl.rotate_v,
+                                   wl.block_h)
+            oracle.decode(q, kc, vc, bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                          case.npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                          threads=threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= max_passes:
+            break
+    nbytes = passes * len(layers) * (case.W.decode_bytes(wl, case.lens.tolist()) +
+                                     case.W.append_bytes(wl, wl.num_seqs))
+    return nbytes / dt / 1e9, dt, passes
 
 
 # ------------------------------------------------------------------ arms
@@ -541,16 +634,18 @@ def run_saw(args):
     app, app_bytes, app_T = append_chunk_measure(device, stream)
     # decode alone on the bandwidth-bound workloads
     dec_cfg, dec_rot = (None, None) if args.no_decode_configs else decode_config_measure(device, stream)
+    sweep = None if args.no_decode_configs else concurrency_sweep(device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         threads = oracle.host_threads()
         layers = list(range(min(args.cpu_layers, wl.num_layers)))
-        gbs, dt = cpu_oracle_decode_sample(case, layers, threads)
+        gbs, dt, passes = cpu_oracle_decode_sample(case, layers, threads)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{len(layers)} of 36 layers of the step (1-token append + fp64 decode "
-                         f"of all 32 q-heads over 32768 tokens), {dt:.1f} s wall"}
+               "sample": f"{passes} pass(es) over {len(layers)} of the 36 layers of the step "
+                         f"(1-token append + fp64 decode of all 32 q-heads over 32768 tokens), "
+                         f"{dt:.1f} s wall"}
 
     if rank != 0:
         return
@@ -609,6 +704,13 @@ def run_saw(args):
             "peak": peak,
             "results": {k: dict(v, frac=v["gbs"] / peak) for k, v in dec_cfg.items()},
             "rotation_overhead": dec_rot,
+        },
+        "int4_vs_bf16": None if sweep is None else {
+            "what": "decode attention of one layer, INT4 (K and V rotated, h 128) vs the BF16 "
+                    "cache baseline, qwen3-8b-concurrent shape (Hq 32, Hkv 8, page 16, lengths "
+                    "uniform in [2048, 16384]) at 1..256 concurrent sequences; tokens/s = "
+                    "sequences / (36 layers x time per layer), attention only",
+            "results": sweep,
         },
         "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -692,7 +794,9 @@ def run_profile(args):
     """Small, fixed loops for ncu captures (no timing, no JSON):
     decode: the latency case's decode over --profile-layers layer caches
     (35.7 MB each, more than L2 in total), three passes;
-    append: three quantize-appends of the 131072-token chunk."""
+    append: three quantize-appends of the 131072-token chunk;
+    bf16: three BF16-cache decodes of 16 qwen3-8b-concurrent sequences
+    (about 600 MB of cache, more than L2)."""
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     import __graft_entry__
@@ -706,6 +810,25 @@ def run_profile(args):
                 case.decode_step(layer)
         torch.cuda.synchronize()
         assert int(case.status.item()) == 0
+    elif args.profile == "bf16":
+        import bit_paged_kv_gb300 as saw
+        wl = W.QWEN3_8B_CONCURRENT.variant(num_seqs=16)
+        lens = W.seq_lens(wl)
+        bt, npages = W.page_tables(wl, lens)
+        kc, vc = fill_caches_bf16(wl, 0, lens, bt, npages, device)
+        B, Hq, D = wl.num_seqs, wl.num_q_heads, wl.head_dim
+        Lmax = int(lens.max())
+        q = W.q_rows(wl, 0, device)
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        wsb = saw.saw_decode_bf16_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            saw.saw_paged_decode_bf16(q, kc, vc, bt.to(device), lens.to(device), Lmax,
+                                      wl.num_kv_heads, npages, wl.page_size, out, ws,
+                                      dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
     else:
         append_chunk_measure(device, torch.cuda.current_stream(device), iters=1)
     torch.cuda.synchronize()
@@ -718,11 +841,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["saw", "reference"], default="saw")
-    ap.add_argument("--cpu-layers", type=int, default=12)
+    ap.add_argument("--cpu-layers", type=int, default=36)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-configs", action="store_true",
                     help="skip the decode-only measurements of the other workloads")
-    ap.add_argument("--profile", choices=["decode", "append"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "bf16"], default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)
     args = ap.parse_args(argv)

@@ -213,6 +213,16 @@ def decode_bytes(wl: Workload, lens) -> int:
     return 2 * per_row * toks * Hkv + 4 * pages + B * Hq * D * (2 + 4) + 4 * B
 
 
+def decode_bytes_bf16(wl: Workload, lens) -> int:
+    """The same for a BF16 cache: K and V bfloat16 rows of every attended
+    (token, kv-head), block-table entries, q in and the output out."""
+    P, D, Hkv, Hq = wl.page_size, wl.head_dim, wl.num_kv_heads, wl.num_q_heads
+    toks = sum(int(L) for L in lens)
+    pages = sum((int(L) + P - 1) // P for L in lens)
+    B = len(list(lens))
+    return 2 * 2 * D * toks * Hkv + 4 * pages + B * Hq * D * (2 + 4) + 4 * B
+
+
 def append_bytes(wl: Workload, num_tokens: int, with_v: bool = True) -> int:
     """Algorithmic HBM bytes of one quantize-append of num_tokens tokens:
     bfloat16 rows in, codes and (scale, zero) out, one slot id per token."""
