@@ -53,6 +53,8 @@ def load() -> C.CDLL:
                                          i32, i32, i32]),
         "oracle_decode_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f64,
                                     P]),
+        "oracle_prefill_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                     f64, P]),
         "oracle_bf16_cache_bytes": (i64, [i32, i32, i32, i32]),
         "oracle_bf16_append": (i64, [P, P, i64, i64, P, i32, i32, i32, i32, P, P, i32, i32]),
         "oracle_decode_bf16_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P]),
@@ -256,6 +258,60 @@ def decode(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
     else:
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(run, range(len(pairs))))
+    return out
+
+
+def prefill(q_bits, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
+            num_kv_heads: int, head_dim: int, num_pages: int, page_size: int, rotate_k: bool,
+            rotate_v: bool, block_h: int, sm_scale: float | None = None, rows=None,
+            threads: int = 1) -> np.ndarray:
+    """fp64 chunked-prefill attention (causal) for the (query row, q_head)
+    pairs given (default: all).
+
+    q_bits: uint16 [T, Hq, D] bfloat16, the query rows of every sequence's
+    chunk, sequence after sequence; rows cu_q_lens[b] .. cu_q_lens[b+1] - 1
+    belong to sequence b and are its last q_len = cu_q_lens[b+1] - cu_q_lens[b]
+    tokens, so row i sits at position seq_lens[b] - q_len + (i - cu_q_lens[b]).
+    Returns float64 [len(rows), D].
+    """
+    q = np.ascontiguousarray(np.asarray(q_bits, dtype=np.uint16))
+    T = q.shape[0]
+    q = q.reshape(T, num_q_heads, head_dim)
+    cu = np.asarray(cu_q_lens, dtype=np.int64)
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    G = num_q_heads // num_kv_heads
+    if sm_scale is None or sm_scale == 0.0:
+        sm_scale = 1.0 / np.sqrt(head_dim)
+    seq_of = np.zeros(T, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        seq_of[cu[b]:cu[b + 1]] = b
+    if rows is None:
+        rows = [(i, hq) for i in range(T) for hq in range(num_q_heads)]
+    rows = list(rows)
+    out = np.zeros((len(rows), head_dim), dtype=np.float64)
+    lib = load()
+
+    def run(n):
+        i, hq = rows[n]
+        b = int(seq_of[i])
+        pos = int(sl[b] - (cu[b + 1] - cu[b]) + (i - cu[b]))
+        qrow = np.ascontiguousarray(q[i, hq])
+        row = np.ascontiguousarray(bt[b])
+        o = np.zeros(head_dim, dtype=np.float64)
+        rc = lib.oracle_prefill_one(_ptr(qrow), _ptr(k_cache), _ptr(v_cache), _ptr(row), pos,
+                                    hq // G, num_kv_heads, head_dim, num_pages, page_size,
+                                    int(rotate_k), int(rotate_v), block_h, float(sm_scale),
+                                    _ptr(o))
+        _check(rc, "prefill_one")
+        out[n] = o
+
+    if threads <= 1 or len(rows) <= 1:
+        for n in range(len(rows)):
+            run(n)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(run, range(len(rows))))
     return out
 
 

@@ -450,6 +450,28 @@ done:
   return rc;
 }
 
+/*
+ * Chunked-prefill attention of one query row over the INT4 cache.  The pages
+ * place SAW-INT4 inside engines that run fused (FlashAttention-style)
+ * attention over paged KV ([EN] "Why the KV Cache Is the Real Bottleneck";
+ * [IT] s.1), and define attention only through decode; the reading taken
+ * here is plain causal self-attention: the query of the token at position
+ * `query_pos` (0-based) of its sequence attends to that sequence's cached
+ * tokens 0 .. query_pos (its own K/V included, appended before the
+ * attention).
+ * That is exactly the decode above over the first query_pos + 1 tokens, so
+ * the arithmetic is oracle_decode_one's.
+ */
+int32_t oracle_prefill_one(const uint16_t* q_bf16, const uint8_t* k_cache,
+                           const uint8_t* v_cache, const int32_t* block_table_row,
+                           int32_t query_pos, int32_t kv_head, int32_t Hkv, int32_t D,
+                           int32_t num_pages, int32_t P, int32_t rotate_k, int32_t rotate_v,
+                           int32_t h, double sm_scale, double* out) {
+  if (query_pos < 0) return ORACLE_EINVAL;
+  return oracle_decode_one(q_bf16, k_cache, v_cache, block_table_row, query_pos + 1, kv_head,
+                           Hkv, D, num_pages, P, rotate_k, rotate_v, h, sm_scale, out);
+}
+
 /* ------------------------------------------------------------------ */
 /* BF16 paged cache: the unquantized baseline ([IT] s.4 compares the   */
 /* throughput of INT4 + rotation against a BF16 KV cache)              */
