@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     saw_paged_decode_bf16,
     saw_paged_decode_int4,
     saw_paged_decode_int4_noalloc,
+    saw_prefill_attn_int4,
     saw_quantize_append,
     saw_status_string,
 )

@@ -26,7 +26,7 @@ SAW_STEP_EARLY_PAGES = 1
 EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_decode_plan",
            "saw_decode_workspace_bytes", "saw_paged_decode_int4", "saw_decode_step",
            "saw_paged_decode_int4_noalloc", "saw_bf16_cache_bytes", "saw_bf16_append",
-           "saw_decode_bf16_workspace_bytes", "saw_paged_decode_bf16")
+           "saw_decode_bf16_workspace_bytes", "saw_paged_decode_bf16", "saw_prefill_attn_int4")
 
 _lib = None
 
@@ -78,6 +78,9 @@ def lib() -> C.CDLL:
     L.saw_paged_decode_bf16.restype = i32
     L.saw_paged_decode_bf16.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                         P, P, sz, P, P]
+    L.saw_prefill_attn_int4.restype = i32
+    L.saw_prefill_attn_int4.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, i32, i32, i32, f32, P, P, P]
     _lib = L
     return L
 
@@ -258,3 +261,28 @@ def saw_paged_decode_bf16(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         float(sm_scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
         _stream(q, stream))
     _raise(rc, "saw_paged_decode_bf16")
+
+
+def saw_prefill_attn_int4(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, block_tables: torch.Tensor,
+                          seq_lens: torch.Tensor, max_q_len: int, max_seq_len: int,
+                          num_kv_heads: int, num_pages: int, page_size: int, rotate_k: bool,
+                          rotate_v: bool, block_h: int, out: torch.Tensor, sm_scale: float = 0.0,
+                          dev_status=None, stream=None) -> None:
+    """Chunked-prefill attention.  q: bfloat16 [T, Hq, D] (the chunks of all
+    sequences, sequence after sequence); cu_q_lens: int32 [B + 1]; out:
+    float32 [T, Hq, D]."""
+    T, hq, d = q.shape
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (T, hq, d)
+    assert cu_q_lens.dtype == torch.int32 and cu_q_lens.is_contiguous()
+    assert block_tables.dtype == torch.int32 and block_tables.is_contiguous()
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    B = seq_lens.shape[0]
+    assert cu_q_lens.shape[0] == B + 1
+    rc = lib().saw_prefill_attn_int4(
+        _ptr(q), _ptr(cu_q_lens), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), B, T, max_q_len, max_seq_len, hq, num_kv_heads,
+        d, num_pages, page_size, int(rotate_k), int(rotate_v), block_h, float(sm_scale),
+        _ptr(out), _ptr(dev_status), _stream(q, stream))
+    _raise(rc, "saw_prefill_attn_int4")

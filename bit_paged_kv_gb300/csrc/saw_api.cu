@@ -354,6 +354,69 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
 }
 
 
+// ---------------------------------------------------------------- prefill
+
+int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                              int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t num_pages, int32_t page_size,
+                              int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
+                              float* out, int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || total_q < 0 ||
+      max_q_len < 0 || max_seq_len < 0 || max_q_len > max_seq_len)
+    return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
+  if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
+    return SAW_ERR_INVALID_ARG;
+  if (rotate_k || rotate_v) {
+    if (!pow2(block_h) || block_h > head_dim || head_dim % block_h) return SAW_ERR_INVALID_ARG;
+    if (!block_h_ok(block_h)) return SAW_ERR_UNSUPPORTED;
+  }
+  if (!(sm_scale >= 0.0f) || std::isinf(sm_scale)) return SAW_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return SAW_ERR_UNSUPPORTED;
+  const int64_t rows = int64_t(max_q_len) * (num_q_heads / num_kv_heads);
+  const int64_t row_blocks = ceil_div(rows, saw::prefill_rows_per_cta());
+  if (row_blocks > INT32_MAX || int64_t(total_q) * num_q_heads * head_dim > INT64_MAX / 8)
+    return SAW_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return SAW_OK;
+  if (!q || !cu_q_lens || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+    return SAW_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
+    return SAW_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * page_size < int64_t(max_seq_len)) return SAW_ERR_INVALID_ARG;
+  saw::PrefillParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.cu_q = cu_q_lens;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.dev_status = dev_status;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.max_q_len = max_q_len;
+  p.max_seq_len = max_seq_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.num_pages = num_pages;
+  p.page_size = page_size;
+  p.rotate_k = rotate_k;
+  p.rotate_v = rotate_v;
+  p.block_h = block_h;
+  p.row_blocks = int32_t(row_blocks);
+  p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
+  const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
+  p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  const cudaError_t err = saw::launch_prefill_attn(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- BF16 baseline
 
 size_t saw_bf16_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads,

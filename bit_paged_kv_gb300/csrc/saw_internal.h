@@ -98,6 +98,38 @@ inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t strea
   return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
 }
 
+// ---------------------------------------------------------------- prefill
+
+struct PrefillParams {
+  const uint16_t* q;            // [total_q][Hq][D] bfloat16 bits, sequence after sequence
+  const int32_t* cu_q;          // [B + 1] first query row of each sequence
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* seq_lens;      // [B] cached tokens, the chunk included
+  float* out;                   // [total_q][Hq][D]
+  int32_t* dev_status;
+  int32_t max_blocks;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_q_len;
+  int32_t max_seq_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t rotate_k;
+  int32_t rotate_v;
+  int32_t block_h;
+  int32_t row_blocks;           // grid x: ceil(max_q_len * group / rows per CTA)
+  float c_h;
+  float q_scale;                // sm_scale * log2(e)
+};
+
+int prefill_rows_per_cta();
+cudaError_t launch_prefill_attn(const PrefillParams& p, cudaStream_t stream);
+
 // Split-K workspace layout: the merge's counter words first, two per
 // (sequence, kv-head), rounded to 16 bytes; then the numerators
 // [B][Hq][splits][D], then (m, l) pairs [B][Hq][splits][2].

@@ -255,6 +255,47 @@ int32_t saw_paged_decode_int4_noalloc(const void* q, const void* k_cache, const 
                                       int32_t block_h, float sm_scale, float* out,
                                       int32_t pages_per_split, int32_t* dev_status, void* stream);
 
+/*
+ * saw_prefill_attn_int4 -- chunked-prefill attention over the INT4 cache.
+ *
+ * Pages: youngju.dev "INT4 KV-cache quantization", "Why the KV Cache Is the
+ * Real Bottleneck", and gist.science "SAW-INT4", s.1: the method has to work
+ * inside engines that run fused attention over paged KV.  Reading: the
+ * query of the token at position p of its sequence attends causally to that
+ * sequence's cached tokens 0..p; dequantization, q rotation and the inverse
+ * V rotation are those of saw_paged_decode_int4.  Append the chunk's K/V
+ * with saw_quantize_append first (same stream).
+ *
+ *  q             device bfloat16 [total_q][num_q_heads][head_dim]: the query
+ *                rows of every sequence's chunk, sequence after sequence.
+ *  cu_q_lens     device int32 [num_seqs + 1]: rows cu_q_lens[b] ..
+ *                cu_q_lens[b+1] - 1 belong to sequence b and are its last
+ *                q_len_b = cu_q_lens[b+1] - cu_q_lens[b] tokens, so row i sits
+ *                at position seq_lens[b] - q_len_b + (i - cu_q_lens[b]).
+ *  seq_lens      device int32 [num_seqs]: cached tokens, the chunk included.
+ *  max_q_len     a bound on every q_len_b (sizes the grid; <= max_seq_len).
+ *  k/v caches, block tables, rotation and block_h, sm_scale (0 = 1/sqrt(D)):
+ *                as in saw_paged_decode_int4.
+ *  out           device float32 [total_q][num_q_heads][head_dim].
+ *
+ * No workspace.  head_dim 128 and page_size 16/32/64 (else
+ * SAW_ERR_UNSUPPORTED); any number of q-heads per kv-head.  A sequence
+ * whose q_len, seq_len or cu_q_lens entries are inconsistent (q_len < 0,
+ * q_len > seq_len, q_len > max_q_len, seq_len > max_seq_len, rows beyond
+ * total_q) is skipped and
+ * SAW_ERR_DEVICE_INDEX is stored in *dev_status; a bad page id is skipped
+ * and reported the same way; a copy that never lands ends the wait after
+ * about a second with SAW_ERR_DEVICE_TIMEOUT.  Asynchronous on `stream`.
+ */
+int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                              int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t num_pages, int32_t page_size,
+                              int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
+                              float* out, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * BF16 baseline.  gist.science "SAW-INT4: System-Aware 4-Bit KV-Cache
  * Quantization for Real-World LLM Serving", s.4 measures SAW-INT4's serving

@@ -247,3 +247,35 @@ def test_bf16_workspace(L):
     # one split (short context) needs none
     assert saw.saw_decode_bf16_workspace_bytes(2, 32, 8, 128, 16, 512) == 0
     assert saw.saw_decode_bf16_workspace_bytes(2, 32, 8, 64, 16, 8192) == 0
+
+
+def _prefill(L, **kw):
+    a = dict(q=A, cu=B, kc=A, vc=B, bt=A, mb=64, sl=B, B=2, T=100, mq=64, maxlen=1024, hq=32,
+             hkv=8, d=128, pages=128, P=16, rk=1, rv=1, h=128, scale=0.0, out=A, status=None,
+             stream=None)
+    a.update(kw)
+    return L.saw_prefill_attn_int4(a["q"], a["cu"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"],
+                                   a["B"], a["T"], a["mq"], a["maxlen"], a["hq"], a["hkv"],
+                                   a["d"], a["pages"], a["P"], a["rk"], a["rv"], a["h"],
+                                   a["scale"], a["out"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
+    (dict(P=8), saw.SAW_ERR_UNSUPPORTED),
+    (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
+    (dict(h=48), saw.SAW_ERR_INVALID_ARG),
+    (dict(rk=2), saw.SAW_ERR_INVALID_ARG),
+    (dict(scale=-1.0), saw.SAW_ERR_INVALID_ARG),
+    (dict(mq=2048), saw.SAW_ERR_INVALID_ARG),        # max_q_len above max_seq_len
+    (dict(T=-1), saw.SAW_ERR_INVALID_ARG),
+    (dict(q=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(cu=None), saw.SAW_ERR_INVALID_ARG),
+    (dict(out=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(kc=MIS), saw.SAW_ERR_INVALID_ARG),
+    (dict(mb=63), saw.SAW_ERR_INVALID_ARG),           # 63 * 16 < 1024 tokens
+    (dict(B=0), saw.SAW_OK),
+    (dict(T=0), saw.SAW_OK),
+])
+def test_prefill_rejects_before_launch(L, kw, expect):
+    assert _prefill(L, **kw) == expect
