@@ -114,6 +114,18 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def read_tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s), burst figure: the prefill kernel is
+    timed on its own.  Its MMAs are binary16, which runs at the bf16 rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except Exception:
+        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -511,6 +523,68 @@ def concurrency_sweep(device, stream, batches=(1, 4, 16, 64, 128, 256), reps=10,
     return rows
 
 
+def prefill_flops(num_q_heads: int, head_dim: int, seq_len: int, q_len: int) -> int:
+    """Useful FLOPs of causal attention for one chunk: each query at position
+    p does 2 D FLOPs per key for Q K^T and 2 D for P V over p + 1 keys."""
+    first = seq_len - q_len + 1        # keys seen by the first query
+    keys = (first + seq_len) * q_len // 2
+    return 4 * head_dim * num_q_heads * keys
+
+
+def prefill_measure(device, stream, reps: int = 5):
+    """saw_prefill_attn_int4 on the long-context workload (Hq 32, Hkv 8, page
+    64, h 128, K and V rotated; the cache holds 131072 tokens): the last
+    8192-token chunk at context 131072, and a whole 16384-token prompt.  L2
+    is flushed (a 256 MB write) before every timed launch."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    wl = W.LONG_PREFILL.variant(num_seqs=1)
+    Lfull = wl.len_hi
+    lens_full = torch.tensor([Lfull], dtype=torch.int32)
+    bt, npages = W.page_tables(wl, lens_full)
+    kc, vc = fill_caches(wl, 0, lens_full, bt, npages, device)
+    btd = bt.to(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    peak, peak_src = read_tensor_peak()
+    g = torch.Generator(device=device).manual_seed(11)
+    res = {}
+    for name, L, n in (("chunk 8192 at context 131072", Lfull, 8192),
+                       ("prompt 16384", 16384, 16384)):
+        q = torch.randn(n, wl.num_q_heads, wl.head_dim, generator=g, device=device).to(torch.bfloat16)
+        out = torch.empty(n, wl.num_q_heads, wl.head_dim, dtype=torch.float32, device=device)
+        cu = torch.tensor([0, n], dtype=torch.int32, device=device)
+        sl = torch.tensor([L], dtype=torch.int32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+        def run():
+            saw.saw_prefill_attn_int4(q, cu, kc, vc, btd, sl, n, L, wl.num_kv_heads, npages,
+                                      wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h, out,
+                                      dev_status=status)
+        times = []
+        with torch.cuda.stream(stream):
+            run()
+            for _ in range(reps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                run()
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b))
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        t = statistics.median(times)
+        fl = prefill_flops(wl.num_q_heads, wl.head_dim, L, n)
+        tf = fl / (t * 1e-3) / 1e12
+        res[name] = {"ms": t, "flops": fl, "tflops": tf, "frac": tf / peak,
+                     "tokens_per_s": n / (t * 1e-3)}
+        del q, out
+    del kc, vc, flush
+    torch.cuda.empty_cache()
+    return res, peak, peak_src
+
+
 def cpu_oracle_decode_sample(case, layers, threads, min_seconds=10.0, max_passes=40):
     """Time the oracle (as it stands) on the step's work for `layers`:
     append the new token, then decode every q-head over the layer's pages;
@@ -635,6 +709,7 @@ def run_saw(args):
     # decode alone on the bandwidth-bound workloads
     dec_cfg, dec_rot = (None, None) if args.no_decode_configs else decode_config_measure(device, stream)
     sweep = None if args.no_decode_configs else concurrency_sweep(device, stream)
+    pre = None if args.no_decode_configs else prefill_measure(device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -711,6 +786,14 @@ def run_saw(args):
                     "uniform in [2048, 16384]) at 1..256 concurrent sequences; tokens/s = "
                     "sequences / (36 layers x time per layer), attention only",
             "results": sweep,
+        },
+        "prefill_attn": None if pre is None else {
+            "what": "saw_prefill_attn_int4 (causal, INT4 cache, q and V-output rotation), "
+                    "long-context shape: Hq 32, Hkv 8, page 64, h 128, K and V rotated",
+            "roofline": {"bound": "tensor", "peak": pre[1], "unit": "TFLOP/s",
+                         "peak_source": pre[2],
+                         "flops": "useful causal FLOPs: 4 * head_dim * Hq per (query, visible key)"},
+            "results": pre[0],
         },
         "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -796,7 +879,8 @@ def run_profile(args):
     (35.7 MB each, more than L2 in total), three passes;
     append: three quantize-appends of the 131072-token chunk;
     bf16: three BF16-cache decodes of 16 qwen3-8b-concurrent sequences
-    (about 600 MB of cache, more than L2)."""
+    (about 600 MB of cache, more than L2);
+    prefill: three 2048-token chunks at context 16384 (long-context shape)."""
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     import __graft_entry__
@@ -810,6 +894,23 @@ def run_profile(args):
                 case.decode_step(layer)
         torch.cuda.synchronize()
         assert int(case.status.item()) == 0
+    elif args.profile == "prefill":
+        import bit_paged_kv_gb300 as saw
+        wl = W.LONG_PREFILL.variant(num_seqs=1)
+        L, n = 16384, 2048
+        lens = torch.tensor([L], dtype=torch.int32)
+        bt, npages = W.page_tables(wl, lens)
+        kc, vc = fill_caches(wl, 0, lens, bt, npages, device)
+        q = torch.randn(n, wl.num_q_heads, wl.head_dim, device=device).to(torch.bfloat16)
+        out = torch.empty(n, wl.num_q_heads, wl.head_dim, dtype=torch.float32, device=device)
+        cu = torch.tensor([0, n], dtype=torch.int32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            saw.saw_prefill_attn_int4(q, cu, kc, vc, bt.to(device), lens.to(device), n, L,
+                                      wl.num_kv_heads, npages, wl.page_size, wl.rotate_k,
+                                      wl.rotate_v, wl.block_h, out, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
     elif args.profile == "bf16":
         import bit_paged_kv_gb300 as saw
         wl = W.QWEN3_8B_CONCURRENT.variant(num_seqs=16)
@@ -845,7 +946,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-configs", action="store_true",
                     help="skip the decode-only measurements of the other workloads")
-    ap.add_argument("--profile", choices=["decode", "append", "bf16"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "bf16", "prefill"], default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)
     args = ap.parse_args(argv)

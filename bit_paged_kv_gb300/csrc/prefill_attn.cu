@@ -8,12 +8,14 @@
 // The chunk's K/V are appended (saw_quantize_append) before this runs.
 //
 // Design (sm_103a), FlashAttention-2 shape on the legacy warp MMA:
-//  * CTA = (block of 64 query rows, kv-head, sequence); a row is one
+//  * CTA = (block of 112 query rows, kv-head, sequence); a row is one
 //    (query token, q-head of the kv-head's group) pair, token-major, so the
-//    whole GQA group shares every K/V tile.  Four consumer warps own 16 rows
-//    each; a fifth warp streams 16-key tiles (K codes + metadata, V codes +
-//    metadata: 2176 B) through an 8-stage ring with the bulk-copy engine,
-//    full/empty mbarriers (every wait bounded).
+//    whole GQA group shares every K/V tile.  Seven consumer warps own 16 rows
+//    each (about 200 registers a thread: eight warps of it fit an SM's four
+//    register files, two per file); an eighth warp streams 16-key tiles
+//    (K codes + metadata, V codes + metadata: 2176 B) through an 8-stage
+//    ring with the bulk-copy engine, full/empty mbarriers (every wait
+//    bounded).
 //  * S = Q K^T on mma.m16n8k16: rows on M, keys on N, dims on K.  The K
 //    operand is the raw codes masked into binary16 subnormals (n * 2^-24 for
 //    a low nibble, n * 2^-20 for a high one), so no dequantization pass; q'
@@ -31,7 +33,7 @@
 namespace saw {
 namespace {
 
-constexpr int kPW = 4;                       // consumer warps
+constexpr int kPW = 7;                       // consumer warps
 constexpr int kPThreads = 32 * (kPW + 1);    // + one producer warp
 constexpr int kPRows = 16 * kPW;             // query rows per CTA
 constexpr int kPStages = 8;
@@ -296,8 +298,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const Prefil
       const bool ok = stage_ok[s] != 0;
       // ---- S = Q K^T: n-tile 0 = keys k0..k0+7 (B column g <- key g),
       // n-tile 1 = keys k0+8..k0+15
+      // four independent accumulators (q' hi / lo x two n-tiles): chains of
+      // 8 dependent MMAs instead of 16
       float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       {
+        float u0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, u1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         const uint4 wk0 = *reinterpret_cast<const uint4*>(st + g * 64 + 16 * c);
         const uint4 wk1 = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + 16 * c);
         const uint32_t w0[4] = {wk0.x, wk0.y, wk0.z, wk0.w};
@@ -307,9 +312,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const Prefil
           const uint32_t x0 = (ks & 1) ? (w0[ks >> 1] >> 8) : w0[ks >> 1];
           const uint32_t x1 = (ks & 1) ? (w1[ks >> 1] >> 8) : w1[ks >> 1];
           mma_16816(s0, ah[ks], x0 & kLo, x0 & kHi);
-          mma_16816(s0, al[ks], x0 & kLo, x0 & kHi);
           mma_16816(s1, ah[ks], x1 & kLo, x1 & kHi);
-          mma_16816(s1, al[ks], x1 & kLo, x1 & kHi);
+          mma_16816(u0, al[ks], x0 & kLo, x0 & kHi);
+          mma_16816(u1, al[ks], x1 & kLo, x1 & kHi);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s0[j] += u0[j];
+          s1[j] += u1[j];
         }
       }
       // ---- logits: this lane holds keys 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c
