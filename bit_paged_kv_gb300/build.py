@@ -30,6 +30,7 @@ UNITS = [("saw_api.cu", "saw_api.o", []),
          ("paged_decode.cu", "paged_decode_w8.o", ["-DSAW_DECODE_WARPS=8"]),
          ("paged_decode_bf16.cu", "paged_decode_bf16.o", []),
          ("prefill_attn.cu", "prefill_attn.o", []),
+         ("variants.cu", "variants.o", []),
          ("decode_static_scratch.cu", "decode_static_scratch.o", [])]
 
 

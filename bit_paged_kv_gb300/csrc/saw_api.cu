@@ -15,7 +15,9 @@ using saw::kHeadDim;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 bool page_size_ok(int p) { return p == 16 || p == 32 || p == 64; }
-bool block_h_ok(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+bool block_h_ok(int h) { return h == 16 || h == 32 || h == 64 || h == 128 || h == 256; }
+// head_dim 128 runs the specialised kernels; 64 and 256 the variant kernels
+bool head_dim_ok(int d) { return d == 64 || d == kHeadDim || d == 256; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -161,7 +163,7 @@ int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride
                             int32_t rotate_k, int32_t rotate_v, int32_t block_h,
                             int32_t* dev_status, void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_pages < 0) return SAW_ERR_INVALID_ARG;
-  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (!head_dim_ok(head_dim) || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
   if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
     return SAW_ERR_INVALID_ARG;
   const bool has_v = v != nullptr;
@@ -198,7 +200,9 @@ int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride
   p.num_slots = int64_t(num_pages) * page_size;
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   cudaError_t err =
-      saw::launch_quantize_append(p, has_v ? 2 : 1, static_cast<cudaStream_t>(stream));
+      head_dim == kHeadDim
+          ? saw::launch_quantize_append(p, has_v ? 2 : 1, static_cast<cudaStream_t>(stream))
+          : saw::launch_quantize_append_var(p, head_dim, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 
@@ -213,7 +217,7 @@ int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_siz
 size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t page_size, int32_t max_seq_len,
                                   int32_t pages_per_split) {
-  if (head_dim != kHeadDim || num_q_heads <= 0) return 0;
+  if (!head_dim_ok(head_dim) || num_q_heads <= 0) return 0;
   int32_t splits = 0, pps = 0;
   if (make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, &splits, &pps) !=
       SAW_OK)
@@ -239,7 +243,7 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
                        int32_t* dev_status) {
   if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || max_seq_len < 0)
     return SAW_ERR_INVALID_ARG;
-  if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
+  if (!head_dim_ok(head_dim) || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
   if (num_q_heads / num_kv_heads > saw::kMaxGroup) return SAW_ERR_UNSUPPORTED;
   if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
@@ -294,6 +298,7 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.pages_per_split = pps;
   p.num_splits = splits;
   p.warps = warps;
+  p.head_dim = head_dim;
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
@@ -319,7 +324,9 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
                                     sm_scale, out, workspace, workspace_bytes, pages_per_split,
                                     dev_status);
   if (rc != SAW_OK || num_seqs == 0) return rc;
-  cudaError_t err = saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream));
+  cudaError_t err = head_dim == kHeadDim
+                        ? saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream))
+                        : saw::launch_paged_decode_var(p, head_dim, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 
@@ -333,6 +340,7 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
                         int32_t* dev_status, void* stream) {
   saw::DecodeParams p{};
   if (flags & ~int32_t(SAW_STEP_EARLY_PAGES)) return SAW_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return SAW_ERR_UNSUPPORTED;  // the fused step is built for 128
   const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                     seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
                                     head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,

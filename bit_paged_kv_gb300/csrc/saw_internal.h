@@ -83,11 +83,15 @@ struct DecodeParams {
   float c_h;                    // 1/sqrt(block_h)
   float q_scale;                // sm_scale * log2(e)
   int32_t warps;                // CTA shape: 16 (one per SM) or 8 (two per SM)
+  int32_t head_dim;             // 128, or 64 / 256 (variant kernels)
 };
 
 // One launcher per CTA shape (paged_decode.cu compiled once per shape).
 cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
+// head_dim 64 and 256 (variants.cu)
+cudaError_t launch_quantize_append_var(const AppendParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_paged_decode_var(const DecodeParams& p, int head_dim, cudaStream_t stream);
 // BF16 baseline (paged_decode_bf16.cu)
 cudaError_t launch_paged_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_stride,

@@ -69,7 +69,7 @@ def _append(L, **kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(d=64), saw.SAW_ERR_UNSUPPORTED),
+    (dict(d=96), saw.SAW_ERR_UNSUPPORTED),   # head_dim 64, 128, 256 only
     (dict(P=8), saw.SAW_ERR_UNSUPPORTED),
     (dict(h=3), saw.SAW_ERR_INVALID_ARG),
     (dict(h=256), saw.SAW_ERR_INVALID_ARG),
@@ -103,7 +103,7 @@ def _decode(L, **kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(d=256), saw.SAW_ERR_UNSUPPORTED),
+    (dict(d=96), saw.SAW_ERR_UNSUPPORTED),
     (dict(P=128), saw.SAW_ERR_UNSUPPORTED),
     (dict(hq=12), saw.SAW_ERR_INVALID_ARG),
     (dict(hq=72), saw.SAW_ERR_UNSUPPORTED),        # 9 q-heads per kv-head
