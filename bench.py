@@ -585,6 +585,71 @@ def prefill_measure(device, stream, reps: int = 5):
     return res, peak, peak_src
 
 
+def variants_measure(device, stream, reps: int = 10):
+    """head_dim 64 and 256 (variant kernels): decode alone on the
+    qwen3-8b-concurrent shape (64 sequences, lengths in [2048, 16384], K and V
+    rotated with h = head_dim, two layer caches decoded in turn), and the
+    quantize-append of a 131072-token chunk (Hkv 8, K and V, page 64)."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    res = {}
+    for D in (64, 256):
+        wl = W.QWEN3_8B_CONCURRENT.variant(head_dim=D, block_h=D)
+        lens = W.seq_lens(wl)
+        bt, npages = W.page_tables(wl, lens)
+        btd, lensd = bt.to(device), lens.to(device)
+        B, Hq = wl.num_seqs, wl.num_q_heads
+        Lmax = int(lens.max())
+        caches = [fill_caches(wl, l, lens, bt, npages, device, chunk_tokens=1 << 20) for l in range(2)]
+        qs = [W.q_rows(wl, l, device) for l in range(2)]
+        wsb = saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, 0)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+        def one_pass():
+            for l in range(2):
+                saw.saw_paged_decode_int4(qs[l], caches[l][0], caches[l][1], btd, lensd, Lmax,
+                                          wl.num_kv_heads, npages, wl.page_size, True, True, D,
+                                          out, ws, dev_status=status)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                one_pass()
+            t = statistics.median(time_events(one_pass, reps, stream)) / 2
+        assert int(status.item()) == 0
+        nbytes = W.decode_bytes(wl, lens.tolist())
+        res[f"decode head_dim {D}"] = {"ms_per_layer": t, "gbs": nbytes / (t * 1e-3) / 1e9,
+                                       "bytes_per_layer": nbytes}
+        del caches, qs, ws, out
+        torch.cuda.empty_cache()
+        # bulk append
+        wa = W.LONG_PREFILL.variant(num_seqs=1, head_dim=D, block_h=D)
+        T = wa.len_hi
+        lens1 = torch.tensor([T], dtype=torch.int32)
+        bt1, np1 = W.page_tables(wa, lens1)
+        k = W.kv_rows(wa, 0, W.K, T, device)
+        v = W.kv_rows(wa, 0, W.V, T, device)
+        slots = W.prefill_slots(bt1.to(device), [T], wa.page_size)
+        nb = saw.saw_cache_bytes(np1, wa.page_size, wa.num_kv_heads, D)
+        kc = torch.empty(nb, dtype=torch.uint8, device=device)
+        vc = torch.empty(nb, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+        def app():
+            saw.saw_quantize_append(k, v, slots, kc, vc, np1, wa.page_size, True, True, D)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                app()
+            t = statistics.median(time_events(app, reps, stream))
+        ab = W.append_bytes(wa, T)
+        res[f"append head_dim {D}"] = {"ms": t, "gbs": ab / (t * 1e-3) / 1e9,
+                                       "tokens_per_s": T / (t * 1e-3), "bytes": ab}
+        del k, v, kc, vc
+        torch.cuda.empty_cache()
+    return res
+
+
 def cpu_oracle_decode_sample(case, layers, threads, min_seconds=10.0, max_passes=40):
     """Time the oracle (as it stands) on the step's work for `layers`:
     append the new token, then decode every q-head over the layer's pages;
@@ -710,6 +775,7 @@ def run_saw(args):
     dec_cfg, dec_rot = (None, None) if args.no_decode_configs else decode_config_measure(device, stream)
     sweep = None if args.no_decode_configs else concurrency_sweep(device, stream)
     pre = None if args.no_decode_configs else prefill_measure(device, stream)
+    var = None if args.no_decode_configs else variants_measure(device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -794,6 +860,13 @@ def run_saw(args):
                          "peak_source": pre[2],
                          "flops": "useful causal FLOPs: 4 * head_dim * Hq per (query, visible key)"},
             "results": pre[0],
+        },
+        "head_dim_variants": None if var is None else {
+            "what": "head_dim 64 and 256 (CUDA-core decode kernel, warp-per-row append), "
+                    "h = head_dim; decode on the qwen3-8b-concurrent shape, append on a "
+                    "131072-token chunk; GB/s = algorithmic bytes / time",
+            "peak": peak,
+            "results": {k: dict(v, frac=v["gbs"] / peak) for k, v in var.items()},
         },
         "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

@@ -92,8 +92,8 @@ size_t saw_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_head
  * rotate_k, rotate_v  0 or 1: apply the block-diagonal Hadamard rotation
  *               before quantizing.  The gist.science page (s.4) reports that
  *               rotating K only matches rotating both.
- * block_h       rotation block size h: 16, 32, 64 or 128, dividing head_dim
- *               (ignored when neither tensor is rotated).
+ * block_h       rotation block size h: 16, 32, 64, 128 or 256, at most
+ *               head_dim (ignored when neither tensor is rotated).
  *
  * Per row, exactly: widen to binary32; if rotated, an in-place butterfly per
  * h-block with strides 1, 2, ..., h/2 (each a+b, a-b rounded to nearest),
@@ -104,7 +104,9 @@ size_t saw_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_head
  * one binary32 round-to-nearest step, so the bytes are fully determined.
  * Inputs are expected finite; non-finite inputs give unspecified codes.
  *
- * Supported: head_dim 128; page_size 16, 32 or 64; num_kv_heads >= 1.
+ * Supported: head_dim 64, 128 or 256 (128 runs the tiled bulk kernel, 64
+ * and 256 a warp-per-row kernel; the bytes follow the same rule); page_size
+ * 16, 32 or 64; num_kv_heads >= 1.  Other sizes: SAW_ERR_UNSUPPORTED.
  * Rows whose slot is written by two tokens of the same call race.
  */
 int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride,
@@ -172,10 +174,13 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  * Computes, per (sequence, q-head): q' = (1/sqrt(h)) H q if K was rotated;
  * t_j = sm_scale * q'.(code_j*s_j + z_j); p = softmax(t); o' = sum_j p_j
  * (code_j*s_j + z_j) over V; o = (1/sqrt(h)) H o' if V was rotated.  The
- * GQA group of a kv-head is served by one pass over its pages.  Arithmetic:
- * q' and p*s in binary16 on the tensor cores with binary32 accumulation,
- * softmax in binary32; results match a float64 evaluation to about 1e-3 of
- * the output's largest magnitude.
+ * GQA group of a kv-head is served by one pass over its pages.  Arithmetic
+ * at head_dim 128: q' and p*s in binary16 on the tensor cores with binary32
+ * accumulation, softmax in binary32; results match a float64 evaluation to
+ * about 1e-3 of the output's largest magnitude.  head_dim 64 and 256 run a
+ * binary32 CUDA-core kernel (same split plan, workspace layout and merge).
+ * Up to 8 q-heads per kv-head; head_dim 64, 128 or 256 (else
+ * SAW_ERR_UNSUPPORTED).
  */
 int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -208,7 +213,8 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
  *               waits for it before reading q, k_new, v_new or writing.
  * Other arguments as saw_paged_decode_int4.  The appended bytes equal those
  * of saw_quantize_append on the same row, and the output equals
- * saw_quantize_append followed by saw_paged_decode_int4.
+ * saw_quantize_append followed by saw_paged_decode_int4.  head_dim 128 only
+ * (SAW_ERR_UNSUPPORTED otherwise).
  */
 #define SAW_STEP_EARLY_PAGES 1
 int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
