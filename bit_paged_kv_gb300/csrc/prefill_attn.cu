@@ -1,4 +1,5 @@
-// prefill_attn.cu -- chunked-prefill attention over the paged INT4 cache.
+// prefill_attn.cu -- chunked-prefill attention over the paged INT4 cache on
+// the 5th-generation tensor cores (tcgen05; accumulators in tensor memory).
 //
 // Pages: youngju.dev "INT4 KV-cache quantization", "Why the KV Cache Is the
 // Real Bottleneck" and gist.science "SAW-INT4", s.1 (the method has to live
@@ -7,59 +8,122 @@
 // at position p of its sequence attends causally to cached tokens 0..p.
 // The chunk's K/V are appended (saw_quantize_append) before this runs.
 //
-// Design (sm_103a), FlashAttention-2 shape on the legacy warp MMA:
-//  * CTA = (block of 112 query rows, kv-head, sequence); a row is one
-//    (query token, q-head of the kv-head's group) pair, token-major, so the
-//    whole GQA group shares every K/V tile.  Seven consumer warps own 16 rows
-//    each (about 200 registers a thread: eight warps of it fit an SM's four
-//    register files, two per file); an eighth warp streams 16-key tiles
-//    (K codes + metadata, V codes + metadata: 2176 B) through an 8-stage
-//    ring with the bulk-copy engine, full/empty mbarriers (every wait
-//    bounded).
-//  * S = Q K^T on mma.m16n8k16: rows on M, keys on N, dims on K.  The K
-//    operand is the raw codes masked into binary16 subnormals (n * 2^-24 for
-//    a low nibble, n * 2^-20 for a high one), so no dequantization pass; q'
-//    is rotated in registers, scaled per row by 2^S (odd dims 2^(S-4)) and
-//    split into binary16 hi + lo, held in registers as A fragments.
-//  * t = sm' (s_k 2^(24-S) acc + z_k sum(q')), online softmax in base 2.
-//  * O += (p s_v) V on the MMA: P straight from the score accumulators (the
-//    C layout of two key n-tiles is the A layout of one k16 step), V codes
-//    paired across keys with byte permutes and masked the same way; sum(p z_v)
-//    is added per row at the end, then the inverse V rotation in registers.
+// Design (sm_103a):
+//  * CTA = (block of 128 query rows, kv-head, sequence); a row is one
+//    (query token, q-head of the group) pair, token-major, so the whole GQA
+//    group shares every K/V tile.  Keys go by tiles of 64.
+//  * Fourteen warps, specialised:
+//      0-7   softmax: two threads per row r (tensor-memory lane r), one per
+//            half: keys 32h .. 32h+31 of a tile, and dims 64h .. 64h+63 of
+//            q' and of the output.  They rotate q' (the stride-64 butterfly
+//            step through shared memory), scale it by 2^S and write it as
+//            binary16 hi + lo operands; per tile they read their half of the
+//            scores from tensor memory, mask, exchange the row max with the
+//            other half (named barrier), rescale their half of the output
+//            accumulator in tensor memory when the max grows, and write p*s_V
+//            as the binary16 A operand of the P.V product; at the end they
+//            normalise, inverse-rotate V and store.
+//      8-11  expanders: widen a raw INT4 tile into the K operand (keys x
+//            dims) and the transposed V operand (dims x keys), each code n
+//            as the binary16 subnormal n * 2^-24 (exact), and unpack the
+//            tile's (s, z) metadata to binary32.
+//      12    producer: 16-key slices (codes and metadata of K and V) through
+//            a 4-stage ring with the bulk-copy engine.
+//      13    MMA: one thread issues S = Q' K^T (M 128, N 64, K 128; q' hi and
+//            lo accumulate into the same scores) and O += P V (M 128, N 128,
+//            K 64) with tcgen05.mma, and signals completion with
+//            tcgen05.commit; the warp also allocates the 256 tensor-memory
+//            columns (S double-buffered at columns 0 and 64, O at 128).
+//  * Operands are K-major, unswizzled, in 8-row x 16-byte core matrices.
+//    Every mbarrier wait is bounded to about a second; the softmax warps,
+//    which also meet at a named barrier, never leave their loop early (a
+//    failed wait only marks the result), so that barrier always completes.
 #include "saw_device.cuh"
 #include "saw_int4.h"
 #include "saw_quant_row.cuh"
+#include "saw_tcgen05.cuh"
 
 namespace saw {
 namespace {
 
-constexpr int kPW = 7;                       // consumer warps
-constexpr int kPThreads = 32 * (kPW + 1);    // + one producer warp
-constexpr int kPRows = 16 * kPW;             // query rows per CTA
-constexpr int kPStages = 8;
-constexpr int kTileTok = 16;
-constexpr int kCodes = kTileTok * kHeadDim / 2;    // 1024 B of codes per tile and tensor
-constexpr int kMeta = kTileTok * 4;                // 64 B of (s, z) per tile and tensor
-constexpr int kHalfStage = kCodes + kMeta;         // 1088
-constexpr int kPStage = 2 * kHalfStage;            // 2176
-constexpr int kOffFull = kPStages * kPStage;
-constexpr int kOffEmpty = kOffFull + kPStages * 8;
-constexpr int kOffOk = kOffEmpty + kPStages * 8;
-constexpr int kPSmem = kOffOk + kPStages * 4;
-constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr uint32_t kLo = 0x000F000Fu;        // low nibbles of bytes 0 and 2 -> two halves
-constexpr uint32_t kHi = 0x00F000F0u;        // high nibbles
+constexpr int kBM = 128;               // query rows per CTA (MMA M)
+constexpr int kBN = 64;                // keys per tile
+constexpr int kRawStages = 4;
+constexpr int kSoftWarps = 8;
+constexpr int kTThreads = 32 * (kSoftWarps + 4 + 2);  // softmax, expanders, producer, MMA
+constexpr int kWarpExp0 = kSoftWarps;
+constexpr int kWarpProd = kSoftWarps + 4;
+constexpr int kWarpMma = kSoftWarps + 5;
+constexpr uint32_t kAllLanes = 0xFFFFFFFFu;
 
-// In-register block-diagonal Sylvester butterfly over one row whose 128
-// values are spread over the 4 lanes of an MMA quad, 32 consecutive dims
-// each (lane c holds dims 32c..32c+31 in v[0..31]).  Strides below 32 are
-// local, 32 and 64 pair lanes c ^ 1 and c ^ 2.  Unscaled: H, not H/sqrt(h).
-__device__ __forceinline__ void quad_fwht(float (&v)[32], int h, int c) {
+constexpr int kQBytes = kBM * kHeadDim * 2;        // one of q' hi / lo
+constexpr int kKxBytes = kBN * kHeadDim * 2;       // K operand of one tile
+constexpr int kVxBytes = kHeadDim * kBN * 2;       // V^T operand of one tile
+constexpr int kPBytes = kBM * kBN * 2;             // P operand of one tile
+constexpr int kRawCodes = kBN * (kHeadDim / 2);    // 4096 code bytes per tensor
+// raw stage: K codes | V codes | K meta | V meta | slice-ok word
+constexpr int kRawV = kRawCodes;
+constexpr int kRawKM = 2 * kRawCodes;
+constexpr int kRawVM = kRawKM + kBN * 4;
+constexpr int kRawOk = kRawVM + kBN * 4;
+constexpr int kRawBytes = kRawOk + 16;
+constexpr int kMetaBytes = kBN * 16 + 16;          // s_k[64], z_k[64], s_v[64], z_v[64] + ok word
+
+constexpr int kOffQh = 0;
+constexpr int kOffQl = kOffQh + kQBytes;
+constexpr int kOffKx = kOffQl + kQBytes;
+constexpr int kOffVx = kOffKx + 2 * kKxBytes;
+constexpr int kOffP = kOffVx + 2 * kVxBytes;
+constexpr int kOffRaw = kOffP + 2 * kPBytes;
+constexpr int kOffMeta = kOffRaw + kRawStages * kRawBytes;
+constexpr int kOffXm = kOffMeta + 2 * kMetaBytes;          // f32 [2 tiles][2 halves][128] row maxima
+constexpr int kOffXl = kOffXm + 2 * 2 * kBM * 4;           // f32x2 [2 halves][128]
+constexpr int kOffBar = kOffXl + 2 * kBM * 8;
+enum {
+  kRawFull = 0, kRawEmpty = 4, kMetaFull = 8, kMetaEmpty = 10, kKxFull = 12, kKxEmpty = 14,
+  kVxFull = 16, kPvDone = 18, kSFull = 20, kSEmpty = 22, kPFull = 24, kMmaDone = 26, kNumBars = 27
+};
+constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kTSmem = kOffTmem + 16;
+static_assert(kTSmem <= 227 * 1024, "shared memory");
+static_assert(kRawBytes % 16 == 0 && kMetaBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
+// the 128 x 128 binary32 exchange of the q' and output rotations reuses the
+// K/V operand buffers (prologue) and the q' buffers (epilogue)
+static_assert(2 * kKxBytes + 2 * kVxBytes >= kBM * kHeadDim * 4 && 2 * kQBytes >= kBM * kHeadDim * 4,
+              "exchange space");
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
+constexpr int kSoftBar = 1;                         // named barrier id of the softmax warps
+
+__device__ __forceinline__ float f16lo_(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16hi_(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
+}
+// 2^e for -126 <= e <= 127, exactly
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
+
+// The softmax warps' barrier; returns the AND of `ok` over its threads.
+__device__ __forceinline__ bool soft_sync_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(ok)), "r"(kSoftBar), "r"(32 * kSoftWarps)
+      : "memory");
+  return r != 0;
+}
+
+// Half of a row's block-diagonal Sylvester butterfly: the 64 values this
+// thread holds (dims 64h .. 64h+63), strides 1 .. 32 (unscaled).
+__device__ __forceinline__ void half_fwht(float (&v)[64], int hblk) {
 #pragma unroll
-  for (int s = 1; s < 32; s <<= 1) {
-    if (s < h) {
+  for (int s = 1; s < 64; s <<= 1) {
+    if (s < hblk) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
+      for (int i = 0; i < 64; ++i)
         if (!(i & s)) {
           const float a = v[i], b = v[i + s];
           v[i] = a + b;
@@ -67,47 +131,60 @@ __device__ __forceinline__ void quad_fwht(float (&v)[32], int h, int c) {
         }
     }
   }
+}
+
+// The stride-64 step (h = 128): lower half gets a + b, upper half a - b,
+// through a [128][128] binary32 scratch row in shared memory.
+__device__ __forceinline__ void stride64_step(float (&v)[64], float* scratch_row, int half) {
 #pragma unroll
-  for (int s = 32; s < 128; s <<= 1) {
-    if (s < h) {
-      const int m = s >> 5;                 // lane bit
-      const bool upper = (c & m) != 0;
+  for (int k = 0; k < 16; ++k)
+    reinterpret_cast<float4*>(scratch_row + 64 * half)[k] =
+        make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  (void)soft_sync_and(true);
+  const float* other = scratch_row + 64 * (1 - half);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float o = __shfl_xor_sync(kFull, v[i], m);
-        v[i] = upper ? (o - v[i]) : (v[i] + o);
-      }
+  for (int k = 0; k < 16; ++k) {
+    const float4 o = reinterpret_cast<const float4*>(other)[k];
+    const float w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 4 * k + e;
+      v[i] = half ? (w[e] - v[i]) : (v[i] + w[e]);
     }
   }
 }
 
-__device__ __forceinline__ float quad_sum(float x) {
-  x += __shfl_xor_sync(kFull, x, 1);
-  return x + __shfl_xor_sync(kFull, x, 2);
-}
-__device__ __forceinline__ float quad_max(float x) {
-  x = fmaxf(x, __shfl_xor_sync(kFull, x, 1));
-  return fmaxf(x, __shfl_xor_sync(kFull, x, 2));
+// Spinning wait for the softmax warps (on the critical path); a wait after
+// a failure returns at once.
+__device__ __forceinline__ bool wait_soft(uint64_t* bar, uint32_t parity, bool& failed) {
+  if (failed) return false;
+  const bool ok = __all_sync(kAllLanes, mbar_wait_bounded(bar, parity));
+  failed = !ok;
+  return ok;
 }
 
-// 2^e for -126 <= e <= 127, exactly
-__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
-
-__device__ __forceinline__ float f16lo(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
+// Waits of the other roles sleep between polls, leaving the issue slots of
+// their scheduler to the softmax warps.
+__device__ __forceinline__ bool wait_sleep(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+    __nanosleep(64);
+  }
+  return true;
 }
-__device__ __forceinline__ float f16hi(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
+__device__ __forceinline__ bool wait_sleep_all(uint64_t* bar, uint32_t parity) {
+  return __all_sync(kAllLanes, wait_sleep(bar, parity));
 }
 
 template <int P>
-__global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   pdl_wait_then_release();
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kOffEmpty);
-  int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + kOffOk);
-  constexpr int kTilesPerPage = P / kTileTok;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  constexpr int kChunk = P * (kHeadDim / 2 + 4);
 
   const int kvh = blockIdx.y, seq = blockIdx.z;
   const int rb = p.row_blocks - 1 - blockIdx.x;  // longest blocks first
@@ -124,67 +201,168 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const Prefil
     return;
   }
   const int R = ql * G;
-  const int row0 = rb * kPRows;
+  const int row0 = rb * kBM;
   if (row0 >= R) return;
-  const int row_end = min(R, row0 + kPRows);
-  const int pos_base = L - ql;                      // position of the chunk's first token
+  const int row_end = min(R, row0 + kBM);
+  const int pos_base = L - ql;
   const int pos_max = pos_base + (row_end - 1) / G;
-  const int n_tiles = pos_max / kTileTok + 1;
+  const int n_tiles = pos_max / kBN + 1;
+  const int n_pages = (L + P - 1) / P;
 
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kPW);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&bars[kRawFull + s], 1);
+      mbar_init(&bars[kRawEmpty + s], 4);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[kMetaFull + b], 4);
+      mbar_init(&bars[kMetaEmpty + b], kSoftWarps);
+      mbar_init(&bars[kKxFull + b], 4);
+      mbar_init(&bars[kKxEmpty + b], 1);
+      mbar_init(&bars[kVxFull + b], 4);
+      mbar_init(&bars[kPvDone + b], 1);
+      mbar_init(&bars[kSFull + b], 1);
+      mbar_init(&bars[kSEmpty + b], kSoftWarps);
+      mbar_init(&bars[kPFull + b], kSoftWarps);
+    }
+    mbar_init(&bars[kMmaDone], 1);
     mbar_fence_init();
   }
-  __syncthreads();
+  if (warp == kWarpMma) tmem_alloc(tslot, kTmemCols);
 
-  // ------------------------------------------------------------ producer
-  if (warp == kPW) {
+  // ---- softmax warps: q' rows into the A operands
+  const int half = warp >> 2;                // softmax threads: keys / dims half
+  const int r = 32 * (warp & 3) + lane;      // and row (tensor-memory lane)
+  bool row_valid = false;
+  int pos_r = -1, out_t = 0, out_h = 0;
+  float rowA = 0.0f, qc = 0.0f;
+  float2* xl = reinterpret_cast<float2*>(smem + kOffXl);
+  if (warp < kSoftWarps) {
+    const int row = row0 + r;
+    row_valid = row < row_end;
+    float v[64];
+    if (row_valid) {
+      out_t = row / G;
+      out_h = row - out_t * G;
+      pos_r = pos_base + out_t;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (int64_t(q0 + out_t) * p.num_q_heads + kvh * G + out_h) * kHeadDim + 64 * half);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 w = src[k];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * k + 2 * j] = bf16_lo(ws[j]);
+          v[8 * k + 2 * j + 1] = bf16_hi(ws[j]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = 0.0f;
+    }
+    if (p.rotate_k) {
+      // the butterfly steps commute: stride 64 first (through shared memory),
+      // then 1 .. 32 in registers
+      if (p.block_h == kHeadDim)
+        stride64_step(v, reinterpret_cast<float*>(smem + kOffKx) + r * kHeadDim, half);
+      half_fwht(v, p.block_h);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] *= p.c_h;
+    }
+    float sum = 0.0f, mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      sum += v[i];
+      mx = fmaxf(mx, fabsf(v[i]));
+    }
+    xl[half * kBM + r] = make_float2(sum, mx);
+    (void)soft_sync_and(true);
+    const float2 o = xl[(1 - half) * kBM + r];
+    sum += o.x;
+    mx = fmaxf(mx, o.y);
+    // 2^S with max |q'| 2^S < 2^14: S = 140 - (biased exponent of the max),
+    // kept within [-100, 100]
+    const int E = int((__float_as_uint(mx) >> 23) & 0xFFu);
+    const int S = min(100, max(-100, 140 - E));
+    const float sc = pow2i(S);
+    // K operand codes are n * 2^-24, so acc = 2^(S-24) q'.n; the logit is
+    // rowA * (s_k acc + qc z_k) with qc = sum(q') / rowA
+    rowA = p.q_scale * pow2i(24 - S);
+    qc = (sum * p.q_scale) / rowA;
+    uint8_t* qh = smem + kOffQh + r * 16;
+    uint8_t* qlo = smem + kOffQl + r * 16;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int kc = 8 * half + kk;
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float x0 = v[8 * kk + 2 * m] * sc, x1 = v[8 * kk + 2 * m + 1] * sc;
+        const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+        hw[m] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
+        lw[m] = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
+      }
+      *reinterpret_cast<uint4*>(qh + kc * 2048) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(qlo + kc * 2048) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    fence_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == kWarpProd) {
+    // ---------------------------------------------------------- producer
     const int32_t* btab = p.block_tables + int64_t(seq) * p.max_blocks;
-    const int chunk = chunk_bytes(P);
-    int issued = 0;
+    int ids = -1, ids_base = -32, issued = 0;
     bool failed = false;
-    int ids = -1;  // page id of logical page (lane + base), refreshed every 32 pages
-    int ids_base = -32;
     for (int i = 0; i < n_tiles; ++i) {
-      const int s = i % kPStages;
-      if (i >= kPStages &&
-          !__all_sync(kFull, mbar_wait_bounded(&empty[s], ((i / kPStages) - 1) & 1))) {
+      const int rs = i % kRawStages;
+      if (i >= kRawStages && !wait_sleep_all(&bars[kRawEmpty + rs], ((i / kRawStages) - 1) & 1)) {
         failed = true;
         break;
       }
-      const int lp = i / kTilesPerPage;
-      if (lp >= ids_base + 32) {
-        ids_base = lp - (lp & 31);
-        const int e = ids_base + lane;
-        ids = (e < p.max_blocks && int64_t(e) * P < L) ? btab[e] : -1;
-      }
-      int pid = __shfl_sync(kFull, ids, lp - ids_base);
-      if (pid < 0 || pid >= p.num_pages) {
-        if (lane == 0) report(p.dev_status, SAW_ERR_DEVICE_INDEX);
-        pid = -1;
+      int pid[4];
+      int okm = 0;
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        const int lp = (i * kBN + 16 * sl) / P;
+        if (lp >= ids_base + 32) {
+          ids_base = lp - (lp & 31);
+          const int e = ids_base + lane;
+          ids = (e < p.max_blocks && e < n_pages) ? btab[e] : -1;
+        }
+        int id = __shfl_sync(kAllLanes, ids, lp - ids_base);
+        if (lp >= n_pages) {
+          id = -1;  // past the sequence: nothing to copy, keys masked
+        } else if (id < 0 || id >= p.num_pages) {
+          if (lane == 0) report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+          id = -1;
+        }
+        pid[sl] = id;
+        okm |= (id >= 0) << sl;
       }
       if (lane == 0) {
-        uint8_t* st = smem + s * kPStage;
-        stage_ok[s] = pid >= 0;
-        if (pid < 0) {
-          mbar_arrive(&full[s]);
+        uint8_t* st = smem + kOffRaw + rs * kRawBytes;
+        *reinterpret_cast<int*>(st + kRawOk) = okm;
+        const uint32_t nbytes = __popc(okm) * (2 * 1024 + 2 * 64);
+        if (nbytes == 0) {
+          mbar_arrive(&bars[kRawFull + rs]);
         } else {
-          mbar_arrive_expect_tx(&full[s], kPStage);
-          const int64_t off = (int64_t(pid) * p.num_kv_heads + kvh) * chunk;
-          const int part = i % kTilesPerPage;
-          if (P == 16) {
-            bulk_g2s(st, p.k_cache + off, kHalfStage, &full[s]);
-            bulk_g2s(st + kHalfStage, p.v_cache + off, kHalfStage, &full[s]);
-          } else {
-            const int64_t codes = off + part * kCodes;
-            const int64_t meta = off + P * (kHeadDim / 2) + part * kMeta;
-            bulk_g2s(st, p.k_cache + codes, kCodes, &full[s]);
-            bulk_g2s(st + kCodes, p.k_cache + meta, kMeta, &full[s]);
-            bulk_g2s(st + kHalfStage, p.v_cache + codes, kCodes, &full[s]);
-            bulk_g2s(st + kHalfStage + kCodes, p.v_cache + meta, kMeta, &full[s]);
+          mbar_arrive_expect_tx(&bars[kRawFull + rs], nbytes);
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) {
+            if (pid[sl] < 0) continue;
+            const int part = ((i * kBN + 16 * sl) % P) / 16;
+            const int64_t off = (int64_t(pid[sl]) * p.num_kv_heads + kvh) * kChunk;
+            const int64_t codes = off + part * 1024;
+            const int64_t meta = off + P * (kHeadDim / 2) + part * 64;
+            bulk_g2s(st + sl * 1024, p.k_cache + codes, 1024, &bars[kRawFull + rs]);
+            bulk_g2s(st + kRawV + sl * 1024, p.v_cache + codes, 1024, &bars[kRawFull + rs]);
+            bulk_g2s(st + kRawKM + sl * 64, p.k_cache + meta, 64, &bars[kRawFull + rs]);
+            bulk_g2s(st + kRawVM + sl * 64, p.v_cache + meta, 64, &bars[kRawFull + rs]);
           }
         }
       }
@@ -193,280 +371,298 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const Prefil
     }
     if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
     // the CTA must not exit while a copy into its shared memory is in flight
-    for (int i = max(0, issued - kPStages); i < issued; ++i)
-      (void)mbar_wait_bounded(&full[i % kPStages], (i / kPStages) & 1);
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int g = lane >> 2, c = lane & 3;
-  const int wrow0 = row0 + 16 * warp;
-  const int ra = wrow0 + g, rbw = wrow0 + g + 8;
-  const bool va = ra < row_end, vb = rbw < row_end;
-  const int pos_a = va ? pos_base + ra / G : -1;
-  const int pos_b = vb ? pos_base + rbw / G : -1;
-  // the warp's rows see keys up to w_max; keys up to w_min are visible to all
-  const int w_last = min(row_end, wrow0 + 16) - 1;
-  const int w_max = (wrow0 < row_end) ? pos_base + w_last / G : -1;
-  const int w_min = (wrow0 < row_end) ? pos_base + wrow0 / G : -1;
-
-  // ---- q: rotate, scale, split into binary16 hi + lo A fragments.
-  // Fragment (k-step ks, half e) of lane c pairs local dims
-  // (8(ks>>1) + 2(ks&1) + f, +4), f = 0 for b0 / a0,a1 and 1 for b1 / a2,a3,
-  // matching the order in which the K codes are unpacked below.
-  uint32_t ah[8][4], al[8][4];
-  float qsum[2], rowA[2];
-  {
-    const float qscale = p.q_scale;
+    for (int i = max(0, issued - kRawStages); i < issued; ++i)
+      (void)wait_sleep(&bars[kRawFull + i % kRawStages], (i / kRawStages) & 1);
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t a_hi = smem_u32(smem + kOffQh), a_lo = smem_u32(smem + kOffQl);
+      const uint32_t kx0 = smem_u32(smem + kOffKx), vx0 = smem_u32(smem + kOffVx);
+      const uint32_t p0 = smem_u32(smem + kOffP);
+      constexpr uint32_t idS = umma_idesc_f16(kBM, kBN);
+      constexpr uint32_t idO = umma_idesc_f16(kBM, kHeadDim);
+      auto pv = [&](int j) -> bool {
+        const int bj = j & 1;
+        if (!wait_sleep(&bars[kPFull + bj], (j >> 1) & 1)) return false;
+        if (!wait_sleep(&bars[kVxFull + bj], (j >> 1) & 1)) return false;
+        tc_fence_after();
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const bool valid = rr ? vb : va;
-      const int r = rr ? rbw : ra;
-      float v[32];
-      if (valid) {
-        const int t = r / G, hh = r - t * G;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (int64_t(q0 + t) * p.num_q_heads + kvh * G + hh) * kHeadDim + 32 * c);
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          umma_f16(tmem + kColO, umma_desc(p0 + bj * kPBytes + ks * 2 * 2048, 2048, 128),
+                   umma_desc(vx0 + bj * kVxBytes + ks * 2 * 2048, 2048, 128), idO,
+                   j > 0 || ks > 0);
+        umma_commit(&bars[kPvDone + bj]);
+        return true;
+      };
+      bool ok = true;
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int b = i & 1;
+        ok = wait_sleep(&bars[kKxFull + b], (i >> 1) & 1) &&
+             (i < 2 || wait_sleep(&bars[kSEmpty + b], ((i >> 1) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sd = tmem + uint32_t(kBN * b);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 w = src[k];
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_f16(sd, umma_desc(a_hi + ks * 2 * 2048, 2048, 128),
+                   umma_desc(kx0 + b * kKxBytes + ks * 2 * 1024, 1024, 128), idS, ks > 0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[8 * k + 2 * j] = bf16_lo(ws[j]);
-            v[8 * k + 2 * j + 1] = bf16_hi(ws[j]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_f16(sd, umma_desc(a_lo + ks * 2 * 2048, 2048, 128),
+                   umma_desc(kx0 + b * kKxBytes + ks * 2 * 1024, 1024, 128), idS, true);
+        umma_commit(&bars[kSFull + b]);
+        umma_commit(&bars[kKxEmpty + b]);
+        if (i >= 1) ok = pv(i - 1);
       }
-      if (p.rotate_k) {
-        quad_fwht(v, p.block_h, c);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= p.c_h;
-      }
-      float sum = 0.0f, mx = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sum += v[i];
-        mx = fmaxf(mx, fabsf(v[i]));
-      }
-      sum = quad_sum(sum);
-      mx = quad_max(mx);
-      // 2^S with max |q'| 2^S < 2^14 (binary16 range, products stay exact):
-      // max |q'| < 2^(E - 126) for biased exponent E, so S = 140 - E, kept
-      // within [-100, 100] (a row of zeros, or one that small, takes 100)
-      const int E = int((__float_as_uint(mx) >> 23) & 0xFFu);
-      const int S = min(100, max(-100, 140 - E));
-      const float sc = pow2f(S), sco = pow2f(S - 4);
-      qsum[rr] = sum * qscale;
-      rowA[rr] = qscale * pow2f(24 - S);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-        for (int f = 0; f < 2; ++f) {
-          const int d0 = 8 * (ks >> 1) + 2 * (ks & 1) + f;
-          const float m = f ? sco : sc;
-          const float x0 = v[d0] * m, x1 = v[d0 + 4] * m;
-          const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-          const float l0 = x0 - __half2float(h0), l1 = x1 - __half2float(h1);
-          const uint32_t hw = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
-          const uint32_t lw = pack_half2(l0, l1);
-          ah[ks][2 * f + rr] = hw;  // a0/a1: f = 0, rows g / g+8; a2/a3: f = 1
-          al[ks][2 * f + rr] = lw;
-        }
-      }
-    }
-  }
-
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f}, pz[2] = {0.0f, 0.0f};
-  bool failed = false;
-
-  for (int i = 0; i < n_tiles; ++i) {
-    const int s = i % kPStages;
-    if (!__all_sync(kFull, mbar_wait_bounded(&full[s], (i / kPStages) & 1))) {
-      failed = true;
-      break;
-    }
-    const int k0 = i * kTileTok;
-    if (k0 <= w_max) {
-      const uint8_t* st = smem + s * kPStage;
-      const bool ok = stage_ok[s] != 0;
-      // ---- S = Q K^T: n-tile 0 = keys k0..k0+7 (B column g <- key g),
-      // n-tile 1 = keys k0+8..k0+15
-      // four independent accumulators (q' hi / lo x two n-tiles): chains of
-      // 8 dependent MMAs instead of 16
-      float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      {
-        float u0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, u1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        const uint4 wk0 = *reinterpret_cast<const uint4*>(st + g * 64 + 16 * c);
-        const uint4 wk1 = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + 16 * c);
-        const uint32_t w0[4] = {wk0.x, wk0.y, wk0.z, wk0.w};
-        const uint32_t w1[4] = {wk1.x, wk1.y, wk1.z, wk1.w};
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t x0 = (ks & 1) ? (w0[ks >> 1] >> 8) : w0[ks >> 1];
-          const uint32_t x1 = (ks & 1) ? (w1[ks >> 1] >> 8) : w1[ks >> 1];
-          mma_16816(s0, ah[ks], x0 & kLo, x0 & kHi);
-          mma_16816(s1, ah[ks], x1 & kLo, x1 & kHi);
-          mma_16816(u0, al[ks], x0 & kLo, x0 & kHi);
-          mma_16816(u1, al[ks], x1 & kLo, x1 & kHi);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          s0[j] += u0[j];
-          s1[j] += u1[j];
-        }
-      }
-      // ---- logits: this lane holds keys 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c
-      const uint2 km0 = *reinterpret_cast<const uint2*>(st + kCodes + 8 * c);
-      const uint2 km1 = *reinterpret_cast<const uint2*>(st + kCodes + 32 + 8 * c);
-      const float ks_[4] = {f16lo(km0.x), f16lo(km0.y), f16lo(km1.x), f16lo(km1.y)};
-      const float kz_[4] = {f16hi(km0.x), f16hi(km0.y), f16hi(km1.x), f16hi(km1.y)};
-      const int key[4] = {k0 + 2 * c, k0 + 2 * c + 1, k0 + 8 + 2 * c, k0 + 9 + 2 * c};
-      // t[row][j]: row 0 = g, row 1 = g+8; j indexes key[]
-      float t[2][4];
-      t[0][0] = fmaf(rowA[0] * ks_[0], s0[0], qsum[0] * kz_[0]);
-      t[0][1] = fmaf(rowA[0] * ks_[1], s0[1], qsum[0] * kz_[1]);
-      t[1][0] = fmaf(rowA[1] * ks_[0], s0[2], qsum[1] * kz_[0]);
-      t[1][1] = fmaf(rowA[1] * ks_[1], s0[3], qsum[1] * kz_[1]);
-      t[0][2] = fmaf(rowA[0] * ks_[2], s1[0], qsum[0] * kz_[2]);
-      t[0][3] = fmaf(rowA[0] * ks_[3], s1[1], qsum[0] * kz_[3]);
-      t[1][2] = fmaf(rowA[1] * ks_[2], s1[2], qsum[1] * kz_[2]);
-      t[1][3] = fmaf(rowA[1] * ks_[3], s1[3], qsum[1] * kz_[3]);
-      const bool partial = !ok || (k0 + kTileTok - 1 > w_min);
-      if (partial) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          t[0][j] = (ok && key[j] <= pos_a) ? t[0][j] : -INFINITY;
-          t[1][j] = (ok && key[j] <= pos_b) ? t[1][j] : -INFINITY;
-        }
-      }
-      // ---- online softmax (base 2)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const float mt = quad_max(fmaxf(fmaxf(t[rr][0], t[rr][1]), fmaxf(t[rr][2], t[rr][3])));
-        if (mt > m_run[rr]) {
-          const float al_ = ex2(m_run[rr] - mt);  // 0 when m_run is -inf
-          m_run[rr] = mt;
-          l_run[rr] *= al_;
-          pz[rr] *= al_;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            o[n][2 * rr] *= al_;
-            o[n][2 * rr + 1] *= al_;
-          }
-        }
-      }
-      const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
-      const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
-      float pr[2][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        pr[0][j] = ex2(t[0][j] - mu0);
-        pr[1][j] = ex2(t[1][j] - mu1);
-      }
-      // ---- V scale / zero of the same keys; keys past the sequence end (or
-      // on a bad page) may hold anything, so their terms are selected away
-      const uint2 vm0 = *reinterpret_cast<const uint2*>(st + kHalfStage + kCodes + 8 * c);
-      const uint2 vm1 = *reinterpret_cast<const uint2*>(st + kHalfStage + kCodes + 32 + 8 * c);
-      float vs[4] = {f16lo(vm0.x), f16lo(vm0.y), f16lo(vm1.x), f16lo(vm1.y)};
-      float vz[4] = {f16hi(vm0.x), f16hi(vm0.y), f16hi(vm1.x), f16hi(vm1.y)};
-      if (partial) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool live = ok && key[j] < L;
-          vs[j] = live ? vs[j] : 0.0f;
-          vz[j] = live ? vz[j] : 0.0f;
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        l_run[rr] += (pr[rr][0] + pr[rr][1]) + (pr[rr][2] + pr[rr][3]);
-        pz[rr] = fmaf(pr[rr][0], vz[0], fmaf(pr[rr][1], vz[1],
-                 fmaf(pr[rr][2], vz[2], fmaf(pr[rr][3], vz[3], pz[rr]))));
-      }
-      // A fragment of p*s: a0 (row g, keys 2c, 2c+1), a1 (row g+8, same),
-      // a2 (row g, keys 8+2c, 9+2c), a3 (row g+8, same)
-      uint32_t pa[4];
-      pa[0] = pack_half2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
-      pa[1] = pack_half2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
-      pa[2] = pack_half2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
-      pa[3] = pack_half2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
-
-      // ---- O += (p s) V: B column g of n-tile nt is dim 16g + nt; its k
-      // pairs are keys (2c, 2c+1) for b0 and (8+2c, 9+2c) for b1, the same
-      // bytes of the two keys' rows side by side (one byte permute)
-      const uint8_t* vc = st + kHalfStage;
-      const uint2 xa = *reinterpret_cast<const uint2*>(vc + (2 * c) * 64 + 8 * g);
-      const uint2 ya = *reinterpret_cast<const uint2*>(vc + (2 * c + 1) * 64 + 8 * g);
-      const uint2 xb = *reinterpret_cast<const uint2*>(vc + (2 * c + 8) * 64 + 8 * g);
-      const uint2 yb = *reinterpret_cast<const uint2*>(vc + (2 * c + 9) * 64 + 8 * g);
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const uint32_t xw0 = w ? xa.y : xa.x, yw0 = w ? ya.y : ya.x;
-        const uint32_t xw1 = w ? xb.y : xb.x, yw1 = w ? yb.y : yb.x;
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const uint32_t sel = pp ? 0x7632u : 0x5410u;
-          const uint32_t r0 = prmt(xw0, yw0, sel), r1 = prmt(xw1, yw1, sel);
-          const uint32_t q0_ = r0 >> 8, q1_ = r1 >> 8;
-          const int nt = 8 * w + 4 * pp;
-          mma_16816(o[nt + 0], pa, r0 & kLo, r1 & kLo);
-          mma_16816(o[nt + 1], pa, r0 & kHi, r1 & kHi);
-          mma_16816(o[nt + 2], pa, q0_ & kLo, q1_ & kLo);
-          mma_16816(o[nt + 3], pa, q0_ & kHi, q1_ & kHi);
-        }
-      }
+      if (ok) ok = pv(n_tiles - 1);
+      if (!ok) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+      // every MMA has completed before tensor memory is released
+      umma_commit(&bars[kMmaDone]);
+      (void)wait_sleep(&bars[kMmaDone], 0);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
-  if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
-
-  // ---- epilogue: code scales, sum(p z), normalise, inverse V rotation
+  } else if (warp >= kWarpExp0) {
+    // ---------------------------------------------------------- expanders
+    const int te = tid - 32 * kWarpExp0;
+    bool failed = false;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int rs = i % kRawStages, b = i & 1;
+      if (!wait_sleep_all(&bars[kRawFull + rs], (i / kRawStages) & 1)) { failed = true; break; }
+      const uint8_t* st = smem + kOffRaw + rs * kRawBytes;
+      // metadata, unpacked to binary32 for the softmax warps
+      if (i >= 2 && !wait_sleep_all(&bars[kMetaEmpty + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
+      uint8_t* mb = smem + kOffMeta + b * kMetaBytes;
+      if (te < kBN) {
+        const uint32_t km = *reinterpret_cast<const uint32_t*>(st + kRawKM + 4 * te);
+        const uint32_t vm = *reinterpret_cast<const uint32_t*>(st + kRawVM + 4 * te);
+        float* mf = reinterpret_cast<float*>(mb);
+        mf[te] = f16lo_(km);
+        mf[kBN + te] = f16hi_(km);
+        mf[2 * kBN + te] = f16lo_(vm);
+        mf[3 * kBN + te] = f16hi_(vm);
+      }
+      if (te == 0) *reinterpret_cast<int*>(mb + kBN * 16) = *reinterpret_cast<const int*>(st + kRawOk);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kMetaFull + b]);
+      // K operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2
+      if (i >= 2 && !wait_sleep_all(&bars[kKxEmpty + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
+      {
+        uint8_t* kx = smem + kOffKx + b * kKxBytes;
+        const int n = te & 63, hk = te >> 6;
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const float l = quad_sum(l_run[rr]);
-    const float z = quad_sum(pz[rr]);
-    const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-    float v[32];
+        for (int s = 0; s < 2; ++s) {
+          const int q = (2 * hk + s + (n >> 1)) & 3;  // 16-byte piece: dims 32q .. 32q+31
+          const uint4 w = *reinterpret_cast<const uint4*>(st + n * 64 + 16 * q);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const float cs = (nt & 1) ? 1048576.0f : 16777216.0f;  // 2^20 : 2^24
-      v[nt] = fmaf(o[nt][2 * rr], cs, z) * inv;              // dim 32c + nt
-      v[16 + nt] = fmaf(o[nt][2 * rr + 1], cs, z) * inv;     // dim 32c + 16 + nt
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t x = ws[u];
+            uint32_t c[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) c[m] = ((x >> (8 * m)) & 0xFu) | (((x >> (8 * m + 4)) & 0xFu) << 16);
+            *reinterpret_cast<uint4*>(kx + (4 * q + u) * 1024 + n * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+          }
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kKxFull + b]);
+      // V^T operand: element (dim d, key k) at (k/8)*2048 + d*16 + (k%8)*2
+      if (i >= 2 && !wait_sleep_all(&bars[kPvDone + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
+      {
+        uint8_t* vx = smem + kOffVx + b * kVxBytes;
+        const int dq = te & 15, kc = te >> 4;  // dims 8dq .. 8dq+7, keys 8kc .. 8kc+7
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          w[j] = *reinterpret_cast<const uint32_t*>(st + kRawV + (8 * kc + j) * 64 + 4 * dq);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int e = (s + lane) & 7;  // rotating the dims spreads the stores over all banks
+          const int sh = 4 * e;
+          uint32_t c[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            c[m] = ((w[2 * m] >> sh) & 0xFu) | (((w[2 * m + 1] >> sh) & 0xFu) << 16);
+          *reinterpret_cast<uint4*>(vx + kc * 2048 + (8 * dq + e) * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kVxFull + b]);
+        mbar_arrive(&bars[kRawEmpty + rs]);
+      }
     }
+    if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+  } else {
+    // ---------------------------------------------------------- softmax
+    const uint32_t trow = tmem + (uint32_t(32 * (warp & 3)) << 16);
+    float* xm = reinterpret_cast<float*>(smem + kOffXm);
+    const int kq = 32 * half;  // this thread's keys within a tile
+    float m_run = -INFINITY, l_run = 0.0f, pz = 0.0f;
+    bool failed = false;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int b = i & 1;
+      // every wait before the named barrier, so that the barrier always meets
+      wait_soft(&bars[kSFull + b], (i >> 1) & 1, failed);
+      wait_soft(&bars[kMetaFull + b], (i >> 1) & 1, failed);
+      if (i >= 2) wait_soft(&bars[kPvDone + b], ((i >> 1) - 1) & 1, failed);  // P buffer b free
+      tc_fence_after();
+      float t[32];
+      tmem_ld32(trow + uint32_t(kBN * b + kq), t);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kSEmpty + b]);
+      const float4* msk = reinterpret_cast<const float4*>(smem + kOffMeta + b * kMetaBytes);
+      const float4* mzk = msk + kBN / 4;
+      const float4* msv = msk + 2 * (kBN / 4);
+      const float4* mzv = msk + 3 * (kBN / 4);
+      const int okm = *reinterpret_cast<const int*>(smem + kOffMeta + b * kMetaBytes + kBN * 16);
+      const int k0 = i * kBN + kq;
+      const bool all_vis = ((okm >> (2 * half)) & 3) == 3 && pos_r >= k0 + 31;
+      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int g4 = 0; g4 < 8; ++g4) {
+        const float4 sk = msk[kq / 4 + g4], zk = mzk[kq / 4 + g4];
+        const float skk[4] = {sk.x, sk.y, sk.z, sk.w}, zkk[4] = {zk.x, zk.y, zk.z, zk.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * g4 + e;
+          float x = fmaf(skk[e], t[j], qc * zkk[e]);
+          if (!all_vis) {
+            const bool vis = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
+            x = vis ? x : -INFINITY;
+          }
+          t[j] = x;
+          tm[e] = fmaxf(tm[e], x);
+        }
+      }
+      // row max over both halves
+      const float th = rowA * fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+      xm[(b * 2 + half) * kBM + r] = th;
+      const bool ok_all = soft_sync_and(!failed);
+      failed = !ok_all;
+      const float tmax = fmaxf(th, xm[(b * 2 + 1 - half) * kBM + r]);
+      const bool grow = tmax > m_run;
+      if (i > 0 && __any_sync(kAllLanes, grow) &&
+          wait_soft(&bars[kPvDone + ((i - 1) & 1)], ((i - 1) >> 1) & 1, failed)) {
+        // rescale this half of the output rows, after the previous P.V
+        tc_fence_after();
+        const float a = grow ? ex2(m_run - tmax) : 1.0f;
+#pragma unroll
+        for (int cblk = 0; cblk < 2; ++cblk) {
+          float o[32];
+          tmem_ld32(trow + kColO + 64 * half + 32 * cblk, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= a;
+          tmem_st32(trow + kColO + 64 * half + 32 * cblk, o);
+        }
+      }
+      if (grow) {
+        const float a = ex2(m_run - tmax);  // 0 while m_run is -inf
+        l_run *= a;
+        pz *= a;
+        m_run = tmax;
+      }
+      const float nmu = (m_run == -INFINITY) ? 0.0f : -m_run;
+      uint8_t* prow = smem + kOffP + b * kPBytes + r * 16;
+      float la[4] = {0.0f, 0.0f, 0.0f, 0.0f}, za[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        float ps[8];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int g4 = 2 * kk + hh;
+          const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
+          const float svv[4] = {sv.x, sv.y, sv.z, sv.w}, zvv[4] = {zv.x, zv.y, zv.z, zv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * g4 + e;
+            const float pr = ex2(fmaf(rowA, t[j], nmu));  // 0 for masked keys
+            float pzv = pr * zvv[e], psv = pr * svv[e];
+            if (!all_vis) {  // keys past the end may hold anything
+              const bool live = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
+              pzv = live ? pzv : 0.0f;
+              psv = live ? psv : 0.0f;
+            }
+            la[e] += pr;
+            za[e] += pzv;
+            ps[4 * hh + e] = psv;
+          }
+        }
+        *reinterpret_cast<uint4*>(prow + (kq / 8 + kk) * 2048) =
+            make_uint4(pack_half2(ps[0], ps[1]), pack_half2(ps[2], ps[3]), pack_half2(ps[4], ps[5]),
+                       pack_half2(ps[6], ps[7]));
+      }
+      l_run += (la[0] + la[1]) + (la[2] + la[3]);
+      pz += (za[0] + za[1]) + (za[2] + za[3]);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kPFull + b]);
+        mbar_arrive(&bars[kMetaEmpty + b]);
+      }
+    }
+    if (failed && lane == 0 && warp == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+    // ---- epilogue: this half of the output row from tensor memory, code
+    // scale, sum(p z) and l over both halves, normalise, inverse V rotation
+    const int last = n_tiles - 1;
+    wait_soft(&bars[kPvDone + (last & 1)], (last >> 1) & 1, failed);
+    tc_fence_after();
+    float v[64];
+    {
+      float o[32];
+      tmem_ld32(trow + kColO + 64 * half, o);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = o[j];
+      tmem_ld32(trow + kColO + 64 * half + 32, o);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[32 + j] = o[j];
+    }
+    xl[half * kBM + r] = make_float2(l_run, pz);
+    (void)soft_sync_and(true);
+    const float2 ot = xl[(1 - half) * kBM + r];
+    const float l = l_run + ot.x, zz = pz + ot.y;
+    const float inv = (!failed && l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = fmaf(v[i], 16777216.0f, zz) * inv;  // codes were n 2^-24
     if (p.rotate_v) {
-      quad_fwht(v, p.block_h, c);
+      // every S product has completed (the last P.V came after it): the q'
+      // buffers are free for the exchange
+      if (p.block_h == kHeadDim)
+        stride64_step(v, reinterpret_cast<float*>(smem + kOffQh) + r * kHeadDim, half);
+      half_fwht(v, p.block_h);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= p.c_h;
+      for (int i = 0; i < 64; ++i) v[i] *= p.c_h;
     }
-    const bool valid = rr ? vb : va;
-    if (valid) {
-      const int r = rr ? rbw : ra;
-      const int t = r / G, hh = r - t * G;
+    if (row_valid) {
       float4* dst = reinterpret_cast<float4*>(
-          p.out + (int64_t(q0 + t) * p.num_q_heads + kvh * G + hh) * kHeadDim + 32 * c);
+          p.out + (int64_t(q0 + out_t) * p.num_q_heads + kvh * G + out_h) * kHeadDim + 64 * half);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      for (int k = 0; k < 16; ++k)
+        dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
     }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <int P>
 cudaError_t launch_prefill_p(const PrefillParams& p, cudaStream_t stream) {
-  auto kernel = prefill_attn_kernel<P>;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+  auto kernel = prefill_tc_kernel<P>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.row_blocks, p.num_kv_heads, p.num_seqs);
-  cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = kPSmem;
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = kTSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -478,7 +674,7 @@ cudaError_t launch_prefill_p(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int prefill_rows_per_cta() { return kPRows; }
+int prefill_rows_per_cta() { return kBM; }
 
 cudaError_t launch_prefill_attn(const PrefillParams& p, cudaStream_t stream) {
   if (p.num_seqs == 0 || p.row_blocks == 0) return cudaSuccess;
