@@ -56,10 +56,8 @@ constexpr int kWarpProd = kSoftWarps + 4;
 constexpr int kWarpMma = kSoftWarps + 5;
 constexpr uint32_t kAllLanes = 0xFFFFFFFFu;
 
-constexpr int kQBytes = kBM * kHeadDim * 2;        // one of q' hi / lo
 constexpr int kKxBytes = kBN * kHeadDim * 2;       // K operand of one tile
 constexpr int kVxBytes = kHeadDim * kBN * 2;       // V^T operand of one tile
-constexpr int kPBytes = kBM * kBN * 2;             // P operand of one tile
 constexpr int kRawCodes = kBN * (kHeadDim / 2);    // 4096 code bytes per tensor
 // raw stage: K codes | V codes | K meta | V meta | slice-ok word
 constexpr int kRawV = kRawCodes;
@@ -69,12 +67,12 @@ constexpr int kRawOk = kRawVM + kBN * 4;
 constexpr int kRawBytes = kRawOk + 16;
 constexpr int kMetaBytes = kBN * 16 + 16;          // s_k[64], z_k[64], s_v[64], z_v[64] + ok word
 
+constexpr int kQBytes = kBM * kHeadDim * 2;        // one of q' hi / lo
 constexpr int kOffQh = 0;
 constexpr int kOffQl = kOffQh + kQBytes;
 constexpr int kOffKx = kOffQl + kQBytes;
 constexpr int kOffVx = kOffKx + 2 * kKxBytes;
-constexpr int kOffP = kOffVx + 2 * kVxBytes;
-constexpr int kOffRaw = kOffP + 2 * kPBytes;
+constexpr int kOffRaw = kOffVx + 2 * kVxBytes;
 constexpr int kOffMeta = kOffRaw + kRawStages * kRawBytes;
 constexpr int kOffXm = kOffMeta + 2 * kMetaBytes;          // f32 [2 tiles][2 halves][128] row maxima
 constexpr int kOffXl = kOffXm + 2 * 2 * kBM * 4;           // f32x2 [2 halves][128]
@@ -88,11 +86,13 @@ constexpr int kTSmem = kOffTmem + 16;
 static_assert(kTSmem <= 227 * 1024, "shared memory");
 static_assert(kRawBytes % 16 == 0 && kMetaBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
 // the 128 x 128 binary32 exchange of the q' and output rotations reuses the
-// K/V operand buffers (prologue) and the q' buffers (epilogue)
-static_assert(2 * kKxBytes + 2 * kVxBytes >= kBM * kHeadDim * 4 && 2 * kQBytes >= kBM * kHeadDim * 4,
-              "exchange space");
-constexpr uint32_t kTmemCols = 256;
+// K/V operand buffers (free before the first tile and after the last)
+static_assert(2 * kKxBytes + 2 * kVxBytes >= kBM * kHeadDim * 4, "exchange space");
+// tensor memory: S (2 x 64 columns), O (128), P (2 x 32 columns of binary16
+// pairs); q' hi and lo are shared-memory operands
+constexpr uint32_t kTmemCols = 512;  // 320 used
 constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 256;
 constexpr int kSoftBar = 1;                         // named barrier id of the softmax warps
 
 __device__ __forceinline__ float f16lo_(uint32_t w) {
@@ -103,6 +103,36 @@ __device__ __forceinline__ float f16hi_(uint32_t w) {
 }
 // 2^e for -126 <= e <= 127, exactly
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
+
+// Byte-permute selectors that build a binary16 pair (x byte m, y byte m) with
+// zero upper bytes from two nibble planes x, y: the zeros replicate the sign
+// bit of a byte below 128 (selector nibble with bit 3 set).
+__device__ __constant__ const uint32_t kPairSel[4] = {0x8480u, 0x9591u, 0xA6A2u, 0xB7B3u};
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// t[j] for a runtime j (the masked, non-unrolled loops) without sending the
+// array to local memory: a select chain over the 32 registers.
+__device__ __forceinline__ float t_at(const float (&t)[32], int j) {
+  float x = t[0];
+#pragma unroll
+  for (int k = 1; k < 32; ++k) x = (j == k) ? t[k] : x;
+  return x;
+}
+__device__ __forceinline__ void t_set(float (&t)[32], int j, float x) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) t[k] = (j == k) ? x : t[k];
+}
 
 // The softmax warps' barrier; returns the AND of `ok` over its threads.
 __device__ __forceinline__ bool soft_sync_and(bool ok) {
@@ -235,12 +265,13 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
   const int r = 32 * (warp & 3) + lane;      // and row (tensor-memory lane)
   bool row_valid = false;
   int pos_r = -1, out_t = 0, out_h = 0;
-  float rowA = 0.0f, qc = 0.0f;
+  float rowA = 0.0f, qc = 0.0f, qsc = 0.0f;
   float2* xl = reinterpret_cast<float2*>(smem + kOffXl);
+  float qv[64];
   if (warp < kSoftWarps) {
     const int row = row0 + r;
     row_valid = row < row_end;
-    float v[64];
+    float (&v)[64] = qv;
     if (row_valid) {
       out_t = row / G;
       out_h = row - out_t * G;
@@ -285,11 +316,19 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
     // kept within [-100, 100]
     const int E = int((__float_as_uint(mx) >> 23) & 0xFFu);
     const int S = min(100, max(-100, 140 - E));
-    const float sc = pow2i(S);
+    qsc = pow2i(S);
     // K operand codes are n * 2^-24, so acc = 2^(S-24) q'.n; the logit is
     // rowA * (s_k acc + qc z_k) with qc = sum(q') / rowA
     rowA = p.q_scale * pow2i(24 - S);
     qc = (sum * p.q_scale) / rowA;
+  }
+  tc_fence_before();
+  __syncthreads();  // tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (warp < kSoftWarps) {
+    // q' as the A operand in shared memory (K-major core matrices): row r,
+    // dims 64h .. 64h+63 = 8-dim chunks 8h .. 8h+7
     uint8_t* qh = smem + kOffQh + r * 16;
     uint8_t* qlo = smem + kOffQl + r * 16;
 #pragma unroll
@@ -298,7 +337,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const float x0 = v[8 * kk + 2 * m] * sc, x1 = v[8 * kk + 2 * m + 1] * sc;
+        const float x0 = qv[8 * kk + 2 * m] * qsc, x1 = qv[8 * kk + 2 * m + 1] * qsc;
         const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
         hw[m] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
         lw[m] = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
@@ -311,7 +350,6 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;
 
   if (warp == kWarpProd) {
     // ---------------------------------------------------------- producer
@@ -376,45 +414,63 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      const uint32_t a_hi = smem_u32(smem + kOffQh), a_lo = smem_u32(smem + kOffQl);
       const uint32_t kx0 = smem_u32(smem + kOffKx), vx0 = smem_u32(smem + kOffVx);
-      const uint32_t p0 = smem_u32(smem + kOffP);
       constexpr uint32_t idS = umma_idesc_f16(kBM, kBN);
       constexpr uint32_t idO = umma_idesc_f16(kBM, kHeadDim);
-      auto pv = [&](int j) -> bool {
-        const int bj = j & 1;
-        if (!wait_sleep(&bars[kPFull + bj], (j >> 1) & 1)) return false;
-        if (!wait_sleep(&bars[kVxFull + bj], (j >> 1) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          umma_f16(tmem + kColO, umma_desc(p0 + bj * kPBytes + ks * 2 * 2048, 2048, 128),
-                   umma_desc(vx0 + bj * kVxBytes + ks * 2 * 2048, 2048, 128), idO,
-                   j > 0 || ks > 0);
-        umma_commit(&bars[kPvDone + bj]);
-        return true;
-      };
+      // descriptors built once: a K step only advances the start address
+      // (in 16-byte units, the descriptor's low field): 2 x 1024 bytes of K
+      // operand, 2 x 2048 bytes of V operand
+      const uint64_t kxd[2] = {umma_desc(kx0, 1024, 128), umma_desc(kx0 + kKxBytes, 1024, 128)};
+      const uint64_t vxd[2] = {umma_desc(vx0, 2048, 128), umma_desc(vx0 + kVxBytes, 2048, 128)};
+      constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 2048) >> 4, kQStep = (2 * 2048) >> 4;
+      const uint64_t qhd = umma_desc(smem_u32(smem + kOffQh), 2048, 128);
+      const uint64_t qld = umma_desc(smem_u32(smem + kOffQl), 2048, 128);
+      // Both products are issued as soon as their operands are ready,
+      // polling the barriers without blocking or sleeping (a sleep's wake-up
+      // is far coarser than an MMA): S(i+1) needs the K operand of tile i+1,
+      // P.V(i) the softmax of tile i; neither waits for the other.
+      int nS = 0, nP = 0;
       bool ok = true;
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int b = i & 1;
-        ok = wait_sleep(&bars[kKxFull + b], (i >> 1) & 1) &&
-             (i < 2 || wait_sleep(&bars[kSEmpty + b], ((i >> 1) - 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sd = tmem + uint32_t(kBN * b);
+      long long t_last = clock64();
+      while (nP < n_tiles) {
+        bool prog = false;
+        if (nS < n_tiles && mbar_test(&bars[kKxFull + (nS & 1)], (nS >> 1) & 1) &&
+            (nS < 2 || mbar_test(&bars[kSEmpty + (nS & 1)], ((nS >> 1) - 1) & 1))) {
+          const int b = nS & 1;
+          tc_fence_after();
+          const uint32_t sd = tmem + uint32_t(kBN * b);
+          const uint64_t bd = kxd[b];
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_f16(sd, umma_desc(a_hi + ks * 2 * 2048, 2048, 128),
-                   umma_desc(kx0 + b * kKxBytes + ks * 2 * 1024, 1024, 128), idS, ks > 0);
+          for (int ks = 0; ks < kHeadDim / 16; ++ks)
+            umma_f16(sd, qhd + ks * kQStep, bd + ks * kKxStep, idS, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_f16(sd, umma_desc(a_lo + ks * 2 * 2048, 2048, 128),
-                   umma_desc(kx0 + b * kKxBytes + ks * 2 * 1024, 1024, 128), idS, true);
-        umma_commit(&bars[kSFull + b]);
-        umma_commit(&bars[kKxEmpty + b]);
-        if (i >= 1) ok = pv(i - 1);
+          for (int ks = 0; ks < kHeadDim / 16; ++ks)
+            umma_f16(sd, qld + ks * kQStep, bd + ks * kKxStep, idS, true);
+          umma_commit(&bars[kSFull + b]);
+          umma_commit(&bars[kKxEmpty + b]);
+          ++nS;
+          prog = true;
+        }
+        if (nP < nS && mbar_test(&bars[kPFull + (nP & 1)], (nP >> 1) & 1) &&
+            mbar_test(&bars[kVxFull + (nP & 1)], (nP >> 1) & 1)) {
+          const int bj = nP & 1;
+          tc_fence_after();
+          const uint64_t bd = vxd[bj];
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            umma_f16_ta(tmem + kColO, tmem + kColP + 32 * bj + 8 * ks, bd + ks * kVxStep, idO,
+                        nP > 0 || ks > 0);
+          umma_commit(&bars[kPvDone + bj]);
+          ++nP;
+          prog = true;
+        }
+        if (prog) {
+          t_last = clock64();
+        } else if (clock64() - t_last > kWaitLimitCycles) {
+          ok = false;
+          break;
+        }
       }
-      if (ok) ok = pv(n_tiles - 1);
       if (!ok) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
       // every MMA has completed before tensor memory is released
       umma_commit(&bars[kMmaDone]);
@@ -456,11 +512,12 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t x = ws[u];
-            uint32_t c[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) c[m] = ((x >> (8 * m)) & 0xFu) | (((x >> (8 * m + 4)) & 0xFu) << 16);
-            *reinterpret_cast<uint4*>(kx + (4 * q + u) * 1024 + n * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+            // byte m of the word holds dims 2m (low nibble) and 2m+1: one
+            // permute per pair from the low- and high-nibble planes
+            const uint32_t lo = ws[u] & 0x0F0F0F0Fu, hi = (ws[u] >> 4) & 0x0F0F0F0Fu;
+            *reinterpret_cast<uint4*>(kx + (4 * q + u) * 1024 + n * 16) =
+                make_uint4(prmt(lo, hi, kPairSel[0]), prmt(lo, hi, kPairSel[1]),
+                           prmt(lo, hi, kPairSel[2]), prmt(lo, hi, kPairSel[3]));
           }
         }
       }
@@ -472,18 +529,23 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       {
         uint8_t* vx = smem + kOffVx + b * kVxBytes;
         const int dq = te & 15, kc = te >> 4;  // dims 8dq .. 8dq+7, keys 8kc .. 8kc+7
-        uint32_t w[8];
+        // nibble planes of the 8 keys' words: even dims (low nibbles) and odd
+        uint32_t lo[8], hi[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          w[j] = *reinterpret_cast<const uint32_t*>(st + kRawV + (8 * kc + j) * 64 + 4 * dq);
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(st + kRawV + (8 * kc + j) * 64 + 4 * dq);
+          lo[j] = w & 0x0F0F0F0Fu;
+          hi[j] = (w >> 4) & 0x0F0F0F0Fu;
+        }
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const int e = (s + lane) & 7;  // rotating the dims spreads the stores over all banks
-          const int sh = 4 * e;
+          // dim 8dq+e is byte e/2 of each key's word, plane e&1; pair keys (2m, 2m+1)
+          const uint32_t sel = kPairSel[0] + 0x1111u * uint32_t(e >> 1);
           uint32_t c[4];
 #pragma unroll
           for (int m = 0; m < 4; ++m)
-            c[m] = ((w[2 * m] >> sh) & 0xFu) | (((w[2 * m + 1] >> sh) & 0xFu) << 16);
+            c[m] = (e & 1) ? prmt(hi[2 * m], hi[2 * m + 1], sel) : prmt(lo[2 * m], lo[2 * m + 1], sel);
           *reinterpret_cast<uint4*>(vx + kc * 2048 + (8 * dq + e) * 16) = make_uint4(c[0], c[1], c[2], c[3]);
         }
       }
@@ -522,20 +584,30 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       const int k0 = i * kBN + kq;
       const bool all_vis = ((okm >> (2 * half)) & 3) == 3 && pos_r >= k0 + 31;
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // two copies of each loop: fully unrolled with no mask for the tiles a
+      // row sees whole (nearly all), compact with the mask for the others --
+      // the warps of four roles share each scheduler's instruction cache
+      if (all_vis) {
 #pragma unroll
-      for (int g4 = 0; g4 < 8; ++g4) {
-        const float4 sk = msk[kq / 4 + g4], zk = mzk[kq / 4 + g4];
-        const float skk[4] = {sk.x, sk.y, sk.z, sk.w}, zkk[4] = {zk.x, zk.y, zk.z, zk.w};
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const float4 sk = msk[kq / 4 + g4], zk = mzk[kq / 4 + g4];
+          const float skk[4] = {sk.x, sk.y, sk.z, sk.w}, zkk[4] = {zk.x, zk.y, zk.z, zk.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * g4 + e;
-          float x = fmaf(skk[e], t[j], qc * zkk[e]);
-          if (!all_vis) {
-            const bool vis = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
-            x = vis ? x : -INFINITY;
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * g4 + e;
+            t[j] = fmaf(skk[e], t[j], qc * zkk[e]);
+            tm[e] = fmaxf(tm[e], t[j]);
           }
-          t[j] = x;
-          tm[e] = fmaxf(tm[e], x);
+        }
+      } else {
+        const float* fsk = reinterpret_cast<const float*>(msk) + kq;
+        const float* fzk = reinterpret_cast<const float*>(mzk) + kq;
+#pragma unroll 1
+        for (int j = 0; j < 32; ++j) {
+          const bool vis = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
+          const float x = vis ? fmaf(fsk[j], t_at(t, j), qc * fzk[j]) : -INFINITY;
+          t_set(t, j, x);
+          tm[0] = fmaxf(tm[0], x);
         }
       }
       // row max over both halves
@@ -566,38 +638,62 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         m_run = tmax;
       }
       const float nmu = (m_run == -INFINITY) ? 0.0f : -m_run;
-      uint8_t* prow = smem + kOffP + b * kPBytes + r * 16;
+      // p*s_V, binary16 pairs, into this lane's P columns: keys kq .. kq+31
+      uint32_t pw[16];
       float la[4] = {0.0f, 0.0f, 0.0f, 0.0f}, za[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (all_vis) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        float ps[8];
+        for (int kk = 0; kk < 4; ++kk) {
+          float ps[8];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int g4 = 2 * kk + hh;
-          const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
-          const float svv[4] = {sv.x, sv.y, sv.z, sv.w}, zvv[4] = {zv.x, zv.y, zv.z, zv.w};
+          for (int hh = 0; hh < 2; ++hh) {
+            const int g4 = 2 * kk + hh;
+            const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
+            const float svv[4] = {sv.x, sv.y, sv.z, sv.w}, zvv[4] = {zv.x, zv.y, zv.z, zv.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * g4 + e;
-            const float pr = ex2(fmaf(rowA, t[j], nmu));  // 0 for masked keys
-            float pzv = pr * zvv[e], psv = pr * svv[e];
-            if (!all_vis) {  // keys past the end may hold anything
-              const bool live = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
-              pzv = live ? pzv : 0.0f;
-              psv = live ? psv : 0.0f;
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * g4 + e;
+              const float pr = ex2(fmaf(rowA, t[j], nmu));
+              la[e] += pr;
+              za[e] = fmaf(pr, zvv[e], za[e]);
+              ps[4 * hh + e] = pr * svv[e];
             }
-            la[e] += pr;
-            za[e] += pzv;
-            ps[4 * hh + e] = psv;
           }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) pw[4 * kk + m] = pack_half2(ps[2 * m], ps[2 * m + 1]);
         }
-        *reinterpret_cast<uint4*>(prow + (kq / 8 + kk) * 2048) =
-            make_uint4(pack_half2(ps[0], ps[1]), pack_half2(ps[2], ps[3]), pack_half2(ps[4], ps[5]),
-                       pack_half2(ps[6], ps[7]));
+      } else {
+        const float* fsv = reinterpret_cast<const float*>(msv) + kq;
+        const float* fzv = reinterpret_cast<const float*>(mzv) + kq;
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t c[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float ps2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = 8 * kk + 2 * m + e;
+              const float pr = ex2(fmaf(rowA, t_at(t, j), nmu));  // 0 for masked keys
+              // keys past the end may hold anything: their terms are selected away
+              const bool live = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
+              la[0] += pr;
+              za[0] += live ? pr * fzv[j] : 0.0f;
+              ps2[e] = live ? pr * fsv[j] : 0.0f;
+            }
+            c[m] = pack_half2(ps2[0], ps2[1]);
+          }
+          // (a runtime kk cannot index pw: place the four words by selects)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) pw[4 * u + m] = (u == kk) ? c[m] : pw[4 * u + m];
+        }
       }
+      tmem_st16u(trow + kColP + 32 * b + 16 * half, pw);
+      tmem_wait_st();
       l_run += (la[0] + la[1]) + (la[2] + la[3]);
       pz += (za[0] + za[1]) + (za[2] + za[3]);
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -629,10 +725,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = fmaf(v[i], 16777216.0f, zz) * inv;  // codes were n 2^-24
     if (p.rotate_v) {
-      // every S product has completed (the last P.V came after it): the q'
-      // buffers are free for the exchange
+      // every product has completed (the last P.V came after all of them):
+      // the K/V operand buffers are free for the exchange
       if (p.block_h == kHeadDim)
-        stride64_step(v, reinterpret_cast<float*>(smem + kOffQh) + r * kHeadDim, half);
+        stride64_step(v, reinterpret_cast<float*>(smem + kOffKx) + r * kHeadDim, half);
       half_fwht(v, p.block_h);
 #pragma unroll
       for (int i = 0; i < 64; ++i) v[i] *= p.c_h;
