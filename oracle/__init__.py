@@ -41,20 +41,21 @@ def load() -> C.CDLL:
     sig = {
         "oracle_f16_to_f64": (f64, [C.c_uint16]),
         "oracle_f32_to_f16": (C.c_uint16, [C.c_float, i32]),
+        "oracle_f32_to_bf16": (C.c_uint16, [C.c_float, i32]),
         "oracle_sylvester": (i32, [i32, P]),
         "oracle_rotate_exact": (i32, [P, i32, i32, P]),
         "oracle_block_scale_f32": (C.c_float, [i32]),
         "oracle_rotate_canon": (i32, [P, i32, i32]),
-        "oracle_quantize_row": (i32, [P, i32, i32, i32, P, P, P]),
-        "oracle_dequant_row": (i32, [P, C.c_uint16, C.c_uint16, i32, P]),
+        "oracle_quantize_row": (i32, [P, i32, i32, i32, i32, i32, P, P, P]),
+        "oracle_dequant_row": (i32, [P, C.c_uint16, C.c_uint16, i32, i32, P]),
         "oracle_chunk_bytes": (i64, [i32, i32]),
         "oracle_cache_bytes": (i64, [i32, i32, i32, i32]),
         "oracle_quantize_append": (i64, [P, P, i64, i64, P, i32, i32, i32, i32, P, P, i32, i32,
-                                         i32, i32, i32]),
+                                         i32, i32, i32, i32, i32]),
         "oracle_decode_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f64,
-                                    P]),
+                                    P, i32, i32]),
         "oracle_prefill_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                     f64, P]),
+                                     f64, P, i32, i32]),
         "oracle_bf16_cache_bytes": (i64, [i32, i32, i32, i32]),
         "oracle_bf16_append": (i64, [P, P, i64, i64, P, i32, i32, i32, i32, P, P, i32, i32]),
         "oracle_decode_bf16_one": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P]),
@@ -89,6 +90,13 @@ def f32_to_f16_bits(x, mode: int) -> np.ndarray:
     lib = load()
     a = np.asarray(x, dtype=np.float32)
     return np.array([lib.oracle_f32_to_f16(float(v), mode) for v in a.ravel()],
+                    dtype=np.uint16).reshape(a.shape)
+
+
+def f32_to_bf16_bits(x, mode: int) -> np.ndarray:
+    lib = load()
+    a = np.asarray(x, dtype=np.float32)
+    return np.array([lib.oracle_f32_to_bf16(float(v), mode) for v in a.ravel()],
                     dtype=np.uint16).reshape(a.shape)
 
 
@@ -129,9 +137,11 @@ def rotate_canon(x, h: int) -> np.ndarray:
 
 # ---------------------------------------------------------------- quantizer
 
-def quantize_rows(x_bf16_bits, rotate: bool, h: int):
-    """Quantize rows of bfloat16 bit patterns [N, D] -> (codes [N, D/2] u8, s [N] u16, z [N] u16)."""
-    x = np.ascontiguousarray(np.asarray(x_bf16_bits, dtype=np.uint16))
+def quantize_rows(x_bits, rotate: bool, h: int, in_f16: bool = False, meta_bf16: bool = False):
+    """Quantize rows of bfloat16 (binary16 if in_f16) bit patterns [N, D] ->
+    (codes [N, D/2] u8, s [N] u16, z [N] u16); s and z are binary16 bits, or
+    bfloat16 bits if meta_bf16."""
+    x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
     if x.ndim == 1:
         x = x[None]
     N, D = x.shape
@@ -140,12 +150,13 @@ def quantize_rows(x_bf16_bits, rotate: bool, h: int):
     z = np.zeros(N, dtype=np.uint16)
     lib = load()
     for r in range(N):
-        _check(lib.oracle_quantize_row(_ptr(x[r]), D, int(rotate), h, _ptr(codes[r]),
-                                       s[r:].ctypes.data, z[r:].ctypes.data), "quantize_row")
+        _check(lib.oracle_quantize_row(_ptr(x[r]), int(in_f16), D, int(rotate), h, int(meta_bf16),
+                                       _ptr(codes[r]), s[r:].ctypes.data, z[r:].ctypes.data),
+               "quantize_row")
     return codes, s, z
 
 
-def dequant_rows(codes, s_bits, z_bits) -> np.ndarray:
+def dequant_rows(codes, s_bits, z_bits, meta_bf16: bool = False) -> np.ndarray:
     c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
     if c.ndim == 1:
         c = c[None]
@@ -155,8 +166,8 @@ def dequant_rows(codes, s_bits, z_bits) -> np.ndarray:
     out = np.zeros((N, 2 * half), dtype=np.float64)
     lib = load()
     for r in range(N):
-        _check(lib.oracle_dequant_row(_ptr(c[r]), int(s_bits[r]), int(z_bits[r]), 2 * half,
-                                      _ptr(out[r])), "dequant_row")
+        _check(lib.oracle_dequant_row(_ptr(c[r]), int(s_bits[r]), int(z_bits[r]), int(meta_bf16),
+                                      2 * half, _ptr(out[r])), "dequant_row")
     return out
 
 
@@ -178,10 +189,13 @@ def _ranges(n: int, parts: int):
 
 def quantize_append(k_bits, v_bits, slot_mapping, num_kv_heads: int, head_dim: int,
                     k_cache: np.ndarray, v_cache, num_pages: int, page_size: int,
-                    rotate_k: bool, rotate_v: bool, block_h: int, threads: int = 1) -> int:
+                    rotate_k: bool, rotate_v: bool, block_h: int, threads: int = 1,
+                    in_f16: bool = False, meta_bf16: bool = False) -> int:
     """Quantize-append every token of k (and v) into the caches in place.
 
-    k_bits / v_bits: uint16 [T, stride] (or [T, Hkv, D]) bfloat16 bit patterns.
+    k_bits / v_bits: uint16 [T, stride] (or [T, Hkv, D]) bfloat16 bit
+    patterns (binary16 if in_f16); meta_bf16 stores the (scale, zero) pairs
+    as bfloat16.
     Returns the number of out-of-range slots that were skipped.
     """
     k = np.ascontiguousarray(np.asarray(k_bits, dtype=np.uint16))
@@ -203,7 +217,7 @@ def quantize_append(k_bits, v_bits, slot_mapping, num_kv_heads: int, head_dim: i
             _ptr(k2), _ptr(v2) if v2 is not None else None, k2.shape[1],
             v2.shape[1] if v2 is not None else 0, _ptr(slots), b, e, num_kv_heads, head_dim,
             _ptr(k_cache), _ptr(v_cache) if v2 is not None else None, num_pages, page_size,
-            int(rotate_k), int(rotate_v), block_h)
+            int(rotate_k), int(rotate_v), block_h, int(in_f16), int(meta_bf16))
 
     rngs = _ranges(T, threads)
     if threads <= 1 or len(rngs) <= 1:
@@ -219,10 +233,11 @@ def quantize_append(k_bits, v_bits, slot_mapping, num_kv_heads: int, head_dim: i
 def decode(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
            num_kv_heads: int, head_dim: int, num_pages: int, page_size: int, rotate_k: bool,
            rotate_v: bool, block_h: int, sm_scale: float | None = None, pairs=None,
-           threads: int = 1) -> np.ndarray:
+           threads: int = 1, in_f16: bool = False, meta_bf16: bool = False) -> np.ndarray:
     """fp64 decode attention for the (seq, q_head) pairs given (default: all).
 
-    q_bits: uint16 [B, Hq, D] bfloat16 bit patterns.  The q-head -> kv-head map
+    q_bits: uint16 [B, Hq, D] bfloat16 bit patterns (binary16 if in_f16);
+    meta_bf16: the caches hold bfloat16 (scale, zero) pairs.  The q-head -> kv-head map
     is contiguous groups: kv = q_head // (Hq / Hkv) (a reading; the pages do
     not say).  Returns float64 [len(pairs), D].
     """
@@ -248,7 +263,7 @@ def decode(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
         rc = lib.oracle_decode_one(_ptr(qrow), _ptr(k_cache), _ptr(v_cache), _ptr(row),
                                    int(sl[b]), hq // G, num_kv_heads, head_dim, num_pages,
                                    page_size, int(rotate_k), int(rotate_v), block_h,
-                                   float(sm_scale), _ptr(o))
+                                   float(sm_scale), _ptr(o), int(in_f16), int(meta_bf16))
         _check(rc, "decode_one")
         out[i] = o
 
@@ -264,11 +279,12 @@ def decode(q_bits, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
 def prefill(q_bits, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int,
             num_kv_heads: int, head_dim: int, num_pages: int, page_size: int, rotate_k: bool,
             rotate_v: bool, block_h: int, sm_scale: float | None = None, rows=None,
-            threads: int = 1) -> np.ndarray:
+            threads: int = 1, in_f16: bool = False, meta_bf16: bool = False) -> np.ndarray:
     """fp64 chunked-prefill attention (causal) for the (query row, q_head)
     pairs given (default: all).
 
-    q_bits: uint16 [T, Hq, D] bfloat16, the query rows of every sequence's
+    q_bits: uint16 [T, Hq, D] bfloat16 (binary16 if in_f16; meta_bf16 as for
+    decode), the query rows of every sequence's
     chunk, sequence after sequence; rows cu_q_lens[b] .. cu_q_lens[b+1] - 1
     belong to sequence b and are its last q_len = cu_q_lens[b+1] - cu_q_lens[b]
     tokens, so row i sits at position seq_lens[b] - q_len + (i - cu_q_lens[b]).
@@ -302,7 +318,7 @@ def prefill(q_bits, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, num_q_h
         rc = lib.oracle_prefill_one(_ptr(qrow), _ptr(k_cache), _ptr(v_cache), _ptr(row), pos,
                                     hq // G, num_kv_heads, head_dim, num_pages, page_size,
                                     int(rotate_k), int(rotate_v), block_h, float(sm_scale),
-                                    _ptr(o))
+                                    _ptr(o), int(in_f16), int(meta_bf16))
         _check(rc, "prefill_one")
         out[n] = o
 

@@ -38,6 +38,14 @@
 #define ORACLE_RD 1 /* toward -infinity      */
 #define ORACLE_RU 2 /* toward +infinity      */
 
+/*
+ * Number formats.  K, V and q rows arrive as bfloat16 (in_f16 = 0) or as
+ * binary16 (in_f16 = 1: the [EN] fused-kernel diagram feeds "K,V (fp16)");
+ * the per-row (scale, zero) pair is stored as binary16 (meta_bf16 = 0) or
+ * as bfloat16 (meta_bf16 = 1).  Both input formats widen exactly to binary32,
+ * so the quantizer's arithmetic after step 1 is the same for either.
+ */
+
 static int is_pow2(int32_t h) { return h > 0 && (h & (h - 1)) == 0; }
 
 /* ------------------------------------------------------------------ */
@@ -123,6 +131,69 @@ uint16_t oracle_f32_to_f16(float x, int32_t mode) {
   return bits;
 }
 
+/*
+ * binary32 -> bfloat16 with an explicit rounding mode, by the same
+ * definition.  bfloat16 has binary32's exponent range and 8 significant
+ * bits: for |x| in [2^(e-1), 2^e) the spacing is 2^(e-8), and below 2^-126
+ * (the subnormals) it is 2^-133.  Magnitudes beyond the largest finite
+ * bfloat16, 2^128 - 2^120, saturate to it; a zero result is +0; NaN ->
+ * 0x7FC0.  Every bfloat16 value is a binary32 value, so the bits of the
+ * result are the upper half of its binary32 encoding.
+ */
+uint16_t oracle_f32_to_bf16(float x, int32_t mode) {
+  if (isnan(x)) return 0x7FC0;
+  const double max_bf16 = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+  int neg = signbit(x) ? 1 : 0;
+  double a = fabs((double)x);
+  double v;
+  if (a > max_bf16) {
+    v = max_bf16;
+  } else {
+    double ulp;
+    if (a < ldexp(1.0, -126)) {
+      ulp = ldexp(1.0, -133);
+    } else {
+      int e;
+      frexp(a, &e); /* a in [2^(e-1), 2^e) */
+      ulp = ldexp(1.0, (e - 1) - 7);
+    }
+    double m = a / ulp; /* exact */
+    double lo = floor(m), hi = ceil(m), r;
+    if (mode == ORACLE_RN) {
+      double frac = m - lo;
+      if (frac > 0.5)
+        r = hi;
+      else if (frac < 0.5)
+        r = lo;
+      else
+        r = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    } else if ((mode == ORACLE_RD) != (neg != 0)) {
+      r = lo;
+    } else {
+      r = hi;
+    }
+    v = r * ulp;
+    if (v > max_bf16) v = max_bf16;
+  }
+  if (v == 0.0) return 0;
+  float f = (float)v; /* exact */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint16_t bits = (uint16_t)(u >> 16);
+  if (neg) bits |= 0x8000;
+  return bits;
+}
+
+/* A stored metadata value in double. */
+static double meta_to_f64(uint16_t b, int32_t meta_bf16) {
+  return meta_bf16 ? (double)bf16_to_f32(b) : oracle_f16_to_f64(b);
+}
+
+/* An input element widened to binary32 (exact for either format). */
+static float in_to_f32(uint16_t b, int32_t in_f16) {
+  return in_f16 ? (float)oracle_f16_to_f64(b) : bf16_to_f32(b);
+}
+
 /* ------------------------------------------------------------------ */
 /* Rotation: block-diagonal Sylvester Hadamard, blocks of size h        */
 /* [EN] "The Rotation Trick"; [IT] s.2 "Rotazione Block-Diagonale"      */
@@ -203,23 +274,28 @@ int32_t oracle_rotate_canon(float* u, int32_t D, int32_t h) {
 /* ------------------------------------------------------------------ */
 
 /*
- * Quantize one row of D bfloat16 values.  Steps, in this order:
+ * Quantize one row of D bfloat16 (or binary16, in_f16) values.  Steps, in
+ * this order:
  *  1. widen to binary32 (exact);
  *  2. if rotate: R-canon rotation with blocks of h;
  *  3. mn, mx = min and max over all D values (one scale per row, spanning
  *     every h-block);
  *  4. zero-point z = fp16(mn) rounded toward -inf, scale
- *     s = fp16((mx - z) / 15) rounded toward +inf; so every value lies in
- *     [z, z + 15 s] and the dequantization error is at most s/2;
+ *     s = fp16((mx - z) / 15) rounded toward +inf (bfloat16 for both when
+ *     meta_bf16); so every value lies in [z, z + 15 s] and the
+ *     dequantization error is at most s/2;
  *  5. r = 1/s (0 when s == 0), code_i = clamp(rne((y_i - z) * r), 0, 15);
  *  6. pack two codes per byte, the even index in the low nibble.
  * The asymmetric fp16 (scale, zero) pair, directed rounding, round-half-even
- * and nibble order are readings taken where the pages are silent.
- * codes: D/2 bytes.  *s_bits, *z_bits: binary16 bit patterns.
+ * and nibble order are readings taken where the pages are silent; so are
+ * the bfloat16 metadata variant and its saturation at the largest finite
+ * bfloat16.
+ * codes: D/2 bytes.  *s_bits, *z_bits: binary16 (or bfloat16) bit patterns.
  */
-int32_t oracle_quantize_row(const uint16_t* x_bf16, int32_t D, int32_t rotate, int32_t h,
-                            uint8_t* codes, uint16_t* s_bits, uint16_t* z_bits) {
-  if (!x_bf16 || !codes || !s_bits || !z_bits || D <= 0 || (D & 1)) return ORACLE_EINVAL;
+int32_t oracle_quantize_row(const uint16_t* x, int32_t in_f16, int32_t D, int32_t rotate,
+                            int32_t h, int32_t meta_bf16, uint8_t* codes, uint16_t* s_bits,
+                            uint16_t* z_bits) {
+  if (!x || !codes || !s_bits || !z_bits || D <= 0 || (D & 1)) return ORACLE_EINVAL;
   if (rotate && (!is_pow2(h) || D % h != 0)) return ORACLE_EINVAL;
   float* y = (float*)malloc(sizeof(float) * (size_t)D);
   uint8_t* q = (uint8_t*)malloc((size_t)D);
@@ -228,7 +304,7 @@ int32_t oracle_quantize_row(const uint16_t* x_bf16, int32_t D, int32_t rotate, i
     free(q);
     return ORACLE_ENOMEM;
   }
-  for (int32_t i = 0; i < D; ++i) y[i] = bf16_to_f32(x_bf16[i]);
+  for (int32_t i = 0; i < D; ++i) y[i] = in_to_f32(x[i], in_f16);
   if (rotate) oracle_rotate_canon(y, D, h);
 
   float mn = y[0], mx = y[0];
@@ -236,12 +312,13 @@ int32_t oracle_quantize_row(const uint16_t* x_bf16, int32_t D, int32_t rotate, i
     if (y[i] < mn) mn = y[i];
     if (y[i] > mx) mx = y[i];
   }
-  uint16_t zb = oracle_f32_to_f16(mn, ORACLE_RD);
-  float z = (float)oracle_f16_to_f64(zb);
+  uint16_t zb = meta_bf16 ? oracle_f32_to_bf16(mn, ORACLE_RD) : oracle_f32_to_f16(mn, ORACLE_RD);
+  float z = (float)meta_to_f64(zb, meta_bf16);
   float range = mx - z;
   float step = range / 15.0f;
-  uint16_t sb = oracle_f32_to_f16(step, ORACLE_RU);
-  float s = (float)oracle_f16_to_f64(sb);
+  uint16_t sb =
+      meta_bf16 ? oracle_f32_to_bf16(step, ORACLE_RU) : oracle_f32_to_f16(step, ORACLE_RU);
+  float s = (float)meta_to_f64(sb, meta_bf16);
   float r = (s == 0.0f) ? 0.0f : 1.0f / s;
 
   for (int32_t i = 0; i < D; ++i) {
@@ -261,10 +338,10 @@ int32_t oracle_quantize_row(const uint16_t* x_bf16, int32_t D, int32_t rotate, i
 }
 
 /* Dequantize one row: y_hat_i = code_i * s + z, in double. */
-int32_t oracle_dequant_row(const uint8_t* codes, uint16_t s_bits, uint16_t z_bits, int32_t D,
-                           double* out) {
+int32_t oracle_dequant_row(const uint8_t* codes, uint16_t s_bits, uint16_t z_bits,
+                           int32_t meta_bf16, int32_t D, double* out) {
   if (!codes || !out || D <= 0 || (D & 1)) return ORACLE_EINVAL;
-  double s = oracle_f16_to_f64(s_bits), z = oracle_f16_to_f64(z_bits);
+  double s = meta_to_f64(s_bits, meta_bf16), z = meta_to_f64(z_bits, meta_bf16);
   for (int32_t j = 0; j < D / 2; ++j) {
     out[2 * j] = (double)(codes[j] & 15) * s + z;
     out[2 * j + 1] = (double)(codes[j] >> 4) * s + z;
@@ -279,8 +356,8 @@ int32_t oracle_dequant_row(const uint8_t* codes, uint16_t s_bits, uint16_t z_bit
  * Reading (the pages fix only "paged layout, token-wise, appended"): one
  * tensor (K or V) of a layer is [num_pages][num_kv_heads][chunk] bytes, a
  * chunk being P*D/2 code bytes (token offset o at o*D/2) followed by P
- * metadata words (token offset o at P*D/2 + 4*o: binary16 scale, then
- * binary16 zero, each little-endian).  Slot s of the cache is page s / P,
+ * metadata words (token offset o at P*D/2 + 4*o: scale, then zero, each a
+ * little-endian binary16 -- or bfloat16 in the meta_bf16 variant).  Slot s of the cache is page s / P,
  * offset s % P.
  */
 int64_t oracle_chunk_bytes(int32_t P, int32_t D) { return (int64_t)P * (D / 2) + (int64_t)P * 4; }
@@ -309,8 +386,8 @@ static void store_row(uint8_t* cache, int64_t slot, int32_t head, int32_t Hkv, i
 
 /*
  * Quantize and append tokens [token_begin, token_end) of k (and v, unless
- * NULL) into the caches at slot_mapping[t].  k/v are bfloat16 bits laid out
- * [token][Hkv][D] with a token stride in elements.  A slot of -1 is padding
+ * NULL) into the caches at slot_mapping[t].  k/v are bfloat16 (binary16 when
+ * in_f16) bits laid out [token][Hkv][D] with a token stride in elements.  A slot of -1 is padding
  * and skipped; any other slot outside [0, num_pages*P) is skipped and
  * counted.  Returns the count of such bad slots, or a negative error.
  * Every row is quantized on its own: no other token's values are read and no
@@ -320,7 +397,8 @@ int64_t oracle_quantize_append(const uint16_t* k, const uint16_t* v, int64_t k_s
                                int64_t v_stride, const int32_t* slot_mapping,
                                int32_t token_begin, int32_t token_end, int32_t Hkv, int32_t D,
                                uint8_t* k_cache, uint8_t* v_cache, int32_t num_pages, int32_t P,
-                               int32_t rotate_k, int32_t rotate_v, int32_t h) {
+                               int32_t rotate_k, int32_t rotate_v, int32_t h, int32_t in_f16,
+                               int32_t meta_bf16) {
   if (!k || !slot_mapping || !k_cache || (v && !v_cache) || Hkv <= 0 || D <= 0 || P <= 0 ||
       num_pages < 0 || token_begin < 0 || token_end < token_begin)
     return ORACLE_EINVAL;
@@ -337,16 +415,16 @@ int64_t oracle_quantize_append(const uint16_t* k, const uint16_t* v, int64_t k_s
     }
     for (int32_t hd = 0; hd < Hkv; ++hd) {
       uint16_t sb, zb;
-      int32_t rc = oracle_quantize_row(k + (int64_t)t * k_stride + (int64_t)hd * D, D, rotate_k,
-                                       h, codes, &sb, &zb);
+      int32_t rc = oracle_quantize_row(k + (int64_t)t * k_stride + (int64_t)hd * D, in_f16, D,
+                                       rotate_k, h, meta_bf16, codes, &sb, &zb);
       if (rc) {
         free(codes);
         return rc;
       }
       store_row(k_cache, slot, hd, Hkv, P, D, codes, sb, zb);
       if (v) {
-        rc = oracle_quantize_row(v + (int64_t)t * v_stride + (int64_t)hd * D, D, rotate_v, h,
-                                 codes, &sb, &zb);
+        rc = oracle_quantize_row(v + (int64_t)t * v_stride + (int64_t)hd * D, in_f16, D,
+                                 rotate_v, h, meta_bf16, codes, &sb, &zb);
         if (rc) {
           free(codes);
           return rc;
@@ -364,12 +442,12 @@ int64_t oracle_quantize_append(const uint16_t* k, const uint16_t* v, int64_t k_s
 /* ------------------------------------------------------------------ */
 
 static void read_row(const uint8_t* cache, int64_t page, int32_t off, int32_t head, int32_t Hkv,
-                     int32_t P, int32_t D, double* out) {
+                     int32_t P, int32_t D, int32_t meta_bf16, double* out) {
   const uint8_t* base = chunk_ptr((uint8_t*)cache, page, head, Hkv, P, D);
   const uint8_t* meta = base + (int64_t)P * (D / 2) + 4 * off;
   uint16_t sb = (uint16_t)(meta[0] | (meta[1] << 8));
   uint16_t zb = (uint16_t)(meta[2] | (meta[3] << 8));
-  oracle_dequant_row(base + (int64_t)off * (D / 2), sb, zb, D, out);
+  oracle_dequant_row(base + (int64_t)off * (D / 2), sb, zb, meta_bf16, D, out);
 }
 
 /*
@@ -382,15 +460,18 @@ static void read_row(const uint8_t* cache, int64_t page, int32_t off, int32_t he
  *   o     = (1/sqrt(h)) H o'  if V was rotated, else o'.
  * (1/sqrt(h)) H is symmetric and orthogonal, so q'.k^ = q.(H^-1 k^) and
  * H o' is the un-rotated output ([EN] "orthogonal ... undoable later").
+ * q is bfloat16 (binary16 when in_f16) bits; the cache's metadata is
+ * binary16 (bfloat16 when meta_bf16).
  * The caller passes the kv-head that serves this q-head.  seq_len == 0
  * gives a zero output.  Returns ORACLE_EPAGE for a page id outside
  * [0, num_pages).
  */
-int32_t oracle_decode_one(const uint16_t* q_bf16, const uint8_t* k_cache, const uint8_t* v_cache,
+int32_t oracle_decode_one(const uint16_t* q_bits, const uint8_t* k_cache, const uint8_t* v_cache,
                           const int32_t* block_table_row, int32_t seq_len, int32_t kv_head,
                           int32_t Hkv, int32_t D, int32_t num_pages, int32_t P, int32_t rotate_k,
-                          int32_t rotate_v, int32_t h, double sm_scale, double* out) {
-  if (!q_bf16 || !k_cache || !v_cache || !out || (seq_len > 0 && !block_table_row) || D <= 0 ||
+                          int32_t rotate_v, int32_t h, double sm_scale, double* out,
+                          int32_t in_f16, int32_t meta_bf16) {
+  if (!q_bits || !k_cache || !v_cache || !out || (seq_len > 0 && !block_table_row) || D <= 0 ||
       P <= 0 || seq_len < 0 || kv_head < 0 || kv_head >= Hkv)
     return ORACLE_EINVAL;
   if ((rotate_k || rotate_v) && (!is_pow2(h) || D % h != 0)) return ORACLE_EINVAL;
@@ -407,7 +488,7 @@ int32_t oracle_decode_one(const uint16_t* q_bf16, const uint8_t* k_cache, const 
     rc = ORACLE_ENOMEM;
     goto done;
   }
-  for (int32_t i = 0; i < D; ++i) q[i] = (double)bf16_to_f32(q_bf16[i]);
+  for (int32_t i = 0; i < D; ++i) q[i] = (double)in_to_f32(q_bits[i], in_f16);
   if (rotate_k)
     oracle_rotate_exact(q, D, h, qr);
   else
@@ -419,7 +500,7 @@ int32_t oracle_decode_one(const uint16_t* q_bf16, const uint8_t* k_cache, const 
       rc = ORACLE_EPAGE;
       goto done;
     }
-    read_row(k_cache, page, j % P, kv_head, Hkv, P, D, row);
+    read_row(k_cache, page, j % P, kv_head, Hkv, P, D, meta_bf16, row);
     double dot = 0.0;
     for (int32_t i = 0; i < D; ++i) dot += qr[i] * row[i];
     t[j] = sm_scale * dot;
@@ -432,7 +513,7 @@ int32_t oracle_decode_one(const uint16_t* q_bf16, const uint8_t* k_cache, const 
     double p = exp(t[j] - m);
     l += p;
     int64_t page = block_table_row[j / P];
-    read_row(v_cache, page, j % P, kv_head, Hkv, P, D, row);
+    read_row(v_cache, page, j % P, kv_head, Hkv, P, D, meta_bf16, row);
     for (int32_t i = 0; i < D; ++i) acc[i] += p * row[i];
   }
   for (int32_t i = 0; i < D; ++i) acc[i] /= l;
@@ -462,14 +543,16 @@ done:
  * That is exactly the decode above over the first query_pos + 1 tokens, so
  * the arithmetic is oracle_decode_one's.
  */
-int32_t oracle_prefill_one(const uint16_t* q_bf16, const uint8_t* k_cache,
+int32_t oracle_prefill_one(const uint16_t* q_bits, const uint8_t* k_cache,
                            const uint8_t* v_cache, const int32_t* block_table_row,
                            int32_t query_pos, int32_t kv_head, int32_t Hkv, int32_t D,
                            int32_t num_pages, int32_t P, int32_t rotate_k, int32_t rotate_v,
-                           int32_t h, double sm_scale, double* out) {
+                           int32_t h, double sm_scale, double* out, int32_t in_f16,
+                           int32_t meta_bf16) {
   if (query_pos < 0) return ORACLE_EINVAL;
-  return oracle_decode_one(q_bf16, k_cache, v_cache, block_table_row, query_pos + 1, kv_head,
-                           Hkv, D, num_pages, P, rotate_k, rotate_v, h, sm_scale, out);
+  return oracle_decode_one(q_bits, k_cache, v_cache, block_table_row, query_pos + 1, kv_head,
+                           Hkv, D, num_pages, P, rotate_k, rotate_v, h, sm_scale, out, in_f16,
+                           meta_bf16);
 }
 
 /* ------------------------------------------------------------------ */
