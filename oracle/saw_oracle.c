@@ -282,8 +282,8 @@ int32_t oracle_rotate_canon(float* u, int32_t D, int32_t h) {
  *     every h-block);
  *  4. zero-point z = fp16(mn) rounded toward -inf, scale
  *     s = fp16((mx - z) / 15) rounded toward +inf (bfloat16 for both when
- *     meta_bf16); so every value lies in [z, z + 15 s] and the
- *     dequantization error is at most s/2;
+ *     meta_bf16, a nonzero scale then at least 2^-126); so every value lies
+ *     in [z, z + 15 s] and the dequantization error is at most s/2;
  *  5. r = 1/s (0 when s == 0), code_i = clamp(rne((y_i - z) * r), 0, 15);
  *  6. pack two codes per byte, the even index in the low nibble.
  * The asymmetric fp16 (scale, zero) pair, directed rounding, round-half-even
@@ -318,6 +318,10 @@ int32_t oracle_quantize_row(const uint16_t* x, int32_t in_f16, int32_t D, int32_
   float step = range / 15.0f;
   uint16_t sb =
       meta_bf16 ? oracle_f32_to_bf16(step, ORACLE_RU) : oracle_f32_to_f16(step, ORACLE_RU);
+  /* A bfloat16 scale below 2^-126 would make 1/s overflow binary32; such a
+   * scale is raised to 2^-126, the smallest normal bfloat16 (a coarser step
+   * still covers [z, z + 15 s]).  Binary16 scales are >= 2^-24: no floor. */
+  if (meta_bf16 && step > 0.0f && bf16_to_f32(sb) < ldexpf(1.0f, -126)) sb = 0x0080;
   float s = (float)meta_to_f64(sb, meta_bf16);
   float r = (s == 0.0f) ? 0.0f : 1.0f / s;
 

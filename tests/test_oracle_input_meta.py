@@ -64,6 +64,12 @@ def _brute_bf16(x, mode):
     return out
 
 
+def _bf16_scale(step):
+    """The bfloat16 metadata scale: round up, and at least 2^-126 if nonzero."""
+    sb = _brute_bf16(step, oracle.RU)
+    return np.where((np.asarray(step) > 0) & (sb < 0x0080), 0x0080, sb).astype(np.uint16)
+
+
 def _random_f32(rng, n):
     mag = np.exp2(rng.uniform(-140, 127.9, n)).astype(np.float32)
     sign = np.where(rng.random(n) < 0.5, -1, 1).astype(np.float32)
@@ -173,7 +179,7 @@ def test_bf16_meta_rounding_and_error_bound(kind, rotate, h):
     np.testing.assert_array_equal(z, _brute_bf16(mn, oracle.RD))
     zf = bits_to_f32(z)
     step = ((mx - zf).astype(np.float32) / np.float32(15)).astype(np.float32)
-    np.testing.assert_array_equal(s, _brute_bf16(step, oracle.RU))
+    np.testing.assert_array_equal(s, _bf16_scale(step))
     sv = bits_to_f32(s).astype(np.float64)[:, None]
     zv = zf.astype(np.float64)[:, None]
     yd = y.astype(np.float64)
@@ -184,6 +190,23 @@ def test_bf16_meta_rounding_and_error_bound(kind, rotate, h):
     r = np.where(sv[:, 0] == 0, 0, (np.float32(1) / sv[:, 0].astype(np.float32))).astype(np.float32)
     v = ((y - zf[:, None]).astype(np.float32) * r[:, None]).astype(np.float32)
     np.testing.assert_array_equal(unpack(codes), np.clip(np.rint(v), 0, 15).astype(np.uint8))
+
+
+def test_bf16_meta_subnormal_rows_floor_the_scale():
+    """Rows of bfloat16 subnormals: the scale rounded up would be subnormal
+    too, and its reciprocal would overflow binary32; it is raised to 2^-126,
+    and every value still lies within s/2 of its dequantized value."""
+    m = np.tile(np.arange(16, dtype=np.uint16), 8)  # m 2^-133
+    codes, s, z = oracle.quantize_rows(m[None], False, 128, meta_bf16=True)
+    assert int(z[0]) == 0 and int(s[0]) == 0x0080
+    assert np.all(unpack(codes[0]) == 0)  # every value is below 2^-127 = s/2
+    y = bits_to_f32(m).astype(np.float64)
+    deq = oracle.dequant_rows(codes, s, z, meta_bf16=True)[0]
+    assert np.all(np.abs(y - deq) <= 2.0 ** -127)
+    big = np.concatenate([m[:64], np.full(64, 0x0100, np.uint16)])  # 2^-125 at the top
+    codes, s, z = oracle.quantize_rows(big[None], False, 128, meta_bf16=True)
+    assert int(s[0]) == 0x0080
+    np.testing.assert_array_equal(unpack(codes[0])[64:], 2)
 
 
 def test_bf16_meta_closed_form():
