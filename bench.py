@@ -356,9 +356,11 @@ def append_chunk_measure(device, stream, iters: int = 20):
     return res, nbytes, T
 
 
-def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
+def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18,
+                dtype=torch.bfloat16, meta_bf16=False):
     """One layer's K and V caches holding every token of every sequence,
-    written by the library's quantize-append (seeded synthetic rows)."""
+    written by the library's quantize-append (seeded synthetic rows of
+    `dtype`, metadata as bfloat16 if meta_bf16)."""
     import bit_paged_kv_gb300 as saw
     from bit_paged_kv_gb300 import workloads as W
     P = wl.page_size
@@ -371,10 +373,10 @@ def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
     status = torch.zeros(1, dtype=torch.int32, device=device)
     for a in range(0, total, chunk_tokens):
         b = min(total, a + chunk_tokens)
-        k = W.kv_rows(wl, layer, W.K, b - a, device, token_offset=a)
-        v = W.kv_rows(wl, layer, W.V, b - a, device, token_offset=a)
+        k = W.kv_rows(wl, layer, W.K, b - a, device, token_offset=a, dtype=dtype)
+        v = W.kv_rows(wl, layer, W.V, b - a, device, token_offset=a, dtype=dtype)
         saw.saw_quantize_append(k, v, slots[a:b], kc, vc, npages, P, wl.rotate_k, wl.rotate_v,
-                                wl.block_h, dev_status=status)
+                                wl.block_h, dev_status=status, meta_bf16=meta_bf16)
         del k, v
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -650,6 +652,78 @@ def variants_measure(device, stream, reps: int = 10):
     return res
 
 
+def formats_measure(device, stream, reps: int = 10):
+    """The format variants (binary16 input, bfloat16 metadata, both) beside
+    the plain formats, on two shapes: decode alone on qwen3-8b-concurrent
+    (64 sequences, lengths in [2048, 16384], head_dim 128, K and V rotated,
+    two layer caches decoded in turn), and the quantize-append of a
+    131072-token chunk (Hkv 8, K and V, page 64, h 128).  The algorithmic
+    bytes are the same for every format."""
+    import bit_paged_kv_gb300 as saw
+    from bit_paged_kv_gb300 import workloads as W
+    res = {}
+    fmts = [("bf16 input, fp16 meta", torch.bfloat16, False),
+            ("fp16 input, fp16 meta", torch.float16, False),
+            ("bf16 input, bf16 meta", torch.bfloat16, True),
+            ("fp16 input, bf16 meta", torch.float16, True)]
+    wl = W.QWEN3_8B_CONCURRENT
+    lens = W.seq_lens(wl)
+    bt, npages = W.page_tables(wl, lens)
+    btd, lensd = bt.to(device), lens.to(device)
+    B, Hq, D = wl.num_seqs, wl.num_q_heads, wl.head_dim
+    Lmax = int(lens.max())
+    nbytes = W.decode_bytes(wl, lens.tolist())
+    wa = W.LONG_PREFILL.variant(num_seqs=1)
+    T = wa.len_hi
+    lens1 = torch.tensor([T], dtype=torch.int32)
+    bt1, np1 = W.page_tables(wa, lens1)
+    slots = W.prefill_slots(bt1.to(device), [T], wa.page_size)
+    ab = W.append_bytes(wa, T)
+    for name, dt, bfm in fmts:
+        caches = [fill_caches(wl, l, lens, bt, npages, device, chunk_tokens=1 << 20, dtype=dt,
+                              meta_bf16=bfm) for l in range(2)]
+        qs = [W.q_rows(wl, l, device, dtype=dt) for l in range(2)]
+        wsb = saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, 0)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device) if wsb else None
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+        def one_pass():
+            for l in range(2):
+                saw.saw_paged_decode_int4(qs[l], caches[l][0], caches[l][1], btd, lensd, Lmax,
+                                          wl.num_kv_heads, npages, wl.page_size, wl.rotate_k,
+                                          wl.rotate_v, wl.block_h, out, ws, dev_status=status,
+                                          meta_bf16=bfm)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                one_pass()
+            t = statistics.median(time_events(one_pass, reps, stream)) / 2
+        assert int(status.item()) == 0
+        entry = {"decode_ms_per_layer": t, "decode_gbs": nbytes / (t * 1e-3) / 1e9}
+        del caches, qs, ws, out
+        torch.cuda.empty_cache()
+        k = W.kv_rows(wa, 0, W.K, T, device, dtype=dt)
+        v = W.kv_rows(wa, 0, W.V, T, device, dtype=dt)
+        nb = saw.saw_cache_bytes(np1, wa.page_size, wa.num_kv_heads, wa.head_dim)
+        kc = torch.empty(nb, dtype=torch.uint8, device=device)
+        vc = torch.empty(nb, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+        def app():
+            saw.saw_quantize_append(k, v, slots, kc, vc, np1, wa.page_size, True, True,
+                                    wa.block_h, meta_bf16=bfm)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                app()
+            ta = statistics.median(time_events(app, reps, stream))
+        entry.update({"append_ms": ta, "append_gbs": ab / (ta * 1e-3) / 1e9})
+        res[name] = entry
+        del k, v, kc, vc
+        torch.cuda.empty_cache()
+    return res
+
+
 def cpu_oracle_decode_sample(case, layers, threads, min_seconds=10.0, max_passes=40):
     """Time the oracle (as it stands) on the step's work for `layers`:
     append the new token, then decode every q-head over the layer's pages;
@@ -776,6 +850,7 @@ def run_saw(args):
     sweep = None if args.no_decode_configs else concurrency_sweep(device, stream)
     pre = None if args.no_decode_configs else prefill_measure(device, stream)
     var = None if args.no_decode_configs else variants_measure(device, stream)
+    fmtv = None if args.no_decode_configs else formats_measure(device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -867,6 +942,15 @@ def run_saw(args):
                     "131072-token chunk; GB/s = algorithmic bytes / time",
             "peak": peak,
             "results": {k: dict(v, frac=v["gbs"] / peak) for k, v in var.items()},
+        },
+        "format_variants": None if fmtv is None else {
+            "what": "binary16 input and bfloat16 metadata beside the plain formats (head_dim "
+                    "128, h 128); decode on the qwen3-8b-concurrent shape, append on a "
+                    "131072-token chunk; GB/s = algorithmic bytes / time (the same bytes "
+                    "for every format)",
+            "peak": peak,
+            "results": {k: dict(v, decode_frac=v["decode_gbs"] / peak,
+                                append_frac=v["append_gbs"] / peak) for k, v in fmtv.items()},
         },
         "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

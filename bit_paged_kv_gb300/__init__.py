@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     SAW_ERR_DEVICE_TIMEOUT,
     SAW_ERR_INVALID_ARG,
     SAW_ERR_UNSUPPORTED,
+    SAW_FMT_BF16_META,
+    SAW_FMT_F16_INPUT,
     SAW_OK,
     SAW_STEP_EARLY_PAGES,
     SawError,
@@ -23,11 +25,15 @@ from ._binding import (  # noqa: F401
     saw_decode_bf16_workspace_bytes,
     saw_decode_plan,
     saw_decode_step,
+    saw_decode_step_ex,
     saw_decode_workspace_bytes,
     saw_paged_decode_bf16,
     saw_paged_decode_int4,
+    saw_paged_decode_int4_ex,
     saw_paged_decode_int4_noalloc,
     saw_prefill_attn_int4,
+    saw_prefill_attn_int4_ex,
     saw_quantize_append,
+    saw_quantize_append_ex,
     saw_status_string,
 )

@@ -119,20 +119,15 @@ __device__ void smem_fwht(float* buf, int nvec, int h) {
 constexpr uint32_t kLoNib = 0x000F000Fu;  // bits 0-3 of both halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 
-__device__ __forceinline__ float half_lo(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
-}
-__device__ __forceinline__ float half_hi(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
-}
-
 // PACKED (group <= 4): the MMA's 8 columns carry the hi parts of the (up to)
 // 4 heads in columns 0-3 and the lo parts in columns 4-7, both for q' in the
 // score product and for p*s in the output product; lanes c and c^2 of an
 // MMA quad then hold the two halves of the same heads and are summed with one
 // shuffle.  WIDE (group 5..8): all 8 columns are heads; the score product
 // runs twice (q' hi, then lo) and p*s is one binary16 value.
-template <int P, bool PACKED, bool APPEND>
+// BFM: the caches' (scale, zero) words are bfloat16 instead of binary16;
+// they are widened to binary32 either way, so only that step differs.
+template <int P, bool PACKED, bool APPEND, bool BFM>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(const DecodeParams p) {
   using C = Cfg<P>;
   // Wait for the previous kernel in the stream before reading anything --
@@ -264,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
                           int64_t(kvh) * kHeadDim;
     const bool rot = (tensor == 0 ? p.rotate_k : p.rotate_v) != 0;
     uint32_t meta;
-    const uint16_t codes = warp_quantize_row(src, rot, p.block_h, p.c_h, lane, &meta);
+    const uint16_t codes =
+        warp_quantize_row(src, rot, p.block_h, p.c_h, lane, &meta, p.in_f16 != 0, BFM);
     uint8_t* nr = newrow + tensor * (kCodeRow + 16);
     reinterpret_cast<uint16_t*>(nr)[lane] = codes;
     if (lane == 0) *reinterpret_cast<uint32_t*>(nr + kCodeRow) = meta;
@@ -300,10 +296,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     if (h < G) {
       const uint2 raw = *reinterpret_cast<const uint2*>(
           p.q + (int64_t(seq) * p.num_q_heads + hq0 + h) * kHeadDim + 4 * lane);
-      x[0] = bf16_lo(raw.x);
-      x[1] = bf16_hi(raw.x);
-      x[2] = bf16_lo(raw.y);
-      x[3] = bf16_hi(raw.y);
+      const bool f16 = p.in_f16 != 0;
+      x[0] = in_lo(raw.x, f16);
+      x[1] = in_hi(raw.x, f16);
+      x[2] = in_lo(raw.y, f16);
+      x[3] = in_hi(raw.y, f16);
       if (p.rotate_k) {
         const int hb = p.block_h;
         const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
@@ -475,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       }
       const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g));
       const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8));
-      const float s0 = half_lo(mk0), z0 = half_hi(mk0);
-      const float s1 = half_lo(mk1), z1 = half_hi(mk1);
+      const float s0 = meta_lo(mk0, BFM), z0 = meta_hi(mk0, BFM);
+      const float s1 = meta_lo(mk1, BFM), z1 = meta_hi(mk1, BFM);
       sc[t][0] = fmaf(s0 * skA, d[0], z0 * qsA);
       sc[t][1] = fmaf(s0 * skB, d[1], z0 * qsB);
       sc[t][2] = fmaf(s1 * skA, d[2], z1 * qsA);
@@ -530,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       const float p2 = ex2(sc[t][2] - mu0), p3 = ex2(sc[t][3] - mu1);
       const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g));
       const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8));
-      float sv0 = half_lo(mv0), zv0 = half_hi(mv0);
-      float sv1 = half_lo(mv1), zv1 = half_hi(mv1);
+      float sv0 = meta_lo(mv0, BFM), zv0 = meta_hi(mv0, BFM);
+      float sv1 = meta_lo(mv1, BFM), zv1 = meta_hi(mv1, BFM);
       if (!full[t]) {  // rows past the end may hold anything, even inf
         sv0 = v0[t] ? sv0 : 0.0f;
         zv0 = v0[t] ? zv0 : 0.0f;
@@ -839,10 +836,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 // Launched with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream drains; it waits for it (griddepcontrol)
 // before reading anything.
-template <int P, bool PACKED, bool APPEND>
+template <int P, bool PACKED, bool APPEND, bool BFM>
 cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<P>;
-  auto kernel = paged_decode_kernel<P, PACKED, APPEND>;
+  auto kernel = paged_decode_kernel<P, PACKED, APPEND, BFM>;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
@@ -859,12 +856,19 @@ cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int P>
-cudaError_t launch_page(const DecodeParams& p, cudaStream_t stream) {
+template <int P, bool BFM>
+cudaError_t launch_page_m(const DecodeParams& p, cudaStream_t stream) {
   const bool packed = p.group <= kMaxGroup / 2;
   if (p.append)
-    return packed ? launch_p<P, true, true>(p, stream) : launch_p<P, false, true>(p, stream);
-  return packed ? launch_p<P, true, false>(p, stream) : launch_p<P, false, false>(p, stream);
+    return packed ? launch_p<P, true, true, BFM>(p, stream)
+                  : launch_p<P, false, true, BFM>(p, stream);
+  return packed ? launch_p<P, true, false, BFM>(p, stream)
+                : launch_p<P, false, false, BFM>(p, stream);
+}
+
+template <int P>
+cudaError_t launch_page(const DecodeParams& p, cudaStream_t stream) {
+  return p.meta_bf16 ? launch_page_m<P, true>(p, stream) : launch_page_m<P, false>(p, stream);
 }
 
 }  // namespace

@@ -26,7 +26,7 @@
 //      8-11  expanders: widen a raw INT4 tile into the K operand (keys x
 //            dims) and the transposed V operand (dims x keys), each code n
 //            as the binary16 subnormal n * 2^-24 (exact), and unpack the
-//            tile's (s, z) metadata to binary32.
+//            tile's (s, z) metadata (binary16 or bfloat16) to binary32.
 //      12    producer: 16-key slices (codes and metadata of K and V) through
 //            a 4-stage ring with the bulk-copy engine.
 //      13    MMA: one thread issues S = Q' K^T (M 128, N 64, K 128; q' hi and
@@ -95,12 +95,6 @@ constexpr uint32_t kColO = 128;
 constexpr uint32_t kColP = 256;
 constexpr int kSoftBar = 1;                         // named barrier id of the softmax warps
 
-__device__ __forceinline__ float f16lo_(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
-}
-__device__ __forceinline__ float f16hi_(uint32_t w) {
-  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
-}
 // 2^e for -126 <= e <= 127, exactly
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
 
@@ -278,14 +272,15 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       pos_r = pos_base + out_t;
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (int64_t(q0 + out_t) * p.num_q_heads + kvh * G + out_h) * kHeadDim + 64 * half);
+      const bool f16 = p.in_f16 != 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 w = src[k];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          v[8 * k + 2 * j] = bf16_lo(ws[j]);
-          v[8 * k + 2 * j + 1] = bf16_hi(ws[j]);
+          v[8 * k + 2 * j] = in_lo(ws[j], f16);
+          v[8 * k + 2 * j + 1] = in_hi(ws[j], f16);
         }
       }
     } else {
@@ -492,10 +487,11 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         const uint32_t km = *reinterpret_cast<const uint32_t*>(st + kRawKM + 4 * te);
         const uint32_t vm = *reinterpret_cast<const uint32_t*>(st + kRawVM + 4 * te);
         float* mf = reinterpret_cast<float*>(mb);
-        mf[te] = f16lo_(km);
-        mf[kBN + te] = f16hi_(km);
-        mf[2 * kBN + te] = f16lo_(vm);
-        mf[3 * kBN + te] = f16hi_(vm);
+        const bool bfm = p.meta_bf16 != 0;
+        mf[te] = meta_lo(km, bfm);
+        mf[kBN + te] = meta_hi(km, bfm);
+        mf[2 * kBN + te] = meta_lo(vm, bfm);
+        mf[3 * kBN + te] = meta_hi(vm, bfm);
       }
       if (te == 0) *reinterpret_cast<int*>(mb + kBN * 16) = *reinterpret_cast<const int*>(st + kRawOk);
       __syncwarp();

@@ -125,19 +125,28 @@ __device__ __forceinline__ void bfly2_signed(float& x0, float& x1, float& y0, fl
 
 // Butterfly of the row's H-blocks (strides 1, 2, ..., H/2 in ascending
 // order, every step an RN add or subtract), then one multiply by
-// c = binary32(1/sqrt(H)).  The stride-1 step reads the bfloat16 pairs
+// c = binary32(1/sqrt(H)).  The stride-1 step reads the input pairs
 // straight from the loaded words: a mixed-precision add takes the even
-// element as bfloat16 (exact widening) and the odd one as binary32.
-template <int H>
+// element as bfloat16 (binary16 with F16IN; exact widening either way) and
+// the odd one as binary32.
+template <int H, bool F16IN>
 __device__ __forceinline__ void rotate_half(const uint32_t (&wd)[kHalfRow / 2],
                                             float (&u)[kHalfRow], float c, int h) {
 #pragma unroll
   for (int i = 0; i < kHalfRow / 2; ++i) {
-    const float odd = bf16_hi(wd[i]);
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.bf16 %0, lo, %3;\n\tsub.rn.f32.bf16 %1, lo, %3;\n\t}"
-        : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
-        : "r"(wd[i]), "f"(odd));
+    if (F16IN) {
+      const float odd = f16_hi(wd[i]);
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.f16 %0, lo, %3;\n\tsub.rn.f32.f16 %1, lo, %3;\n\t}"
+          : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
+          : "r"(wd[i]), "f"(odd));
+    } else {
+      const float odd = bf16_hi(wd[i]);
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.bf16 %0, lo, %3;\n\tsub.rn.f32.bf16 %1, lo, %3;\n\t}"
+          : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
+          : "r"(wd[i]), "f"(odd));
+    }
   }
 #pragma unroll
   for (int len = 2; len < (H < 32 ? H : 32); len *= 2) {
@@ -263,7 +272,8 @@ __device__ __forceinline__ int chunk_slot(int r, int c) { return c ^ (r & 3); }
 // Tiles 0 .. tiles_per_tensor-1 are K rows, the rest V rows.  Each warp is
 // an independent worker with its own ring of kTileStages tiles: no CTA-wide
 // barrier, so a warp waiting for its data never holds up the others.
-template <int H>
+// F16IN: the rows are binary16 instead of bfloat16.
+template <int H, bool F16IN>
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     quantize_append_tiled_kernel(const AppendParams p, int tiles_per_tensor, int num_tiles) {
   extern __shared__ __align__(128) uint8_t ring_all[];
@@ -341,7 +351,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
 
     // Every thread computes (rows past the end or without a slot on stale
     // data) so that the pair shuffles run converged; only stores are guarded.
-    uint32_t wd[kHalfRow / 2];  // this thread's 64 bfloat16 values, in pairs
+    uint32_t wd[kHalfRow / 2];  // this thread's 64 input values, in pairs
     {
       // local chunk j of thread h: chunk j (h = 0), chunk 8 + (j ^ 4) (h = 1)
       const uint8_t* rowp = buf + r * kRowBytes + h * (kRowBytes / 2);
@@ -358,29 +368,20 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     float u[kHalfRow];
     const bool rot = tensor ? p.rotate[1] != 0 : p.rotate[0] != 0;
     if (rot) {
-      rotate_half<H>(wd, u, p.c_h, h);
+      rotate_half<H, F16IN>(wd, u, p.c_h, h);
     } else {
 #pragma unroll
       for (int i = 0; i < kHalfRow / 2; ++i) {
-        u[2 * i] = bf16_lo(wd[i]);
-        u[2 * i + 1] = bf16_hi(wd[i]);
+        u[2 * i] = F16IN ? f16_lo(wd[i]) : bf16_lo(wd[i]);
+        u[2 * i + 1] = F16IN ? f16_hi(wd[i]) : bf16_hi(wd[i]);
       }
     }
     float mn, mx;
     half_min_max(u, mn, mx);
-    const uint16_t zb = f16_round_down_sat(mn);
-    const float z = f16_bits_to_f32(zb);
-    const float step = __fdiv_rn(__fsub_rn(mx, z), 15.0f);
-    const uint16_t sb = f16_round_up_sat(step);
-    const float sv = f16_bits_to_f32(sb);
-    const float rcp = (sv == 0.0f) ? 0.0f : __frcp_rn(sv);
-    // No clamp can bite when z <= every element (min not below -65504) and
-    // the scale did not saturate: then 0 <= y - z <= max - z and
-    // r <= (1 + 2^-24) / s with s >= (max - z) / 15 (1 - 2^-24), so
-    // (y - z) * r stays below 15.5.
-    const bool fast = (mn >= -65504.0f) && (step <= 65504.0f);
+    const RowMeta m = row_meta(mn, mx, p.meta_bf16 != 0);
+    const uint16_t zb = m.zb, sb = m.sb;
     uint32_t word[8];
-    quantize_half(u, z, rcp, fast, word);
+    quantize_half(u, m.z, m.rcp, m.fast, word);
 
     if (live && slot != -1) {
       if (slot < 0 || int64_t(slot) >= p.num_slots) {
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta) quantize_append_warp_ker
       (tensor ? p.src[1] : p.src[0]) + int64_t(t) * (tensor ? p.stride[1] : p.stride[0]) +
           int64_t(hd) * kHeadDim,
       (tensor ? p.rotate[1] : p.rotate[0]) != 0,
-      H, p.c_h, lane, &meta);
+      H, p.c_h, lane, &meta, p.in_f16 != 0, p.meta_bf16 != 0);
   const int P = p.page_size;
   const int page = slot / P;
   const int off = slot - page * P;
@@ -490,6 +491,18 @@ cudaError_t launch_tiled(K kernel, dim3 grid, cudaStream_t stream, const AppendP
   return cudaLaunchKernelEx(&cfg, kernel, p, tiles_per_tensor, num_tiles);
 }
 
+template <bool F16IN>
+cudaError_t launch_tiled_h(int h, dim3 grid, cudaStream_t stream, const AppendParams& q,
+                           int tiles_per_tensor, int num_tiles) {
+  switch (h) {
+    case 16: return launch_tiled(quantize_append_tiled_kernel<16, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 32: return launch_tiled(quantize_append_tiled_kernel<32, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 64: return launch_tiled(quantize_append_tiled_kernel<64, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 128: return launch_tiled(quantize_append_tiled_kernel<128, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream) {
   const int num_rows = p.num_tokens * p.num_kv_heads;
   if (num_rows == 0) return cudaSuccess;
@@ -524,13 +537,8 @@ cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaS
   q.hkv_mul = uint32_t(((uint64_t(1) << q.hkv_shift) + q.num_kv_heads - 1) / q.num_kv_heads);
   q.page_shift = 0;
   while ((1 << q.page_shift) < q.page_size) ++q.page_shift;
-  switch (h) {
-    case 16: return launch_tiled(quantize_append_tiled_kernel<16>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 32: return launch_tiled(quantize_append_tiled_kernel<32>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 64: return launch_tiled(quantize_append_tiled_kernel<64>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 128: return launch_tiled(quantize_append_tiled_kernel<128>, grid, stream, q, tiles_per_tensor, num_tiles);
-    default: return cudaErrorInvalidValue;
-  }
+  return q.in_f16 ? launch_tiled_h<true>(h, grid, stream, q, tiles_per_tensor, num_tiles)
+                  : launch_tiled_h<false>(h, grid, stream, q, tiles_per_tensor, num_tiles);
 }
 
 }  // namespace saw

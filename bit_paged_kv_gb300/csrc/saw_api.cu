@@ -18,6 +18,7 @@ bool page_size_ok(int p) { return p == 16 || p == 32 || p == 64; }
 bool block_h_ok(int h) { return h == 16 || h == 32 || h == 64 || h == 128 || h == 256; }
 // head_dim 128 runs the specialised kernels; 64 and 256 the variant kernels
 bool head_dim_ok(int d) { return d == 64 || d == kHeadDim || d == 256; }
+bool formats_ok(int32_t f) { return (f & ~int32_t(SAW_FMT_F16_INPUT | SAW_FMT_BF16_META)) == 0; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -156,13 +157,15 @@ size_t saw_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_head
   return size_t(num_pages) * size_t(num_kv_heads) * chunk;
 }
 
-int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride,
-                            int64_t v_token_stride, const int32_t* slot_mapping,
-                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
-                            void* k_cache, void* v_cache, int32_t num_pages, int32_t page_size,
-                            int32_t rotate_k, int32_t rotate_v, int32_t block_h,
-                            int32_t* dev_status, void* stream) {
+int32_t saw_quantize_append_ex(const void* k, const void* v, int64_t k_token_stride,
+                               int64_t v_token_stride, const int32_t* slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                               void* k_cache, void* v_cache, int32_t num_pages,
+                               int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                               int32_t block_h, int32_t formats, int32_t* dev_status,
+                               void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_pages < 0) return SAW_ERR_INVALID_ARG;
+  if (!formats_ok(formats)) return SAW_ERR_INVALID_ARG;
   if (!head_dim_ok(head_dim) || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
   if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
     return SAW_ERR_INVALID_ARG;
@@ -199,11 +202,24 @@ int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride
   p.block_h = block_h;
   p.num_slots = int64_t(num_pages) * page_size;
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
+  p.in_f16 = (formats & SAW_FMT_F16_INPUT) ? 1 : 0;
+  p.meta_bf16 = (formats & SAW_FMT_BF16_META) ? 1 : 0;
   cudaError_t err =
       head_dim == kHeadDim
           ? saw::launch_quantize_append(p, has_v ? 2 : 1, static_cast<cudaStream_t>(stream))
           : saw::launch_quantize_append_var(p, head_dim, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride,
+                            int64_t v_token_stride, const int32_t* slot_mapping,
+                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                            void* k_cache, void* v_cache, int32_t num_pages, int32_t page_size,
+                            int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                            int32_t* dev_status, void* stream) {
+  return saw_quantize_append_ex(k, v, k_token_stride, v_token_stride, slot_mapping, num_tokens,
+                                num_kv_heads, head_dim, k_cache, v_cache, num_pages, page_size,
+                                rotate_k, rotate_v, block_h, 0, dev_status, stream);
 }
 
 int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size,
@@ -240,9 +256,10 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
                        int32_t head_dim, int32_t num_pages, int32_t page_size, int32_t rotate_k,
                        int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
                        void* workspace, size_t workspace_bytes, int32_t pages_per_split,
-                       int32_t* dev_status) {
+                       int32_t formats, int32_t* dev_status) {
   if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || max_seq_len < 0)
     return SAW_ERR_INVALID_ARG;
+  if (!formats_ok(formats)) return SAW_ERR_INVALID_ARG;
   if (!head_dim_ok(head_dim) || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
   if (num_q_heads / num_kv_heads > saw::kMaxGroup) return SAW_ERR_UNSUPPORTED;
@@ -302,12 +319,36 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  p.in_f16 = (formats & SAW_FMT_F16_INPUT) ? 1 : 0;
+  p.meta_bf16 = (formats & SAW_FMT_BF16_META) ? 1 : 0;
   return SAW_OK;
 }
 
 }  // namespace
 
 extern "C" {
+
+int32_t saw_paged_decode_int4_ex(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                                 int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t pages_per_split, int32_t formats, int32_t* dev_status,
+                                 void* stream) {
+  saw::DecodeParams p{};
+  const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
+                                    head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+                                    sm_scale, out, workspace, workspace_bytes, pages_per_split,
+                                    formats, dev_status);
+  if (rc != SAW_OK || num_seqs == 0) return rc;
+  cudaError_t err = head_dim == kHeadDim
+                        ? saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream))
+                        : saw::launch_paged_decode_var(p, head_dim, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
 
 int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -317,27 +358,21 @@ int32_t saw_paged_decode_int4(const void* q, const void* k_cache, const void* v_
                               int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
                               void* workspace, size_t workspace_bytes, int32_t pages_per_split,
                               int32_t* dev_status, void* stream) {
-  saw::DecodeParams p{};
-  const int32_t rc = prepare_decode(p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                    seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
-                                    head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
-                                    sm_scale, out, workspace, workspace_bytes, pages_per_split,
-                                    dev_status);
-  if (rc != SAW_OK || num_seqs == 0) return rc;
-  cudaError_t err = head_dim == kHeadDim
-                        ? saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream))
-                        : saw::launch_paged_decode_var(p, head_dim, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+  return saw_paged_decode_int4_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
+                                  head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+                                  sm_scale, out, workspace, workspace_bytes, pages_per_split, 0,
+                                  dev_status, stream);
 }
 
-int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
-                        void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
-                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                        int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
-                        int32_t block_h, float sm_scale, float* out, void* workspace,
-                        size_t workspace_bytes, int32_t pages_per_split, int32_t flags,
-                        int32_t* dev_status, void* stream) {
+int32_t saw_decode_step_ex(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                           void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                           int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                           int32_t flags, int32_t formats, int32_t* dev_status, void* stream) {
   saw::DecodeParams p{};
   if (flags & ~int32_t(SAW_STEP_EARLY_PAGES)) return SAW_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return SAW_ERR_UNSUPPORTED;  // the fused step is built for 128
@@ -345,7 +380,7 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
                                     seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
                                     head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
                                     sm_scale, out, workspace, workspace_bytes, pages_per_split,
-                                    dev_status);
+                                    formats, dev_status);
   if (rc != SAW_OK) return rc;
   if (num_seqs == 0) return SAW_OK;
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SAW_ERR_INVALID_ARG;
@@ -361,20 +396,37 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 
+int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                        int32_t block_h, float sm_scale, float* out, void* workspace,
+                        size_t workspace_bytes, int32_t pages_per_split, int32_t flags,
+                        int32_t* dev_status, void* stream) {
+  return saw_decode_step_ex(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                            num_pages, page_size, rotate_k, rotate_v, block_h, sm_scale, out,
+                            workspace, workspace_bytes, pages_per_split, flags, 0, dev_status,
+                            stream);
+}
+
 
 // ---------------------------------------------------------------- prefill
 
-int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const void* k_cache,
-                              const void* v_cache, const int32_t* block_tables,
-                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                              int32_t num_seqs, int32_t total_q, int32_t max_q_len,
-                              int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t num_pages, int32_t page_size,
-                              int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
-                              float* out, int32_t* dev_status, void* stream) {
+int32_t saw_prefill_attn_int4_ex(const void* q, const int32_t* cu_q_lens, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                                 int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_pages, int32_t page_size,
+                                 int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                                 float sm_scale, float* out, int32_t formats,
+                                 int32_t* dev_status, void* stream) {
   if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_pages < 0 || total_q < 0 ||
       max_q_len < 0 || max_seq_len < 0 || max_q_len > max_seq_len)
     return SAW_ERR_INVALID_ARG;
+  if (!formats_ok(formats)) return SAW_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || !page_size_ok(page_size)) return SAW_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads) return SAW_ERR_INVALID_ARG;
   if ((rotate_k != 0 && rotate_k != 1) || (rotate_v != 0 && rotate_v != 1))
@@ -421,8 +473,25 @@ int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const voi
   p.c_h = (rotate_k || rotate_v) ? float(1.0 / std::sqrt(double(block_h))) : 1.0f;
   const double scale = sm_scale > 0.0f ? double(sm_scale) : 1.0 / std::sqrt(double(head_dim));
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
+  p.in_f16 = (formats & SAW_FMT_F16_INPUT) ? 1 : 0;
+  p.meta_bf16 = (formats & SAW_FMT_BF16_META) ? 1 : 0;
   const cudaError_t err = saw::launch_prefill_attn(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
+}
+
+int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                              int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t num_pages, int32_t page_size,
+                              int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
+                              float* out, int32_t* dev_status, void* stream) {
+  return saw_prefill_attn_int4_ex(q, cu_q_lens, k_cache, v_cache, block_tables,
+                                  max_blocks_per_seq, seq_lens, num_seqs, total_q, max_q_len,
+                                  max_seq_len, num_q_heads, num_kv_heads, head_dim, num_pages,
+                                  page_size, rotate_k, rotate_v, block_h, sm_scale, out, 0,
+                                  dev_status, stream);
 }
 
 // ---------------------------------------------------------------- BF16 baseline

@@ -126,5 +126,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(uint16_t(w >> 16)));
+}
+// Input rows (q, K, V) are bfloat16 or, with f16 set, binary16; either widens
+// to binary32 exactly.
+__device__ __forceinline__ float in_lo(uint32_t w, bool f16) { return f16 ? f16_lo(w) : bf16_lo(w); }
+__device__ __forceinline__ float in_hi(uint32_t w, bool f16) { return f16 ? f16_hi(w) : bf16_hi(w); }
+// A metadata word {scale, zero}: binary16, or bfloat16 with bfm set.
+__device__ __forceinline__ float meta_lo(uint32_t w, bool bfm) { return bfm ? bf16_lo(w) : f16_lo(w); }
+__device__ __forceinline__ float meta_hi(uint32_t w, bool bfm) { return bfm ? bf16_hi(w) : f16_hi(w); }
 
 }  // namespace saw

@@ -21,7 +21,7 @@ __host__ __device__ constexpr int chunk_bytes(int page_size) {
 // ---------------------------------------------------------------- append
 
 struct AppendParams {
-  const uint16_t* src[2];       // K, V bfloat16 bits [T][Hkv][D] with token stride
+  const uint16_t* src[2];       // K, V bfloat16 (binary16 if in_f16) bits [T][Hkv][D] with token stride
   int64_t stride[2];            // token stride in elements
   uint8_t* cache[2];            // K, V caches
   int32_t rotate[2];
@@ -34,6 +34,8 @@ struct AppendParams {
   int32_t block_h;
   int64_t num_slots;            // num_pages * page_size
   float c_h;                    // binary32(1/sqrt(block_h))
+  int32_t in_f16;               // 1: the rows are binary16
+  int32_t meta_bf16;            // 1: (scale, zero) stored as bfloat16
   // set by the launcher: row / num_kv_heads = (row * hkv_mul) >> hkv_shift
   // for rows below 2^31, and page_size = 1 << page_shift
   uint32_t hkv_mul;
@@ -46,7 +48,7 @@ cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaS
 // ---------------------------------------------------------------- decode
 
 struct DecodeParams {
-  const uint16_t* q;            // [B][Hq][D] bfloat16 bits
+  const uint16_t* q;            // [B][Hq][D] bfloat16 (binary16 if in_f16) bits
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   const int32_t* block_tables;  // [B][max_blocks]
@@ -55,7 +57,8 @@ struct DecodeParams {
   float* part_o;                // [B][Hq][num_splits][D]
   float* part_ml;               // [B][Hq][num_splits][2]
   uint32_t* tickets;            // [B][Hkv][2] split counters (arrived, published), zero between calls
-  // decode step only: the new token's K and V rows, bfloat16 [B][Hkv][D]
+  // decode step only: the new token's K and V rows, bfloat16 (binary16 if
+  // in_f16) [B][Hkv][D]
   // with a per-sequence stride, quantized and appended at position
   // seq_len - 1 before attending
   const uint16_t* k_new;
@@ -84,6 +87,8 @@ struct DecodeParams {
   float q_scale;                // sm_scale * log2(e)
   int32_t warps;                // CTA shape: 16 (one per SM) or 8 (two per SM)
   int32_t head_dim;             // 128, or 64 / 256 (variant kernels)
+  int32_t in_f16;               // 1: q, k_new and v_new are binary16
+  int32_t meta_bf16;            // 1: the caches' (scale, zero) words are bfloat16
 };
 
 // One launcher per CTA shape (paged_decode.cu compiled once per shape).
@@ -105,7 +110,7 @@ inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t strea
 // ---------------------------------------------------------------- prefill
 
 struct PrefillParams {
-  const uint16_t* q;            // [total_q][Hq][D] bfloat16 bits, sequence after sequence
+  const uint16_t* q;            // [total_q][Hq][D] bfloat16 (binary16 if in_f16) bits, sequence after sequence
   const int32_t* cu_q;          // [B + 1] first query row of each sequence
   const uint8_t* k_cache;
   const uint8_t* v_cache;
@@ -129,6 +134,8 @@ struct PrefillParams {
   int32_t row_blocks;           // grid x: ceil(max_q_len * group / rows per CTA)
   float c_h;
   float q_scale;                // sm_scale * log2(e)
+  int32_t in_f16;               // 1: q is binary16
+  int32_t meta_bf16;            // 1: the caches' (scale, zero) words are bfloat16
 };
 
 int prefill_rows_per_cta();

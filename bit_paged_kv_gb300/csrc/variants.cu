@@ -6,8 +6,8 @@
 // (blocks of h); gist.science "SAW-INT4", s.2.  The method is stated for any
 // head size; the head_dim-128 kernels (quantize_append.cu, paged_decode.cu)
 // are specialised for 128, and these serve the other sizes with the same
-// cache layout (chunk = P*D/2 code bytes, then P words {fp16 s, fp16 z}) and
-// the same bits.
+// cache layout (chunk = P*D/2 code bytes, then P words {s, z}, binary16 or
+// bfloat16) and the same bits, for bfloat16 or binary16 input rows.
 //
 //  * Append: one warp per (token, kv-head) row, lane l holding elements
 //    E l .. E l + E - 1 (E = D/32).  The butterfly is the ascending-stride
@@ -52,18 +52,19 @@ __global__ void __launch_bounds__(32 * kVarRowsPerCta) quantize_append_var_kerne
   // (selects, not p.x[tensor]: indexing the parameter arrays would copy them to the stack)
   const uint16_t* src = (tensor ? p.src[1] : p.src[0]) +
                         int64_t(t) * (tensor ? p.stride[1] : p.stride[0]) + int64_t(hd) * D + E * lane;
+  const bool f16 = p.in_f16 != 0;
   float x[E];
   if (E == 2) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-    x[0] = bf16_lo(w);
-    x[1] = bf16_hi(w);
+    x[0] = in_lo(w, f16);
+    x[1] = in_hi(w, f16);
   } else {
     const uint4 w = *reinterpret_cast<const uint4*>(src);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) {
-      x[2 * j] = bf16_lo(ws[j]);
-      x[2 * j + 1] = bf16_hi(ws[j]);
+      x[2 * j] = in_lo(ws[j], f16);
+      x[2 * j + 1] = in_hi(ws[j], f16);
     }
   }
   if ((tensor ? p.rotate[1] : p.rotate[0]) != 0) {
@@ -101,15 +102,12 @@ __global__ void __launch_bounds__(32 * kVarRowsPerCta) quantize_append_var_kerne
     mn = fminf(mn, __shfl_xor_sync(kAll, mn, m));
     mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, m));
   }
-  const uint16_t zb = f16_round_down_sat(mn);
-  const float z = f16_bits_to_f32(zb);
-  const uint16_t sb = f16_round_up_sat(__fdiv_rn(__fsub_rn(mx, z), 15.0f));
-  const float sv = f16_bits_to_f32(sb);
-  const float r = (sv == 0.0f) ? 0.0f : __frcp_rn(sv);
+  const RowMeta m = row_meta(mn, mx, p.meta_bf16 != 0);
+  const uint16_t zb = m.zb, sb = m.sb;
   uint32_t codes = 0;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    int q = __float2int_rn(__fmul_rn(__fsub_rn(x[i], z), r));
+    int q = __float2int_rn(__fmul_rn(__fsub_rn(x[i], m.z), m.rcp));
     q = min(max(q, 0), 15);
     codes |= uint32_t(q) << (4 * i);
   }
@@ -201,7 +199,7 @@ __global__ void __launch_bounds__(kVThreads) paged_decode_var_kernel(const Decod
   // ---- q' = (1/sqrt h) H q per head of the group, and sum(q')
   for (int idx = tid; idx < G * D; idx += kVThreads) {
     const uint16_t b = p.q[(int64_t(seq) * p.num_q_heads + hq0) * D + idx];
-    qr[idx] = __uint_as_float(uint32_t(b) << 16);
+    qr[idx] = in_lo(b, p.in_f16 != 0);
   }
   __syncthreads();
   if (p.rotate_k) smem_fwht<D>(qr, G, p.block_h, p.c_h);
@@ -249,10 +247,10 @@ __global__ void __launch_bounds__(kVThreads) paged_decode_var_kernel(const Decod
       const uint8_t* vcb = p.v_cache + (int64_t(pid) * p.num_kv_heads + kvh) * kChunk;
       const uint32_t km = *reinterpret_cast<const uint32_t*>(kc + P * kRowB + 4 * off);
       const uint32_t vm = *reinterpret_cast<const uint32_t*>(vcb + P * kRowB + 4 * off);
-      const float ks = __half2float(__ushort_as_half(uint16_t(km & 0xFFFFu)));
-      const float kz = __half2float(__ushort_as_half(uint16_t(km >> 16)));
-      vs = __half2float(__ushort_as_half(uint16_t(vm & 0xFFFFu)));
-      vz = __half2float(__ushort_as_half(uint16_t(vm >> 16)));
+      const bool bfm = p.meta_bf16 != 0;
+      const float ks = meta_lo(km, bfm), kz = meta_hi(km, bfm);
+      vs = meta_lo(vm, bfm);
+      vz = meta_hi(vm, bfm);
       float dot[kMaxGroup];
 #pragma unroll
       for (int h = 0; h < kMaxGroup; ++h) dot[h] = 0.0f;

@@ -170,13 +170,14 @@ def k_bias(wl: Workload, layer: int, device) -> torch.Tensor | None:
 
 
 def kv_rows(wl: Workload, layer: int, tensor: int, num_tokens: int, device,
-            token_offset: int = 0) -> torch.Tensor:
-    """bfloat16 [num_tokens, Hkv, D] of K (tensor=K) or V (tensor=V) rows for
-    tokens [token_offset, token_offset + num_tokens) of the layer's stream."""
+            token_offset: int = 0, dtype=torch.bfloat16) -> torch.Tensor:
+    """[num_tokens, Hkv, D] of K (tensor=K) or V (tensor=V) rows for tokens
+    [token_offset, token_offset + num_tokens) of the layer's stream, rounded
+    to `dtype` (bfloat16, or float16 for the binary16-input variant)."""
     Hkv, D = wl.num_kv_heads, wl.head_dim
     gain = outlier_gain(wl, layer, tensor, device)
     bias = k_bias(wl, layer, device) if tensor == K else None
-    out = torch.empty(num_tokens, Hkv, D, dtype=torch.bfloat16, device=device)
+    out = torch.empty(num_tokens, Hkv, D, dtype=dtype, device=device)
     g = generator(wl, layer, tensor, device)
     # walk the stream chunk by chunk so a slice does not depend on its neighbours
     first = token_offset // GEN_CHUNK_TOKENS
@@ -190,15 +191,15 @@ def kv_rows(wl: Workload, layer: int, tensor: int, num_tokens: int, device,
         x = x.view(GEN_CHUNK_TOKENS, Hkv, D)[a - lo:b - lo] * gain
         if bias is not None:
             x = x + bias
-        out[a - token_offset:b - token_offset] = x.to(torch.bfloat16)
+        out[a - token_offset:b - token_offset] = x.to(dtype)
     return out
 
 
-def q_rows(wl: Workload, layer: int, device, num_seqs: int | None = None) -> torch.Tensor:
+def q_rows(wl: Workload, layer: int, device, num_seqs: int | None = None,
+           dtype=torch.bfloat16) -> torch.Tensor:
     B = wl.num_seqs if num_seqs is None else num_seqs
     g = generator(wl, layer, Q, device)
-    return torch.randn(B, wl.num_q_heads, wl.head_dim, generator=g,
-                       device=device).to(torch.bfloat16)
+    return torch.randn(B, wl.num_q_heads, wl.head_dim, generator=g, device=device).to(dtype)
 
 
 def decode_bytes(wl: Workload, lens) -> int:

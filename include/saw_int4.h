@@ -303,6 +303,73 @@ int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const voi
                               float* out, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Format variants.  The fused-kernel diagram of youngju.dev ("The System Is
+ * the Design -- A Fused Kernel") feeds the kernel binary16 ("fp16") K and V;
+ * engines also run in bfloat16.  The pages fix one scale per token but not
+ * the storage format of the (scale, zero) pair.  The *_ex calls below are
+ * the calls above with one extra argument, `formats`, an OR of:
+ *
+ *   SAW_FMT_F16_INPUT  q, K and V (and k_new, v_new) are binary16 instead of
+ *                      bfloat16.  Both widen to binary32 exactly, so every
+ *                      rule after that step is unchanged.
+ *   SAW_FMT_BF16_META  the caches' per-row words hold {scale, zero} as
+ *                      bfloat16 instead of binary16 (same place, same
+ *                      order).  zero = bfloat16 round-down(min), scale =
+ *                      bfloat16 round-up((max - zero)/15), both saturating
+ *                      at +-(2^128 - 2^120), a zero stored as +0, and a
+ *                      nonzero scale raised to at least 2^-126 (so that
+ *                      1/scale is finite); codes as before.  A cache must be
+ *                      written and read with the same metadata format.
+ *
+ * formats 0 is the plain call.  Any other bit: SAW_ERR_INVALID_ARG.
+ * Supported shapes are those of the plain calls (all head dims for append
+ * and decode; head_dim 128 for the decode step and the prefill).
+ * Precision note: the head_dim-128 decode and the prefill carry p * scale_V
+ * as a binary16 MMA operand, as they do for binary16 metadata, so their
+ * error bound assumes V scales below 65504 (rows spanning less than about
+ * 9.8e5); the head_dim 64/256 decode computes in binary32 throughout.
+ * ------------------------------------------------------------------------ */
+#define SAW_FMT_F16_INPUT 1
+#define SAW_FMT_BF16_META 2
+
+int32_t saw_quantize_append_ex(const void* k, const void* v, int64_t k_token_stride,
+                               int64_t v_token_stride, const int32_t* slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                               void* k_cache, void* v_cache, int32_t num_pages,
+                               int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                               int32_t block_h, int32_t formats, int32_t* dev_status,
+                               void* stream);
+
+int32_t saw_paged_decode_int4_ex(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                                 int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t pages_per_split, int32_t formats, int32_t* dev_status,
+                                 void* stream);
+
+int32_t saw_decode_step_ex(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                           void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t num_pages, int32_t page_size, int32_t rotate_k,
+                           int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t pages_per_split,
+                           int32_t flags, int32_t formats, int32_t* dev_status, void* stream);
+
+int32_t saw_prefill_attn_int4_ex(const void* q, const int32_t* cu_q_lens, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                                 int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_pages, int32_t page_size,
+                                 int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                                 float sm_scale, float* out, int32_t formats,
+                                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * BF16 baseline.  gist.science "SAW-INT4: System-Aware 4-Bit KV-Cache
  * Quantization for Real-World LLM Serving", s.4 measures SAW-INT4's serving
  * throughput against an unquantized BF16 KV cache.  These two calls are that

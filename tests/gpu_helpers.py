@@ -18,7 +18,7 @@ SENTINEL = 0xAB
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """bfloat16 tensor (any device) -> numpy uint16 bit patterns."""
+    """bfloat16 or float16 tensor (any device) -> numpy uint16 bit patterns."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
@@ -29,18 +29,20 @@ def new_caches(num_pages, P, Hkv, D, device="cuda", with_v=True):
     return kc, vc
 
 
-def gpu_append(k, v, slots, num_pages, P, rotate_k, rotate_v, h, kc=None, vc=None):
+def gpu_append(k, v, slots, num_pages, P, rotate_k, rotate_v, h, kc=None, vc=None,
+               meta_bf16=False):
     T, Hkv, D = k.shape
     if kc is None:
         kc, vc = new_caches(num_pages, P, Hkv, D, with_v=v is not None)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     saw.saw_quantize_append(k, v, slots, kc, vc, num_pages, P, rotate_k, rotate_v, h,
-                            dev_status=status)
+                            dev_status=status, meta_bf16=meta_bf16)
     torch.cuda.synchronize()
     return kc, vc, int(status.item())
 
 
-def oracle_append(k, v, slots, num_pages, P, rotate_k, rotate_v, h, kc=None, vc=None):
+def oracle_append(k, v, slots, num_pages, P, rotate_k, rotate_v, h, kc=None, vc=None,
+                  meta_bf16=False):
     T, Hkv, D = k.shape
     n = oracle.cache_bytes(num_pages, P, Hkv, D)
     if kc is None:
@@ -49,7 +51,8 @@ def oracle_append(k, v, slots, num_pages, P, rotate_k, rotate_v, h, kc=None, vc=
     kb = bits(k).reshape(T, -1)
     vb = bits(v).reshape(T, -1) if v is not None else None
     bad = oracle.quantize_append(kb, vb, slots.cpu().numpy(), Hkv, D, kc, vc, num_pages, P,
-                                 rotate_k, rotate_v, h, threads=oracle.host_threads())
+                                 rotate_k, rotate_v, h, threads=oracle.host_threads(),
+                                 in_f16=k.dtype == torch.float16, meta_bf16=meta_bf16)
     return kc, vc, bad
 
 
@@ -62,7 +65,7 @@ def assert_bytes_equal(gpu: torch.Tensor, ref: np.ndarray, what: str):
 
 
 def gpu_decode(q, kc, vc, bt, lens, num_kv_heads, num_pages, P, rotate_k, rotate_v, h,
-               max_seq_len=None, pages_per_split=0, sm_scale=0.0):
+               max_seq_len=None, pages_per_split=0, sm_scale=0.0, meta_bf16=False):
     B, Hq, D = q.shape
     if max_seq_len is None:
         max_seq_len = max(int(x) for x in lens.tolist()) if B else 0
@@ -72,17 +75,19 @@ def gpu_decode(q, kc, vc, bt, lens, num_kv_heads, num_pages, P, rotate_k, rotate
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     saw.saw_paged_decode_int4(q, kc, vc, bt, lens, max_seq_len, num_kv_heads, num_pages, P,
                               rotate_k, rotate_v, h, out, ws, sm_scale=sm_scale,
-                              pages_per_split=pages_per_split, dev_status=status)
+                              pages_per_split=pages_per_split, dev_status=status,
+                              meta_bf16=meta_bf16)
     torch.cuda.synchronize()
     return out, int(status.item())
 
 
 def oracle_decode(q, kc_host, vc_host, bt, lens, num_kv_heads, num_pages, P, rotate_k, rotate_v,
-                  h, pairs=None, sm_scale=None):
+                  h, pairs=None, sm_scale=None, meta_bf16=False):
     B, Hq, D = q.shape
     return oracle.decode(bits(q), kc_host, vc_host, bt.cpu().numpy(), lens.cpu().numpy(), Hq,
                          num_kv_heads, D, num_pages, P, rotate_k, rotate_v, h,
-                         sm_scale=sm_scale, pairs=pairs, threads=oracle.host_threads())
+                         sm_scale=sm_scale, pairs=pairs, threads=oracle.host_threads(),
+                         in_f16=q.dtype == torch.float16, meta_bf16=meta_bf16)
 
 
 ERRORS = []  # (label, relative error) of every attention comparison, for the log
@@ -99,17 +104,18 @@ def rel_err(got: np.ndarray, ref: np.ndarray, label: str = "") -> float:
 
 
 def fill_layer(wl: W.Workload, layer: int, lens, bt, num_pages, device="cuda", upto=None,
-               kc=None, vc=None, chunk_tokens=1 << 18):
+               kc=None, vc=None, chunk_tokens=1 << 18, dtype=torch.bfloat16, meta_bf16=False):
     """Quantize-append every token of every sequence (or the first `upto`
     tokens of each) of one layer into fresh caches with the CUDA path.
-    Returns (kc, vc, k_rows, v_rows, slots) with the bf16 rows appended."""
+    Returns (kc, vc, k_rows, v_rows, slots) with the rows appended (`dtype`:
+    bfloat16, or float16 for the binary16-input variant)."""
     P = wl.page_size
     lens_l = [int(x) for x in lens.tolist()]
     if upto is not None:
         lens_l = [min(L, upto(L)) for L in lens_l]
     total = sum(lens_l)
-    k = W.kv_rows(wl, layer, W.K, total, device)
-    v = W.kv_rows(wl, layer, W.V, total, device)
+    k = W.kv_rows(wl, layer, W.K, total, device, dtype=dtype)
+    v = W.kv_rows(wl, layer, W.V, total, device, dtype=dtype)
     slots = W.prefill_slots(bt.to(device), lens_l, P)
     if kc is None:
         kc, vc = new_caches(num_pages, P, wl.num_kv_heads, wl.head_dim, device)
@@ -117,7 +123,7 @@ def fill_layer(wl: W.Workload, layer: int, lens, bt, num_pages, device="cuda", u
     for a in range(0, total, chunk_tokens):
         b = min(total, a + chunk_tokens)
         saw.saw_quantize_append(k[a:b], v[a:b], slots[a:b], kc, vc, num_pages, P, wl.rotate_k,
-                                wl.rotate_v, wl.block_h, dev_status=status)
+                                wl.rotate_v, wl.block_h, dev_status=status, meta_bf16=meta_bf16)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return kc, vc, k, v, slots

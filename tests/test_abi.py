@@ -279,3 +279,78 @@ def _prefill(L, **kw):
 ])
 def test_prefill_rejects_before_launch(L, kw, expect):
     assert _prefill(L, **kw) == expect
+
+
+# ---------------------------------------------------------------- format variants (*_ex)
+
+def _append_ex(L, fmt, **kw):
+    a = dict(k=A, v=B, ks=1024, vs=1024, slots=A, T=4, hkv=8, d=128, kc=A, vc=B, pages=4, P=16,
+             rk=1, rv=1, h=128, status=None, stream=None)
+    a.update(kw)
+    return L.saw_quantize_append_ex(a["k"], a["v"], a["ks"], a["vs"], a["slots"], a["T"],
+                                    a["hkv"], a["d"], a["kc"], a["vc"], a["pages"], a["P"],
+                                    a["rk"], a["rv"], a["h"], fmt, a["status"], a["stream"])
+
+
+def _decode_ex(L, fmt, **kw):
+    a = dict(q=A, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128, pages=8,
+             P=16, rk=1, rv=1, h=128, scale=0.0, out=A, ws=B, wsb=1 << 20, pps=0, status=None,
+             stream=None)
+    a.update(kw)
+    return L.saw_paged_decode_int4_ex(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"],
+                                      a["B"], a["maxlen"], a["hq"], a["hkv"], a["d"], a["pages"],
+                                      a["P"], a["rk"], a["rv"], a["h"], a["scale"], a["out"],
+                                      a["ws"], a["wsb"], a["pps"], fmt, a["status"], a["stream"])
+
+
+def _step_ex(L, fmt, **kw):
+    a = dict(q=A, kn=A, vn=B, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128,
+             pages=8, P=16, rk=1, rv=1, h=128, scale=0.0, out=A, ws=B, wsb=1 << 20, pps=0,
+             flags=0, status=None, stream=None)
+    a.update(kw)
+    return L.saw_decode_step_ex(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["mb"],
+                                a["sl"], a["B"], a["maxlen"], a["hq"], a["hkv"], a["d"],
+                                a["pages"], a["P"], a["rk"], a["rv"], a["h"], a["scale"],
+                                a["out"], a["ws"], a["wsb"], a["pps"], a["flags"], fmt,
+                                a["status"], a["stream"])
+
+
+def _prefill_ex(L, fmt, **kw):
+    a = dict(q=A, cu=B, kc=A, vc=B, bt=A, mb=64, sl=B, B=2, T=100, mq=64, maxlen=1024, hq=32,
+             hkv=8, d=128, pages=128, P=16, rk=1, rv=1, h=128, scale=0.0, out=A, status=None,
+             stream=None)
+    a.update(kw)
+    return L.saw_prefill_attn_int4_ex(a["q"], a["cu"], a["kc"], a["vc"], a["bt"], a["mb"],
+                                      a["sl"], a["B"], a["T"], a["mq"], a["maxlen"], a["hq"],
+                                      a["hkv"], a["d"], a["pages"], a["P"], a["rk"], a["rv"],
+                                      a["h"], a["scale"], a["out"], fmt, a["status"], a["stream"])
+
+
+EX_CALLS = [_append_ex, _decode_ex, _step_ex, _prefill_ex]
+
+
+@pytest.mark.parametrize("call", EX_CALLS)
+@pytest.mark.parametrize("fmt", [4, 8, -1, 1 << 30])
+def test_ex_rejects_unknown_format_bits(L, call, fmt):
+    # B=0 / T=0 would otherwise return SAW_OK before any launch
+    kw = dict(T=0) if call is _append_ex else dict(B=0)
+    assert call(L, fmt, **kw) == saw.SAW_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("call", EX_CALLS)
+@pytest.mark.parametrize("fmt", [0, saw.SAW_FMT_F16_INPUT, saw.SAW_FMT_BF16_META,
+                                 saw.SAW_FMT_F16_INPUT | saw.SAW_FMT_BF16_META])
+def test_ex_known_formats_keep_the_plain_checks(L, call, fmt):
+    # the empty call succeeds without a launch, and the plain calls' argument
+    # checks still apply under every format
+    empty = dict(T=0) if call is _append_ex else dict(B=0)
+    assert call(L, fmt, **empty) == saw.SAW_OK
+    assert call(L, fmt, d=96) == saw.SAW_ERR_UNSUPPORTED
+    assert call(L, fmt, kc=MIS) == saw.SAW_ERR_INVALID_ARG
+    assert call(L, fmt, h=3) == saw.SAW_ERR_INVALID_ARG
+
+
+def test_ex_step_and_prefill_stay_head_dim_128(L):
+    for fmt in (saw.SAW_FMT_F16_INPUT, saw.SAW_FMT_BF16_META):
+        assert _step_ex(L, fmt, d=64) == saw.SAW_ERR_UNSUPPORTED
+        assert _prefill_ex(L, fmt, d=256) == saw.SAW_ERR_UNSUPPORTED
