@@ -30,7 +30,8 @@ int sm_count() {
 }
 
 // Split plan.  A split should give every warp several 16-token tiles (at
-// least 1024 tokens per split).  Among the split counts allowed, take the one
+// least 1024 tokens per split, 4096 when the units fill the GPU without
+// splitting).  Among the split counts allowed, take the one
 // whose CTA count (sequences x kv-heads x splits) wastes the least of its
 // last wave, preferring fewer splits (a smaller merge) unless more splits
 // fill the waves clearly better.
@@ -88,7 +89,12 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
     splits = ceil_div(max_pages, pps);
     warps = shape_for(splits, pps);
   } else {
-    const int64_t min_pps = ceil_div(1024, page_size);
+    // When the (sequence, kv-head) units alone fill every CTA slot of the
+    // 8-warp shape, splitting only adds CTA prologues and merges (several
+    // waves balance the load anyway): splits of at least 4096 tokens then.
+    // Smaller grids split down to 1024 tokens to reach every SM.
+    const int64_t min_tokens = units >= 2 * sms ? 4096 : 1024;
+    const int64_t min_pps = ceil_div(min_tokens, page_size);
     const int64_t max_splits = std::min<int64_t>(64, ceil_div(max_pages, min_pps));
     int64_t s16 = best_splits(units, sms, max_splits);
     int64_t p16 = ceil_div(max_pages, s16);
