@@ -202,7 +202,9 @@ __device__ __forceinline__ bool wait_sleep_all(uint64_t* bar, uint32_t parity) {
   return __all_sync(kAllLanes, wait_sleep(bar, parity));
 }
 
-template <int P>
+// F16IN: q is binary16 (else bfloat16); BFM: the caches' (scale, zero)
+// words are bfloat16 (else binary16).
+template <int P, bool F16IN, bool BFM>
 __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   pdl_wait_then_release();
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -272,15 +274,14 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       pos_r = pos_base + out_t;
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (int64_t(q0 + out_t) * p.num_q_heads + kvh * G + out_h) * kHeadDim + 64 * half);
-      const bool f16 = p.in_f16 != 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 w = src[k];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          v[8 * k + 2 * j] = in_lo(ws[j], f16);
-          v[8 * k + 2 * j + 1] = in_hi(ws[j], f16);
+          v[8 * k + 2 * j] = in_lo(ws[j], F16IN);
+          v[8 * k + 2 * j + 1] = in_hi(ws[j], F16IN);
         }
       }
     } else {
@@ -487,11 +488,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         const uint32_t km = *reinterpret_cast<const uint32_t*>(st + kRawKM + 4 * te);
         const uint32_t vm = *reinterpret_cast<const uint32_t*>(st + kRawVM + 4 * te);
         float* mf = reinterpret_cast<float*>(mb);
-        const bool bfm = p.meta_bf16 != 0;
-        mf[te] = meta_lo(km, bfm);
-        mf[kBN + te] = meta_hi(km, bfm);
-        mf[2 * kBN + te] = meta_lo(vm, bfm);
-        mf[3 * kBN + te] = meta_hi(vm, bfm);
+        mf[te] = meta_lo(km, BFM);
+        mf[kBN + te] = meta_hi(km, BFM);
+        mf[2 * kBN + te] = meta_lo(vm, BFM);
+        mf[3 * kBN + te] = meta_hi(vm, BFM);
       }
       if (te == 0) *reinterpret_cast<int*>(mb + kBN * 16) = *reinterpret_cast<const int*>(st + kRawOk);
       __syncwarp();
@@ -746,9 +746,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
   }
 }
 
-template <int P>
-cudaError_t launch_prefill_p(const PrefillParams& p, cudaStream_t stream) {
-  auto kernel = prefill_tc_kernel<P>;
+template <int P, bool F16IN, bool BFM>
+cudaError_t launch_prefill_f(const PrefillParams& p, cudaStream_t stream) {
+  auto kernel = prefill_tc_kernel<P, F16IN, BFM>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -762,6 +762,15 @@ cudaError_t launch_prefill_p(const PrefillParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int P>
+cudaError_t launch_prefill_p(const PrefillParams& p, cudaStream_t stream) {
+  if (p.in_f16)
+    return p.meta_bf16 ? launch_prefill_f<P, true, true>(p, stream)
+                       : launch_prefill_f<P, true, false>(p, stream);
+  return p.meta_bf16 ? launch_prefill_f<P, false, true>(p, stream)
+                     : launch_prefill_f<P, false, false>(p, stream);
 }
 
 }  // namespace
