@@ -16,8 +16,10 @@
 //    the codes and (s, z) are the oracle's to the bit, as in the 128 path.
 //  * Decode: CUDA-core kernel, one 4-warp CTA per (split, kv-head, sequence),
 //    the GQA group fused (a page is read once).  Scores with lane = token
-//    (q' broadcast from shared memory); P.V with lane = 2D/64 dims (the
-//    chunk's p*s broadcast from shared memory); online softmax per head;
+//    (q' broadcast from shared memory), each lane also staging its token's
+//    V row in shared memory; P.V with lane = 2D/64 dims (the chunk's p*s
+//    broadcast from shared memory, V rows from the staged copy); online
+//    softmax per head;
 //    split partials merged in the last split to arrive (two counters per
 //    (sequence, kv-head), bounded wait), as in the 128 path.
 #include "saw_device.cuh"
@@ -136,7 +138,11 @@ struct VarCfg {
   static constexpr int kRedM = kRed + kVW * kMaxGroup * D * 4;    // f32 [warps][8] m, l, z
   static constexpr int kTot = kRedM + 3 * kVW * kMaxGroup * 4;    // f32 [3][8]: den, M, Z
   static constexpr int kFlag = kTot + 3 * kMaxGroup * 4;          // int [4]
-  static constexpr int kSmem = kFlag + 16;
+  // each warp's 32 V rows of the current chunk, rows padded by 16 bytes so
+  // that the lanes' 16-byte stores of their own rows hit distinct banks
+  static constexpr int kVRow = D / 2 + 16;
+  static constexpr int kVbuf = (kFlag + 16 + 15) / 16 * 16;       // u8 [warps][32][kVRow]
+  static constexpr int kSmem = kVbuf + kVW * 32 * kVRow;
 };
 
 // In-place Sylvester butterfly over the first `rows` rows of a [rows][D]
@@ -225,6 +231,7 @@ __global__ void __launch_bounds__(kVThreads) paged_decode_var_kernel(const Decod
     for (int e = 0; e < E; ++e) o[h][e] = 0.0f;
   }
   float* ps = psb + warp * kMaxGroup * 32;
+  uint8_t* vbuf = smem + C::kVbuf + warp * 32 * C::kVRow;
 
   for (int t0 = tok_begin + 32 * warp; t0 < tok_end; t0 += 32 * kVW) {
     const int tok = t0 + lane;
@@ -251,6 +258,14 @@ __global__ void __launch_bounds__(kVThreads) paged_decode_var_kernel(const Decod
       const float ks = meta_lo(km, bfm), kz = meta_hi(km, bfm);
       vs = meta_lo(vm, bfm);
       vz = meta_hi(vm, bfm);
+      // this token's V row into the warp's buffer: all 32 rows arrive in one
+      // round of memory latency, not one round per token of the P.V loop
+      {
+        const uint4* vsrc = reinterpret_cast<const uint4*>(vcb + off * kRowB);
+        uint4* vdst = reinterpret_cast<uint4*>(vbuf + lane * C::kVRow);
+#pragma unroll
+        for (int piece = 0; piece < kRowB / 16; ++piece) vdst[piece] = vsrc[piece];
+      }
       float dot[kMaxGroup];
 #pragma unroll
       for (int h = 0; h < kMaxGroup; ++h) dot[h] = 0.0f;
@@ -311,9 +326,7 @@ __global__ void __launch_bounds__(kVThreads) paged_decode_var_kernel(const Decod
     for (int j = 0; j < n_tok; ++j) {
       const int pj = __shfl_sync(kAll, pid, j);
       if (pj < 0) continue;  // warp-uniform
-      const int offj = (t0 + j) % P;
-      const uint8_t* vrow =
-          p.v_cache + (int64_t(pj) * p.num_kv_heads + kvh) * kChunk + offj * kRowB + NB * lane;
+      const uint8_t* vrow = vbuf + j * C::kVRow + NB * lane;
       uint32_t cw;
       if (NB == 1)
         cw = *vrow;
