@@ -143,6 +143,18 @@ def test_plan_and_workspace(L):
     s, pps = saw.saw_decode_plan(256, 8, 16, 8192, 0)
     assert s * pps * 16 >= 8192
     assert saw.saw_decode_plan(1, 8, 64, 0, 0) == (1, 1)
+    # many units (enough to fill every CTA slot unsplit on any GPU this targets):
+    # splits of at least 4096 tokens, still covering the context
+    for B, L_ in [(256, 8192), (128, 16384), (512, 32768)]:
+        s, pps = saw.saw_decode_plan(B, 8, 16, L_, 0)
+        assert pps * 16 >= min(4096, L_) and s * pps * 16 >= L_
+    # few units: splits may go down to 1024 tokens to reach every SM
+    s, pps = saw.saw_decode_plan(1, 8, 16, 32768, 0)
+    assert 1024 <= pps * 16 < 4096 and s > 8
+    # the workspace of an automatic head_dim-128 plan is that plan's partials
+    w128 = saw.saw_decode_workspace_bytes(64, 32, 8, 128, 16, 16384, 0)
+    s128, _ = saw.saw_decode_plan(64, 8, 16, 16384, 0)
+    assert s128 > 1 and w128 == (64 * 8 * 8 + 15) // 16 * 16 + 64 * 32 * s128 * (128 + 2) * 4
     with pytest.raises(saw.SawError):
         saw.saw_decode_plan(1, 8, 12, 100, 0)
 
