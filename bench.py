@@ -1087,6 +1087,27 @@ def run_profile(args):
                                       dev_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
+    elif args.profile == "variant":
+        # head_dim 256 decode on 16 sequences of the qwen3-8b-concurrent shape
+        import bit_paged_kv_gb300 as saw
+        wl = W.QWEN3_8B_CONCURRENT.variant(num_seqs=16, head_dim=256, block_h=256)
+        lens = W.seq_lens(wl)
+        bt, npages = W.page_tables(wl, lens)
+        kc, vc = fill_caches(wl, 0, lens, bt, npages, device)
+        B, Hq, D = wl.num_seqs, wl.num_q_heads, wl.head_dim
+        Lmax = int(lens.max())
+        q = W.q_rows(wl, 0, device)
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=device)
+        wsb = saw.saw_decode_workspace_bytes(B, Hq, wl.num_kv_heads, D, wl.page_size, Lmax, 0)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            saw.saw_paged_decode_int4(q, kc, vc, bt.to(device), lens.to(device), Lmax,
+                                      wl.num_kv_heads, npages, wl.page_size, True, True, D, out,
+                                      ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
     else:
         append_chunk_measure(device, torch.cuda.current_stream(device), iters=1)
     torch.cuda.synchronize()
@@ -1103,7 +1124,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-configs", action="store_true",
                     help="skip the decode-only measurements of the other workloads")
-    ap.add_argument("--profile", choices=["decode", "append", "bf16", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "bf16", "prefill", "variant"],
+                    default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)
     args = ap.parse_args(argv)
