@@ -21,6 +21,12 @@
  *     q is rotated once (q.k = Hq.Hk because H is orthogonal), and the output
  *     is rotated back when V was rotated.
  *
+ * Further calls build on these two: saw_decode_step (both in one launch),
+ * saw_prefill_attn_int4 (causal attention of a chunk of queries over the
+ * same cache), the *_ex forms with binary16 inputs or bfloat16 scale/zero
+ * metadata, and a BF16 paged cache with the same decode (saw_bf16_*), the
+ * baseline the pages compare INT4 against.
+ *
  * Readings taken where the pages are silent: Sylvester ordering of H, the
  * 1/sqrt(h) scale applied after an ascending-stride butterfly, one binary16
  * (scale, zero) pair per (token, kv-head) from the rotated row's min/max
@@ -30,7 +36,8 @@
  *
  * Common rules for every entry point:
  *  - All buffers are owned by the caller.  The library allocates nothing and
- *    keeps no state between calls; every call is thread-safe.
+ *    keeps no state between calls (saw_paged_decode_int4_noalloc's fixed
+ *    scratch array aside); every call is thread-safe.
  *  - Pointers marked "device" must be device memory of the current device.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it.  The return value reports argument
