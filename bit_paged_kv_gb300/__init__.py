@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     saw_paged_decode_int4,
     saw_paged_decode_int4_ex,
     saw_paged_decode_int4_noalloc,
+    saw_paged_decode_int4_noalloc_ex,
     saw_prefill_attn_int4,
     saw_prefill_attn_int4_ex,
     saw_quantize_append,

@@ -30,7 +30,7 @@ EXPORTS = ("saw_status_string", "saw_cache_bytes", "saw_quantize_append", "saw_d
            "saw_paged_decode_int4_noalloc", "saw_bf16_cache_bytes", "saw_bf16_append",
            "saw_decode_bf16_workspace_bytes", "saw_paged_decode_bf16", "saw_prefill_attn_int4",
            "saw_quantize_append_ex", "saw_paged_decode_int4_ex", "saw_decode_step_ex",
-           "saw_prefill_attn_int4_ex")
+           "saw_prefill_attn_int4_ex", "saw_paged_decode_int4_noalloc_ex")
 
 _lib = None
 
@@ -87,7 +87,7 @@ def lib() -> C.CDLL:
                                         i32, i32, i32, i32, i32, f32, P, P, P]
     # the *_ex calls: the same arguments plus `formats` before dev_status
     for name in ("saw_quantize_append", "saw_paged_decode_int4", "saw_decode_step",
-                 "saw_prefill_attn_int4"):
+                 "saw_prefill_attn_int4", "saw_paged_decode_int4_noalloc"):
         base = getattr(L, name).argtypes
         ex = getattr(L, name + "_ex")
         ex.restype = i32
@@ -232,21 +232,23 @@ def saw_paged_decode_int4_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cach
                                   max_seq_len: int, num_kv_heads: int, num_pages: int,
                                   page_size: int, rotate_k: bool, rotate_v: bool, block_h: int,
                                   out: torch.Tensor, sm_scale: float = 0.0,
-                                  pages_per_split: int = 0, dev_status=None, stream=None) -> None:
+                                  pages_per_split: int = 0, dev_status=None, stream=None,
+                                  meta_bf16: bool = False) -> None:
     """saw_paged_decode_int4 without a workspace argument: the split-K
     scratch is the library's own fixed 4 MiB device array (for callers that
     cannot allocate).  Raises SawError(SAW_ERR_UNSUPPORTED) if the plan needs
-    more than that."""
+    more than that.  q: bfloat16 or float16."""
     B, hq, d = q.shape
-    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    fmt = _formats(q, meta_bf16)
+    assert q.is_contiguous()
     assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, hq, d)
     assert block_tables.dtype == torch.int32 and block_tables.is_contiguous()
     assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
-    rc = lib().saw_paged_decode_int4_noalloc(
+    rc = _call("saw_paged_decode_int4_noalloc", fmt, [
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), B, max_seq_len, hq, num_kv_heads, d, num_pages, page_size,
         int(rotate_k), int(rotate_v), block_h, float(sm_scale), _ptr(out), pages_per_split,
-        _ptr(dev_status), _stream(q, stream))
+        _ptr(dev_status), _stream(q, stream)])
     _raise(rc, "saw_paged_decode_int4_noalloc")
 
 
@@ -373,3 +375,14 @@ def saw_prefill_attn_int4_ex(q, cu_q_lens, k_cache, v_cache, block_tables, seq_l
                           max_seq_len, num_kv_heads, num_pages, page_size, rotate_k, rotate_v,
                           block_h, out, sm_scale, dev_status, stream,
                           meta_bf16=_ex_meta(q, formats))
+
+
+def saw_paged_decode_int4_noalloc_ex(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
+                                     num_kv_heads, num_pages, page_size, rotate_k, rotate_v,
+                                     block_h, out, formats: int, sm_scale: float = 0.0,
+                                     pages_per_split: int = 0, dev_status=None,
+                                     stream=None) -> None:
+    saw_paged_decode_int4_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
+                                  num_kv_heads, num_pages, page_size, rotate_k, rotate_v,
+                                  block_h, out, sm_scale, pages_per_split, dev_status, stream,
+                                  meta_bf16=_ex_meta(q, formats))

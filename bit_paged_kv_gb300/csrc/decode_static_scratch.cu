@@ -49,12 +49,13 @@ int32_t scratch_for_current_device(void** out) {
 
 }  // namespace
 
-extern "C" int32_t saw_paged_decode_int4_noalloc(
+extern "C" int32_t saw_paged_decode_int4_noalloc_ex(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
     int32_t page_size, int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
-    float* out, int32_t pages_per_split, int32_t* dev_status, void* stream) {
+    float* out, int32_t pages_per_split, int32_t formats, int32_t* dev_status, void* stream) {
+  if (formats & ~int32_t(SAW_FMT_F16_INPUT | SAW_FMT_BF16_META)) return SAW_ERR_INVALID_ARG;
   const size_t need = saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  page_size, max_seq_len, pages_per_split);
   if (need > kStaticScratchBytes) return SAW_ERR_UNSUPPORTED;
@@ -71,9 +72,22 @@ extern "C" int32_t saw_paged_decode_int4_noalloc(
     if (cudaMemsetAsync(scratch, 0, tb, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return SAW_ERR_CUDA;
   }
-  return saw_paged_decode_int4(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
-                               num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim,
-                               num_pages, page_size, rotate_k, rotate_v, block_h, sm_scale, out,
-                               scratch, need > 0 ? kStaticScratchBytes : 0, pages_per_split,
-                               dev_status, stream);
+  return saw_paged_decode_int4_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
+                                  head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+                                  sm_scale, out, scratch, need > 0 ? kStaticScratchBytes : 0,
+                                  pages_per_split, formats, dev_status, stream);
+}
+
+extern "C" int32_t saw_paged_decode_int4_noalloc(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
+    int32_t page_size, int32_t rotate_k, int32_t rotate_v, int32_t block_h, float sm_scale,
+    float* out, int32_t pages_per_split, int32_t* dev_status, void* stream) {
+  return saw_paged_decode_int4_noalloc_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                          seq_lens, num_seqs, max_seq_len, num_q_heads,
+                                          num_kv_heads, head_dim, num_pages, page_size, rotate_k,
+                                          rotate_v, block_h, sm_scale, out, pages_per_split, 0,
+                                          dev_status, stream);
 }

@@ -330,7 +330,8 @@ int32_t saw_prefill_attn_int4(const void* q, const int32_t* cu_q_lens, const voi
  *                      1/scale is finite); codes as before.  A cache must be
  *                      written and read with the same metadata format.
  *
- * formats 0 is the plain call.  Any other bit: SAW_ERR_INVALID_ARG.
+ * formats 0 is the plain call.  Any other bit: SAW_ERR_INVALID_ARG, before
+ * anything is enqueued.
  * Supported shapes are those of the plain calls (all head dims for append
  * and decode; head_dim 128 for the decode step and the prefill).
  * Precision note: the head_dim-128 decode and the prefill carry p * scale_V
@@ -367,6 +368,16 @@ int32_t saw_decode_step_ex(const void* q, const void* k_new, const void* v_new, 
                            int32_t rotate_v, int32_t block_h, float sm_scale, float* out,
                            void* workspace, size_t workspace_bytes, int32_t pages_per_split,
                            int32_t flags, int32_t formats, int32_t* dev_status, void* stream);
+
+int32_t saw_paged_decode_int4_noalloc_ex(const void* q, const void* k_cache,
+                                         const void* v_cache, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                         int32_t num_seqs, int32_t max_seq_len,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_pages, int32_t page_size,
+                                         int32_t rotate_k, int32_t rotate_v, int32_t block_h,
+                                         float sm_scale, float* out, int32_t pages_per_split,
+                                         int32_t formats, int32_t* dev_status, void* stream);
 
 int32_t saw_prefill_attn_int4_ex(const void* q, const int32_t* cu_q_lens, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,

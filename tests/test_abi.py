@@ -338,7 +338,25 @@ def _prefill_ex(L, fmt, **kw):
                                       a["h"], a["scale"], a["out"], fmt, a["status"], a["stream"])
 
 
+def _noalloc_ex(L, fmt, **kw):
+    a = dict(q=A, kc=A, vc=B, bt=A, mb=4, sl=B, B=2, maxlen=64, hq=32, hkv=8, d=128, pages=8,
+             P=16, rk=1, rv=1, h=128, scale=0.0, out=A, pps=0, status=None, stream=None)
+    a.update(kw)
+    return L.saw_paged_decode_int4_noalloc_ex(a["q"], a["kc"], a["vc"], a["bt"], a["mb"],
+                                              a["sl"], a["B"], a["maxlen"], a["hq"], a["hkv"],
+                                              a["d"], a["pages"], a["P"], a["rk"], a["rv"],
+                                              a["h"], a["scale"], a["out"], a["pps"], fmt,
+                                              a["status"], a["stream"])
+
+
 EX_CALLS = [_append_ex, _decode_ex, _step_ex, _prefill_ex]
+
+
+@pytest.mark.parametrize("fmt", [4, -1])
+def test_noalloc_ex_rejects_unknown_format_bits_first(L, fmt):
+    # refused before the scratch is looked up or cleared (B = 2, a real plan)
+    assert _noalloc_ex(L, fmt) == saw.SAW_ERR_INVALID_ARG
+    assert _noalloc_ex(L, 0, B=0) == saw.SAW_OK
 
 
 @pytest.mark.parametrize("call", EX_CALLS)

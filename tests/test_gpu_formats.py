@@ -241,3 +241,23 @@ def test_ex_twins_agree_with_dtype_dispatch():
     with pytest.raises(AssertionError):
         saw.saw_quantize_append_ex(k, v, slots, kc1, vc1, pages, P, True, True, 128,
                                    saw.SAW_FMT_BF16_META)
+
+
+@pytest.mark.parametrize("fmt", FORMATS, ids=FMT_IDS)
+def test_noalloc_decode(fmt):
+    """The no-alloc decode under each format equals the oracle."""
+    dt, bfm = fmt
+    wl = W.TINY.variant(num_q_heads=8, shuffle_pages=True, dist="student_t", nu=4)
+    lens, bt, npages, kc, vc, q = _setup(wl, [900, 40, 2000], dt, bfm)
+    B, Hq, D = q.shape
+    ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, wl.num_kv_heads, npages,
+                        wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h, meta_bf16=bfm)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    saw.saw_paged_decode_int4_noalloc(q, kc, vc, bt.cuda(), lens.cuda(), 2000, wl.num_kv_heads,
+                                      npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                                      out, pages_per_split=8, dev_status=st, meta_bf16=bfm)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    err = rel_err(out.cpu().numpy().reshape(-1, D), ref, f"fmt-noalloc-{_label(dt, bfm)}")
+    assert err <= ATTN_TOL, f"relative error {err:.3e}"
