@@ -59,24 +59,32 @@ extern "C" int32_t saw_paged_decode_int4_noalloc_ex(
   const size_t need = saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  page_size, max_seq_len, pages_per_split);
   if (need > kStaticScratchBytes) return SAW_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
+  // Every argument check runs before anything is enqueued, so a call that
+  // fails leaves the stream (and the shared array) untouched.  The checks
+  // only need to know that a large enough workspace exists: a stand-in
+  // address is passed, never dereferenced, and replaced below.
+  saw::DecodeParams p{};
+  void* const stand_in = reinterpret_cast<void*>(uintptr_t(256));
+  const int32_t rc = saw::prepare_decode(
+      p, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+      num_q_heads, num_kv_heads, head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
+      sm_scale, out, need > 0 ? stand_in : nullptr, need > 0 ? kStaticScratchBytes : 0,
+      pages_per_split, formats, dev_status);
+  if (rc != SAW_OK || num_seqs == 0) return rc;
   if (need > 0) {
-    const int32_t rc = scratch_for_current_device(&scratch);
-    if (rc != SAW_OK) return rc;
-  }
-  // The merge counts finished splits in the first words of the scratch;
-  // they must start at zero, so clear them (the split partials need no
-  // clearing: every partial the merge reads is written earlier in the call).
-  if (need > 0) {
+    void* scratch = nullptr;
+    const int32_t rs = scratch_for_current_device(&scratch);
+    if (rs != SAW_OK) return rs;
+    saw::bind_decode_workspace(p, scratch);
+    // The merge counts finished splits in the first words of the array;
+    // they must start at zero, so clear them (the split partials need no
+    // clearing: every partial the merge reads is written earlier in the call).
     const size_t tb = saw::decode_ticket_bytes(num_seqs, num_kv_heads);
     if (cudaMemsetAsync(scratch, 0, tb, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return SAW_ERR_CUDA;
   }
-  return saw_paged_decode_int4_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                  seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads,
-                                  head_dim, num_pages, page_size, rotate_k, rotate_v, block_h,
-                                  sm_scale, out, scratch, need > 0 ? kStaticScratchBytes : 0,
-                                  pages_per_split, formats, dev_status, stream);
+  const cudaError_t err = saw::launch_decode_any(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 
 extern "C" int32_t saw_paged_decode_int4_noalloc(

@@ -59,7 +59,10 @@ constexpr int kRedStride = kHeadDim + 8;  // padded row of the cross-warp reduct
 __device__ __forceinline__ int red_col(int d) { return d + (d >> 4); }
 constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
 constexpr int kStepTok = 16;              // tokens per step (one MMA tile, one softmax update)
-constexpr int kStages = 4;
+#ifndef SAW_DECODE_STAGES
+#define SAW_DECODE_STAGES 4
+#endif
+constexpr int kStages = SAW_DECODE_STAGES;  // tiles in flight per warp
 constexpr int kCodeRow = kHeadDim / 2;    // code bytes per token
 
 // Stage layout for a 16-token step, the same for every page size:

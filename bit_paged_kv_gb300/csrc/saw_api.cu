@@ -253,9 +253,10 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
 
 }  // extern "C"
 
-namespace {
+namespace saw {
 
 // Checks shared by the decode entry points; fills the kernel parameters.
+// Makes no CUDA call that enqueues work.
 int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
                        const void* v_cache, const int32_t* block_tables,
                        int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
@@ -300,13 +301,6 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.out = out;
-  const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
-  if (need > 0) {
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.tickets = reinterpret_cast<uint32_t*>(ws);
-    p.part_o = reinterpret_cast<float*>(ws + saw::decode_ticket_bytes(num_seqs, num_kv_heads));
-    p.part_ml = p.part_o + rows * head_dim;
-  }
   p.dev_status = dev_status;
   p.max_blocks = max_blocks_per_seq;
   p.num_seqs = num_seqs;
@@ -328,10 +322,26 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
   p.in_f16 = (formats & SAW_FMT_F16_INPUT) ? 1 : 0;
   p.meta_bf16 = (formats & SAW_FMT_BF16_META) ? 1 : 0;
+  if (need > 0) bind_decode_workspace(p, workspace);
   return SAW_OK;
 }
 
-}  // namespace
+void bind_decode_workspace(DecodeParams& p, void* workspace) {
+  const size_t rows = size_t(p.num_seqs) * size_t(p.num_q_heads) * size_t(p.num_splits);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.tickets = reinterpret_cast<uint32_t*>(ws);
+  p.part_o = reinterpret_cast<float*>(ws + decode_ticket_bytes(p.num_seqs, p.num_kv_heads));
+  p.part_ml = p.part_o + rows * p.head_dim;
+}
+
+cudaError_t launch_decode_any(const DecodeParams& p, cudaStream_t stream) {
+  return p.head_dim == kHeadDim ? launch_paged_decode(p, stream)
+                                : launch_paged_decode_var(p, p.head_dim, stream);
+}
+
+}  // namespace saw
+
+using saw::prepare_decode;
 
 extern "C" {
 
@@ -351,9 +361,7 @@ int32_t saw_paged_decode_int4_ex(const void* q, const void* k_cache, const void*
                                     sm_scale, out, workspace, workspace_bytes, pages_per_split,
                                     formats, dev_status);
   if (rc != SAW_OK || num_seqs == 0) return rc;
-  cudaError_t err = head_dim == kHeadDim
-                        ? saw::launch_paged_decode(p, static_cast<cudaStream_t>(stream))
-                        : saw::launch_paged_decode_var(p, head_dim, static_cast<cudaStream_t>(stream));
+  const cudaError_t err = saw::launch_decode_any(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SAW_OK : SAW_ERR_CUDA;
 }
 

@@ -107,6 +107,24 @@ inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t strea
   return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
 }
 
+// Host side of the INT4 decode entry points (saw_api.cu).  prepare_decode
+// checks every argument and fills p (split plan, CTA shape, scales) without
+// enqueueing anything; when the plan needs a workspace, `workspace` must be
+// non-null, 16-byte aligned and at least workspace_bytes long, and p's
+// workspace fields point into it.  bind_decode_workspace points them at
+// another buffer of the same layout.  launch_decode_any picks the head_dim
+// 128 kernel or the 64/256 variant.
+int32_t prepare_decode(DecodeParams& p, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t num_pages, int32_t page_size, int32_t rotate_k, int32_t rotate_v,
+                       int32_t block_h, float sm_scale, float* out, void* workspace,
+                       size_t workspace_bytes, int32_t pages_per_split, int32_t formats,
+                       int32_t* dev_status);
+void bind_decode_workspace(DecodeParams& p, void* workspace);
+cudaError_t launch_decode_any(const DecodeParams& p, cudaStream_t stream);
+
 // ---------------------------------------------------------------- prefill
 
 struct PrefillParams {

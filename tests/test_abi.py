@@ -384,3 +384,17 @@ def test_ex_step_and_prefill_stay_head_dim_128(L):
     for fmt in (saw.SAW_FMT_F16_INPUT, saw.SAW_FMT_BF16_META):
         assert _step_ex(L, fmt, d=64) == saw.SAW_ERR_UNSUPPORTED
         assert _prefill_ex(L, fmt, d=256) == saw.SAW_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [dict(q=None), dict(out=None), dict(kc=MIS), dict(mb=3),
+                                dict(h=48), dict(hq=72), dict(scale=-1.0)])
+def test_noalloc_checks_every_argument_before_touching_the_scratch(L, kw):
+    # a plan with 4 splits (pps 1 over 64 tokens) needs the shared scratch:
+    # the bad argument must be refused before the array is looked up or its
+    # counters cleared.  Without a GPU the look-up itself would fail with
+    # SAW_ERR_CUDA, so an argument error here shows that nothing ran first.
+    s, _ = saw.saw_decode_plan(2, 8, 16, 64, 1)
+    assert s > 1
+    rc = _noalloc_ex(L, 0, pps=1, **kw)
+    assert rc in (saw.SAW_ERR_INVALID_ARG, saw.SAW_ERR_UNSUPPORTED)
+    assert rc != saw.SAW_ERR_CUDA

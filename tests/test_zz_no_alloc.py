@@ -4,9 +4,12 @@ It serves callers that cannot allocate device memory -- a plugin whose host
 framework owns all allocations, code running under CUDA graph capture, or a
 loop that cannot afford cudaMalloc's synchronisation.  Its split-K scratch is
 the library's fixed 4 MiB device array instead of a caller workspace.  These
-tests call it through the C-ABI and check it against saw_paged_decode_int4
-(with a workspace) on two calls in a row, within the attention tolerance the
-other tests use.  The file is named to be collected last.
+tests call it through the C-ABI three times in a row on the same inputs (the
+array keeps the previous call's contents, so each call must clear what has
+to start at zero) and then on a second shape, and check every result against
+saw_paged_decode_int4 with a workspace, within the attention tolerance the
+other tests use, and against the oracle.  The file is named to be collected
+last.
 """
 import ctypes as C
 
@@ -17,7 +20,7 @@ import torch
 import bit_paged_kv_gb300 as saw
 from bit_paged_kv_gb300 import build as saw_build
 from bit_paged_kv_gb300 import workloads as W
-from gpu_helpers import ATTN_TOL, fill_layer, gpu_decode, rel_err
+from gpu_helpers import ATTN_TOL, fill_layer, gpu_decode, oracle_decode, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +49,7 @@ def _case(wl, lens_list):
     return q, kc, vc, bt.cuda(), lens.cuda(), npages
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls():
+def test_noalloc_matches_workspace_entry_on_repeated_calls():
     saw_build.build()
     cases = [
         (W.TINY, W.seq_lens(W.TINY).tolist(), 2),
@@ -61,11 +64,17 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         ref, st = gpu_decode(q, kc, vc, bt, lens, wl.num_kv_heads, npages, wl.page_size,
                              wl.rotate_k, wl.rotate_v, wl.block_h, pages_per_split=pps)
         assert st == 0
-        rc, got, st2 = _noalloc(wl, q, kc, vc, bt, lens, npages, pps)
-        assert rc == saw.SAW_OK and st2 == 0
-        g, r = got.cpu().numpy(), ref.cpu().numpy()
-        assert np.all(np.isfinite(g))
-        assert rel_err(g.reshape(-1, 128), r.reshape(-1, 128), "noalloc-vs-decode") <= ATTN_TOL
+        r = ref.cpu().numpy().reshape(-1, 128)
+        exact = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt.cpu(), lens.cpu(),
+                              wl.num_kv_heads, npages, wl.page_size, wl.rotate_k, wl.rotate_v,
+                              wl.block_h)
+        for call in range(3):
+            rc, got, st2 = _noalloc(wl, q, kc, vc, bt, lens, npages, pps)
+            assert rc == saw.SAW_OK and st2 == 0, f"call {call}"
+            g = got.cpu().numpy().reshape(-1, 128)
+            assert np.all(np.isfinite(g))
+            assert rel_err(g, r, "noalloc-vs-decode") <= ATTN_TOL, f"call {call}"
+            assert rel_err(g, exact, "noalloc-vs-oracle") <= ATTN_TOL, f"call {call}"
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
