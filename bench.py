@@ -1,22 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of the SAW-INT4 hot path on one GB300 (per rank).
 
-Default workload (the Qwen3-4B-shaped latency case): 36 layers, 32 q-heads,
-8 kv-heads, head_dim 128, h = 128, page 16, batch 1, context 32768, K-only
-rotation.  One step = for every layer, quantize-append the new token's K/V
-into that layer's paged INT4 cache, then decode-attend over the 32768
-cached tokens (saw_decode_step: one fused launch per layer).  The step is
-replayed as one CUDA graph.
+Headline workload (the largest single-GPU configuration, Qwen3-32B-shaped
+high concurrency): 64 layers, 64 q-heads, 8 kv-heads, head_dim 128, h = 128,
+page 16, 256 sequences with contexts uniform in [4096, 8192], shuffled page
+tables, K and V rotated.  One step = for every layer, append each sequence's
+new token into that layer's paged INT4 cache and decode-attend over its
+whole context (saw_decode_step: one fused launch per layer), replayed as one
+CUDA graph.  value = algorithmic bytes of the step / step time (GB/s).
 
-Printed (rank 0, one JSON line): KV GB/s of the whole step (algorithmic
-bytes / step time), the decode kernel's HBM roofline fraction, the
-quantize-append throughput of a 131072-token prefill chunk, the end-to-end
-rate through the public API with host buffers, and the CPU oracle's rate.
+Also printed (rank 0, one JSON line): the decode kernel's HBM roofline
+fraction, the quantize-append throughput of a 131072-token prefill chunk
+(top-level tokens/s and fraction), the Qwen3-4B-shaped latency step (batch 1,
+context 32768), decode alone on the other workloads, the end-to-end rate
+through the public API with host buffers, and the CPU oracle timed on
+bounded samples (all host cores and one core) together with its parity check
+of the GPU's outputs on those samples.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl saw|reference]
 
 --impl reference times the CPU oracle (test infrastructure) on the host
-cores on a bounded sample of the same workload: this method has no
+cores on a bounded sample of the headline workload: this method has no
 installable reference implementation.  Under torchrun each rank runs an
 independent replica (the path has no exchange step): value = bytes of all
 ranks / the slowest rank's time.
@@ -48,26 +52,42 @@ L2_BYTES = 129 * 1024 * 1024
 # ------------------------------------------------------------------ ncu traffic record
 
 DECODE_SOURCES = ["paged_decode.cu", "saw_device.cuh", "saw_internal.h", "saw_quant_row.cuh"]
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def decode_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    record (profiles/dram_traffic.txt), or None when the kernel's sources
-    have changed since that capture."""
+def decode_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
         with open(os.path.join(ROOT, "bit_paged_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
+    return h.hexdigest()
+
+
+def decode_traffic(workload: str):
+    """(DRAM bytes per launch, where the figure comes from) of the fused
+    decode-step kernel on `workload`, from the committed ncu record
+    (dram__bytes_read.sum + dram__bytes_write.sum of one capture).  The
+    figure holds only for the sources it was captured from: when the
+    kernel's sources have changed since, (None, the reason) is returned."""
+    digest = decode_sources_sha256()
+    recorded = []
     try:
-        with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as fh:
+        with open(TRAFFIC_RECORD) as fh:
             for line in fh:
                 parts = line.split()
-                if len(parts) == 4 and not line.startswith("#") and parts[2] == h.hexdigest():
-                    return int(parts[3]), "ncu capture in profiles/paged_decode_qwen3-4b-latency.md"
+                if line.startswith("#") or len(parts) != 5 or parts[1] != workload:
+                    continue
+                recorded.append(parts[3])
+                if parts[3] == digest:
+                    return int(parts[4]), (f"ncu capture of {parts[0]} on {workload} "
+                                           f"({parts[2]}), scaled per launch")
     except OSError:
-        pass
-    return None, "no ncu capture of the current kernel sources"
+        return None, "no ncu traffic record"
+    if recorded:
+        return None, (f"the decode kernel's sources (sha256 {digest[:12]}) changed since the "
+                      f"ncu capture of {workload} (sha256 {recorded[-1][:12]}): not re-measured")
+    return None, f"no ncu capture of the decode kernel on {workload}"
 
 
 # ------------------------------------------------------------------ ranks
@@ -198,8 +218,11 @@ def time_events(fn, iters: int, stream) -> list[float]:
     return [a.elapsed_time(b) for a, b in evs]
 
 
-class LatencyCase:
-    """Qwen3-4B-shaped decode step: per layer a 1-token append + decode."""
+class StepCase:
+    """A decode step over every layer of a workload: per layer, the fused
+    saw_decode_step appends each sequence's new token (position seq_len - 1)
+    and attends over its whole context (one launch per layer).  Each layer's
+    cache is prefilled with every token but the last of each sequence."""
 
     def __init__(self, wl, device):
         import bit_paged_kv_gb300 as saw
@@ -212,25 +235,30 @@ class LatencyCase:
         self.lens_d = self.lens.to(device)
         B, Hq, Hkv, D, P = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
         nb = saw.saw_cache_bytes(self.npages, P, Hkv, D)
-        self.kc = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(wl.num_layers)]
-        self.vc = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(wl.num_layers)]
+        self.pre = [int(x) - 1 for x in self.lens.tolist()]
+        self.n_pre = sum(self.pre)
+        self.pre_slots = W.prefill_slots(self.bt, self.pre, P)
+        self.kc, self.vc = [], []
         status = torch.zeros(1, dtype=torch.int32, device=device)
-        # prefill every layer's cache with all but the last token of each sequence
+        # per-step inputs: each layer's new token of every sequence (the next
+        # rows of the layer's stream after the prefill) and q
+        self.knew = torch.empty(wl.num_layers, B, Hkv, D, dtype=torch.bfloat16, device=device)
+        self.vnew = torch.empty(wl.num_layers, B, Hkv, D, dtype=torch.bfloat16, device=device)
         for layer in range(wl.num_layers):
-            pre = [int(x) - 1 for x in self.lens.tolist()]
-            k = W.kv_rows(wl, layer, W.K, sum(pre), device)
-            v = W.kv_rows(wl, layer, W.V, sum(pre), device)
-            slots = W.prefill_slots(self.bt, pre, P)
-            saw.saw_quantize_append(k, v, slots, self.kc[layer], self.vc[layer], self.npages, P,
-                                    wl.rotate_k, wl.rotate_v, wl.block_h, dev_status=status)
+            kc = torch.empty(nb, dtype=torch.uint8, device=device)
+            vc = torch.empty(nb, dtype=torch.uint8, device=device)
+            k = W.kv_rows(wl, layer, W.K, self.n_pre + B, device)
+            v = W.kv_rows(wl, layer, W.V, self.n_pre + B, device)
+            saw.saw_quantize_append(k[:self.n_pre], v[:self.n_pre], self.pre_slots, kc, vc,
+                                    self.npages, P, wl.rotate_k, wl.rotate_v, wl.block_h,
+                                    dev_status=status)
+            self.knew[layer] = k[self.n_pre:]
+            self.vnew[layer] = v[self.n_pre:]
             del k, v
-        # per-step inputs: each layer's new token (the last one of each sequence) and q
+            self.kc.append(kc)
+            self.vc.append(vc)
         self.slot = torch.cat([W.slots_for(self.bt, P, b, int(Lb) - 1, int(Lb))
                                for b, Lb in enumerate(self.lens.tolist())])
-        self.knew = torch.stack([W.kv_rows(wl, l, W.K, 1, device, token_offset=self.L - 1)
-                                 for l in range(wl.num_layers)]).expand(-1, B, -1, -1).contiguous()
-        self.vnew = torch.stack([W.kv_rows(wl, l, W.V, 1, device, token_offset=self.L - 1)
-                                 for l in range(wl.num_layers)]).expand(-1, B, -1, -1).contiguous()
         self.q = torch.stack([W.q_rows(wl, l, device) for l in range(wl.num_layers)])
         self.out = torch.empty(wl.num_layers, B, Hq, D, dtype=torch.float32, device=device)
         self.splits, self.pps = saw.saw_decode_plan(B, Hkv, P, self.L, 0)
@@ -240,22 +268,14 @@ class LatencyCase:
         torch.cuda.synchronize()
         assert int(status.item()) == 0
 
-    def append(self, layer):
-        wl = self.wl
-        self.saw.saw_quantize_append(self.knew[layer], self.vnew[layer], self.slot,
-                                     self.kc[layer], self.vc[layer], self.npages, wl.page_size,
-                                     wl.rotate_k, wl.rotate_v, wl.block_h,
-                                     dev_status=self.status)
-
-    def decode(self, layer):
-        wl = self.wl
-        self.saw.saw_paged_decode_int4(self.q[layer], self.kc[layer], self.vc[layer], self.bt,
-                                       self.lens_d, self.L, wl.num_kv_heads, self.npages,
-                                       wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
-                                       self.out[layer], self.ws, dev_status=self.status)
+    def pre_rows(self, layer):
+        """The bfloat16 K and V rows the prefill appended to `layer`."""
+        W, wl = self.W, self.wl
+        return (W.kv_rows(wl, layer, W.K, self.n_pre, self.dev),
+                W.kv_rows(wl, layer, W.V, self.n_pre, self.dev))
 
     def decode_step(self, layer):
-        """The fused step of one layer: append the new token, then attend."""
+        """The fused step of one layer: append the new tokens, then attend."""
         wl = self.wl
         self.saw.saw_decode_step(self.q[layer], self.knew[layer], self.vnew[layer],
                                  self.kc[layer], self.vc[layer], self.bt, self.lens_d, self.L,
@@ -270,17 +290,19 @@ class LatencyCase:
     def launches_per_step(self) -> int:
         return self.wl.num_layers
 
-    def step_bytes(self) -> int:
-        W, wl = self.W, self.wl
-        return wl.num_layers * (W.decode_bytes(wl, self.lens.tolist()) +
-                                W.append_bytes(wl, wl.num_seqs))
-
     def decode_bytes(self) -> int:
         return self.W.decode_bytes(self.wl, self.lens.tolist())
 
     def layer_bytes(self) -> int:
         """Algorithmic bytes of one fused decode step of one layer."""
         return self.decode_bytes() + self.W.append_bytes(self.wl, self.wl.num_seqs)
+
+    def step_bytes(self) -> int:
+        return self.wl.num_layers * self.layer_bytes()
+
+    def release(self):
+        del self.kc, self.vc, self.q, self.knew, self.vnew, self.out, self.ws
+        torch.cuda.empty_cache()
 
 
 def capture(fn, stream):
@@ -294,42 +316,11 @@ def capture(fn, stream):
     return g
 
 
-def decode_kernel_times(case, stream, reps: int):
-    """Average device time of one layer's fused decode step (one kernel),
-    from external event records captured around every layer's call inside a
-    graph of the step; falls back to graph time / layers."""
-    nl = case.wl.num_layers
-    try:
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)]
-    except TypeError:
-        evs = None
-    if evs is not None:
-        def fn():
-            s = torch.cuda.current_stream()
-            for layer in range(nl):
-                evs[layer][0].record(s)
-                case.decode_step(layer)
-                evs[layer][1].record(s)
-        try:
-            g = capture(fn, stream)
-            acc = []
-            for _ in range(reps):
-                g.replay()
-                torch.cuda.synchronize()
-                acc.extend(a.elapsed_time(b) for a, b in evs)
-            return statistics.mean(acc), "external events around each layer's call in the step graph"
-        except Exception:
-            pass
-    g = capture(case.step, stream)
-    t = time_events(g.replay, reps, stream)
-    return statistics.mean(t) / nl, "step graph time / layers (includes launch gaps)"
-
-
-def append_chunk_measure(device, stream, iters: int = 20):
+def append_chunk_measure(device, stream, iters: int = 20, keep: bool = False):
     """Quantize-append of one 131072-token prefill chunk (8 kv-heads, K and V,
     page 64), rotated (h = 128 and 64) and unrotated.  Inputs are 512 MB,
-    larger than L2."""
+    larger than L2.  keep: also return host copies of the rows, slots and
+    the h = 128 cache bytes (for the oracle's leg)."""
     import bit_paged_kv_gb300 as saw
     from bit_paged_kv_gb300 import workloads as W
     wl = W.LONG_PREFILL.variant(num_seqs=1)
@@ -353,7 +344,17 @@ def append_chunk_measure(device, stream, iters: int = 20):
                 fn()
             t = statistics.median(time_events(fn, iters, stream))
         res[name] = {"tokens_per_s": T / (t * 1e-3), "ms": t, "gbs": nbytes / (t * 1e-3) / 1e9}
-    return res, nbytes, T
+    kept = None
+    if keep:
+        # the h = 128 result, for the oracle's leg (rows, slots, cache bytes)
+        saw.saw_quantize_append(k, v, slots, kc, vc, npages, wl.page_size, True, True, 128)
+        torch.cuda.synchronize()
+        kept = {"wl": wl, "k": np_bits(k).reshape(T, -1), "v": np_bits(v).reshape(T, -1),
+                "slots": slots.cpu().numpy(), "npages": npages,
+                "kc_gpu": kc.cpu().numpy(), "vc_gpu": vc.cpu().numpy()}
+    del k, v, kc, vc
+    torch.cuda.empty_cache()
+    return res, nbytes, T, kept
 
 
 def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18,
@@ -383,13 +384,16 @@ def fill_caches(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18,
     return kc, vc
 
 
-def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=None):
+def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=None, keep=None):
     """Decode-only throughput of the bandwidth-bound workloads (Qwen3-8B
     concurrent, Qwen3-32B high concurrency in its three rotation variants,
     long context at h 128 and 64): `layers` distinct layer caches (each
-    larger than L2) decoded in turn, CUDA events around reps passes."""
+    larger than L2) decoded in turn, CUDA events around reps passes.  keep:
+    names whose first layer (cache, q, output) is copied to the host for the
+    oracle's leg; returned as a third item."""
     import bit_paged_kv_gb300 as saw
     from bit_paged_kv_gb300 import workloads as W
+    kept = {}
     c32 = W.QWEN3_32B_HIGH_CONCURRENCY
     cases = [("qwen3-8b-concurrent", W.QWEN3_8B_CONCURRENT),
              ("qwen3-32b-high-concurrency k+v", c32),
@@ -424,6 +428,16 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=
                 one_pass()
             t = statistics.median(time_events(one_pass, reps, stream)) / layers
         assert int(status.item()) == 0
+        if keep and name in keep:
+            saw.saw_paged_decode_int4(qs[0], caches[0][0], caches[0][1], btd, lensd, Lmax,
+                                      wl.num_kv_heads, npages, wl.page_size, wl.rotate_k,
+                                      wl.rotate_v, wl.block_h, out, ws, dev_status=status)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            kept[name] = {"wl": wl, "kc": caches[0][0].cpu().numpy(),
+                          "vc": caches[0][1].cpu().numpy(), "q": np_bits(qs[0]),
+                          "out": out.cpu().numpy(), "bt": bt.numpy(), "lens": lens.numpy(),
+                          "npages": npages}
         nbytes = W.decode_bytes(wl, lens.tolist())
         splits, pps = saw.saw_decode_plan(B, wl.num_kv_heads, wl.page_size, Lmax, 0)
         res[name] = {"ms_per_layer": t, "gbs": nbytes / (t * 1e-3) / 1e9,
@@ -432,12 +446,12 @@ def decode_config_measure(device, stream, layers: int = 2, reps: int = 10, only=
         del caches, qs, ws, out
         torch.cuda.empty_cache()
     if only is not None:
-        return res, None
+        return res, None, kept
     a = res["qwen3-32b-high-concurrency k+v"]["ms_per_layer"]
     k1 = res["qwen3-32b-high-concurrency k-only"]["ms_per_layer"]
     u = res["qwen3-32b-high-concurrency unrotated"]["ms_per_layer"]
     overhead = {"k+v_vs_unrotated": a / u - 1.0, "k-only_vs_unrotated": k1 / u - 1.0}
-    return res, overhead
+    return res, overhead, kept
 
 
 def fill_caches_bf16(wl, layer, lens, bt, npages, device, chunk_tokens=1 << 18):
@@ -724,98 +738,188 @@ def formats_measure(device, stream, reps: int = 10):
     return res
 
 
-def cpu_oracle_decode_sample(case, layers, threads, min_seconds=10.0, max_passes=40):
-    """Time the oracle (as it stands) on the step's work for `layers`:
-    append the new token, then decode every q-head over the layer's pages;
-    whole passes over the layers are repeated until min_seconds have gone."""
+def np_bits(t):
+    """bfloat16 / float16 tensor -> numpy uint16 bit patterns on the host."""
     import numpy as np
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
-    import oracle
-    wl = case.wl
 
-    def bits(t):
-        return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+def sample_decode_bytes(wl, lens, seqs, kv_heads_per_seq: int, pairs: int, appended: bool) -> int:
+    """Algorithmic bytes of an oracle decode sample: K and V codes and
+    (scale, zero) of every attended (token, kv-head), the sequences' block
+    tables, q in and out for each (sequence, q-head) pair, and the appended
+    token's rows when the sample includes the step's append."""
+    from bit_paged_kv_gb300 import workloads as W
+    P, D = wl.page_size, wl.head_dim
+    per_row = D // 2 + 4
+    n = 0
+    for b in seqs:
+        L = int(lens[b])
+        n += 2 * per_row * L * kv_heads_per_seq + 4 * ((L + P - 1) // P)
+    n += pairs * D * (2 + 4)
+    if appended:
+        n += len(seqs) * W.append_bytes(wl.variant(num_kv_heads=kv_heads_per_seq), 1)
+    return n
 
-    hosts = []
-    for layer in layers:
-        hosts.append((case.kc[layer].cpu().numpy(), case.vc[layer].cpu().numpy(),
-                      bits(case.knew[layer]).reshape(wl.num_seqs, -1),
-                      bits(case.vnew[layer]).reshape(wl.num_seqs, -1), bits(case.q[layer])))
-    slots = case.slot.cpu().numpy()
-    bt = case.bt_cpu.numpy()
-    lens = case.lens.numpy()
-    passes = 0
-    t0 = time.perf_counter()
-    while True:  # whole passes over the layers until min_seconds (re-appending is idempotent)
-        for kc, vc, kn, vn, q in hosts:
-            oracle.quantize_append(kn, vn, slots, wl.num_kv_heads, wl.head_dim, kc, vc,
-                                   case.npages, wl.page_size, wl.rotate_k, wl.rotate_v,
-                                   wl.block_h)
-            oracle.decode(q, kc, vc, bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                          case.npages, wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
-                          threads=threads)
+
+def timed_passes(fn, min_seconds: float, max_passes: int):
+    """Call fn() until min_seconds have gone (at least once); (seconds, passes)."""
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        fn()
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_seconds or passes >= max_passes:
-            break
-    nbytes = passes * len(layers) * (case.W.decode_bytes(wl, case.lens.tolist()) +
-                                     case.W.append_bytes(wl, wl.num_seqs))
-    return nbytes / dt / 1e9, dt, passes
+            return dt, passes
+
+
+def rel_max_err(got, ref) -> float:
+    import numpy as np
+    scale = float(np.max(np.abs(ref)))
+    d = float(np.max(np.abs(got - ref)))
+    return d / scale if scale > 0 else d
+
+
+def cpu_oracle_legs(samples, threads: int, min_seconds: float = 1.5):
+    """The oracle (as it stands), timed on the host cores on bounded samples
+    of the GPU workloads, at all cores and at one core; while it runs, its
+    results are compared with the GPU's outputs of the same inputs.
+
+    samples: host copies of what the GPU computed (see run_saw).  Returns
+    (legs, parity): legs[name] = {value, unit, cores, sample}; parity[name]
+    = the comparison of that sample with the GPU (cache bytes equal, attention
+    max |o_gpu - o_ref| / max |o_ref| against 2e-3)."""
+    import numpy as np
+
+    import oracle
+    oracle.load()
+    legs, parity = {}, {}
+
+    # quantize-append: the long-context prefill chunk, R-canon butterfly
+    a = samples["append"]
+    wl = a["wl"]
+    T = a["k"].shape[0]
+    for cores, n in ((threads, T), (1, min(T, 8192))):
+        kc = np.zeros_like(a["kc_gpu"])
+        vc = np.zeros_like(a["vc_gpu"])
+
+        def run(n=n, kc=kc, vc=vc, cores=cores):
+            oracle.quantize_append(a["k"][:n], a["v"][:n], a["slots"][:n], wl.num_kv_heads,
+                                   wl.head_dim, kc, vc, a["npages"], wl.page_size, wl.rotate_k,
+                                   wl.rotate_v, wl.block_h, threads=cores)
+        dt, passes = timed_passes(run, min_seconds, 20)
+        legs[f"append cores={cores}"] = {
+            "value": n * passes / dt, "unit": "tokens/s", "cores": cores,
+            "sample": f"{n} tokens of the {T}-token chunk (Hkv {wl.num_kv_heads}, K and V, "
+                      f"h {wl.block_h}), {passes} pass(es), {dt:.1f} s"}
+        if n == T:
+            parity["append long-131072 chunk"] = {
+                "bytes_equal": bool(np.array_equal(kc, a["kc_gpu"]) and
+                                    np.array_equal(vc, a["vc_gpu"])),
+                "what": f"every cache byte of the {T}-token chunk"}
+
+    # decode legs: the fused step's layer (configs 2 and 4), decode alone (config 5)
+    for name, d in samples["decode"].items():
+        wl = d["wl"]
+        G = wl.num_q_heads // wl.num_kv_heads
+        kc, vc = d["kc"], d["vc"]
+        if d.get("new") is not None:
+            # the step appended each sequence's new token: the oracle appends
+            # the same rows into a copy of the GPU's cache; identical bytes
+            # mean the GPU wrote exactly the oracle's codes and (scale, zero)
+            kn, vn, sl = d["new"]
+            kr, vr = kc.copy(), vc.copy()
+            oracle.quantize_append(kn, vn, sl, wl.num_kv_heads, wl.head_dim, kr, vr, d["npages"],
+                                   wl.page_size, wl.rotate_k, wl.rotate_v, wl.block_h,
+                                   threads=threads)
+            if d.get("pre") is not None:
+                # and the whole layer from scratch: prefill rows, then the new tokens
+                kp, vp, sp = d["pre"]
+                kr, vr = np.zeros_like(kc), np.zeros_like(vc)
+                oracle.quantize_append(kp, vp, sp, wl.num_kv_heads, wl.head_dim, kr, vr,
+                                       d["npages"], wl.page_size, wl.rotate_k, wl.rotate_v,
+                                       wl.block_h, threads=threads)
+                oracle.quantize_append(kn, vn, sl, wl.num_kv_heads, wl.head_dim, kr, vr,
+                                       d["npages"], wl.page_size, wl.rotate_k, wl.rotate_v,
+                                       wl.block_h, threads=threads)
+            eq = bool(np.array_equal(kr, kc) and np.array_equal(vr, vc))
+            del kr, vr
+        else:
+            eq = None
+        for cores, seqs, heads in ((threads, d["seqs_all"], range(wl.num_q_heads)),
+                                   (1, d["seqs_one"], range(d.get("heads_one", wl.num_q_heads)))):
+            pairs = [(b, h) for b in seqs for h in heads]
+            ref = {}
+
+            def run(pairs=pairs, cores=cores, ref=ref):
+                ref["o"] = oracle.decode(d["q"], kc, vc, d["bt"], d["lens"], wl.num_q_heads,
+                                         wl.num_kv_heads, wl.head_dim, d["npages"], wl.page_size,
+                                         wl.rotate_k, wl.rotate_v, wl.block_h, pairs=pairs,
+                                         threads=cores)
+            dt, passes = timed_passes(run, min_seconds, 50)
+            kvh = len({h // G for h in heads})
+            nbytes = sample_decode_bytes(wl, d["lens"], seqs, kvh, len(pairs),
+                                         appended=d.get("new") is not None)
+            legs[f"{name} cores={cores}"] = {
+                "value": nbytes * passes / dt / 1e9, "unit": "GB/s", "cores": cores,
+                "sample": f"one layer, {len(seqs)} sequence(s) x {len(list(heads))} q-head(s) "
+                          f"({len(pairs)} rows, fp64), {passes} pass(es), {dt:.1f} s"}
+            if cores == threads:
+                got = d["out"][[b for b, _ in pairs], [h for _, h in pairs]]
+                err = rel_max_err(got, ref["o"])
+                parity[name] = {"cache_bytes_equal": eq, "attn_rel_err": err, "tol": 2e-3,
+                                "finite": bool(np.all(np.isfinite(got))),
+                                "ok": bool(err <= 2e-3 and eq is not False and
+                                           np.all(np.isfinite(got))),
+                                "what": f"{len(pairs)} rows of one layer's output" +
+                                        (", and the cache bytes after the step's append"
+                                         if eq is not None else "")}
+    return legs, parity
 
 
 # ------------------------------------------------------------------ arms
 
-def run_saw(args):
-    rank, world, local = dist_env()
-    init_group(world)
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    import __graft_entry__
-    __graft_entry__.build()
-    from bit_paged_kv_gb300 import workloads as W
+HEADLINE_WORKLOAD = ("qwen3-32b-high-concurrency: 64 layers, Hq 64, Hkv 8 (GQA 8), head_dim 128, "
+                     "h 128, page 16, 256 sequences, context uniform in [4096, 8192], shuffled "
+                     "page tables, K and V rotated; step = per layer, append each sequence's new "
+                     "token and attend over its whole context (saw_decode_step, one launch per "
+                     "layer)")
 
-    wl = W.QWEN3_4B_LATENCY
-    case = LatencyCase(wl, device)
-    stream = torch.cuda.Stream(device)
+
+def headline_config(world: int) -> dict:
+    """The `config` object of both arms (the same workload and metric)."""
+    step_bytes = StepBytes.headline()
+    return {"workload": HEADLINE_WORKLOAD,
+            "l2": f"inputs larger than L2: 64 distinct layer caches of 1.71 GB, "
+                  f"{step_bytes / 1e9:.1f} GB read per step",
+            "parallelism": f"replicas x{world}"}
+
+
+def graph_step_timing(case, stream, steps: int, warmup: int, sampler=None):
+    """CUDA-graph the step, warm it up, and time `steps` replays with CUDA
+    events on the launching stream (synchronised on both sides)."""
     graph = capture(case.step, stream)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler.mark(True)
+    if sampler is not None:
+        sampler.mark(True)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             graph.replay()
         end.record(stream)
     torch.cuda.synchronize()
-    sampler.mark(False)
-    clocks = sampler.stop()
-    barrier(world)
-    elapsed = start.elapsed_time(end) * 1e-3
-    step_bytes = case.step_bytes()
-    t_max, bytes_all = reduce_over_ranks(elapsed, step_bytes * args.steps, world)
-    value = bytes_all / t_max / 1e9
-    status = int(case.status.item())
+    if sampler is not None:
+        sampler.mark(False)
+    return graph, start.elapsed_time(end) * 1e-3
 
-    # dominant (and only) kernel: one fused decode step per layer.  Its
-    # average launch duration is the timed region's device time over the
-    # launches in it; launches overlap slightly (programmatic dependent
-    # launch), so this is what a launch costs in the step.
-    dec_ms = elapsed * 1e3 / (args.steps * case.launches_per_step())
-    dec_how = ("CUDA events around the timed region on the launching stream / "
-               f"{case.launches_per_step()} launches per step")
-    iso_ms, iso_how = decode_kernel_times(case, stream, reps=max(20, min(200, args.steps // 10)))
-    peak, peak_src = read_peaks()
-    achieved = case.layer_bytes() / (dec_ms * 1e-3) / 1e9
-    traffic, traffic_src = decode_traffic()
 
-    # end to end through the public API with host buffers
+def e2e_measure(case, graph, stream, iters: int, world: int):
+    """The same step end to end through the public API: every step copies
+    the step's inputs (q, new K and V rows of every layer) in from pinned host
+    memory, replays the step and copies the attention output back."""
     q_h = case.q.cpu().pin_memory()
     k_h = case.knew.cpu().pin_memory()
     v_h = case.vnew.cpu().pin_memory()
@@ -828,40 +932,151 @@ def run_saw(args):
         graph.replay()
         o_h.copy_(case.out, non_blocking=True)
 
-    e2e_iters = max(10, args.steps // 4)
     with torch.cuda.stream(stream):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s2.record(stream)
-        for _ in range(e2e_iters):
+        for _ in range(iters):
             e2e_step()
         e2.record(stream)
     torch.cuda.synchronize()
-    t_e2e, bytes_e2e = reduce_over_ranks(s2.elapsed_time(e2) * 1e-3, step_bytes * e2e_iters, world)
-    h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
+    t, nbytes = reduce_over_ranks(s2.elapsed_time(e2) * 1e-3, case.step_bytes() * iters, world)
+    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2
     d2h = o_h.numel() * 4
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": t / iters * 1e3,
+            "how": "pinned host q and new K/V rows of every layer copied in, graph step, "
+                   "attention output of every layer copied out, every step"}
 
-    # quantize-append of a 131072-token prefill chunk
-    app, app_bytes, app_T = append_chunk_measure(device, stream)
-    # decode alone on the bandwidth-bound workloads
-    dec_cfg, dec_rot = (None, None) if args.no_decode_configs else decode_config_measure(device, stream)
+
+def step_sample_for_oracle(case, layer: int, seqs_all, seqs_one, heads_one=None,
+                           with_prefill=False) -> dict:
+    """Host copies of one layer of a fused step (after the step ran): cache
+    bytes, q, the appended rows and slots, the output; optionally the
+    prefill rows, so that the oracle can rebuild the whole layer."""
+    wl = case.wl
+    B = wl.num_seqs
+    d = {"wl": wl, "kc": case.kc[layer].cpu().numpy(), "vc": case.vc[layer].cpu().numpy(),
+         "q": np_bits(case.q[layer]), "out": case.out[layer].cpu().numpy(),
+         "bt": case.bt_cpu.numpy(), "lens": case.lens.numpy(), "npages": case.npages,
+         "new": (np_bits(case.knew[layer]).reshape(B, -1), np_bits(case.vnew[layer]).reshape(B, -1),
+                 case.slot.cpu().numpy()),
+         "seqs_all": list(seqs_all), "seqs_one": list(seqs_one)}
+    if heads_one is not None:
+        d["heads_one"] = heads_one
+    if with_prefill:
+        k, v = case.pre_rows(layer)
+        d["pre"] = (np_bits(k).reshape(case.n_pre, -1), np_bits(v).reshape(case.n_pre, -1),
+                    case.pre_slots.cpu().numpy())
+        del k, v
+    return d
+
+
+def run_saw(args):
+    rank, world, local = dist_env()
+    init_group(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_paged_kv_gb300 import workloads as W
+
+    peak, peak_src = read_peaks()
+    stream = torch.cuda.Stream(device)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    samples = {"decode": {}}
+
+    # ---- headline: the config-4 decode step over all 64 layers
+    wl = W.QWEN3_32B_HIGH_CONCURRENCY
+    t_fill = time.perf_counter()
+    case = StepCase(wl, device)
+    fill_s = time.perf_counter() - t_fill
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    graph, elapsed = graph_step_timing(case, stream, args.steps, args.warmup, sampler)
+    clocks = sampler.stop()
+    barrier(world)
+    step_bytes = case.step_bytes()
+    t_max, bytes_all = reduce_over_ranks(elapsed, step_bytes * args.steps, world)
+    value = bytes_all / t_max / 1e9
+    status = int(case.status.item())
+    launches = case.launches_per_step() * args.steps
+    dec_ms = elapsed * 1e3 / launches
+    achieved = case.layer_bytes() / (dec_ms * 1e-3) / 1e9
+    traffic, traffic_src = decode_traffic(wl.name)
+    e2e = e2e_measure(case, graph, stream, max(3, args.steps // 4), world)
+    head_plan = {"splits": case.splits, "pages_per_split": case.pps}
+    if want_cpu:
+        last = wl.num_layers - 1
+        samples["decode"]["qwen3-32b-high-concurrency step"] = step_sample_for_oracle(
+            case, last, seqs_all=range(0, wl.num_seqs, 2), seqs_one=[0, 1])
+    del graph
+    case.release()
+    del case
+
+    # ---- the Qwen3-4B-shaped latency step (batch 1, context 32768, 36 layers)
+    lw = W.QWEN3_4B_LATENCY
+    lat = StepCase(lw, device)
+    lat_steps = max(50, 10 * args.steps)
+    lgraph, lt = graph_step_timing(lat, stream, lat_steps, max(args.warmup, 5))
+    lat_ms = lt * 1e3 / (lat_steps * lat.launches_per_step())
+    lat_traffic, lat_traffic_src = decode_traffic(lw.name)
+    latency = {
+        "workload": "qwen3-4b-latency: 36 layers, Hq 32, Hkv 8, head_dim 128, h 128, page 16, "
+                    "batch 1, context 32768, K-only rotation; step = per layer 1-token "
+                    "quantize-append + paged decode (saw_decode_step), one CUDA graph per step",
+        "value": lat.step_bytes() * lat_steps / lt / 1e9, "unit": "GB/s",
+        "ms_per_step": lt * 1e3 / lat_steps, "steps": lat_steps,
+        "decode_plan": {"splits": lat.splits, "pages_per_split": lat.pps},
+        "roofline": {"bound": "hbm", "achieved": lat.layer_bytes() / (lat_ms * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s",
+                     "frac": lat.layer_bytes() / (lat_ms * 1e-3) / 1e9 / peak,
+                     "traffic": lat_traffic, "traffic_source": lat_traffic_src,
+                     "bytes_per_launch": lat.layer_bytes(), "ms_per_launch": lat_ms},
+        "e2e": e2e_measure(lat, lgraph, stream, max(10, lat_steps // 4), world),
+        "device_status": int(lat.status.item()),
+    }
+    if want_cpu:
+        samples["decode"]["qwen3-4b-latency step"] = step_sample_for_oracle(
+            lat, lw.num_layers - 1, seqs_all=[0], seqs_one=[0], heads_one=lw.group,
+            with_prefill=True)
+    del lgraph
+    lat.release()
+    del lat
+
+    # ---- quantize-append of a 131072-token prefill chunk
+    app, app_bytes, app_T, app_keep = append_chunk_measure(device, stream, keep=want_cpu)
+    samples["append"] = app_keep
+    # ---- decode alone on the bandwidth-bound workloads, and the other rows
+    dec_cfg = dec_rot = None
+    if not args.no_decode_configs:
+        dec_cfg, dec_rot, kept = decode_config_measure(device, stream,
+                                                       keep={"long-131072 h128"} if want_cpu else None)
+        if want_cpu:
+            k5 = kept["long-131072 h128"]
+            k5.update(seqs_all=list(range(k5["wl"].num_seqs)), seqs_one=[0],
+                      heads_one=k5["wl"].group)
+            samples["decode"]["long-131072 h128"] = k5
     sweep = None if args.no_decode_configs else concurrency_sweep(device, stream)
     pre = None if args.no_decode_configs else prefill_measure(device, stream)
     var = None if args.no_decode_configs else variants_measure(device, stream)
     fmtv = None if args.no_decode_configs else formats_measure(device, stream)
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    cpu = parity = None
+    if want_cpu:
         import oracle
         threads = oracle.host_threads()
-        layers = list(range(min(args.cpu_layers, wl.num_layers)))
-        gbs, dt, passes = cpu_oracle_decode_sample(case, layers, threads)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{passes} pass(es) over {len(layers)} of the 36 layers of the step "
-                         f"(1-token append + fp64 decode of all 32 q-heads over 32768 tokens), "
-                         f"{dt:.1f} s wall"}
+        legs, parity = cpu_oracle_legs(samples, threads)
+        head = legs["qwen3-32b-high-concurrency step cores=%d" % threads]
+        cpu = {"value": head["value"], "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "fp64 decode of " + head["sample"] + " of the config-4 step (its "
+                         "appended tokens included); the other legs below",
+               "legs": legs}
+    del samples
 
     if rank != 0:
         return
@@ -878,33 +1093,28 @@ def run_saw(args):
         "vs_baseline": None,
         "dtype": "int4 KV (bf16 in, f32 rotation/softmax, f16 MMA f32 accumulate)",
         "data": "synthetic",
-        "config": {
-            "workload": "qwen3-4b-latency: 36 layers, Hq 32, Hkv 8, head_dim 128, h 128, page 16, "
-                        "batch 1, context 32768, K-only rotation; step = per layer 1-token "
-                        "quantize-append + paged decode (saw_decode_step, one launch per layer)",
-            "l2": f"inputs larger than L2: 36 distinct layer caches, "
-                  f"{step_bytes / 1e9:.2f} GB read per step",
-            "execution": "one CUDA graph per step",
-            "decode_plan": {"splits": case.splits, "pages_per_split": case.pps},
-            "parallelism": f"replicas x{world}",
-        },
+        "config": headline_config(world),
+        "execution": "one CUDA graph per step (64 launches)",
+        "decode_plan": head_plan,
+        "fill_s": fill_s,
         "roofline": {
             "bound": "hbm",
-            "kernel": "saw_decode_step: paged_decode_kernel<16, packed, append> (1 token "
-                      "appended, 32768 attended, merge in the last split)",
+            "kernel": "saw_decode_step: paged_decode_kernel<16, wide (GQA 8), append> "
+                      "(256 new tokens appended, 1.57e6 cached tokens attended per layer)",
             "achieved": achieved,
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
             "traffic_source": traffic_src,
-            "bytes_per_launch": case.layer_bytes(),
+            "bytes_per_launch": case_layer_bytes(wl),
             "ms_per_launch": dec_ms,
-            "timing": dec_how,
-            "ms_per_launch_bracketed": iso_ms,
-            "bracketed_timing": iso_how + " (events between launches stop their overlap)",
+            "timing": "CUDA events around the timed region on the launching stream / "
+                      f"{launches} launches",
             "peak_source": peak_src,
         },
+        "quantize_append_tokens_per_s": app["rotated_h128"]["tokens_per_s"],
+        "quantize_append_frac": app["rotated_h128"]["gbs"] / peak,
         "quantize_append": {
             "workload": "131072-token prefill chunk, Hkv 8, head_dim 128, K and V, page 64",
             "tokens_per_s": app["rotated_h128"]["tokens_per_s"],
@@ -914,6 +1124,7 @@ def run_saw(args):
             "variants": app,
             "rotation_overhead": app["rotated_h128"]["ms"] / app["unrotated"]["ms"] - 1.0,
         },
+        "latency_step": latency,
         "decode_configs": None if dec_cfg is None else {
             "what": "saw_paged_decode_int4 alone, automatic split plan, distinct layer caches "
                     "decoded in turn (each larger than L2); GB/s = algorithmic bytes / time",
@@ -937,9 +1148,8 @@ def run_saw(args):
             "results": pre[0],
         },
         "head_dim_variants": None if var is None else {
-            "what": "head_dim 64 and 256 (CUDA-core decode kernel, warp-per-row append), "
-                    "h = head_dim; decode on the qwen3-8b-concurrent shape, append on a "
-                    "131072-token chunk; GB/s = algorithmic bytes / time",
+            "what": "head_dim 64 and 256, h = head_dim; decode on the qwen3-8b-concurrent "
+                    "shape, append on a 131072-token chunk; GB/s = algorithmic bytes / time",
             "peak": peak,
             "results": {k: dict(v, frac=v["gbs"] / peak) for k, v in var.items()},
         },
@@ -952,19 +1162,28 @@ def run_saw(args):
             "results": {k: dict(v, decode_frac=v["decode_gbs"] / peak,
                                 append_frac=v["append_gbs"] / peak) for k, v in fmtv.items()},
         },
-        "e2e": {"value": bytes_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "how": "pinned host q/k/v copied in, graph step, output copied out, every step"},
+        "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": case.launches_per_step() * args.steps,
+        "parity": parity,
+        "gpu_launches": launches,
         "clocks": clocks,
         "device_status": status,
     }
     print(json.dumps(line))
 
 
+def case_layer_bytes(wl) -> int:
+    from bit_paged_kv_gb300 import workloads as W
+    lens = W.seq_lens(wl)
+    return W.decode_bytes(wl, lens.tolist()) + W.append_bytes(wl, wl.num_seqs)
+
+
 def run_reference(args):
-    """The CPU oracle on a bounded sample of the same workload per step."""
+    """The CPU oracle (test infrastructure, as it stands) on a bounded sample
+    of the headline workload per step, on the same host cores the GPU arm's
+    cpu_baseline uses.  Step k: the fused step of layer 0 for sequence k mod 4
+    of the Qwen3-32B-shaped workload -- append its new token (8 kv-heads, K and
+    V), then fp64 decode of its 64 q-heads over its whole context."""
     rank, world, local = dist_env()
     if rank != 0:
         return
@@ -973,67 +1192,78 @@ def run_reference(args):
     import oracle
     from bit_paged_kv_gb300 import workloads as W
     oracle.load()
-    wl = W.QWEN3_4B_LATENCY
-    lens = W.seq_lens(wl)
-    L = int(lens[0])
+    wl = W.QWEN3_32B_HIGH_CONCURRENCY
+    P, Hkv, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_q_heads
+    nseq = 4
+    lens = W.seq_lens(wl)[:nseq]
     bt, npages = W.page_tables(wl, lens)
-    P, Hkv, D, G = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.group
+    threads = oracle.host_threads()
 
     def bits(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
-    # sample: layer 0, kv-head 0 and its G q-heads, full 32768-token context
-    k = W.kv_rows(wl, 0, W.K, L, "cpu")
-    v = W.kv_rows(wl, 0, W.V, L, "cpu")
-    slots = W.prefill_slots(bt, [L], P).numpy()
+    # prefill every token but each sequence's last, the rows drawn on the host
+    pre = [int(x) - 1 for x in lens.tolist()]
+    n_pre = sum(pre)
+    k = bits(W.kv_rows(wl, 0, W.K, n_pre + nseq, "cpu")).reshape(n_pre + nseq, -1)
+    v = bits(W.kv_rows(wl, 0, W.V, n_pre + nseq, "cpu")).reshape(n_pre + nseq, -1)
+    slots = W.prefill_slots(bt, pre, P).numpy()
+    new_slots = np.array([int(bt[b, (int(L) - 1) // P]) * P + (int(L) - 1) % P
+                          for b, L in enumerate(lens.tolist())], dtype=np.int32)
     nb = oracle.cache_bytes(npages, P, Hkv, D)
     kc, vc = np.zeros(nb, np.uint8), np.zeros(nb, np.uint8)
-    kb, vb = bits(k).reshape(L, -1), bits(v).reshape(L, -1)
-    threads = oracle.host_threads()
-    oracle.quantize_append(kb[:-1], vb[:-1], slots[:-1], Hkv, D, kc, vc, npages, P, wl.rotate_k,
+    oracle.quantize_append(k[:n_pre], v[:n_pre], slots, Hkv, D, kc, vc, npages, P, wl.rotate_k,
                            wl.rotate_v, wl.block_h, threads=threads)
-    q = bits(W.q_rows(wl, 0, "cpu"))
-    pairs = [(0, h) for h in range(G)]
+    q = bits(W.q_rows(wl, 0, "cpu", num_seqs=nseq))
+    btn, lensn = bt.numpy(), lens.numpy()
 
-    def step():
-        oracle.quantize_append(kb[-1:], vb[-1:], slots[-1:], Hkv, D, kc, vc, npages, P,
-                               wl.rotate_k, wl.rotate_v, wl.block_h)
-        oracle.decode(q, kc, vc, bt.numpy(), lens.numpy(), wl.num_q_heads, Hkv, D, npages, P,
-                      wl.rotate_k, wl.rotate_v, wl.block_h, pairs=pairs, threads=min(threads, G))
+    def step(i):
+        b = i % nseq
+        oracle.quantize_append(k[n_pre + b:n_pre + b + 1], v[n_pre + b:n_pre + b + 1],
+                               new_slots[b:b + 1], Hkv, D, kc, vc, npages, P, wl.rotate_k,
+                               wl.rotate_v, wl.block_h)
+        oracle.decode(q, kc, vc, btn, lensn, Hq, Hkv, D, npages, P, wl.rotate_k, wl.rotate_v,
+                      wl.block_h, pairs=[(b, h) for h in range(Hq)], threads=threads)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i)
     dt = time.perf_counter() - t0
-    per_row = D // 2 + 4
-    # algorithmic bytes of the sample: one kv-head's K and V rows over the
-    # context, its block-table entries, G q rows in and out, one appended token
-    sample_bytes = (2 * per_row * L + 4 * -(-L // P) + G * D * (2 + 4)
-                    + W.append_bytes(wl, 1))
-    value = sample_bytes * args.steps / dt / 1e9
-    cores = min(threads, G)
+    nbytes = sum(sample_decode_bytes(wl, lensn, [i % nseq], Hkv, Hq, appended=True)
+                 for i in range(args.steps))
+    value = nbytes / dt / 1e9
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantizer",
         "data": "synthetic",
-        "config": {"workload": "qwen3-4b-latency (same as the GPU arm)",
-                   "parallelism": "host threads"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step: layer 0, kv-head 0 with its {G} q-heads over "
-                                   f"{L} tokens (1-token append + fp64 decode)"},
+        "config": headline_config(world),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: layer 0, one of the first {nseq} sequences "
+                                   f"(cycled): append its new token (Hkv {Hkv}, K and V) and "
+                                   f"fp64 decode of its {Hq} q-heads over its context"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
 
 
+class StepBytes:
+    @staticmethod
+    def headline() -> int:
+        from bit_paged_kv_gb300 import workloads as W
+        wl = W.QWEN3_32B_HIGH_CONCURRENCY
+        return wl.num_layers * case_layer_bytes(wl)
+
+
 def run_profile(args):
     """Small, fixed loops for ncu captures (no timing, no JSON):
-    decode: the latency case's decode over --profile-layers layer caches
+    decode: the latency case's fused step over --profile-layers layer caches
     (35.7 MB each, more than L2 in total), three passes;
+    step4: the same on the Qwen3-32B-shaped workload (1.71 GB per layer;
+    use --profile-layers 2), three passes;
     append: three quantize-appends of the 131072-token chunk;
     bf16: three BF16-cache decodes of 16 qwen3-8b-concurrent sequences
     (about 600 MB of cache, more than L2);
@@ -1043,9 +1273,12 @@ def run_profile(args):
     import __graft_entry__
     __graft_entry__.build()
     from bit_paged_kv_gb300 import workloads as W
-    if args.profile == "decode":
-        wl = W.QWEN3_4B_LATENCY.variant(num_layers=args.profile_layers)
-        case = LatencyCase(wl, device)
+    if args.profile in ("decode", "step4"):
+        if args.profile == "decode":
+            wl = W.QWEN3_4B_LATENCY.variant(num_layers=args.profile_layers)
+        else:
+            wl = W.QWEN3_32B_HIGH_CONCURRENCY.variant(num_layers=args.profile_layers)
+        case = StepCase(wl, device)
         for _ in range(3):
             for layer in range(wl.num_layers):
                 case.decode_step(layer)
@@ -1117,14 +1350,14 @@ def run_profile(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["saw", "reference"], default="saw")
-    ap.add_argument("--cpu-layers", type=int, default=36)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-configs", action="store_true",
                     help="skip the decode-only measurements of the other workloads")
-    ap.add_argument("--profile", choices=["decode", "append", "bf16", "prefill", "variant"],
+    ap.add_argument("--profile", choices=["decode", "step4", "append", "bf16", "prefill",
+                                          "variant"],
                     default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)
