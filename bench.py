@@ -80,8 +80,8 @@ def decode_traffic(workload: str):
                     continue
                 recorded.append(parts[3])
                 if parts[3] == digest:
-                    return int(parts[4]), (f"ncu capture of {parts[0]} on {workload} "
-                                           f"({parts[2]}), scaled per launch")
+                    return int(parts[4]), (f"ncu capture of one launch of {parts[0]} on "
+                                           f"{workload} ({parts[2]})")
     except OSError:
         return None, "no ncu traffic record"
     if recorded:
