@@ -602,7 +602,8 @@ def prefill_measure(device, stream, reps: int = 5):
 
 
 def variants_measure(device, stream, reps: int = 10):
-    """head_dim 64 and 256 (variant kernels): decode alone on the
+    """head_dim 64 and 256: decode alone (the tensor-core decode built for
+    those sizes) on the
     qwen3-8b-concurrent shape (64 sequences, lengths in [2048, 16384], K and V
     rotated with h = head_dim, two layer caches decoded in turn), and the
     quantize-append of a 131072-token chunk (Hkv 8, K and V, page 64)."""

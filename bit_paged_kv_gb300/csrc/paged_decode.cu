@@ -11,7 +11,8 @@
 // Design (sm_103a):
 //  * One CTA per (split of the context, kv-head, sequence): 16 warps, one
 //    CTA per SM, or 8 warps, two CTAs per SM (this file is compiled once per
-//    shape; the host plan picks one).  The whole GQA group of the kv-head is
+//    shape, and once more per shape for head_dim 64 and 256; the host plan
+//    picks the shape).  The whole GQA group of the kv-head is
 //    served by the CTA, so each page is read from HBM once, and q is rotated
 //    once per CTA.
 //  * The split is cut into 16-token tiles; warp w of W takes tiles w, w+W, ...
@@ -53,61 +54,75 @@ constexpr int kCtasPerSm = kWarps == 16 ? 1 : 2;      // 128 registers per threa
 static_assert(kWarps == 16 || kWarps == 8, "decode CTAs have 16 or 8 warps");
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kRedStride = kHeadDim + 8;  // padded row of the cross-warp reduction
 // dim d of a reduction row sits at d + d / 16: the stores (lane group g
-// writes dims 16g + ..) and the per-dim reads are then free of bank conflicts
+// writes dims (D/8) g + ..) and the per-dim reads are then free of bank
+// conflicts
 __device__ __forceinline__ int red_col(int d) { return d + (d >> 4); }
 constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
 constexpr int kStepTok = 16;              // tokens per step (one MMA tile, one softmax update)
-#ifndef SAW_DECODE_STAGES
-#define SAW_DECODE_STAGES 4
-#endif
-constexpr int kStages = SAW_DECODE_STAGES;  // tiles in flight per warp
-constexpr int kCodeRow = kHeadDim / 2;    // code bytes per token
+
+// What depends on the head dimension D (64, 128 or 256).
+template <int D>
+struct Dims {
+  static constexpr int kCodeRow = D / 2;           // code bytes per token
+  static constexpr int kStages = D == 256 ? 3 : 4;  // tiles in flight per warp
+  static constexpr int kRedStride = D + D / 16;    // padded row of the cross-warp reduction
+  static constexpr int kE = D / 32;                // q and output elements per lane
+  static constexpr int kKWords = D / 32;           // K-row words per thread-in-group
+  static constexpr int kMT = D / 16;               // 16-dim tiles of the output product
+  static constexpr int kVWords = D / 64;           // V-row words per lane group
+  static constexpr int kKSteps = D / 16;           // k-steps of the score product
+  static constexpr bool kFragSmem = D > kHeadDim;  // q' fragments read per k-step from shared memory
+};
 
 // Stage layout for a 16-token step, the same for every page size:
 // [K codes 16 rows | K meta 16 words | V codes 16 rows | V meta 16 words].
 // A 16-token page is exactly [K chunk | V chunk]; larger pages are copied
 // as 16-row slices of their code and meta regions.
-template <int P>
+template <int D, int P>
 struct Cfg {
-  static constexpr int kChunk = chunk_bytes(P);
+  using DM = Dims<D>;
+  static constexpr int kCodeRow = DM::kCodeRow;
+  static constexpr int kStages = DM::kStages;
+  static constexpr int kChunk = P * kCodeRow + 4 * P;
   static constexpr int kStepsPerPage = P / kStepTok;
-  static constexpr int kHalf = kStepTok * kCodeRow + kStepTok * 4;  // 1088: one tensor
-  static constexpr int kStage = 2 * kHalf;                          // 2176
+  static constexpr int kHalf = kStepTok * kCodeRow + kStepTok * 4;  // one tensor (1088 at D 128)
+  static constexpr int kStage = 2 * kHalf;
   // byte offset of K's code row / meta word `row` in a stage; V's are at the
   // same offsets from kHalf
   __device__ static constexpr int kcode(int row) { return row * kCodeRow; }
   __device__ static constexpr int kmeta(int row) { return kStepTok * kCodeRow + row * 4; }
   static constexpr int kRing = kWarps * kStages * kStage;
   // after the main loop the ring is reused: cross-warp reduction, then rows
-  // red_acc [16][8][132], red_m / red_l / red_z / weights [16][8], per-head
-  // totals [3][8]
-  static constexpr int kRed = (kWarps * kMaxGroup * kRedStride + 4 * kWarps * kMaxGroup + 3 * kMaxGroup) * 4;
-  static constexpr int kOffQ = (kRed + 15) / 16 * 16;                          // f32 [8][128]
-  static_assert(kOffQ + kMaxGroup * kHeadDim * 4 <= kRing, "epilogue scratch must fit the ring");
+  // red_acc [W][8][D + D/16], red_m / red_l / red_z / weights [W][8],
+  // per-head totals [3][8]
+  static constexpr int kRed = (kWarps * kMaxGroup * DM::kRedStride + 4 * kWarps * kMaxGroup + 3 * kMaxGroup) * 4;
+  static constexpr int kOffQ = (kRed + 15) / 16 * 16;                          // f32 [8][D]
+  static_assert(kOffQ + kMaxGroup * D * 4 <= kRing, "epilogue scratch must fit the ring");
   static constexpr int kOffBars = kRing;
-  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [16][4]
-  static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [16][kIdCap]
-  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][8 t][32 lanes][4]
-  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * kHeadDim * 2;      // float [2][8]
+  static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [W][stages]
+  static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [W][kIdCap]
+  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][D/16 t][32 lanes][4]
+  static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * D * 2;             // float [2][8]
   static constexpr int kOffFlag = kOffQsum + 2 * kMaxGroup * 4;               // int
-  static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (64 code bytes, meta)
+  static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (code bytes, meta)
   static constexpr int kSmem = kOffNew + 2 * (kCodeRow + 16);
+  static_assert(kSmem <= (kCtasPerSm == 1 ? 227 * 1024 : 113 * 1024), "shared memory per CTA");
 };
 
-// In-place butterfly over each h-block of nvec vectors of 128 floats in shared
+// In-place butterfly over each h-block of nvec vectors of D floats in shared
 // memory (all threads of the CTA take part).  Mathematically (H x) per block;
 // the 1/sqrt(h) factor is left to the caller.
+template <int D>
 __device__ void smem_fwht(float* buf, int nvec, int h) {
-  const int lanes = nvec * (kHeadDim / 2);
+  const int lanes = nvec * (D / 2);
   for (int len = 1; len < h; len *= 2) {
     for (int idx = threadIdx.x; idx < lanes; idx += blockDim.x) {
-      const int v = idx / (kHeadDim / 2);
-      const int k = idx - v * (kHeadDim / 2);
+      const int v = idx / (D / 2);
+      const int k = idx - v * (D / 2);
       // k-th index with bit `len` clear
       const int i = ((k & ~(len - 1)) << 1) | (k & (len - 1));
-      float* row = buf + v * kHeadDim;
+      float* row = buf + v * D;
       const float a = row[i], b = row[i + len];
       row[i] = a + b;
       row[i + len] = a - b;
@@ -130,9 +145,17 @@ constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 // runs twice (q' hi, then lo) and p*s is one binary16 value.
 // BFM: the caches' (scale, zero) words are bfloat16 instead of binary16;
 // they are widened to binary32 either way, so only that step differs.
-template <int P, bool PACKED, bool APPEND, bool BFM>
+// D: the head dimension.  A thread-in-group c of an MMA quad covers dims
+// [c D/4, (c+1) D/4) of a K row, 32-bit word w of it dims 8w .. 8w+7 of
+// that range; a lane group g covers dims [g D/8, (g+1) D/8) of the output.
+template <int D, int P, bool PACKED, bool APPEND, bool BFM>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(const DecodeParams p) {
-  using C = Cfg<P>;
+  static_assert(!APPEND || D == kHeadDim, "the fused step is built for head_dim 128");
+  using C = Cfg<D, P>;
+  using DM = Dims<D>;
+  constexpr int kStages = DM::kStages;
+  constexpr int kCodeRow = DM::kCodeRow;
+  constexpr int kRedStride = DM::kRedStride;
   // Wait for the previous kernel in the stream before reading anything --
   // unless the caller declared that it writes neither the tables nor the
   // pages: then the page copies start first and the wait comes just before q
@@ -172,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     // nothing to attend over here; an empty sequence still owes a zero row
     if (split == 0 && n_pages == 0) {
       if (early) pdl_wait_then_release();
-      for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
-        p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = 0.0f;
+      for (int idx = tid; idx < G * D; idx += kThreads)
+        p.out[(int64_t(seq) * p.num_q_heads + hq0) * D + idx] = 0.0f;
     }
     return;
   }
@@ -237,14 +260,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const int new_tok = L - 1;
   const bool owner = APPEND && new_tok >= 0 && new_tok / P >= p_begin && new_tok / P < p_end;
   const int new_pid = owner ? btab[new_tok / P] : -1;
-  if (early && lane < 2) {
+  if (early && lane < D / 64) {
     // warm L2 with the rows read right after the wait (a prefetch only
     // hints the cache, which stays coherent with the previous kernel's
     // writes, so it may run before the wait)
     const uint16_t* row = nullptr;
-    if (warp < G) row = p.q + (int64_t(seq) * p.num_q_heads + hq0 + warp) * kHeadDim;
-    if (owner && warp == kWarps - 2) row = p.k_new + int64_t(seq) * p.k_new_stride + int64_t(kvh) * kHeadDim;
-    if (owner && warp == kWarps - 1) row = p.v_new + int64_t(seq) * p.v_new_stride + int64_t(kvh) * kHeadDim;
+    if (warp < G) row = p.q + (int64_t(seq) * p.num_q_heads + hq0 + warp) * D;
+    if (owner && warp == kWarps - 2) row = p.k_new + int64_t(seq) * p.k_new_stride + int64_t(kvh) * D;
+    if (owner && warp == kWarps - 1) row = p.v_new + int64_t(seq) * p.v_new_stride + int64_t(kvh) * D;
     if (row) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + lane * 64));
   }
   __syncwarp();
@@ -259,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     const int tensor = warp - (kWarps - 2);
     const uint16_t* src = (tensor == 0 ? p.k_new + int64_t(seq) * p.k_new_stride
                                        : p.v_new + int64_t(seq) * p.v_new_stride) +
-                          int64_t(kvh) * kHeadDim;
+                          int64_t(kvh) * D;
     const bool rot = (tensor == 0 ? p.rotate_k : p.rotate_v) != 0;
     uint32_t meta;
     const uint16_t codes =
@@ -281,51 +304,76 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 
   // ---- b = 2^S q', q' = (1/sqrt h) H q for the group's heads, as binary16
   // hi + lo parts (b = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8
-  // rotates head h, lane l holding elements 4l..4l+3.  S is per head, the
-  // largest with |b| < 2^14, and odd elements get 2^(S-4): they meet the
-  // high nibbles (n * 2^-20) and even ones the low nibbles (n * 2^-24), so
-  // every product is n q' 2^(S-24).  sm_scale*log2(e) is applied to the
-  // binary32 score, so an unrotated q enters the MMA exactly.
+  // rotates head h, lane l holding elements E l .. E l + E - 1 (E = D/32).
+  // S is per head, the largest with |b| < 2^14, and odd elements get
+  // 2^(S-4): they meet the high nibbles (n * 2^-20) and even ones the low
+  // nibbles (n * 2^-24), so every product is n q' 2^(S-24).
+  // sm_scale*log2(e) is applied to the binary32 score, so an unrotated q
+  // enters the MMA exactly.
   // q' is stored in the B-fragment order of the score MMA: buffer 0 holds,
   // for k-step t and lane (g, c), the four binary16 values of that lane's
   // two fragment registers (PACKED: column g = hi of head g for g < 4, lo
   // of head g - 4 otherwise; WIDE: hi of head g); buffer 1 (WIDE) the lo
-  // parts.  Each lane then loads its fragments with conflict-free 8-byte
-  // reads.  Element d of a head sits at k-step 2((d >> 3) & 3) + ((d >> 1) & 1),
-  // thread-in-group c = d >> 5, register d & 1, half (d >> 2) & 1.
+  // parts.  Element d of a head, with c = d / (D/4), o = d mod (D/4) and
+  // j = o mod 8, sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group
+  // c, register j & 1, half (j >> 2) & 1: the nibble the K codes put there.
+  constexpr int kE = DM::kE;
   if (warp < kMaxGroup) {
     const int h = warp;
-    float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float x[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) x[e] = 0.0f;
     if (h < G) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(
-          p.q + (int64_t(seq) * p.num_q_heads + hq0 + h) * kHeadDim + 4 * lane);
+      const uint16_t* qrow = p.q + (int64_t(seq) * p.num_q_heads + hq0 + h) * D + kE * lane;
       const bool f16 = p.in_f16 != 0;
-      x[0] = in_lo(raw.x, f16);
-      x[1] = in_hi(raw.x, f16);
-      x[2] = in_lo(raw.y, f16);
-      x[3] = in_hi(raw.y, f16);
+      uint32_t raw[kE / 2];
+      if (kE == 2) {
+        raw[0] = *reinterpret_cast<const uint32_t*>(qrow);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kE / 2; u += 2) {
+          const uint2 r2 = *reinterpret_cast<const uint2*>(qrow + 2 * u);
+          raw[u] = r2.x;
+          raw[u + 1] = r2.y;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kE / 2; ++u) {
+        x[2 * u] = in_lo(raw[u], f16);
+        x[2 * u + 1] = in_hi(raw[u], f16);
+      }
       if (p.rotate_k) {
         const int hb = p.block_h;
-        const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
-        if (hb > 2) {
-          x[0] = a0 + a2; x[1] = a1 + a3; x[2] = a0 - a2; x[3] = a1 - a3;
-        } else {
-          x[0] = a0; x[1] = a1; x[2] = a2; x[3] = a3;
+        // strides below E inside the lane, ascending, then across lanes
+#pragma unroll
+        for (int len = 1; len < kE; len *= 2) {
+          if (len < hb) {
+#pragma unroll
+            for (int e = 0; e < kE; ++e) {
+              if (!(e & len)) {
+                const float a = x[e], b = x[e + len];
+                x[e] = a + b;
+                x[e + len] = a - b;
+              }
+            }
+          }
         }
-        for (int len = 4; len < hb; len *= 2) {
-          const int mask = len >> 2;
+        for (int len = kE; len < hb; len *= 2) {
+          const int mask = len / kE;
           const bool upper = (lane & mask) != 0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < kE; ++e) {
             const float o = __shfl_xor_sync(kFull, x[e], mask);
             x[e] = upper ? (o - x[e]) : (x[e] + o);
           }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] *= p.c_h;
+        for (int e = 0; e < kE; ++e) x[e] *= p.c_h;
       }
     }
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kE; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
     for (int x2 = 16; x2 >= 1; x2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, x2));
     int ex;
@@ -333,15 +381,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     const int S = min(max(14 - ex, -100), 100);
     float part = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int se = (e & 1) ? S - 4 : S;
+    for (int e = 0; e < kE; ++e) {
+      const int d = kE * lane + e;
+      const int se = (d & 1) ? S - 4 : S;
       const float y = ldexpf(x[e], se);
       const __half hi = __float2half_rn(y);
       const __half lo = __float2half_rn(y - __half2float(hi));
-      const int d = 4 * lane + e;
-      const int t = 2 * ((d >> 3) & 3) + ((d >> 1) & 1);
-      const int w2 = (d & 1) * 2 + ((d >> 2) & 1);
-      const int c_ = d >> 5;
+      const int c_ = d / (D / 4);
+      const int o = d % (D / 4);
+      const int jj = o & 7;
+      const int t = 2 * (o >> 3) + ((jj >> 1) & 1);
+      const int w2 = (jj & 1) * 2 + ((jj >> 2) & 1);
+      constexpr int kLo = DM::kKSteps * 32 * 4;  // halves in buffer 0
       if (PACKED) {
         if (h < kMaxGroup / 2) {
           qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
@@ -349,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         }
       } else {
         qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
-        qh[8 * 32 * 4 + (t * 32 + h * 4 + c_) * 4 + w2] = lo;
+        qh[kLo + (t * 32 + h * 4 + c_) * 4 + w2] = lo;
       }
       part += ldexpf(__half2float(hi) + __half2float(lo), -se);
     }
@@ -362,20 +413,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   }
   __syncthreads();
 
-  // B fragments of q' for the score MMA (k-step t uses word 4c + t/2 of a
-  // token's codes: bytes (0,2) for even t, (1,3) for odd t).  Column g:
-  // PACKED -> hi of head g (g < 4) or lo of head g - 4; WIDE -> head g.
-  uint32_t bq[8][2];
-  uint32_t bl[PACKED ? 1 : 8][2];
-  {
-    const uint2* qf = reinterpret_cast<const uint2*>(qh);
+  // B fragments of q' for the score MMA (k-step t uses word t/2 of the
+  // thread-in-group's share of a token's codes: bytes (0,2) for even t,
+  // (1,3) for odd t).  Column g: PACKED -> hi of head g (g < 4) or lo of
+  // head g - 4; WIDE -> head g.  Kept in registers up to D = 128; read from
+  // shared memory per k-step beyond (the output accumulators take the room).
+  constexpr int kKS = DM::kKSteps;
+  constexpr int kRegKS = DM::kFragSmem ? 1 : kKS;
+  const uint2* qf = reinterpret_cast<const uint2*>(qh);
+  uint32_t bq[kRegKS][2];
+  uint32_t bl[(PACKED || DM::kFragSmem) ? 1 : kKS][2];
+  if constexpr (!DM::kFragSmem) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int t = 0; t < kRegKS; ++t) {
       const uint2 v = qf[t * 32 + lane];
       bq[t][0] = v.x;
       bq[t][1] = v.y;
       if (!PACKED) {
-        const uint2 u = qf[8 * 32 + t * 32 + lane];
+        const uint2 u = qf[kKS * 32 + t * 32 + lane];
         bl[PACKED ? 0 : t][0] = u.x;
         bl[PACKED ? 0 : t][1] = u.y;
       }
@@ -388,9 +443,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
   const float skA = qsum[kMaxGroup + hb] * p.q_scale, skB = qsum[kMaxGroup + hb + 1] * p.q_scale;
 
-  float acc[8][4];
+  constexpr int kMT = DM::kMT;
+  float acc[kMT][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  for (int i = 0; i < kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.0f, 0.0f};
   float z_run[2] = {0.0f, 0.0f};
@@ -441,16 +497,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       v0[t] = pok && (tok0 + g) < L;
       v1[t] = pok && (tok0 + g + 8) < L;
       full[t] = pok && tok0 + kStepTok <= L;  // warp-uniform
-      const uint8_t* krow = st + C::kcode(g) + 16 * c;
-      const uint4 ka = *reinterpret_cast<const uint4*>(krow);
-      const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow);
-      const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w};
-      const uint32_t kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+      constexpr int kKW = DM::kKWords;
+      const uint8_t* krow = st + C::kcode(g) + (D / 8) * c;
+      uint32_t kaw[kKW], kbw[kKW];
+      if constexpr (kKW == 2) {
+        const uint2 ka = *reinterpret_cast<const uint2*>(krow);
+        const uint2 kb = *reinterpret_cast<const uint2*>(krow + 8 * kCodeRow);
+        kaw[0] = ka.x; kaw[1] = ka.y;
+        kbw[0] = kb.x; kbw[1] = kb.y;
+      } else {
+#pragma unroll
+        for (int u = 0; u < kKW; u += 4) {
+          const uint4 ka = *reinterpret_cast<const uint4*>(krow + 4 * u);
+          const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow + 4 * u);
+          kaw[u] = ka.x; kaw[u + 1] = ka.y; kaw[u + 2] = ka.z; kaw[u + 3] = ka.w;
+          kbw[u] = kb.x; kbw[u + 1] = kb.y; kbw[u + 2] = kb.z; kbw[u + 3] = kb.w;
+        }
+      }
       // two independent accumulator chains (even / odd byte pairs)
       float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       float e2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < kKW; ++w) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           // bytes (0,2) in place, bytes (1,3) moved down by 8: low nibbles
@@ -463,8 +531,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
           a[2] = wa & kHiNib;
           a[3] = wb & kHiNib;
           float (&dst)[4] = hh ? e2 : d;
-          mma_16816(dst, a, bq[2 * w + hh][0], bq[2 * w + hh][1]);
-          if (!PACKED) mma_16816(dst, a, bl[PACKED ? 0 : 2 * w + hh][0], bl[PACKED ? 0 : 2 * w + hh][1]);
+          const int kt = 2 * w + hh;
+          if constexpr (DM::kFragSmem) {
+            const uint2 v = qf[kt * 32 + lane];
+            mma_16816(dst, a, v.x, v.y);
+            if (!PACKED) {
+              const uint2 u = qf[kKS * 32 + kt * 32 + lane];
+              mma_16816(dst, a, u.x, u.y);
+            }
+          } else {
+            mma_16816(dst, a, bq[kt][0], bq[kt][1]);
+            if (!PACKED) mma_16816(dst, a, bl[PACKED ? 0 : kt][0], bl[PACKED ? 0 : kt][1]);
+          }
         }
       }
 #pragma unroll
@@ -512,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       z_run[0] *= al0;
       z_run[1] *= al1;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kMT; ++k) {
         acc[k][0] *= al0;
         acc[k][1] *= al1;
         acc[k][2] *= al0;
@@ -561,17 +639,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       const uint32_t b0 = prmt(va, vb, 0x5410u);
       const uint32_t b1 = prmt(va, vb, 0x7632u);
 
-      const uint8_t* vrow = vst + C::kcode(0) + 8 * g;
-      const uint2 r0w = *reinterpret_cast<const uint2*>(vrow + c * kCodeRow);
-      const uint2 r1w = *reinterpret_cast<const uint2*>(vrow + (c + 4) * kCodeRow);
-      const uint2 r2w = *reinterpret_cast<const uint2*>(vrow + (c + 8) * kCodeRow);
-      const uint2 r3w = *reinterpret_cast<const uint2*>(vrow + (c + 12) * kCodeRow);
+      // lane group g's dims of the four token rows: D/16 bytes each, word
+      // k/4 of them holding (as byte k mod 4) the codes of dims 2k, 2k + 1
+      constexpr int kVW = DM::kVWords;
+      const uint8_t* vrow = vst + C::kcode(0) + (D / 16) * g;
+      uint32_t rw[4][kVW];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t w0 = (k < 4) ? r0w.x : r0w.y;
-        const uint32_t w1 = (k < 4) ? r1w.x : r1w.y;
-        const uint32_t w2 = (k < 4) ? r2w.x : r2w.y;
-        const uint32_t w3 = (k < 4) ? r3w.x : r3w.y;
+      for (int r = 0; r < 4; ++r) {
+        const uint8_t* src = vrow + (c + 4 * r) * kCodeRow;
+        if constexpr (kVW == 1) {
+          rw[r][0] = *reinterpret_cast<const uint32_t*>(src);
+        } else if constexpr (kVW == 2) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(src);
+          rw[r][0] = v2.x;
+          rw[r][1] = v2.y;
+        } else {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(src);
+          rw[r][0] = v4.x;
+          rw[r][1] = v4.y;
+          rw[r][2] = v4.z;
+          rw[r][3] = v4.w;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMT; ++k) {
+        const uint32_t w0 = rw[0][k / 4];
+        const uint32_t w1 = rw[1][k / 4];
+        const uint32_t w2 = rw[2][k / 4];
+        const uint32_t w3 = rw[3][k / 4];
         const uint32_t sel = uint32_t(k & 3) | (uint32_t((k & 3) + 4) << 8);
         const uint32_t x01 = prmt(w0, w1, sel);
         const uint32_t x23 = prmt(w2, w3, sel);
@@ -632,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   }
   // output rows g (even dims) carried n * 2^-24, rows g + 8 (odd) n * 2^-20
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < kMT; ++k) {
     acc[k][0] *= 16777216.0f;
     acc[k][1] *= 16777216.0f;
     acc[k][2] *= 1048576.0f;
@@ -640,8 +735,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   }
   __syncthreads();  // every warp is done with its ring: reuse it
 
-  float* red_acc = reinterpret_cast<float*>(smem);                     // [16][8][132]
-  float* red_m = red_acc + kWarps * kMaxGroup * kRedStride;           // [16][8]
+  float* red_acc = reinterpret_cast<float*>(smem);                     // [W][8][D + D/16]
+  float* red_m = red_acc + kWarps * kMaxGroup * kRedStride;           // [W][8]
   float* red_l = red_m + kWarps * kMaxGroup;
   float* red_z = red_l + kWarps * kMaxGroup;
   float* wgt = red_z + kWarps * kMaxGroup;                            // [16][8]
@@ -658,11 +753,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     float* base0 = red_acc + (warp * kMaxGroup + hb) * kRedStride;
     float* base1 = base0 + kRedStride;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      base0[red_col(16 * g + 2 * k)] = acc[k][0];
-      base1[red_col(16 * g + 2 * k)] = acc[k][1];
-      base0[red_col(16 * g + 2 * k + 1)] = acc[k][2];
-      base1[red_col(16 * g + 2 * k + 1)] = acc[k][3];
+    for (int k = 0; k < kMT; ++k) {
+      base0[red_col((D / 8) * g + 2 * k)] = acc[k][0];
+      base1[red_col((D / 8) * g + 2 * k)] = acc[k][1];
+      base0[red_col((D / 8) * g + 2 * k + 1)] = acc[k][2];
+      base1[red_col((D / 8) * g + 2 * k + 1)] = acc[k][3];
     }
   }
   __syncthreads();
@@ -695,21 +790,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * kHeadDim; idx += kThreads) {
-    const int h = idx / kHeadDim, dd = idx - h * kHeadDim;
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int h = idx / D, dd = idx - h * D;
     float num = tot[kMaxGroup + h];
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
       if (w < nw) num += red_acc[(w * kMaxGroup + h) * kRedStride + red_col(dd)] * wgt[w * kMaxGroup + h];
     if (direct) {
       const float den = tot[h];
-      qs[h * kHeadDim + dd] = (den > 0.0f) ? num / den : 0.0f;
+      qs[h * D + dd] = (den > 0.0f) ? num / den : 0.0f;
     } else {
       // publish the partial, and keep it here in case this split merges
       // (den and M stay in tot)
-      qs[h * kHeadDim + dd] = num;
+      qs[h * D + dd] = num;
       const int64_t row = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits + split;
-      p.part_o[row * kHeadDim + dd] = num;
+      p.part_o[row * D + dd] = num;
       if (dd == 0) {
         p.part_ml[2 * row] = tot[2 * kMaxGroup + h];
         p.part_ml[2 * row + 1] = tot[h];
@@ -759,15 +854,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     // item = (head, 4 dims); four threads per item share the splits.  Every
     // load is issued before any is used (one round of L2 latency).
     constexpr int kMaxSplitsPerThread = 8;
-    for (int base = 0; base < G * 32 * 4; base += kThreads) {
+    constexpr int kItems = D / 4;  // (head, 4 dims) items per head
+    for (int base = 0; base < G * kItems * 4; base += kThreads) {
       const int t = base + tid;
       const int item = t >> 2, part = t & 3;
-      const bool active = item < G * 32;
-      const int h = active ? item >> 5 : 0, ch = item & 31;
+      const bool active = item < G * kItems;
+      const int h = active ? item / kItems : 0, ch = item % kItems;
       const int64_t row0 = (int64_t(seq) * p.num_q_heads + hq0 + h) * p.num_splits;
       const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row0;
-      const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kHeadDim) + ch;
-      const float4* own = reinterpret_cast<const float4*>(qs + h * kHeadDim) + ch;
+      const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * D) + ch;
+      const float4* own = reinterpret_cast<const float4*>(qs + h * D) + ch;
       float M = -INFINITY;
       float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       float den = 0.0f;
@@ -782,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
           v[u] = !in ? make_float2(-INFINITY, 0.0f)
                      : mine ? make_float2(tot[2 * kMaxGroup + h], tot[h]) : __ldcg(&ml[sp]);
           o[u] = !in ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
-                     : mine ? *own : __ldcg(&po[int64_t(sp) * (kHeadDim / 4)]);
+                     : mine ? *own : __ldcg(&po[int64_t(sp) * (D / 4)]);
         }
         float Mb = -INFINITY;
 #pragma unroll
@@ -821,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       }
       if (active && part == 0) {
         const float inv = (den > 0.0f) ? 1.0f / den : 0.0f;
-        float* dst = qs + h * kHeadDim + 4 * ch;
+        float* dst = qs + h * D + 4 * ch;
         dst[0] = a.x * inv;
         dst[1] = a.y * inv;
         dst[2] = a.z * inv;
@@ -830,19 +926,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     }
   }
   __syncthreads();
-  if (p.rotate_v) smem_fwht(qs, G, p.block_h);
+  if (p.rotate_v) smem_fwht<D>(qs, G, p.block_h);
   const float post = p.rotate_v ? p.c_h : 1.0f;
-  for (int idx = tid; idx < G * kHeadDim; idx += kThreads)
-    p.out[(int64_t(seq) * p.num_q_heads + hq0) * kHeadDim + idx] = qs[idx] * post;
+  for (int idx = tid; idx < G * D; idx += kThreads)
+    p.out[(int64_t(seq) * p.num_q_heads + hq0) * D + idx] = qs[idx] * post;
 }
 
 // Launched with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream drains; it waits for it (griddepcontrol)
 // before reading anything.
-template <int P, bool PACKED, bool APPEND, bool BFM>
+template <int D, int P, bool PACKED, bool APPEND, bool BFM>
 cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
-  using C = Cfg<P>;
-  auto kernel = paged_decode_kernel<P, PACKED, APPEND, BFM>;
+  using C = Cfg<D, P>;
+  auto kernel = paged_decode_kernel<D, P, PACKED, APPEND, BFM>;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
@@ -859,34 +955,50 @@ cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int P, bool BFM>
+template <int D, int P, bool BFM>
 cudaError_t launch_page_m(const DecodeParams& p, cudaStream_t stream) {
   const bool packed = p.group <= kMaxGroup / 2;
-  if (p.append)
-    return packed ? launch_p<P, true, true, BFM>(p, stream)
-                  : launch_p<P, false, true, BFM>(p, stream);
-  return packed ? launch_p<P, true, false, BFM>(p, stream)
-                : launch_p<P, false, false, BFM>(p, stream);
+  if constexpr (D == kHeadDim) {
+    if (p.append)
+      return packed ? launch_p<D, P, true, true, BFM>(p, stream)
+                    : launch_p<D, P, false, true, BFM>(p, stream);
+  }
+  return packed ? launch_p<D, P, true, false, BFM>(p, stream)
+                : launch_p<D, P, false, false, BFM>(p, stream);
 }
 
-template <int P>
-cudaError_t launch_page(const DecodeParams& p, cudaStream_t stream) {
-  return p.meta_bf16 ? launch_page_m<P, true>(p, stream) : launch_page_m<P, false>(p, stream);
+template <int D>
+cudaError_t launch_dim(const DecodeParams& p, cudaStream_t stream) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  switch (p.page_size) {
+    case 16: return p.meta_bf16 ? launch_page_m<D, 16, true>(p, stream) : launch_page_m<D, 16, false>(p, stream);
+    case 32: return p.meta_bf16 ? launch_page_m<D, 32, true>(p, stream) : launch_page_m<D, 32, false>(p, stream);
+    case 64: return p.meta_bf16 ? launch_page_m<D, 64, true>(p, stream) : launch_page_m<D, 64, false>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 #define SAW_CAT2(a, b) a##b
 #define SAW_CAT(a, b) SAW_CAT2(a, b)
+#ifndef SAW_DECODE_OTHER_DIMS
+// head_dim 128 (and the fused decode step)
 cudaError_t SAW_CAT(launch_paged_decode_w, SAW_DECODE_WARPS)(const DecodeParams& p,
                                                              cudaStream_t stream) {
-  if (p.num_seqs == 0) return cudaSuccess;
-  switch (p.page_size) {
-    case 16: return launch_page<16>(p, stream);
-    case 32: return launch_page<32>(p, stream);
-    case 64: return launch_page<64>(p, stream);
+  return launch_dim<kHeadDim>(p, stream);
+}
+#else
+// head_dim 64 and 256 (this object is the same source built for those sizes)
+cudaError_t SAW_CAT(launch_paged_decode_dims_w, SAW_DECODE_WARPS)(const DecodeParams& p,
+                                                                  cudaStream_t stream) {
+  if (p.append) return cudaErrorInvalidValue;
+  switch (p.head_dim) {
+    case 64: return launch_dim<64>(p, stream);
+    case 256: return launch_dim<256>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
+#endif
 
 }  // namespace saw

@@ -335,8 +335,7 @@ void bind_decode_workspace(DecodeParams& p, void* workspace) {
 }
 
 cudaError_t launch_decode_any(const DecodeParams& p, cudaStream_t stream) {
-  return p.head_dim == kHeadDim ? launch_paged_decode(p, stream)
-                                : launch_paged_decode_var(p, p.head_dim, stream);
+  return launch_paged_decode(p, stream);
 }
 
 }  // namespace saw

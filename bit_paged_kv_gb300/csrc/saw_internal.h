@@ -86,17 +86,19 @@ struct DecodeParams {
   float c_h;                    // 1/sqrt(block_h)
   float q_scale;                // sm_scale * log2(e)
   int32_t warps;                // CTA shape: 16 (one per SM) or 8 (two per SM)
-  int32_t head_dim;             // 128, or 64 / 256 (variant kernels)
+  int32_t head_dim;             // 128, or 64 / 256
   int32_t in_f16;               // 1: q, k_new and v_new are binary16
   int32_t meta_bf16;            // 1: the caches' (scale, zero) words are bfloat16
 };
 
-// One launcher per CTA shape (paged_decode.cu compiled once per shape).
+// One launcher per CTA shape (paged_decode.cu compiled once per shape), and
+// per shape for head_dim 64 and 256 (the same source built for those sizes).
 cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
-// head_dim 64 and 256 (variants.cu)
+cudaError_t launch_paged_decode_dims_w16(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_paged_decode_dims_w8(const DecodeParams& p, cudaStream_t stream);
+// head_dim 64 and 256 append (variants.cu)
 cudaError_t launch_quantize_append_var(const AppendParams& p, int head_dim, cudaStream_t stream);
-cudaError_t launch_paged_decode_var(const DecodeParams& p, int head_dim, cudaStream_t stream);
 // BF16 baseline (paged_decode_bf16.cu)
 cudaError_t launch_paged_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_stride,
@@ -104,6 +106,9 @@ cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_s
                                uint16_t* kc, uint16_t* vc, int64_t num_slots, int P,
                                int32_t* dev_status, cudaStream_t stream);
 inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
+  if (p.head_dim != kHeadDim)
+    return p.warps == 8 ? launch_paged_decode_dims_w8(p, stream)
+                        : launch_paged_decode_dims_w16(p, stream);
   return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
 }
 

@@ -184,10 +184,9 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  * t_j = sm_scale * q'.(code_j*s_j + z_j); p = softmax(t); o' = sum_j p_j
  * (code_j*s_j + z_j) over V; o = (1/sqrt(h)) H o' if V was rotated.  The
  * GQA group of a kv-head is served by one pass over its pages.  Arithmetic
- * at head_dim 128: q' and p*s in binary16 on the tensor cores with binary32
- * accumulation, softmax in binary32; results match a float64 evaluation to
- * about 1e-3 of the output's largest magnitude.  head_dim 64 and 256 run a
- * binary32 CUDA-core kernel (same split plan, workspace layout and merge).
+ * (head_dim 64, 128 and 256 alike): q' and p*s in binary16 on the tensor
+ * cores with binary32 accumulation, softmax in binary32; results match a
+ * float64 evaluation to about 1e-3 of the output's largest magnitude.
  * Up to 8 q-heads per kv-head; head_dim 64, 128 or 256 (else
  * SAW_ERR_UNSUPPORTED).
  */
