@@ -177,7 +177,8 @@ __device__ __forceinline__ void rotate_half(const uint32_t (&wd)[kHalfRow / 2],
 }
 
 // Min and max of the whole row: 64 values here, three at a time (exact),
-// then the partner's.
+// then (PAIR) the partner's.
+template <bool PAIR = true>
 __device__ __forceinline__ void half_min_max(const float (&u)[kHalfRow], float& mn, float& mx) {
   float lo[22], hi[22];
 #pragma unroll
@@ -196,8 +197,10 @@ __device__ __forceinline__ void half_min_max(const float (&u)[kHalfRow], float& 
   hi[7] = hi[21];
   mn = fminf(min3(lo[0], lo[1], lo[2]), min3(lo[3], lo[4], fminf(lo[5], fminf(lo[6], lo[7]))));
   mx = fmaxf(max3(hi[0], hi[1], hi[2]), max3(hi[3], hi[4], fmaxf(hi[5], fmaxf(hi[6], hi[7]))));
-  mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  if (PAIR) {
+    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  }
 }
 
 // Codes of this thread's 64 elements, packed two per byte (even local index
@@ -410,6 +413,144 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   cp_async_wait<0>();
 }
 
+// ------------------------------------------------------------ head_dim 64
+//
+// The same persistent tiled scheme at head_dim 64: one thread per row (its
+// 64 values), 32 rows per warp tile (4 KB).  Every butterfly stride stays
+// inside the thread, and the row's min/max needs no partner.  Chunk c
+// (16 bytes) of tile row r sits in slot c ^ (r & 7) of the row's 128 bytes,
+// so a thread reading its own row chunk by chunk and the copies (eight
+// chunks of four rows per instruction) both spread over all bank groups.
+constexpr int kD64 = 64;
+constexpr int kRowBytes64 = kD64 * 2;
+constexpr int kTileRows64 = kTileBytes / kRowBytes64;  // 32
+
+template <int H, bool F16IN>
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
+    quantize_append_tiled64_kernel(const AppendParams p, int tiles_per_tensor, int num_tiles) {
+  extern __shared__ __align__(128) uint8_t ring_all[];
+
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* ring = ring_all + warp * (kTileStages * kTileBytes);
+  const int hkv = p.num_kv_heads;
+  const int num_rows = p.num_tokens * hkv;
+
+  // Copies of one tile: 8 per lane, 8 lanes per 128-byte row.
+  auto issue = [&](int tile, uint8_t* buf) {
+    const int tensor = tile >= tiles_per_tensor ? 1 : 0;
+    const int row0 = (tile - tensor * tiles_per_tensor) * kTileRows64;
+    const uint16_t* __restrict__ src = tensor ? p.src[1] : p.src[0];
+    const int64_t stride = tensor ? p.stride[1] : p.stride[0];
+    const int ch = lane & 7;
+    const bool full = row0 + kTileRows64 <= num_rows;
+    if (full && stride == int64_t(hkv) * kD64) {
+      const uint16_t* g = src + int64_t(row0) * kD64 + ch * 8;
+#pragma unroll
+      for (int it = 0; it < kTileRows64 / 4; ++it) {
+        const int r = it * 4 + (lane >> 3);
+        cp_async16(buf + r * kRowBytes64 + ((ch ^ (r & 7)) << 4), g + r * kD64);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < kTileRows64 / 4; ++it) {
+        const int r = it * 4 + (lane >> 3);
+        const int row = row0 + r;
+        if (row < num_rows) {
+          const uint32_t t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
+          const uint32_t hd = uint32_t(row) - t * uint32_t(hkv);
+          cp_async16(buf + r * kRowBytes64 + ((ch ^ (r & 7)) << 4),
+                     src + int64_t(t) * stride + hd * kD64 + ch * 8);
+        }
+      }
+    }
+  };
+
+  const int step = int(gridDim.x) * kTileWarps;
+  int tile = int(blockIdx.x) * kTileWarps + warp;
+#pragma unroll
+  for (int s = 0; s < kTileStages - 1; ++s) {
+    const int pre = tile + s * step;
+    if (pre < num_tiles) issue(pre, ring + s * kTileBytes);
+    cp_async_commit();
+  }
+  int cur = 0;
+  int ahead = kTileStages - 1;
+  for (; tile < num_tiles; tile += step) {
+    uint8_t* buf = ring + cur * kTileBytes;
+    const int nxt = tile + (kTileStages - 1) * step;
+    if (nxt < num_tiles) issue(nxt, ring + ahead * kTileBytes);
+    cp_async_commit();
+    cur = (cur + 1 == kTileStages) ? 0 : cur + 1;
+    ahead = (ahead + 1 == kTileStages) ? 0 : ahead + 1;
+
+    const int tensor = tile >= tiles_per_tensor ? 1 : 0;
+    const int row = (tile - tensor * tiles_per_tensor) * kTileRows64 + lane;
+    const bool live = row < num_rows;
+    uint32_t t = 0, hd = 0;
+    int32_t slot = -1;
+    if (live) {
+      t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
+      hd = uint32_t(row) - t * uint32_t(hkv);
+      slot = __ldg(p.slot_mapping + t);
+    }
+    cp_async_wait<kTileStages - 1>();  // this lane's copies of the current tile landed
+    __syncwarp();                      // ... and the whole warp's
+
+    // rows past the end compute on stale data; only stores are guarded
+    uint32_t wd[kHalfRow / 2];
+    {
+      const uint8_t* rowp = buf + lane * kRowBytes64;
+      const int x = lane & 7;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((j ^ x) << 4));
+        wd[4 * j + 0] = w.x;
+        wd[4 * j + 1] = w.y;
+        wd[4 * j + 2] = w.z;
+        wd[4 * j + 3] = w.w;
+      }
+    }
+    float u[kHalfRow];
+    const bool rot = tensor ? p.rotate[1] != 0 : p.rotate[0] != 0;
+    if (rot) {
+      // the whole row in one thread: the lower-thread form of every step
+      rotate_half<H, F16IN>(wd, u, p.c_h, 0);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kHalfRow / 2; ++i) {
+        u[2 * i] = F16IN ? f16_lo(wd[i]) : bf16_lo(wd[i]);
+        u[2 * i + 1] = F16IN ? f16_hi(wd[i]) : bf16_hi(wd[i]);
+      }
+    }
+    float mn, mx;
+    half_min_max<false>(u, mn, mx);
+    const RowMeta m = row_meta(mn, mx, p.meta_bf16 != 0);
+    uint32_t word[8];
+    quantize_half(u, m.z, m.rcp, m.fast, word);
+
+    if (live && slot != -1) {
+      if (slot < 0 || int64_t(slot) >= p.num_slots) {
+        report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+      } else {
+        const int P = p.page_size;
+        const int page = slot >> p.page_shift;
+        const int off = slot & (P - 1);
+        uint8_t* chunk = (tensor ? p.cache[1] : p.cache[0]) +
+                         (int64_t(page) * hkv + hd) * int64_t(P * (kD64 / 2 + 4));
+        uint8_t* codes = chunk + off * (kD64 / 2);
+        *reinterpret_cast<uint4*>(codes) = make_uint4(word[0], word[1], word[2], word[3]);
+        *reinterpret_cast<uint4*>(codes + 16) = make_uint4(word[4], word[5], word[6], word[7]);
+        *reinterpret_cast<uint32_t*>(chunk + P * (kD64 / 2) + 4 * off) =
+            uint32_t(m.sb) | (uint32_t(m.zb) << 16);
+      }
+    }
+    __syncwarp();  // the buffer is refilled by a later issue
+  }
+  cp_async_wait<0>();
+}
+
 // Small appends (a decode step appends one token: Hkv rows per tensor): one
 // warp per row, lane l holding elements 4l..4l+3.  The butterfly is the same
 // ascending-stride sequence of (a+b, a-b) steps as the row kernel -- strides
@@ -501,6 +642,44 @@ cudaError_t launch_tiled_h(int h, dim3 grid, cudaStream_t stream, const AppendPa
     case 128: return launch_tiled(quantize_append_tiled_kernel<128, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <bool F16IN>
+cudaError_t launch_tiled64_h(int h, dim3 grid, cudaStream_t stream, const AppendParams& q,
+                             int tiles_per_tensor, int num_tiles) {
+  switch (h) {
+    case 16: return launch_tiled(quantize_append_tiled64_kernel<16, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 32: return launch_tiled(quantize_append_tiled64_kernel<32, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 64: return launch_tiled(quantize_append_tiled64_kernel<64, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Bulk appends at head_dim 64 (the warp-per-row kernel in variants.cu
+// serves small ones).
+cudaError_t launch_quantize_append_tiled64(const AppendParams& p, int num_tensors,
+                                           cudaStream_t stream) {
+  const int num_rows = p.num_tokens * p.num_kv_heads;
+  if (num_rows == 0) return cudaSuccess;
+  const bool any_rot = p.rotate[0] || (num_tensors > 1 && p.rotate[1]);
+  const int h = any_rot ? p.block_h : kD64;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int tiles_per_tensor = (num_rows + kTileRows64 - 1) / kTileRows64;
+  const int num_tiles = tiles_per_tensor * num_tensors;
+  const dim3 grid(std::min((num_tiles + kTileWarps - 1) / kTileWarps, sms * kTileCtasPerSm));
+  AppendParams q = p;
+  q.num_tensors = num_tensors;
+  int lg = 0;
+  while ((1 << lg) < q.num_kv_heads) ++lg;
+  q.hkv_shift = uint32_t(31 + lg);
+  q.hkv_mul = uint32_t(((uint64_t(1) << q.hkv_shift) + q.num_kv_heads - 1) / q.num_kv_heads);
+  q.page_shift = 0;
+  while ((1 << q.page_shift) < q.page_size) ++q.page_shift;
+  return q.in_f16 ? launch_tiled64_h<true>(h, grid, stream, q, tiles_per_tensor, num_tiles)
+                  : launch_tiled64_h<false>(h, grid, stream, q, tiles_per_tensor, num_tiles);
 }
 
 cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream) {

@@ -35,6 +35,47 @@ def test_append_bytes(D, h, rot):
     assert_bytes_equal(vc, vr, f"V D{D} h{h}")
 
 
+@pytest.mark.parametrize("h", [64, 32, 16])
+@pytest.mark.parametrize("rot", [(True, True), (True, False), (False, False)])
+@pytest.mark.parametrize("fmt", ["bf16", "f16", "bf16-meta"])
+def test_append_bytes_bulk_head_dim_64(h, rot, fmt):
+    """Bulk appends at head_dim 64 (above 4096 rows: the tiled kernel, one
+    thread per row): 2501 tokens x 4 kv-heads, a ragged last tile, one skipped
+    slot, every byte against the oracle, for both input formats and both
+    metadata formats."""
+    D = 64
+    wl = W.TINY.variant(head_dim=D, block_h=h, num_kv_heads=4, dist="student_t", nu=3)
+    T, P, pages = 2501, 16, 170
+    dt = torch.float16 if fmt == "f16" else torch.bfloat16
+    meta_bf16 = fmt == "bf16-meta"
+    k = W.kv_rows(wl, 0, W.K, T, "cuda", dtype=dt)
+    v = W.kv_rows(wl, 0, W.V, T, "cuda", dtype=dt)
+    perm = torch.randperm(pages * P, generator=torch.Generator().manual_seed(h + T))[:T]
+    slots = perm.to(torch.int32)
+    slots[5] = -1
+    kc, vc, st = gpu_append(k, v, slots.cuda(), pages, P, rot[0], rot[1], h, meta_bf16=meta_bf16)
+    assert st == 0
+    kr, vr, bad = oracle_append(k, v, slots, pages, P, rot[0], rot[1], h, meta_bf16=meta_bf16)
+    assert bad == 0
+    assert_bytes_equal(kc, kr, f"K D64 bulk h{h} {fmt}")
+    assert_bytes_equal(vc, vr, f"V D64 bulk h{h} {fmt}")
+
+
+def test_append_bulk_head_dim_64_strided_k_only_and_bad_slot():
+    D, h, P, pages, Hkv = 64, 64, 64, 60, 2
+    wl = W.TINY.variant(head_dim=D, block_h=h, num_kv_heads=Hkv)
+    T = 3000  # 6000 rows: the tiled kernel
+    raw = W.kv_rows(wl.variant(num_kv_heads=2 * Hkv), 0, W.K, T, "cuda")  # [T, 2 Hkv, D]
+    k = raw[:, :Hkv]                                                      # token stride 2 Hkv D
+    slots = torch.randperm(pages * P, generator=torch.Generator().manual_seed(3))[:T].to(torch.int32)
+    slots[7] = pages * P
+    kc, _, st = gpu_append(k, None, slots.cuda(), pages, P, True, False, h)
+    assert st == saw.SAW_ERR_DEVICE_INDEX
+    kr, _, bad = oracle_append(k.contiguous(), None, slots, pages, P, True, False, h)
+    assert bad == 1
+    assert_bytes_equal(kc, kr, "K strided D64 bulk")
+
+
 def test_append_strided_k_only_and_bad_slot():
     D, h, P, pages, Hkv = 256, 256, 32, 8, 2
     wl = W.TINY.variant(head_dim=D, block_h=h, num_kv_heads=Hkv)
