@@ -275,8 +275,9 @@ __device__ __forceinline__ int chunk_slot(int r, int c) { return c ^ (r & 3); }
 // Tiles 0 .. tiles_per_tensor-1 are K rows, the rest V rows.  Each warp is
 // an independent worker with its own ring of kTileStages tiles: no CTA-wide
 // barrier, so a warp waiting for its data never holds up the others.
-// F16IN: the rows are binary16 instead of bfloat16.
-template <int H, bool F16IN>
+// F16IN: the rows are binary16 instead of bfloat16; BFM: the (scale, zero)
+// words are bfloat16 instead of binary16.
+template <int H, bool F16IN, bool BFM>
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     quantize_append_tiled_kernel(const AppendParams p, int tiles_per_tensor, int num_tiles) {
   extern __shared__ __align__(128) uint8_t ring_all[];
@@ -288,22 +289,26 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   const int hkv = p.num_kv_heads;
   const int num_rows = p.num_tokens * hkv;
 
-  // Copies of one tile: 8 per lane, 16 lanes per 256-byte row.
+  // Copies of one tile: 8 per lane, 16 lanes per 256-byte row.  Copy `it`
+  // of a lane lands in row r = 2 it + rl at slot ch ^ (r & 3), and r & 3 is
+  // rl for even it and 2 + rl for odd it: two offsets per lane, fixed.
+  const int ch = lane & 15;
+  const int rl = lane >> 4;
+  const int so_even = rl * kRowBytes + ((ch ^ rl) << 4);
+  const int so_odd = rl * kRowBytes + ((ch ^ (2 | rl)) << 4);
   auto issue = [&](int tile, uint8_t* buf) {
     const int tensor = tile >= tiles_per_tensor ? 1 : 0;
     const int row0 = (tile - tensor * tiles_per_tensor) * kTileRows;
     const uint16_t* __restrict__ src = tensor ? p.src[1] : p.src[0];
     const int64_t stride = tensor ? p.stride[1] : p.stride[0];
-    const int ch = lane & 15;
     const bool full = row0 + kTileRows <= num_rows;
     if (full && stride == int64_t(hkv) * kHeadDim) {
       // contiguous rows: row i of the tile starts 128 elements after row i-1
-      const uint16_t* g = src + int64_t(row0) * kHeadDim + ch * 8;
+      const uint16_t* g = src + (int64_t(row0) + rl) * kHeadDim + ch * 8;
 #pragma unroll
-      for (int it = 0; it < kTileRows / 2; ++it) {
-        const int r = it * 2 + (lane >> 4);
-        cp_async16(buf + r * kRowBytes + (chunk_slot(r, ch) << 4), g + r * kHeadDim);
-      }
+      for (int it = 0; it < kTileRows / 2; ++it)
+        cp_async16(buf + it * 2 * kRowBytes + ((it & 1) ? so_odd : so_even),
+                   g + it * 2 * kHeadDim);
     } else {
 #pragma unroll
       for (int it = 0; it < kTileRows / 2; ++it) {
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     }
     float mn, mx;
     half_min_max(u, mn, mx);
-    const RowMeta m = row_meta(mn, mx, p.meta_bf16 != 0);
+    const RowMeta m = row_meta(mn, mx, BFM);
     const uint16_t zb = m.zb, sb = m.sb;
     uint32_t word[8];
     quantize_half(u, m.z, m.rcp, m.fast, word);
@@ -632,14 +637,14 @@ cudaError_t launch_tiled(K kernel, dim3 grid, cudaStream_t stream, const AppendP
   return cudaLaunchKernelEx(&cfg, kernel, p, tiles_per_tensor, num_tiles);
 }
 
-template <bool F16IN>
+template <bool F16IN, bool BFM>
 cudaError_t launch_tiled_h(int h, dim3 grid, cudaStream_t stream, const AppendParams& q,
                            int tiles_per_tensor, int num_tiles) {
   switch (h) {
-    case 16: return launch_tiled(quantize_append_tiled_kernel<16, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 32: return launch_tiled(quantize_append_tiled_kernel<32, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 64: return launch_tiled(quantize_append_tiled_kernel<64, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
-    case 128: return launch_tiled(quantize_append_tiled_kernel<128, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 16: return launch_tiled(quantize_append_tiled_kernel<16, F16IN, BFM>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 32: return launch_tiled(quantize_append_tiled_kernel<32, F16IN, BFM>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 64: return launch_tiled(quantize_append_tiled_kernel<64, F16IN, BFM>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 128: return launch_tiled(quantize_append_tiled_kernel<128, F16IN, BFM>, grid, stream, q, tiles_per_tensor, num_tiles);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -716,8 +721,11 @@ cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaS
   q.hkv_mul = uint32_t(((uint64_t(1) << q.hkv_shift) + q.num_kv_heads - 1) / q.num_kv_heads);
   q.page_shift = 0;
   while ((1 << q.page_shift) < q.page_size) ++q.page_shift;
-  return q.in_f16 ? launch_tiled_h<true>(h, grid, stream, q, tiles_per_tensor, num_tiles)
-                  : launch_tiled_h<false>(h, grid, stream, q, tiles_per_tensor, num_tiles);
+  if (q.meta_bf16)
+    return q.in_f16 ? launch_tiled_h<true, true>(h, grid, stream, q, tiles_per_tensor, num_tiles)
+                    : launch_tiled_h<false, true>(h, grid, stream, q, tiles_per_tensor, num_tiles);
+  return q.in_f16 ? launch_tiled_h<true, false>(h, grid, stream, q, tiles_per_tensor, num_tiles)
+                  : launch_tiled_h<false, false>(h, grid, stream, q, tiles_per_tensor, num_tiles);
 }
 
 }  // namespace saw
