@@ -176,27 +176,28 @@ __device__ __forceinline__ void rotate_half(const uint32_t (&wd)[kHalfRow / 2],
   for (int i = 0; i < kHalfRow; i += 2) mul2(u[i], u[i + 1], cc);
 }
 
-// Min and max of the whole row: 64 values here, three at a time (exact),
-// then (PAIR) the partner's.
+// Min and max of the whole row: 64 values here in four chains of 16, three
+// values per instruction (exact, so the order is free), then (PAIR) the
+// partner's.  The chains keep only eight partial results live beside u.
 template <bool PAIR = true>
 __device__ __forceinline__ void half_min_max(const float (&u)[kHalfRow], float& mn, float& mx) {
-  float lo[22], hi[22];
+  float lo[4], hi[4];
 #pragma unroll
-  for (int i = 0; i < 21; ++i) {
-    lo[i] = min3(u[3 * i], u[3 * i + 1], u[3 * i + 2]);
-    hi[i] = max3(u[3 * i], u[3 * i + 1], u[3 * i + 2]);
+  for (int c = 0; c < 4; ++c) {
+    lo[c] = min3(u[16 * c], u[16 * c + 1], u[16 * c + 2]);
+    hi[c] = max3(u[16 * c], u[16 * c + 1], u[16 * c + 2]);
   }
-  lo[21] = u[63];
-  hi[21] = u[63];
 #pragma unroll
-  for (int i = 0; i < 7; ++i) {
-    lo[i] = min3(lo[3 * i], lo[3 * i + 1], lo[3 * i + 2]);
-    hi[i] = max3(hi[3 * i], hi[3 * i + 1], hi[3 * i + 2]);
+  for (int k = 3; k < 15; k += 2) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      lo[c] = min3(lo[c], u[16 * c + k], u[16 * c + k + 1]);
+      hi[c] = max3(hi[c], u[16 * c + k], u[16 * c + k + 1]);
+    }
   }
-  lo[7] = lo[21];
-  hi[7] = hi[21];
-  mn = fminf(min3(lo[0], lo[1], lo[2]), min3(lo[3], lo[4], fminf(lo[5], fminf(lo[6], lo[7]))));
-  mx = fmaxf(max3(hi[0], hi[1], hi[2]), max3(hi[3], hi[4], fmaxf(hi[5], fmaxf(hi[6], hi[7]))));
+  // element 15 of each chain joins the final combination
+  mn = fminf(min3(min3(lo[0], lo[1], u[15]), min3(lo[2], lo[3], u[31]), u[47]), u[63]);
+  mx = fmaxf(max3(max3(hi[0], hi[1], u[15]), max3(hi[2], hi[3], u[31]), u[47]), u[63]);
   if (PAIR) {
     mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
