@@ -67,10 +67,7 @@ constexpr int kRawOk = kRawVM + kBN * 4;
 constexpr int kRawBytes = kRawOk + 16;
 constexpr int kMetaBytes = kBN * 16 + 16;          // s_k[64], z_k[64], s_v[64], z_v[64] + ok word
 
-constexpr int kQBytes = kBM * kHeadDim * 2;        // one of q' hi / lo
-constexpr int kOffQh = 0;
-constexpr int kOffQl = kOffQh + kQBytes;
-constexpr int kOffKx = kOffQl + kQBytes;
+constexpr int kOffKx = 0;
 constexpr int kOffVx = kOffKx + 2 * kKxBytes;
 constexpr int kOffRaw = kOffVx + 2 * kVxBytes;
 constexpr int kOffMeta = kOffRaw + kRawStages * kRawBytes;
@@ -89,11 +86,15 @@ static_assert(kRawBytes % 16 == 0 && kMetaBytes % 16 == 0 && kOffBar % 8 == 0, "
 // K/V operand buffers (free before the first tile and after the last)
 static_assert(2 * kKxBytes + 2 * kVxBytes >= kBM * kHeadDim * 4, "exchange space");
 // tensor memory: S (2 x 64 columns), O (128), P (2 x 32 columns of binary16
-// pairs); q' hi and lo are shared-memory operands
-constexpr uint32_t kTmemCols = 512;  // 320 used
+// pairs), and the A operands q' hi and lo (64 columns of binary16 pairs
+// each): the score products read only K from shared memory
+constexpr uint32_t kTmemCols = 512;  // 448 used
 constexpr uint32_t kColO = 128;
 constexpr uint32_t kColP = 256;
-constexpr int kSoftBar = 1;                         // named barrier id of the softmax warps
+constexpr uint32_t kColQh = 320;
+constexpr uint32_t kColQl = 384;
+// named barriers 1 .. 4: softmax warps w and w + 4, which share rows 32w .. 32w+31
+constexpr int kSoftBar = 1;
 
 // 2^e for -126 <= e <= 127, exactly
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
@@ -128,14 +129,15 @@ __device__ __forceinline__ void t_set(float (&t)[32], int j, float x) {
   for (int k = 0; k < 32; ++k) t[k] = (j == k) ? x : t[k];
 }
 
-// The softmax warps' barrier; returns the AND of `ok` over its threads.
+// The barrier of the two softmax warps that share this thread's rows;
+// returns the AND of `ok` over their threads.
 __device__ __forceinline__ bool soft_sync_and(bool ok) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
       "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(uint32_t(ok)), "r"(kSoftBar), "r"(32 * kSoftWarps)
+      : "r"(uint32_t(ok)), "r"(kSoftBar + int((threadIdx.x >> 5) & 3)), "r"(64)
       : "memory");
   return r != 0;
 }
@@ -323,13 +325,11 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (warp < kSoftWarps) {
-    // q' as the A operand in shared memory (K-major core matrices): row r,
-    // dims 64h .. 64h+63 = 8-dim chunks 8h .. 8h+7
-    uint8_t* qh = smem + kOffQh + r * 16;
-    uint8_t* qlo = smem + kOffQl + r * 16;
+    // q' as the A operand in tensor memory: row r in lane r, dims (2j, 2j+1)
+    // in column j; this thread's dims 64h .. 64h+63 fill columns 32h .. 32h+31
+    const uint32_t trow = tmem + (uint32_t(32 * (warp & 3)) << 16) + 32 * half;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const int kc = 8 * half + kk;
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -338,10 +338,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         hw[m] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
         lw[m] = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
       }
-      *reinterpret_cast<uint4*>(qh + kc * 2048) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(qlo + kc * 2048) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      tmem_st4u(trow + kColQh + 4 * kk, hw);
+      tmem_st4u(trow + kColQl + 4 * kk, lw);
     }
-    fence_async_smem();
+    tmem_wait_st();
   }
   tc_fence_before();
   __syncthreads();
@@ -418,9 +418,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       // operand, 2 x 2048 bytes of V operand
       const uint64_t kxd[2] = {umma_desc(kx0, 1024, 128), umma_desc(kx0 + kKxBytes, 1024, 128)};
       const uint64_t vxd[2] = {umma_desc(vx0, 2048, 128), umma_desc(vx0 + kVxBytes, 2048, 128)};
-      constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 2048) >> 4, kQStep = (2 * 2048) >> 4;
-      const uint64_t qhd = umma_desc(smem_u32(smem + kOffQh), 2048, 128);
-      const uint64_t qld = umma_desc(smem_u32(smem + kOffQl), 2048, 128);
+      constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 2048) >> 4;
       // Both products are issued as soon as their operands are ready,
       // polling the barriers without blocking or sleeping (a sleep's wake-up
       // is far coarser than an MMA): S(i+1) needs the K operand of tile i+1,
@@ -438,10 +436,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
           const uint64_t bd = kxd[b];
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            umma_f16(sd, qhd + ks * kQStep, bd + ks * kKxStep, idS, ks > 0);
+            umma_f16_ta(sd, tmem + kColQh + 8 * ks, bd + ks * kKxStep, idS, ks > 0);
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            umma_f16(sd, qld + ks * kQStep, bd + ks * kKxStep, idS, true);
+            umma_f16_ta(sd, tmem + kColQl + 8 * ks, bd + ks * kKxStep, idS, true);
           umma_commit(&bars[kSFull + b]);
           umma_commit(&bars[kKxEmpty + b]);
           ++nS;
@@ -465,6 +463,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         } else if (clock64() - t_last > kWaitLimitCycles) {
           ok = false;
           break;
+        } else {
+          __nanosleep(20);  // leave the scheduler's issue slots to the other roles
         }
       }
       if (!ok) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
@@ -584,16 +584,21 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       // row sees whole (nearly all), compact with the mask for the others --
       // the warps of four roles share each scheduler's instruction cache
       if (all_vis) {
+        // two keys per instruction: t = s_k acc + (qc z_k)
+        const float2 qc2 = make_float2(qc, qc);
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4) {
           const float4 sk = msk[kq / 4 + g4], zk = mzk[kq / 4 + g4];
-          const float skk[4] = {sk.x, sk.y, sk.z, sk.w}, zkk[4] = {zk.x, zk.y, zk.z, zk.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * g4 + e;
-            t[j] = fmaf(skk[e], t[j], qc * zkk[e]);
-            tm[e] = fmaxf(tm[e], t[j]);
-          }
+          const int j = 4 * g4;
+          const float2 a = fma2(make_float2(sk.x, sk.y), make_float2(t[j], t[j + 1]),
+                                mul2(qc2, make_float2(zk.x, zk.y)));
+          const float2 b = fma2(make_float2(sk.z, sk.w), make_float2(t[j + 2], t[j + 3]),
+                                mul2(qc2, make_float2(zk.z, zk.w)));
+          t[j] = a.x;
+          t[j + 1] = a.y;
+          t[j + 2] = b.x;
+          t[j + 3] = b.y;
+          tm[g4 & 3] = fmaxf(tm[g4 & 3], fmaxf(fmaxf(a.x, a.y), fmaxf(b.x, b.y)));
         }
       } else {
         const float* fsk = reinterpret_cast<const float*>(msk) + kq;
@@ -638,26 +643,34 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       uint32_t pw[16];
       float la[4] = {0.0f, 0.0f, 0.0f, 0.0f}, za[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if (all_vis) {
+        // two keys per instruction (each lane the same RN steps as one key)
+        const float2 rowA2 = make_float2(rowA, rowA), nmu2 = make_float2(nmu, nmu);
+        float2 la01 = make_float2(0.0f, 0.0f), la23 = la01, za01 = la01, za23 = la01;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          float ps[8];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int g4 = 2 * kk + hh;
-            const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
-            const float svv[4] = {sv.x, sv.y, sv.z, sv.w}, zvv[4] = {zv.x, zv.y, zv.z, zv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * g4 + e;
-              const float pr = ex2(fmaf(rowA, t[j], nmu));
-              la[e] += pr;
-              za[e] = fmaf(pr, zvv[e], za[e]);
-              ps[4 * hh + e] = pr * svv[e];
-            }
-          }
-#pragma unroll
-          for (int m = 0; m < 4; ++m) pw[4 * kk + m] = pack_half2(ps[2 * m], ps[2 * m + 1]);
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
+          const int j = 4 * g4;
+          const float2 xa = fma2(rowA2, make_float2(t[j], t[j + 1]), nmu2);
+          const float2 xb = fma2(rowA2, make_float2(t[j + 2], t[j + 3]), nmu2);
+          const float2 pa = make_float2(ex2(xa.x), ex2(xa.y));
+          const float2 pb = make_float2(ex2(xb.x), ex2(xb.y));
+          la01 = add2(la01, pa);
+          la23 = add2(la23, pb);
+          za01 = fma2(pa, make_float2(zv.x, zv.y), za01);
+          za23 = fma2(pb, make_float2(zv.z, zv.w), za23);
+          const float2 sa = mul2(pa, make_float2(sv.x, sv.y));
+          const float2 sb = mul2(pb, make_float2(sv.z, sv.w));
+          pw[2 * g4] = pack_half2(sa.x, sa.y);
+          pw[2 * g4 + 1] = pack_half2(sb.x, sb.y);
         }
+        la[0] = la01.x;
+        la[1] = la01.y;
+        la[2] = la23.x;
+        la[3] = la23.y;
+        za[0] = za01.x;
+        za[1] = za01.y;
+        za[2] = za23.x;
+        za[3] = za23.y;
       } else {
         const float* fsv = reinterpret_cast<const float*>(msv) + kq;
         const float* fzv = reinterpret_cast<const float*>(mzv) + kq;
@@ -697,7 +710,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         mbar_arrive(&bars[kMetaEmpty + b]);
       }
     }
-    if (failed && lane == 0 && warp == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+    if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
     // ---- epilogue: this half of the output row from tensor memory, code
     // scale, sum(p z) and l over both halves, normalise, inverse V rotation
     const int last = n_tiles - 1;

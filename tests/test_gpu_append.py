@@ -67,10 +67,12 @@ def test_ragged_strided_shuffled(P, hkv, size):
     assert_bytes_equal(vc, vr, "V cache")
 
 
-@pytest.mark.parametrize("T", [40, 5000], ids=["warp", "tiled"])
+@pytest.mark.parametrize("T", [40, 5000, 160000], ids=["warp", "tiled", "tiled-many-per-warp"])
 def test_k_only_and_bad_slots(T):
     """K only; a slot one past the end and a negative slot are reported and
-    skipped, padding (-1) is skipped silently, every other row is stored."""
+    skipped, padding (-1) is skipped silently, every other row is stored.
+    At 160000 tokens every warp of the tiled kernel takes several row tiles,
+    so its K-only ring wraps."""
     wl = W.TINY
     P = 16
     num_pages = -(-T // P)
