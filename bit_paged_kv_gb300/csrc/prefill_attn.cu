@@ -23,10 +23,10 @@
 //            accumulator in tensor memory when the max grows, and write p*s_V
 //            as the binary16 A operand of the P.V product; at the end they
 //            normalise, inverse-rotate V and store.
-//      8-11  expanders: widen a raw INT4 tile into the K operand (keys x
-//            dims) and the transposed V operand (dims x keys), each code n
-//            as the binary16 subnormal n * 2^-24 (exact), and unpack the
-//            tile's (s, z) metadata (binary16 or bfloat16) to binary32.
+//      8-11  expanders: widen a raw INT4 tile into the K and V operands
+//            (both keys x dims, the same layout), each code n as the
+//            binary16 subnormal n * 2^-24 (exact), and unpack the tile's
+//            (s, z) metadata (binary16 or bfloat16) to binary32.
 //      12    producer: 16-key slices (codes and metadata of K and V) through
 //            a 4-stage ring with the bulk-copy engine.
 //      13    MMA: one thread issues S = Q' K^T (M 128, N 64, K 128; q' hi and
@@ -34,7 +34,8 @@
 //            K 64) with tcgen05.mma, and signals completion with
 //            tcgen05.commit; the warp also allocates the 256 tensor-memory
 //            columns (S double-buffered at columns 0 and 64, O at 128).
-//  * Operands are K-major, unswizzled, in 8-row x 16-byte core matrices.
+//  * Operands are unswizzled 8-row x 16-byte core matrices: K-major, except
+//    V, which the P.V product reads MN-major (dims contiguous per key).
 //    Every mbarrier wait is bounded to about a second; the softmax warps,
 //    which also meet at a named barrier, never leave their loop early (a
 //    failed wait only marks the result), so that barrier always completes.
@@ -57,7 +58,7 @@ constexpr int kWarpMma = kSoftWarps + 5;
 constexpr uint32_t kAllLanes = 0xFFFFFFFFu;
 
 constexpr int kKxBytes = kBN * kHeadDim * 2;       // K operand of one tile
-constexpr int kVxBytes = kHeadDim * kBN * 2;       // V^T operand of one tile
+constexpr int kVxBytes = kBN * kHeadDim * 2;       // V operand of one tile
 constexpr int kRawCodes = kBN * (kHeadDim / 2);    // 4096 code bytes per tensor
 // raw stage: K codes | V codes | K meta | V meta | slice-ok word
 constexpr int kRawV = kRawCodes;
@@ -202,6 +203,29 @@ __device__ __forceinline__ bool wait_sleep(uint64_t* bar, uint32_t parity) {
 }
 __device__ __forceinline__ bool wait_sleep_all(uint64_t* bar, uint32_t parity) {
   return __all_sync(kAllLanes, wait_sleep(bar, parity));
+}
+
+// One expander thread's share of widening a tile's 64 x 128 codes into a
+// binary16 operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2,
+// each code n as the subnormal n * 2^-24 (exact).  Thread te takes key
+// te % 64 and dims 64 (te / 64) .. + 63 in two 16-byte pieces of codes.
+__device__ __forceinline__ void widen_codes(const uint8_t* codes, uint8_t* dst, int te) {
+  const int n = te & 63, hk = te >> 6;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int q = (2 * hk + s + (n >> 1)) & 3;  // 16-byte piece: dims 32q .. 32q+31
+    const uint4 w = *reinterpret_cast<const uint4*>(codes + n * 64 + 16 * q);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      // byte m of the word holds dims 2m (low nibble) and 2m+1: one
+      // permute per pair from the low- and high-nibble planes
+      const uint32_t lo = ws[u] & 0x0F0F0F0Fu, hi = (ws[u] >> 4) & 0x0F0F0F0Fu;
+      *reinterpret_cast<uint4*>(dst + (4 * q + u) * 1024 + n * 16) =
+          make_uint4(prmt(lo, hi, kPairSel[0]), prmt(lo, hi, kPairSel[1]),
+                     prmt(lo, hi, kPairSel[2]), prmt(lo, hi, kPairSel[3]));
+    }
+  }
 }
 
 // F16IN: q is binary16 (else bfloat16); BFM: the caches' (scale, zero)
@@ -412,13 +436,17 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
     if (lane == 0) {
       const uint32_t kx0 = smem_u32(smem + kOffKx), vx0 = smem_u32(smem + kOffVx);
       constexpr uint32_t idS = umma_idesc_f16(kBM, kBN);
-      constexpr uint32_t idO = umma_idesc_f16(kBM, kHeadDim);
+      // V is the B operand in MN-major form (keys x dims, dims contiguous):
+      // the same shared-memory layout as the K operand
+      constexpr uint32_t idO = umma_idesc_f16(kBM, kHeadDim) | kUmmaBMnMajor;
       // descriptors built once: a K step only advances the start address
       // (in 16-byte units, the descriptor's low field): 2 x 1024 bytes of K
       // operand, 2 x 2048 bytes of V operand
       const uint64_t kxd[2] = {umma_desc(kx0, 1024, 128), umma_desc(kx0 + kKxBytes, 1024, 128)};
-      const uint64_t vxd[2] = {umma_desc(vx0, 2048, 128), umma_desc(vx0 + kVxBytes, 2048, 128)};
-      constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 2048) >> 4;
+      // MN-major: the next 8 keys (K) are 128 bytes on, the next 8 dims (N)
+      // 1024 bytes on; a K = 16 step advances 256 bytes
+      const uint64_t vxd[2] = {umma_desc(vx0, 128, 1024), umma_desc(vx0 + kVxBytes, 128, 1024)};
+      constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 128) >> 4;
       // Both products are issued as soon as their operands are ready,
       // polling the barriers without blocking or sleeping (a sleep's wake-up
       // is far coarser than an MMA): S(i+1) needs the K operand of tile i+1,
@@ -498,53 +526,14 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       if (lane == 0) mbar_arrive(&bars[kMetaFull + b]);
       // K operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2
       if (i >= 2 && !wait_sleep_all(&bars[kKxEmpty + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
-      {
-        uint8_t* kx = smem + kOffKx + b * kKxBytes;
-        const int n = te & 63, hk = te >> 6;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const int q = (2 * hk + s + (n >> 1)) & 3;  // 16-byte piece: dims 32q .. 32q+31
-          const uint4 w = *reinterpret_cast<const uint4*>(st + n * 64 + 16 * q);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            // byte m of the word holds dims 2m (low nibble) and 2m+1: one
-            // permute per pair from the low- and high-nibble planes
-            const uint32_t lo = ws[u] & 0x0F0F0F0Fu, hi = (ws[u] >> 4) & 0x0F0F0F0Fu;
-            *reinterpret_cast<uint4*>(kx + (4 * q + u) * 1024 + n * 16) =
-                make_uint4(prmt(lo, hi, kPairSel[0]), prmt(lo, hi, kPairSel[1]),
-                           prmt(lo, hi, kPairSel[2]), prmt(lo, hi, kPairSel[3]));
-          }
-        }
-      }
+      widen_codes(st, smem + kOffKx + b * kKxBytes, te);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kKxFull + b]);
-      // V^T operand: element (dim d, key k) at (k/8)*2048 + d*16 + (k%8)*2
+      // V operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2, the
+      // K operand's layout (read by the P.V product as MN-major)
       if (i >= 2 && !wait_sleep_all(&bars[kPvDone + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
-      {
-        uint8_t* vx = smem + kOffVx + b * kVxBytes;
-        const int dq = te & 15, kc = te >> 4;  // dims 8dq .. 8dq+7, keys 8kc .. 8kc+7
-        // nibble planes of the 8 keys' words: even dims (low nibbles) and odd
-        uint32_t lo[8], hi[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(st + kRawV + (8 * kc + j) * 64 + 4 * dq);
-          lo[j] = w & 0x0F0F0F0Fu;
-          hi[j] = (w >> 4) & 0x0F0F0F0Fu;
-        }
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const int e = (s + lane) & 7;  // rotating the dims spreads the stores over all banks
-          // dim 8dq+e is byte e/2 of each key's word, plane e&1; pair keys (2m, 2m+1)
-          const uint32_t sel = kPairSel[0] + 0x1111u * uint32_t(e >> 1);
-          uint32_t c[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            c[m] = (e & 1) ? prmt(hi[2 * m], hi[2 * m + 1], sel) : prmt(lo[2 * m], lo[2 * m + 1], sel);
-          *reinterpret_cast<uint4*>(vx + kc * 2048 + (8 * dq + e) * 16) = make_uint4(c[0], c[1], c[2], c[3]);
-        }
-      }
+      widen_codes(st + kRawV, smem + kOffVx + b * kVxBytes, te);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {

@@ -32,6 +32,10 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// Instruction-descriptor bit for a B operand stored MN-major (N contiguous)
+// instead of K-major.
+constexpr uint32_t kUmmaBMnMajor = 1u << 16;
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // one warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
                "r"(ncols)
