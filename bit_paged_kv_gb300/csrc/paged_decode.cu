@@ -54,6 +54,11 @@ constexpr int kCtasPerSm = kWarps == 16 ? 1 : 2;      // 128 registers per threa
 static_assert(kWarps == 16 || kWarps == 8, "decode CTAs have 16 or 8 warps");
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // dim d of a reduction row sits at d + d / 16: the stores (lane group g
 // writes dims (D/8) g + ..) and the per-dim reads are then free of bank
 // conflicts
@@ -301,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   // the step (and its row) that holds the new token, for the patch
   const int new_local = new_tok - p_begin * P;
   const int new_step = owner ? new_local / kStepTok : -1;
+  // this warp's tile index of that step (-1: another warp's, or none)
+  const int new_i = (new_step >= warp && (new_step - warp) % kWarps == 0) ? (new_step - warp) / kWarps : -1;
 
   // ---- b = 2^S q', q' = (1/sqrt h) H q for the group's heads, as binary16
   // hi + lo parts (b = hi + lo to ~22 bits; zeros beyond G).  Warp h < 8
@@ -442,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const int hb = PACKED ? 2 * (c & 1) : 2 * c;
   const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
   const float skA = qsum[kMaxGroup + hb] * p.q_scale, skB = qsum[kMaxGroup + hb + 1] * p.q_scale;
+  const float2 skAB = make_float2(skA, skB), qsAB = make_float2(qsA, qsB);
 
   constexpr int kMT = DM::kMT;
   float acc[kMT][4];
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     if (!__all_sync(kFull, ok)) return false;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      if (APPEND && warp + (i + t) * kWarps == new_step) {
+      if (APPEND && i + t == new_i) {
         // replace the copied row of the new token by its freshly quantized one
         const int row = new_local % kStepTok;
         uint8_t* w = ring + ((i + t) % kStages) * C::kStage;
@@ -555,10 +563,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8));
       const float s0 = meta_lo(mk0, BFM), z0 = meta_hi(mk0, BFM);
       const float s1 = meta_lo(mk1, BFM), z1 = meta_hi(mk1, BFM);
-      sc[t][0] = fmaf(s0 * skA, d[0], z0 * qsA);
-      sc[t][1] = fmaf(s0 * skB, d[1], z0 * qsB);
-      sc[t][2] = fmaf(s1 * skA, d[2], z1 * qsA);
-      sc[t][3] = fmaf(s1 * skB, d[3], z1 * qsB);
+      {
+        // heads (A, B) of rows g and g + 8, two per instruction
+        const float2 r0 = fma2(mul2(make_float2(s0, s0), skAB), make_float2(d[0], d[1]),
+                               mul2(make_float2(z0, z0), qsAB));
+        const float2 r1 = fma2(mul2(make_float2(s1, s1), skAB), make_float2(d[2], d[3]),
+                               mul2(make_float2(z1, z1), qsAB));
+        sc[t][0] = r0.x;
+        sc[t][1] = r0.y;
+        sc[t][2] = r1.x;
+        sc[t][3] = r1.y;
+      }
       if (!full[t]) {  // the tile holding the end of the sequence, or a bad page
         sc[t][0] = v0[t] ? sc[t][0] : -INFINITY;
         sc[t][1] = v0[t] ? sc[t][1] : -INFINITY;
@@ -568,11 +583,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     }
 
     // ---- online softmax: rescale only when a running max grows
-    float mloc0 = fmaxf(sc[0][0], sc[0][2]), mloc1 = fmaxf(sc[0][1], sc[0][3]);
-#pragma unroll
-    for (int t = 1; t < NT; ++t) {
-      mloc0 = fmaxf(mloc0, fmaxf(sc[t][0], sc[t][2]));
-      mloc1 = fmaxf(mloc1, fmaxf(sc[t][1], sc[t][3]));
+    float mloc0, mloc1;
+    if (NT == 2) {
+      mloc0 = fmaxf(fmax3(sc[0][0], sc[0][2], sc[1][0]), sc[1][2]);
+      mloc1 = fmaxf(fmax3(sc[0][1], sc[0][3], sc[1][1]), sc[1][3]);
+    } else {
+      mloc0 = fmaxf(sc[0][0], sc[0][2]);
+      mloc1 = fmaxf(sc[0][1], sc[0][3]);
     }
 #pragma unroll
     for (int x = 4; x < 32; x <<= 1) {
@@ -585,27 +602,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       const float al1 = ex2(m_run[1] - ((mn1 == -INFINITY) ? 0.0f : mn1));
       m_run[0] = mn0;
       m_run[1] = mn1;
-      l_run[0] *= al0;
-      l_run[1] *= al1;
-      z_run[0] *= al0;
-      z_run[1] *= al1;
+      const float2 al = make_float2(al0, al1);  // columns 0, 2 are head A, 1, 3 head B
+      const float2 lz = mul2(make_float2(l_run[0], l_run[1]), al);
+      const float2 zz = mul2(make_float2(z_run[0], z_run[1]), al);
+      l_run[0] = lz.x;
+      l_run[1] = lz.y;
+      z_run[0] = zz.x;
+      z_run[1] = zz.y;
 #pragma unroll
       for (int k = 0; k < kMT; ++k) {
-        acc[k][0] *= al0;
-        acc[k][1] *= al1;
-        acc[k][2] *= al0;
-        acc[k][3] *= al1;
+        const float2 a01 = mul2(make_float2(acc[k][0], acc[k][1]), al);
+        const float2 a23 = mul2(make_float2(acc[k][2], acc[k][3]), al);
+        acc[k][0] = a01.x;
+        acc[k][1] = a01.y;
+        acc[k][2] = a23.x;
+        acc[k][3] = a23.y;
       }
     }
     const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
     const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
+    const float2 nmu = make_float2(-mu0, -mu1);  // x - mu = x + (-mu), exactly
 
     // ---- probabilities, V terms, and the PV products
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const uint8_t* vst = ring + ((i + t) % kStages) * C::kStage + C::kHalf;
-      const float p0 = ex2(sc[t][0] - mu0), p1 = ex2(sc[t][1] - mu1);
-      const float p2 = ex2(sc[t][2] - mu0), p3 = ex2(sc[t][3] - mu1);
+      const float2 x01 = add2(make_float2(sc[t][0], sc[t][1]), nmu);
+      const float2 x23 = add2(make_float2(sc[t][2], sc[t][3]), nmu);
+      const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+      const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
       const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g));
       const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8));
       float sv0 = meta_lo(mv0, BFM), zv0 = meta_hi(mv0, BFM);
@@ -616,14 +641,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         sv1 = v1[t] ? sv1 : 0.0f;
         zv1 = v1[t] ? zv1 : 0.0f;
       }
-      l_run[0] += p0 + p2;
-      l_run[1] += p1 + p3;
-      z_run[0] += p0 * zv0 + p2 * zv1;
-      z_run[1] += p1 * zv0 + p3 * zv1;
+      {
+        const float2 l2 = add2(make_float2(l_run[0], l_run[1]), add2(p01, p23));
+        const float2 z2 = add2(make_float2(z_run[0], z_run[1]),
+                               fma2(p23, make_float2(zv1, zv1), mul2(p01, make_float2(zv0, zv0))));
+        l_run[0] = l2.x;
+        l_run[1] = l2.y;
+        z_run[0] = z2.x;
+        z_run[1] = z2.y;
+      }
       // (p*s) for this thread's columns over tokens (g, g+8) as binary16.
       // PACKED: lanes c >= 2 repeat the heads of lanes c - 2, so output
       // columns 4-7 duplicate 0-3 and are never read.
-      const float ps0 = p0 * sv0, ps1 = p1 * sv0, ps2 = p2 * sv1, ps3 = p3 * sv1;
+      const float2 ps01 = mul2(p01, make_float2(sv0, sv0));
+      const float2 ps23 = mul2(p23, make_float2(sv1, sv1));
+      const float ps0 = ps01.x, ps1 = ps01.y, ps2 = ps23.x, ps3 = ps23.y;
       const uint32_t X = pack_half2(ps0, ps2);
       const uint32_t Y = pack_half2(ps1, ps3);
       // PV k-columns (2c, 2c+1, 2c+8, 2c+9) carry tokens (c, c+4, c+8, c+12):
