@@ -612,14 +612,21 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         // rescale this half of the output rows, after the previous P.V
         tc_fence_after();
         const float a = grow ? ex2(m_run - tmax) : 1.0f;
+        const float2 a2 = make_float2(a, a);
+        // eight columns at a time: few registers live beside the scores
 #pragma unroll
-        for (int cblk = 0; cblk < 2; ++cblk) {
-          float o[32];
-          tmem_ld32(trow + kColO + 64 * half + 32 * cblk, o);
+        for (int cblk = 0; cblk < 8; ++cblk) {
+          float o[8];
+          tmem_ld8(trow + kColO + 64 * half + 8 * cblk, o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= a;
-          tmem_st32(trow + kColO + 64 * half + 32 * cblk, o);
+          for (int j = 0; j < 8; j += 2) {
+            const float2 v = mul2(make_float2(o[j], o[j + 1]), a2);
+            o[j] = v.x;
+            o[j + 1] = v.y;
+          }
+          tmem_st8(trow + kColO + 64 * half + 8 * cblk, o);
         }
+        tmem_wait_st();
       }
       if (grow) {
         const float a = ex2(m_run - tmax);  // 0 while m_run is -inf
@@ -706,15 +713,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
     wait_soft(&bars[kPvDone + (last & 1)], (last >> 1) & 1, failed);
     tc_fence_after();
     float v[64];
-    {
-      float o[32];
-      tmem_ld32(trow + kColO + 64 * half, o);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = o[j];
-      tmem_ld32(trow + kColO + 64 * half + 32, o);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[32 + j] = o[j];
-    }
+    for (int cblk = 0; cblk < 8; ++cblk)
+      tmem_ld8(trow + kColO + 64 * half + 8 * cblk, *reinterpret_cast<float(*)[8]>(v + 8 * cblk));
     xl[half * kBM + r] = make_float2(l_run, pz);
     (void)soft_sync_and(true);
     const float2 ot = xl[(1 - half) * kBM + r];
