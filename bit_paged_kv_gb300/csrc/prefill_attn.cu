@@ -39,6 +39,8 @@
 //    Every mbarrier wait is bounded to about a second; the softmax warps,
 //    which also meet at a named barrier, never leave their loop early (a
 //    failed wait only marks the result), so that barrier always completes.
+#include <type_traits>
+
 #include "saw_device.cuh"
 #include "saw_int4.h"
 #include "saw_quant_row.cuh"
@@ -115,19 +117,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// t[j] for a runtime j (the masked, non-unrolled loops) without sending the
-// array to local memory: a select chain over the 32 registers.
-__device__ __forceinline__ float t_at(const float (&t)[32], int j) {
-  float x = t[0];
-#pragma unroll
-  for (int k = 1; k < 32; ++k) x = (j == k) ? t[k] : x;
-  return x;
-}
-__device__ __forceinline__ void t_set(float (&t)[32], int j, float x) {
-#pragma unroll
-  for (int k = 0; k < 32; ++k) t[k] = (j == k) ? x : t[k];
 }
 
 // The barrier of the two softmax warps that share this thread's rows;
@@ -569,37 +558,46 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       const int k0 = i * kBN + kq;
       const bool all_vis = ((okm >> (2 * half)) & 3) == 3 && pos_r >= k0 + 31;
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      // two copies of each loop: fully unrolled with no mask for the tiles a
-      // row sees whole (nearly all), compact with the mask for the others --
-      // the warps of four roles share each scheduler's instruction cache
-      if (all_vis) {
-        // two keys per instruction: t = s_k acc + (qc z_k)
+      // Visible keys of this thread as bits of vm (bit j: key kq + j is at or
+      // before the row's position and on a page that was copied).  Each loop
+      // below has two unrolled copies: without the mask for the tiles a row
+      // sees whole (nearly all), with it for the others.
+      uint32_t vm = 0xFFFFFFFFu;
+      if (!all_vis) {
+        const int lim = pos_r - k0;  // keys j <= lim are at or before the row
+        vm = lim >= 31 ? 0xFFFFFFFFu : (lim < 0 ? 0u : (2u << lim) - 1u);
+        const int sl = (okm >> (2 * half)) & 3;  // 16-key slices 2h, 2h+1 copied
+        vm &= ((sl & 1) ? 0x0000FFFFu : 0u) | ((sl & 2) ? 0xFFFF0000u : 0u);
+      }
+      // t = s_k acc + (qc z_k), two keys per instruction; masked keys -inf
+      auto logits = [&](auto maskc) {
+        constexpr bool kMask = decltype(maskc)::value;
         const float2 qc2 = make_float2(qc, qc);
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4) {
           const float4 sk = msk[kq / 4 + g4], zk = mzk[kq / 4 + g4];
           const int j = 4 * g4;
-          const float2 a = fma2(make_float2(sk.x, sk.y), make_float2(t[j], t[j + 1]),
-                                mul2(qc2, make_float2(zk.x, zk.y)));
-          const float2 b = fma2(make_float2(sk.z, sk.w), make_float2(t[j + 2], t[j + 3]),
-                                mul2(qc2, make_float2(zk.z, zk.w)));
+          float2 a = fma2(make_float2(sk.x, sk.y), make_float2(t[j], t[j + 1]),
+                          mul2(qc2, make_float2(zk.x, zk.y)));
+          float2 b = fma2(make_float2(sk.z, sk.w), make_float2(t[j + 2], t[j + 3]),
+                          mul2(qc2, make_float2(zk.z, zk.w)));
+          if (kMask) {
+            a.x = ((vm >> j) & 1u) ? a.x : -INFINITY;
+            a.y = ((vm >> (j + 1)) & 1u) ? a.y : -INFINITY;
+            b.x = ((vm >> (j + 2)) & 1u) ? b.x : -INFINITY;
+            b.y = ((vm >> (j + 3)) & 1u) ? b.y : -INFINITY;
+          }
           t[j] = a.x;
           t[j + 1] = a.y;
           t[j + 2] = b.x;
           t[j + 3] = b.y;
           tm[g4 & 3] = fmaxf(tm[g4 & 3], fmaxf(fmaxf(a.x, a.y), fmaxf(b.x, b.y)));
         }
-      } else {
-        const float* fsk = reinterpret_cast<const float*>(msk) + kq;
-        const float* fzk = reinterpret_cast<const float*>(mzk) + kq;
-#pragma unroll 1
-        for (int j = 0; j < 32; ++j) {
-          const bool vis = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
-          const float x = vis ? fmaf(fsk[j], t_at(t, j), qc * fzk[j]) : -INFINITY;
-          t_set(t, j, x);
-          tm[0] = fmaxf(tm[0], x);
-        }
-      }
+      };
+      if (all_vis)
+        logits(std::false_type{});
+      else
+        logits(std::true_type{});
       // row max over both halves
       const float th = rowA * fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
       xm[(b * 2 + half) * kBM + r] = th;
@@ -638,14 +636,23 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       // p*s_V, binary16 pairs, into this lane's P columns: keys kq .. kq+31
       uint32_t pw[16];
       float la[4] = {0.0f, 0.0f, 0.0f, 0.0f}, za[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (all_vis) {
-        // two keys per instruction (each lane the same RN steps as one key)
+      // p = 2^(rowA t - m), two keys per instruction (each lane the same RN
+      // steps as one key).  Masked keys have p = 0, and their (s_V, z_V) are
+      // taken as 0: rows past the end may hold anything, even inf.
+      auto probs = [&](auto maskc) {
+        constexpr bool kMask = decltype(maskc)::value;
         const float2 rowA2 = make_float2(rowA, rowA), nmu2 = make_float2(nmu, nmu);
         float2 la01 = make_float2(0.0f, 0.0f), la23 = la01, za01 = la01, za23 = la01;
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4) {
-          const float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
+          float4 sv = msv[kq / 4 + g4], zv = mzv[kq / 4 + g4];
           const int j = 4 * g4;
+          if (kMask) {
+            const bool l0 = (vm >> j) & 1u, l1 = (vm >> (j + 1)) & 1u;
+            const bool l2 = (vm >> (j + 2)) & 1u, l3 = (vm >> (j + 3)) & 1u;
+            sv = make_float4(l0 ? sv.x : 0.0f, l1 ? sv.y : 0.0f, l2 ? sv.z : 0.0f, l3 ? sv.w : 0.0f);
+            zv = make_float4(l0 ? zv.x : 0.0f, l1 ? zv.y : 0.0f, l2 ? zv.z : 0.0f, l3 ? zv.w : 0.0f);
+          }
           const float2 xa = fma2(rowA2, make_float2(t[j], t[j + 1]), nmu2);
           const float2 xb = fma2(rowA2, make_float2(t[j + 2], t[j + 3]), nmu2);
           const float2 pa = make_float2(ex2(xa.x), ex2(xa.y));
@@ -667,34 +674,11 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         za[1] = za01.y;
         za[2] = za23.x;
         za[3] = za23.y;
-      } else {
-        const float* fsv = reinterpret_cast<const float*>(msv) + kq;
-        const float* fzv = reinterpret_cast<const float*>(mzv) + kq;
-#pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t c[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float ps2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int j = 8 * kk + 2 * m + e;
-              const float pr = ex2(fmaf(rowA, t_at(t, j), nmu));  // 0 for masked keys
-              // keys past the end may hold anything: their terms are selected away
-              const bool live = (k0 + j <= pos_r) && ((okm >> ((kq + j) >> 4)) & 1);
-              la[0] += pr;
-              za[0] += live ? pr * fzv[j] : 0.0f;
-              ps2[e] = live ? pr * fsv[j] : 0.0f;
-            }
-            c[m] = pack_half2(ps2[0], ps2[1]);
-          }
-          // (a runtime kk cannot index pw: place the four words by selects)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) pw[4 * u + m] = (u == kk) ? c[m] : pw[4 * u + m];
-        }
-      }
+      };
+      if (all_vis)
+        probs(std::false_type{});
+      else
+        probs(std::true_type{});
       tmem_st16u(trow + kColP + 32 * b + 16 * half, pw);
       tmem_wait_st();
       l_run += (la[0] + la[1]) + (la[2] + la[3]);
