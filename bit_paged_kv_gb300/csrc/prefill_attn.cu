@@ -170,8 +170,13 @@ __device__ __forceinline__ void stride64_step(float (&v)[64], float* scratch_row
   }
 }
 
-// Spinning wait for the softmax warps (on the critical path); a wait after
-// a failure returns at once.
+// The other roles' waiting threads are parked on the mbarrier (woken when
+// its phase completes, or after kSuspendNs to re-check the time limit)
+// rather than polling, leaving their scheduler's issue slots to the softmax
+// warps, which spin (they are on the critical path).
+constexpr uint32_t kSuspendNs = 20000;
+
+// The softmax warps' wait; a wait after a failure returns at once.
 __device__ __forceinline__ bool wait_soft(uint64_t* bar, uint32_t parity, bool& failed) {
   if (failed) return false;
   const bool ok = __all_sync(kAllLanes, mbar_wait_bounded(bar, parity));
@@ -179,16 +184,9 @@ __device__ __forceinline__ bool wait_soft(uint64_t* bar, uint32_t parity, bool& 
   return ok;
 }
 
-// Waits of the other roles sleep between polls, leaving the issue slots of
-// their scheduler to the softmax warps.
+// The other roles' wait.
 __device__ __forceinline__ bool wait_sleep(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-    __nanosleep(64);
-  }
-  return true;
+  return mbar_wait_bounded_for(bar, parity, kSuspendNs);
 }
 __device__ __forceinline__ bool wait_sleep_all(uint64_t* bar, uint32_t parity) {
   return __all_sync(kAllLanes, wait_sleep(bar, parity));
