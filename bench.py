@@ -1100,7 +1100,8 @@ def run_saw(args):
         "fill_s": fill_s,
         "roofline": {
             "bound": "hbm",
-            "kernel": "saw_decode_step: paged_decode_kernel<16, wide (GQA 8), append> "
+            "kernel": "saw_decode_step: paged_decode_kernel<head_dim 128, page 16, wide (GQA 8), "
+                      "append>, 8-warp CTAs, one per (sequence, kv-head) "
                       "(256 new tokens appended, 1.57e6 cached tokens attended per layer)",
             "achieved": achieved,
             "peak": peak,

@@ -170,6 +170,31 @@ __device__ __forceinline__ void stride64_step(float (&v)[64], float* scratch_row
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed
+// may be parked for up to `ns` nanoseconds (woken earlier when the phase
+// completes) instead of returning at once to poll again.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded with the suspend hint on every try.
+__device__ __forceinline__ bool mbar_wait_bounded_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  if (mbar_try_wait_for(bar, parity, ns)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_for(bar, parity, ns)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
 // The other roles' waiting threads are parked on the mbarrier (woken when
 // its phase completes, or after kSuspendNs to re-check the time limit)
 // rather than polling, leaving their scheduler's issue slots to the softmax

@@ -68,31 +68,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase has not completed
-// may be parked for up to `ns` nanoseconds (woken earlier when the phase
-// completes) instead of returning at once to poll again.
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait_bounded with the suspend hint on every try.
-__device__ __forceinline__ bool mbar_wait_bounded_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  if (mbar_try_wait_for(bar, parity, ns)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_for(bar, parity, ns)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  }
-  return true;
-}
-
 // A GPU-scope acquire load (pairs with a release by another CTA).
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
   uint32_t v;
