@@ -2,10 +2,9 @@
 // point for callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc: a plugin or custom op inside an
-// inference server whose framework owns every device allocation, code that
-// runs while a CUDA graph is being captured (allocation is not allowed
-// then), or a latency-critical loop that must not pay cudaMalloc/cudaFree's
-// implicit device synchronisation.  This entry point takes the split-K
+// inference server whose framework owns every device allocation (the
+// plugin may not allocate on its own), or a latency-critical loop that must
+// not pay cudaMalloc/cudaFree's implicit device synchronisation.  This entry point takes the split-K
 // scratch from a fixed array in device memory that the library itself
 // declares, so the caller passes only inputs and outputs.
 //

@@ -240,9 +240,8 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
  * counterpart: this is a deployment convenience of this library.
  *
  * Who needs it: a plugin or custom op whose host framework owns every device
- * allocation, code running while a CUDA graph is captured (no allocation is
- * allowed then), or a latency-critical loop that cannot afford
- * cudaMalloc/cudaFree's device synchronisation.  The split-K scratch comes
+ * allocation (it may not call cudaMalloc itself), or a latency-critical loop
+ * that cannot afford cudaMalloc/cudaFree's device synchronisation.  The split-K scratch comes
  * from a fixed 4 MiB array in device memory declared by the library itself;
  * the caller passes only inputs and outputs (arguments as in
  * saw_paged_decode_int4, without the workspace).
@@ -253,8 +252,7 @@ int32_t saw_decode_step(const void* q, const void* k_new, const void* v_new, voi
  *  - Memory: every GPU that loads the library holds the 4 MiB until the
  *    process exits.  No cudaMalloc/cudaFree is ever called.
  *  - Set-up: the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it.
  *  - Sharing: all calls on a device share the array, so calls whose kernels
  *    may overlap on the GPU (different streams without ordering) race.
  *    Each call first clears the merge's counter words in it

@@ -1,8 +1,8 @@
 """The allocation-free decode entry point, saw_paged_decode_int4_noalloc.
 
 It serves callers that cannot allocate device memory -- a plugin whose host
-framework owns all allocations, code running under CUDA graph capture, or a
-loop that cannot afford cudaMalloc's synchronisation.  Its split-K scratch is
+framework owns all allocations, or a loop that cannot afford cudaMalloc's
+synchronisation.  Its split-K scratch is
 the library's fixed 4 MiB device array instead of a caller workspace.  These
 tests call it through the C-ABI three times in a row on the same inputs (the
 array keeps the previous call's contents, so each call must clear what has
