@@ -64,7 +64,7 @@ int64_t best_splits(int64_t units, int64_t slots, int64_t max_splits) {
 // CTAs, two per SM, so that one CTA's prologue and merge overlap the other's
 // streaming.
 int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int32_t max_seq_len,
-                  int32_t pages_per_split, int32_t head_dim, int32_t* splits_out,
+                  int32_t pages_per_split, int32_t* splits_out,
                   int32_t* pps_out, int32_t* warps_out = nullptr) {
   if (num_seqs < 0 || num_kv_heads <= 0 || !page_size_ok(page_size) || max_seq_len < 0 ||
       pages_per_split < 0)
@@ -91,10 +91,10 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
   } else {
     // When the (sequence, kv-head) units alone fill every CTA slot of the
     // 8-warp shape, splitting only adds CTA prologues and merges (several
-    // waves balance the load anyway): splits of at least 4096 tokens then.
-    // Smaller grids split down to 1024 tokens to reach every SM.  (The
-    // head_dim 64/256 kernels run small 4-warp CTAs and keep 1024.)
-    const int64_t min_tokens = (units >= 2 * sms && head_dim == kHeadDim) ? 4096 : 1024;
+    // waves balance the load anyway): splits of at least 4096 tokens then,
+    // at every head dimension.  Smaller grids split down to 1024 tokens to
+    // reach every SM.
+    const int64_t min_tokens = units >= 2 * sms ? 4096 : 1024;
     const int64_t min_pps = ceil_div(min_tokens, page_size);
     const int64_t max_splits = std::min<int64_t>(64, ceil_div(max_pages, min_pps));
     int64_t s16 = best_splits(units, sms, max_splits);
@@ -233,8 +233,8 @@ int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_siz
                         int32_t max_seq_len, int32_t pages_per_split, int32_t* num_splits,
                         int32_t* pages_per_split_out) {
   if (!num_splits || !pages_per_split_out) return SAW_ERR_INVALID_ARG;
-  return make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, kHeadDim,
-                   num_splits, pages_per_split_out);
+  return make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, num_splits,
+                   pages_per_split_out);
 }
 
 size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -242,8 +242,8 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
                                   int32_t pages_per_split) {
   if (!head_dim_ok(head_dim) || num_q_heads <= 0) return 0;
   int32_t splits = 0, pps = 0;
-  if (make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, head_dim, &splits,
-                &pps) != SAW_OK)
+  if (make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, &splits, &pps) !=
+      SAW_OK)
     return 0;
   if (splits <= 1) return 0;
   const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
@@ -287,8 +287,8 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   if (int64_t(max_blocks_per_seq) * page_size < int64_t(max_seq_len)) return SAW_ERR_INVALID_ARG;
 
   int32_t splits = 0, pps = 0, warps = 16;
-  int32_t rc = make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split,
-                         head_dim, &splits, &pps, &warps);
+  int32_t rc = make_plan(num_seqs, num_kv_heads, page_size, max_seq_len, pages_per_split, &splits,
+                         &pps, &warps);
   if (rc != SAW_OK) return rc;
   const size_t need = saw_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  page_size, max_seq_len, pages_per_split);

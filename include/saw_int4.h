@@ -126,9 +126,8 @@ int32_t saw_quantize_append(const void* k, const void* v, int64_t k_token_stride
 /*
  * How many splits of the context the decode will use, and how many pages
  * each split covers, for these sizes on the current device
- * (pages_per_split = 0 picks them from the SM count; > 0 forces it), at
- * head_dim 128.  (At head_dim 64 and 256 an automatic plan may split more
- * finely; saw_decode_workspace_bytes takes head_dim and sizes for either.)
+ * (pages_per_split = 0 picks them from the SM count; > 0 forces it).  The
+ * plan is the same at every head dimension.
  * Writes *num_splits and *pages_per_split_out; returns a saw_status.
  */
 int32_t saw_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size,
