@@ -1269,7 +1269,9 @@ def run_profile(args):
     append: three quantize-appends of the 131072-token chunk;
     bf16: three BF16-cache decodes of 16 qwen3-8b-concurrent sequences
     (about 600 MB of cache, more than L2);
-    prefill: three 2048-token chunks at context 16384 (long-context shape)."""
+    prefill: three 2048-token chunks at context 16384 (long-context shape);
+    variant: three head_dim 256 (--profile-head-dim 64: 64) decodes of 16
+    qwen3-8b-concurrent sequences."""
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     import __graft_entry__
@@ -1323,9 +1325,11 @@ def run_profile(args):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
     elif args.profile == "variant":
-        # head_dim 256 decode on 16 sequences of the qwen3-8b-concurrent shape
+        # head_dim 256 (or --profile-head-dim) decode on 16 sequences of the
+        # qwen3-8b-concurrent shape
         import bit_paged_kv_gb300 as saw
-        wl = W.QWEN3_8B_CONCURRENT.variant(num_seqs=16, head_dim=256, block_h=256)
+        hd = args.profile_head_dim
+        wl = W.QWEN3_8B_CONCURRENT.variant(num_seqs=16, head_dim=hd, block_h=hd)
         lens = W.seq_lens(wl)
         bt, npages = W.page_tables(wl, lens)
         kc, vc = fill_caches(wl, 0, lens, bt, npages, device)
@@ -1363,6 +1367,8 @@ def main(argv=None):
                     default=None,
                     help="run a small fixed loop for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-layers", type=int, default=8)
+    ap.add_argument("--profile-head-dim", type=int, default=256, choices=[64, 256],
+                    help="head dimension of --profile variant")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
