@@ -557,6 +557,240 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   cp_async_wait<0>();
 }
 
+// ------------------------------------------------------------ head_dim 256
+//
+// The persistent tiled scheme at head_dim 256: four threads per row (64
+// values each, as two 32-value blocks X and Y), 8 rows per 4 KB warp tile.
+// Writing B0..B7 for the row's 32-value blocks, thread T = 0..3 of a row
+// holds X = B0, B3, B5, B6 and Y = B1, B2, B4, B7.  Stride 32 pairs X with
+// Y inside the thread; stride 64 pairs threads T and T ^ 1, stride 128
+// threads T and T ^ 3, and in both each thread keeps X and trades Y with its
+// partner.  Every step is x' = RN(sg x + y), y' = RN(-sg y + x) (exact +-1
+// products) with sg = -1 where X is the upper member of the pair, so X keeps
+// its block and Y takes the block it received: after the steps Y holds B1,
+// B2, B4, B7 (h <= 64), B2, B1, B7, B4 (h = 128) or B4, B7, B1, B2 (h = 256).
+constexpr int kD256 = 256;
+constexpr int kRowBytes256 = kD256 * 2;
+constexpr int kTileRows256 = kTileBytes / kRowBytes256;  // 8
+
+__device__ __forceinline__ int xblock256(int t) { return (0x6530 >> (4 * t)) & 15; }
+// Y's block after the butterfly steps of block size h (rot) or none.
+__device__ __forceinline__ int yblock256(int t, int h, bool rot) {
+  const int table = !rot || h <= 64 ? 0x7421 : (h == 128 ? 0x4712 : 0x2174);
+  return (table >> (4 * t)) & 15;
+}
+
+// Chunk c (16 bytes, elements 8c .. 8c+7) of tile row r sits in slot
+// c ^ (2 ((c >> 4) & 1) + (r & 1)) of the row's 512 bytes: the 8 lanes of a
+// quarter warp (rows 2k and 2k+1, threads 0-3) reading chunk j of their X
+// (or of their Y) blocks then hit 8 distinct 16-byte bank groups.
+__device__ __forceinline__ int slot256(int r, int c) { return c ^ ((((c >> 4) & 1) << 1) | (r & 1)); }
+
+// The butterfly of this thread's 64 values (X in local 0..31, Y in 32..63)
+// for blocks of h, then the multiply by c = binary32(1/sqrt(h)).  Strides
+// 1..16 inside each block as in rotate_half; the signs of the stride-32, 64
+// and 128 steps follow from X's block (bits 0, 1, 2 set: X is the upper
+// member).
+template <int H, bool F16IN>
+__device__ __forceinline__ void rotate_quarter(const uint32_t (&wd)[kHalfRow / 2],
+                                               float (&u)[kHalfRow], float c, int xb) {
+#pragma unroll
+  for (int i = 0; i < kHalfRow / 2; ++i) {
+    if (F16IN) {
+      const float odd = f16_hi(wd[i]);
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.f16 %0, lo, %3;\n\tsub.rn.f32.f16 %1, lo, %3;\n\t}"
+          : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
+          : "r"(wd[i]), "f"(odd));
+    } else {
+      const float odd = bf16_hi(wd[i]);
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.bf16 %0, lo, %3;\n\tsub.rn.f32.bf16 %1, lo, %3;\n\t}"
+          : "=f"(u[2 * i]), "=f"(u[2 * i + 1])
+          : "r"(wd[i]), "f"(odd));
+    }
+  }
+#pragma unroll
+  for (int len = 2; len < (H < 32 ? H : 32); len *= 2) {
+#pragma unroll
+    for (int i = 0; i < kHalfRow; i += 2) {
+      if ((i & len) == 0) bfly2(u[i], u[i + 1], u[i + len], u[i + len + 1]);
+    }
+  }
+  if (H >= 64) {
+    const float sg = (xb & 1) ? -1.0f : 1.0f;
+    const uint64_t sp = pair(sg, sg), sm = pair(-sg, -sg);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sp, sm);
+  }
+  if (H >= 128) {
+    const float sg = (xb & 2) ? -1.0f : 1.0f;
+    const uint64_t sp = pair(sg, sg), sm = pair(-sg, -sg);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float o0 = __shfl_xor_sync(0xFFFFFFFFu, u[32 + j], 1);
+      const float o1 = __shfl_xor_sync(0xFFFFFFFFu, u[33 + j], 1);
+      u[32 + j] = o0;
+      u[33 + j] = o1;
+      bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sp, sm);
+    }
+  }
+  if (H >= 256) {
+    const float sg = (xb & 4) ? -1.0f : 1.0f;
+    const uint64_t sp = pair(sg, sg), sm = pair(-sg, -sg);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float o0 = __shfl_xor_sync(0xFFFFFFFFu, u[32 + j], 3);
+      const float o1 = __shfl_xor_sync(0xFFFFFFFFu, u[33 + j], 3);
+      u[32 + j] = o0;
+      u[33 + j] = o1;
+      bfly2_signed(u[j], u[j + 1], u[32 + j], u[33 + j], sp, sm);
+    }
+  }
+  const uint64_t cc = pair(c, c);
+#pragma unroll
+  for (int i = 0; i < kHalfRow; i += 2) mul2(u[i], u[i + 1], cc);
+}
+
+template <int H, bool F16IN>
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
+    quantize_append_tiled256_kernel(const AppendParams p, int tiles_per_tensor, int num_tiles) {
+  extern __shared__ __align__(128) uint8_t ring_all[];
+
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* ring = ring_all + warp * (kTileStages * kTileBytes);
+  const int hkv = p.num_kv_heads;
+  const int num_rows = p.num_tokens * hkv;
+
+  // Copies of one tile: 8 per lane, one 512-byte row per instruction (lane
+  // l moves chunk l); the slot depends on the row only through its parity.
+  const int so_even = slot256(0, lane) << 4, so_odd = slot256(1, lane) << 4;
+  auto issue = [&](int tile, uint8_t* buf) {
+    const int tensor = tile >= tiles_per_tensor ? 1 : 0;
+    const int row0 = (tile - tensor * tiles_per_tensor) * kTileRows256;
+    const uint16_t* __restrict__ src = tensor ? p.src[1] : p.src[0];
+    const int64_t stride = tensor ? p.stride[1] : p.stride[0];
+    if (row0 + kTileRows256 <= num_rows && stride == int64_t(hkv) * kD256) {
+      const uint16_t* g = src + int64_t(row0) * kD256 + lane * 8;
+#pragma unroll
+      for (int it = 0; it < kTileRows256; ++it)
+        cp_async16(buf + it * kRowBytes256 + ((it & 1) ? so_odd : so_even), g + it * kD256);
+    } else {
+#pragma unroll
+      for (int it = 0; it < kTileRows256; ++it) {
+        const int row = row0 + it;
+        if (row < num_rows) {
+          const uint32_t t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
+          const uint32_t hd = uint32_t(row) - t * uint32_t(hkv);
+          cp_async16(buf + it * kRowBytes256 + ((it & 1) ? so_odd : so_even),
+                     src + int64_t(t) * stride + hd * kD256 + lane * 8);
+        }
+      }
+    }
+  };
+
+  const int r = lane >> 2;   // this thread's row in the tile
+  const int th = lane & 3;   // and its place in the row
+  const int xb = xblock256(th);
+  const int yb0 = yblock256(th, 0, false);
+  const int step = int(gridDim.x) * kTileWarps;
+  int tile = int(blockIdx.x) * kTileWarps + warp;
+#pragma unroll
+  for (int s = 0; s < kTileStages - 1; ++s) {
+    const int pre = tile + s * step;
+    if (pre < num_tiles) issue(pre, ring + s * kTileBytes);
+    cp_async_commit();
+  }
+  int cur = 0;
+  int ahead = kTileStages - 1;
+  for (; tile < num_tiles; tile += step) {
+    uint8_t* buf = ring + cur * kTileBytes;
+    const int nxt = tile + (kTileStages - 1) * step;
+    if (nxt < num_tiles) issue(nxt, ring + ahead * kTileBytes);
+    cp_async_commit();
+    cur = (cur + 1 == kTileStages) ? 0 : cur + 1;
+    ahead = (ahead + 1 == kTileStages) ? 0 : ahead + 1;
+
+    const int tensor = tile >= tiles_per_tensor ? 1 : 0;
+    const int row = (tile - tensor * tiles_per_tensor) * kTileRows256 + r;
+    const bool live = row < num_rows;
+    uint32_t t = 0, hd = 0;
+    int32_t slot = -1;
+    if (live) {
+      t = div_rows(uint32_t(row), p.hkv_mul, p.hkv_shift);
+      hd = uint32_t(row) - t * uint32_t(hkv);
+      slot = __ldg(p.slot_mapping + t);
+    }
+    cp_async_wait<kTileStages - 1>();  // this lane's copies of the current tile landed
+    __syncwarp();                      // ... and the whole warp's
+
+    // rows past the end compute on stale data (the shuffles run converged);
+    // only stores are guarded
+    uint32_t wd[kHalfRow / 2];  // X's 32 values, then Y's, in pairs
+    {
+      const uint8_t* rowp = buf + r * kRowBytes256;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 a = *reinterpret_cast<const uint4*>(rowp + (slot256(r, 4 * xb + j) << 4));
+        const uint4 b = *reinterpret_cast<const uint4*>(rowp + (slot256(r, 4 * yb0 + j) << 4));
+        wd[4 * j + 0] = a.x;
+        wd[4 * j + 1] = a.y;
+        wd[4 * j + 2] = a.z;
+        wd[4 * j + 3] = a.w;
+        wd[16 + 4 * j + 0] = b.x;
+        wd[16 + 4 * j + 1] = b.y;
+        wd[16 + 4 * j + 2] = b.z;
+        wd[16 + 4 * j + 3] = b.w;
+      }
+    }
+    float u[kHalfRow];
+    const bool rot = tensor ? p.rotate[1] != 0 : p.rotate[0] != 0;
+    if (rot) {
+      rotate_quarter<H, F16IN>(wd, u, p.c_h, xb);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kHalfRow / 2; ++i) {
+        u[2 * i] = F16IN ? f16_lo(wd[i]) : bf16_lo(wd[i]);
+        u[2 * i + 1] = F16IN ? f16_hi(wd[i]) : bf16_hi(wd[i]);
+      }
+    }
+    float mn, mx;
+    half_min_max<false>(u, mn, mx);
+#pragma unroll
+    for (int x = 1; x <= 2; x <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, x));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, x));
+    }
+    const RowMeta m = row_meta(mn, mx, p.meta_bf16 != 0);
+    uint32_t word[8];
+    quantize_half(u, m.z, m.rcp, m.fast, word);
+
+    if (live && slot != -1) {
+      if (slot < 0 || int64_t(slot) >= p.num_slots) {
+        if (th == 0) report(p.dev_status, SAW_ERR_DEVICE_INDEX);
+      } else {
+        const int P = p.page_size;
+        const int page = slot >> p.page_shift;
+        const int off = slot & (P - 1);
+        uint8_t* chunk = (tensor ? p.cache[1] : p.cache[0]) +
+                         (int64_t(page) * hkv + hd) * int64_t(P * (kD256 / 2 + 4));
+        // block b's 32 codes are bytes 16b .. 16b+15 of the token's code row
+        uint8_t* codes = chunk + off * (kD256 / 2);
+        const int yb = yblock256(th, H, rot);
+        *reinterpret_cast<uint4*>(codes + 16 * xb) = make_uint4(word[0], word[1], word[2], word[3]);
+        *reinterpret_cast<uint4*>(codes + 16 * yb) = make_uint4(word[4], word[5], word[6], word[7]);
+        if (th == 0)
+          *reinterpret_cast<uint32_t*>(chunk + P * (kD256 / 2) + 4 * off) =
+              uint32_t(m.sb) | (uint32_t(m.zb) << 16);
+      }
+    }
+    __syncwarp();  // the buffer is refilled by a later issue
+  }
+  cp_async_wait<0>();
+}
+
 // Small appends (a decode step appends one token: Hkv rows per tensor): one
 // warp per row, lane l holding elements 4l..4l+3.  The butterfly is the same
 // ascending-stride sequence of (a+b, a-b) steps as the row kernel -- strides
@@ -661,31 +895,71 @@ cudaError_t launch_tiled64_h(int h, dim3 grid, cudaStream_t stream, const Append
   }
 }
 
-// Bulk appends at head_dim 64 (the warp-per-row kernel in variants.cu
-// serves small ones).
-cudaError_t launch_quantize_append_tiled64(const AppendParams& p, int num_tensors,
-                                           cudaStream_t stream) {
+template <bool F16IN>
+cudaError_t launch_tiled256_h(int h, dim3 grid, cudaStream_t stream, const AppendParams& q,
+                              int tiles_per_tensor, int num_tiles) {
+  switch (h) {
+    case 16: return launch_tiled(quantize_append_tiled256_kernel<16, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 32: return launch_tiled(quantize_append_tiled256_kernel<32, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 64: return launch_tiled(quantize_append_tiled256_kernel<64, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 128: return launch_tiled(quantize_append_tiled256_kernel<128, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    case 256: return launch_tiled(quantize_append_tiled256_kernel<256, F16IN>, grid, stream, q, tiles_per_tensor, num_tiles);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// The tiled kernels' launch: the grid (at most kTileCtasPerSm CTAs per SM)
+// and the divisions the kernels replace by multiplies.
+struct TiledLaunch {
+  AppendParams q;
+  dim3 grid;
+  int tiles_per_tensor = 0, num_tiles = 0;
+};
+cudaError_t tiled_launch(const AppendParams& p, int num_tensors, int rows_per_tile, TiledLaunch& l) {
   const int num_rows = p.num_tokens * p.num_kv_heads;
-  if (num_rows == 0) return cudaSuccess;
-  const bool any_rot = p.rotate[0] || (num_tensors > 1 && p.rotate[1]);
-  const int h = any_rot ? p.block_h : kD64;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int tiles_per_tensor = (num_rows + kTileRows64 - 1) / kTileRows64;
-  const int num_tiles = tiles_per_tensor * num_tensors;
-  const dim3 grid(std::min((num_tiles + kTileWarps - 1) / kTileWarps, sms * kTileCtasPerSm));
-  AppendParams q = p;
-  q.num_tensors = num_tensors;
+  l.tiles_per_tensor = (num_rows + rows_per_tile - 1) / rows_per_tile;
+  l.num_tiles = l.tiles_per_tensor * num_tensors;
+  l.grid = dim3(std::min((l.num_tiles + kTileWarps - 1) / kTileWarps, sms * kTileCtasPerSm));
+  l.q = p;
+  l.q.num_tensors = num_tensors;
   int lg = 0;
-  while ((1 << lg) < q.num_kv_heads) ++lg;
-  q.hkv_shift = uint32_t(31 + lg);
-  q.hkv_mul = uint32_t(((uint64_t(1) << q.hkv_shift) + q.num_kv_heads - 1) / q.num_kv_heads);
-  q.page_shift = 0;
-  while ((1 << q.page_shift) < q.page_size) ++q.page_shift;
-  return q.in_f16 ? launch_tiled64_h<true>(h, grid, stream, q, tiles_per_tensor, num_tiles)
-                  : launch_tiled64_h<false>(h, grid, stream, q, tiles_per_tensor, num_tiles);
+  while ((1 << lg) < l.q.num_kv_heads) ++lg;
+  l.q.hkv_shift = uint32_t(31 + lg);
+  l.q.hkv_mul = uint32_t(((uint64_t(1) << l.q.hkv_shift) + l.q.num_kv_heads - 1) / l.q.num_kv_heads);
+  l.q.page_shift = 0;
+  while ((1 << l.q.page_shift) < l.q.page_size) ++l.q.page_shift;
+  return cudaSuccess;
+}
+
+// Bulk appends at head_dim 64 and 256 (the warp-per-row kernel in
+// variants.cu serves small ones).
+cudaError_t launch_quantize_append_tiled64(const AppendParams& p, int num_tensors,
+                                           cudaStream_t stream) {
+  if (p.num_tokens * p.num_kv_heads == 0) return cudaSuccess;
+  const bool any_rot = p.rotate[0] || (num_tensors > 1 && p.rotate[1]);
+  const int h = any_rot ? p.block_h : kD64;
+  TiledLaunch l;
+  cudaError_t e = tiled_launch(p, num_tensors, kTileRows64, l);
+  if (e != cudaSuccess) return e;
+  return l.q.in_f16 ? launch_tiled64_h<true>(h, l.grid, stream, l.q, l.tiles_per_tensor, l.num_tiles)
+                    : launch_tiled64_h<false>(h, l.grid, stream, l.q, l.tiles_per_tensor, l.num_tiles);
+}
+
+cudaError_t launch_quantize_append_tiled256(const AppendParams& p, int num_tensors,
+                                            cudaStream_t stream) {
+  if (p.num_tokens * p.num_kv_heads == 0) return cudaSuccess;
+  const bool any_rot = p.rotate[0] || (num_tensors > 1 && p.rotate[1]);
+  const int h = any_rot ? p.block_h : kD256;
+  TiledLaunch l;
+  cudaError_t e = tiled_launch(p, num_tensors, kTileRows256, l);
+  if (e != cudaSuccess) return e;
+  return l.q.in_f16
+             ? launch_tiled256_h<true>(h, l.grid, stream, l.q, l.tiles_per_tensor, l.num_tiles)
+             : launch_tiled256_h<false>(h, l.grid, stream, l.q, l.tiles_per_tensor, l.num_tiles);
 }
 
 cudaError_t launch_quantize_append(const AppendParams& p, int num_tensors, cudaStream_t stream) {

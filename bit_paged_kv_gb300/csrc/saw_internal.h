@@ -97,11 +97,13 @@ cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_dims_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_dims_w8(const DecodeParams& p, cudaStream_t stream);
-// head_dim 64 and 256 append (variants.cu); bulk appends at head_dim 64 run
-// the tiled kernel of quantize_append.cu
+// head_dim 64 and 256 append (variants.cu); bulk appends run the tiled
+// kernels of quantize_append.cu
 cudaError_t launch_quantize_append_var(const AppendParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_quantize_append_tiled64(const AppendParams& p, int num_tensors,
                                            cudaStream_t stream);
+cudaError_t launch_quantize_append_tiled256(const AppendParams& p, int num_tensors,
+                                            cudaStream_t stream);
 // BF16 baseline (paged_decode_bf16.cu)
 cudaError_t launch_paged_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_stride,

@@ -147,13 +147,15 @@ cudaError_t launch_append_var_d(const AppendParams& p, int h, cudaStream_t strea
 
 }  // namespace
 
-// Rows from which a head_dim-64 append runs the tiled kernel.
-constexpr int64_t kTiled64MinRows = 4096;
+// Rows from which a head_dim-64 or -256 append runs the tiled kernel.
+constexpr int64_t kTiledMinRows = 4096;
 
 cudaError_t launch_quantize_append_var(const AppendParams& p, int head_dim, cudaStream_t stream) {
   if (int64_t(p.num_tokens) * p.num_kv_heads == 0) return cudaSuccess;
-  if (head_dim == 64 && int64_t(p.num_tokens) * p.num_kv_heads > kTiled64MinRows)
-    return launch_quantize_append_tiled64(p, p.num_tensors, stream);
+  if (int64_t(p.num_tokens) * p.num_kv_heads > kTiledMinRows) {
+    if (head_dim == 64) return launch_quantize_append_tiled64(p, p.num_tensors, stream);
+    if (head_dim == 256) return launch_quantize_append_tiled256(p, p.num_tensors, stream);
+  }
   const bool any_rot = p.rotate[0] || (p.num_tensors > 1 && p.rotate[1]);
   const int h = any_rot ? p.block_h : 16;  // unrotated: h is not used
   switch (head_dim) {

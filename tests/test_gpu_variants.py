@@ -35,15 +35,17 @@ def test_append_bytes(D, h, rot):
     assert_bytes_equal(vc, vr, f"V D{D} h{h}")
 
 
-@pytest.mark.parametrize("h", [64, 32, 16])
-@pytest.mark.parametrize("rot", [(True, True), (True, False), (False, False)])
+@pytest.mark.parametrize("D,h", [(64, 64), (64, 32), (64, 16), (256, 256), (256, 128),
+                                 (256, 64), (256, 32), (256, 16)])
+@pytest.mark.parametrize("rot", [(True, True), (True, False), (False, True), (False, False)])
 @pytest.mark.parametrize("fmt", ["bf16", "f16", "bf16-meta"])
-def test_append_bytes_bulk_head_dim_64(h, rot, fmt):
-    """Bulk appends at head_dim 64 (above 4096 rows: the tiled kernel, one
-    thread per row): 2501 tokens x 4 kv-heads, a ragged last tile, one skipped
-    slot, every byte against the oracle, for both input formats and both
-    metadata formats."""
-    D = 64
+def test_append_bytes_bulk(D, h, rot, fmt):
+    """Bulk appends at head_dim 64 and 256 (above 4096 rows: the tiled
+    kernels, one thread per row at 64 and four per row at 256, where the
+    stride-64 and stride-128 steps cross threads): 2501 tokens x 4 kv-heads,
+    a ragged last tile, one skipped slot, every byte against the oracle, for
+    each tensor rotated or not, both input formats and both metadata
+    formats."""
     wl = W.TINY.variant(head_dim=D, block_h=h, num_kv_heads=4, dist="student_t", nu=3)
     T, P, pages = 2501, 16, 170
     dt = torch.float16 if fmt == "f16" else torch.bfloat16
@@ -57,12 +59,13 @@ def test_append_bytes_bulk_head_dim_64(h, rot, fmt):
     assert st == 0
     kr, vr, bad = oracle_append(k, v, slots, pages, P, rot[0], rot[1], h, meta_bf16=meta_bf16)
     assert bad == 0
-    assert_bytes_equal(kc, kr, f"K D64 bulk h{h} {fmt}")
-    assert_bytes_equal(vc, vr, f"V D64 bulk h{h} {fmt}")
+    assert_bytes_equal(kc, kr, f"K D{D} bulk h{h} {fmt}")
+    assert_bytes_equal(vc, vr, f"V D{D} bulk h{h} {fmt}")
 
 
-def test_append_bulk_head_dim_64_strided_k_only_and_bad_slot():
-    D, h, P, pages, Hkv = 64, 64, 64, 60, 2
+@pytest.mark.parametrize("D", [64, 256])
+def test_append_bulk_strided_k_only_and_bad_slot(D):
+    h, P, pages, Hkv = D, 64, 60, 2
     wl = W.TINY.variant(head_dim=D, block_h=h, num_kv_heads=Hkv)
     T = 3000  # 6000 rows: the tiled kernel
     raw = W.kv_rows(wl.variant(num_kv_heads=2 * Hkv), 0, W.K, T, "cuda")  # [T, 2 Hkv, D]
@@ -73,7 +76,7 @@ def test_append_bulk_head_dim_64_strided_k_only_and_bad_slot():
     assert st == saw.SAW_ERR_DEVICE_INDEX
     kr, _, bad = oracle_append(k.contiguous(), None, slots, pages, P, True, False, h)
     assert bad == 1
-    assert_bytes_equal(kc, kr, "K strided D64 bulk")
+    assert_bytes_equal(kc, kr, f"K strided D{D} bulk")
 
 
 def test_append_strided_k_only_and_bad_slot():
