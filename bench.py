@@ -918,38 +918,71 @@ def graph_step_timing(case, stream, steps: int, warmup: int, sampler=None):
 
 
 def e2e_measure(case, graph, stream, iters: int, world: int):
-    """The same step end to end through the public API: every step copies
-    the step's inputs (q, new K and V rows of every layer) in from pinned host
-    memory, replays the step and copies the attention output back."""
+    """The same step end to end through the public API: every step's inputs
+    (q, new K and V rows of every layer) come in from pinned host memory and
+    its attention output goes back, pipelined as a server would: two sets of
+    device inputs and outputs, each with its own captured step, so that
+    while step s runs on `stream`, a copy stream brings step s-1's output
+    out and step s+1's inputs in.  The timed region runs from the first
+    step's input copy to the last step's output copy."""
     q_h = case.q.cpu().pin_memory()
     k_h = case.knew.cpu().pin_memory()
     v_h = case.vnew.cpu().pin_memory()
     o_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    first = (case.q, case.knew, case.vnew, case.out)
+    second = tuple(torch.empty_like(t) for t in first)
+    case.q, case.knew, case.vnew, case.out = second
+    graphs = [graph, capture(case.step, stream)]
+    case.q, case.knew, case.vnew, case.out = first
+    sets = [first, second]
+    copy = torch.cuda.Stream(device=case.q.device)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    inputs_in = [ev(), ev()]   # set b holds its step's inputs
+    step_done = [ev(), ev()]   # set b's step has run (its output is ready)
 
-    def e2e_step():
-        case.q.copy_(q_h, non_blocking=True)
-        case.knew.copy_(k_h, non_blocking=True)
-        case.vnew.copy_(v_h, non_blocking=True)
-        graph.replay()
-        o_h.copy_(case.out, non_blocking=True)
+    def upload(b):
+        q, kn, vn, _ = sets[b]
+        q.copy_(q_h, non_blocking=True)
+        kn.copy_(k_h, non_blocking=True)
+        vn.copy_(v_h, non_blocking=True)
+        inputs_in[b].record(copy)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(iters):
-            e2e_step()
-        e2.record(stream)
+    def run(n):
+        with torch.cuda.stream(copy):
+            upload(0)
+        for s in range(n):
+            b = s & 1
+            stream.wait_event(inputs_in[b])
+            with torch.cuda.stream(stream):
+                graphs[b].replay()
+            step_done[b].record(stream)
+            with torch.cuda.stream(copy):
+                if s >= 1:  # step s-1's output, then step s+1's inputs into its set
+                    copy.wait_event(step_done[b ^ 1])
+                    o_h.copy_(sets[b ^ 1][3], non_blocking=True)
+                if s + 1 < n:  # set b^1 is free: its step has run (waited above)
+                    upload(b ^ 1)
+        with torch.cuda.stream(copy):
+            copy.wait_event(step_done[(n - 1) & 1])
+            o_h.copy_(sets[(n - 1) & 1][3], non_blocking=True)
+
+    run(3)
     torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(copy)
+    run(iters)
+    e2.record(copy)
+    torch.cuda.synchronize()
+    del graphs[1], second
     t, nbytes = reduce_over_ranks(s2.elapsed_time(e2) * 1e-3, case.step_bytes() * iters, world)
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2
     d2h = o_h.numel() * 4
     return {"value": nbytes / t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": t / iters * 1e3,
-            "how": "pinned host q and new K/V rows of every layer copied in, graph step, "
-                   "attention output of every layer copied out, every step"}
+            "how": "every step: pinned host q and new K/V rows of every layer copied in, "
+                   "graph step, attention output of every layer copied out; double-buffered "
+                   "device inputs/outputs, the copies of steps s-1 and s+1 on a second "
+                   "stream overlapping step s"}
 
 
 def step_sample_for_oracle(case, layer: int, seqs_all, seqs_one, heads_one=None,
