@@ -51,16 +51,24 @@ L2_BYTES = 129 * 1024 * 1024
 
 # ------------------------------------------------------------------ ncu traffic record
 
-DECODE_SOURCES = ["paged_decode.cu", "saw_device.cuh", "saw_internal.h", "saw_quant_row.cuh"]
+# The decode kernel's device code: these files whole, and the kernel's
+# parameter block from saw_internal.h (the host-side declarations there do
+# not change the kernel).
+DECODE_SOURCES = ["paged_decode.cu", "saw_device.cuh", "saw_quant_row.cuh"]
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 def decode_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_paged_kv_gb300", "csrc")
     for f in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "bit_paged_kv_gb300", "csrc", f), "rb") as fh:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(csrc, "saw_internal.h"), "rb") as fh:
+        text = fh.read()
+    start = text.index(b"struct DecodeParams {")
+    h.update(text[start:text.index(b"};", start) + 2])
     return h.hexdigest()
 
 
