@@ -19,8 +19,10 @@
 // neighbouring threads own one row, 64 binary32 values each: butterfly
 // strides up to 32 stay inside a thread (two lanes per packed f32x2
 // instruction), stride 64 is one shuffle with the partner, min/max reduce
-// three at a time, and each thread stores its 32 code bytes; the (scale,
-// zero) word goes to the page's metadata run.
+// in four chains three at a time, and each thread stores its 32 code
+// bytes; the (scale, zero) word goes to the page's metadata run.  The same
+// scheme serves head_dim 64 (one thread per row) and 256 (four per row)
+// below.
 #include <algorithm>
 
 #include "saw_device.cuh"

@@ -10,8 +10,10 @@
 // bits, for bfloat16 or binary16 input rows.  (The decode at these sizes is
 // paged_decode.cu built for head_dim 64 and 256.)
 //
-//  * One warp per (token, kv-head) row, lane l holding elements
-//    E l .. E l + E - 1 (E = D/32).  The butterfly is the ascending-stride
+//  * Small appends (up to 4096 rows, e.g. a decode step): one warp per
+//    (token, kv-head) row, lane l holding elements E l .. E l + E - 1
+//    (E = D/32).  Bulk appends run the tiled kernels of quantize_append.cu
+//    (one thread per row at head_dim 64, four per row at 256).  The butterfly is the ascending-stride
 //    sequence of RN(a + b), RN(a - b) steps -- strides below E inside a lane,
 //    the rest across lanes -- then one RN multiply by binary32(1/sqrt h), so
 //    the codes and (s, z) are the oracle's to the bit, as in the 128 path.
