@@ -84,19 +84,29 @@ struct Dims {
 // [K codes 16 rows | K meta 16 words | V codes 16 rows | V meta 16 words].
 // A 16-token page is exactly [K chunk | V chunk]; larger pages are copied
 // as 16-row slices of their code and meta regions.
-template <int D, int P>
+//
+// PAIR (D = 128 standing for two head_dim-64 kv-heads, 16-token pages):
+// each tensor's part of a stage is the two kv-heads' page chunks back to
+// back, [codes 16 x 32 B | meta 16 words] twice, one copy; dims 0..63 of the
+// pair head are the first kv-head's, 64..127 the second's.  The lanes whose
+// K bytes, V dims or head columns fall in the second half read there.
+template <int D, int P, bool PAIR = false>
 struct Cfg {
   using DM = Dims<D>;
-  static constexpr int kCodeRow = DM::kCodeRow;
+  static_assert(!PAIR || (D == 128 && P == kStepTok), "pairs are two head_dim-64 heads, page 16");
+  static constexpr int kCodeRow = PAIR ? D / 4 : DM::kCodeRow;  // code bytes of one row in a chunk
   static constexpr int kStages = DM::kStages;
   static constexpr int kChunk = P * kCodeRow + 4 * P;
   static constexpr int kStepsPerPage = P / kStepTok;
-  static constexpr int kHalf = kStepTok * kCodeRow + kStepTok * 4;  // one tensor (1088 at D 128)
+  // one tensor (1088 at D 128; 1152 for a pair)
+  static constexpr int kHalf = (PAIR ? 2 : 1) * (kStepTok * kCodeRow + kStepTok * 4);
   static constexpr int kStage = 2 * kHalf;
-  // byte offset of K's code row / meta word `row` in a stage; V's are at the
-  // same offsets from kHalf
-  __device__ static constexpr int kcode(int row) { return row * kCodeRow; }
-  __device__ static constexpr int kmeta(int row) { return kStepTok * kCodeRow + row * 4; }
+  // byte offset of K's code row / meta word `row` in a stage (of the pair's
+  // kv-head `hb`); V's are at the same offsets from kHalf
+  __device__ static constexpr int kcode(int row, int hb = 0) { return hb * kChunk + row * kCodeRow; }
+  __device__ static constexpr int kmeta(int row, int hb = 0) {
+    return hb * kChunk + kStepTok * kCodeRow + row * 4;
+  }
   static constexpr int kRing = kWarps * kStages * kStage;
   // after the main loop the ring is reused: cross-warp reduction, then rows
   // red_acc [W][8][D + D/16], red_m / red_l / red_z / weights [W][8],
@@ -153,10 +163,16 @@ constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 // D: the head dimension.  A thread-in-group c of an MMA quad covers dims
 // [c D/4, (c+1) D/4) of a K row, 32-bit word w of it dims 8w .. 8w+7 of
 // that range; a lane group g covers dims [g D/8, (g+1) D/8) of the output.
-template <int D, int P, bool PACKED, bool APPEND, bool BFM>
+// PAIR: D = 128 stands for two neighbouring head_dim-64 kv-heads of GQA 4
+// (Cfg above): q-head column v < 4 is a q-head of the first kv-head, its q
+// zero in dims 64..127, v >= 4 one of the second, zero in dims 0..63; each
+// column's output is its own half of the 128 dims.  The tensor cores do the
+// zero products; every per-tile cost is shared by the two kv-heads.
+template <int D, int P, bool PACKED, bool APPEND, bool BFM, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(const DecodeParams p) {
   static_assert(!APPEND || D == kHeadDim, "the fused step is built for head_dim 128");
-  using C = Cfg<D, P>;
+  static_assert(!PAIR || (!PACKED && !APPEND), "pairs use the wide form, without the fused step");
+  using C = Cfg<D, P, PAIR>;
   using DM = Dims<D>;
   constexpr int kStages = DM::kStages;
   constexpr int kCodeRow = DM::kCodeRow;
@@ -183,8 +199,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const int lane = tid & 31;
   const int g = lane >> 2;  // MMA group id
   const int c = lane & 3;   // thread in group
-  const int G = p.group;
+  const int hkc = PAIR ? c >> 1 : 0;  // a pair's kv-head of this lane's head columns
+  const int G = PAIR ? kMaxGroup : p.group;  // q-head columns of this CTA
   const int hq0 = kvh * G;
+  constexpr int kOutD = PAIR ? D / 2 : D;     // dims of an output row
+  const int kv0 = PAIR ? 2 * kvh : kvh;       // (first) kv-head of this CTA
 
   int L = p.seq_lens[seq];
   if (L < 0 || L > p.max_seq_len) {
@@ -200,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     // nothing to attend over here; an empty sequence still owes a zero row
     if (split == 0 && n_pages == 0) {
       if (early) pdl_wait_then_release();
-      for (int idx = tid; idx < G * D; idx += kThreads)
-        p.out[(int64_t(seq) * p.num_q_heads + hq0) * D + idx] = 0.0f;
+      for (int idx = tid; idx < G * kOutD; idx += kThreads)
+        p.out[(int64_t(seq) * p.num_q_heads + hq0) * kOutD + idx] = 0.0f;
     }
     return;
   }
@@ -241,10 +260,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       return;
     }
     mbar_arrive_expect_tx(&wbars[s], C::kStage);
-    const int64_t off = (int64_t(pid) * p.num_kv_heads + kvh) * C::kChunk;
-    if (P == 16) {
-      bulk_g2s(st, p.k_cache + off, C::kChunk, &wbars[s]);
-      bulk_g2s(st + C::kHalf, p.v_cache + off, C::kChunk, &wbars[s]);
+    const int64_t off = (int64_t(pid) * p.num_kv_heads + kv0) * C::kChunk;
+    if (P == 16) {  // the page's chunk (a pair: both kv-heads' chunks), K then V
+      bulk_g2s(st, p.k_cache + off, C::kHalf, &wbars[s]);
+      bulk_g2s(st + C::kHalf, p.v_cache + off, C::kHalf, &wbars[s]);
     } else {
       const int part = (warp + i * kWarps) % C::kStepsPerPage;
       const int64_t codes = off + part * (kStepTok * kCodeRow);
@@ -270,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     // hints the cache, which stays coherent with the previous kernel's
     // writes, so it may run before the wait)
     const uint16_t* row = nullptr;
-    if (warp < G) row = p.q + (int64_t(seq) * p.num_q_heads + hq0 + warp) * D;
+    if (warp < G) row = p.q + (int64_t(seq) * p.num_q_heads + hq0 + warp) * kOutD;
     if (owner && warp == kWarps - 2) row = p.k_new + int64_t(seq) * p.k_new_stride + int64_t(kvh) * D;
     if (owner && warp == kWarps - 1) row = p.v_new + int64_t(seq) * p.v_new_stride + int64_t(kvh) * D;
     if (row) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + lane * 64));
@@ -331,23 +350,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 #pragma unroll
     for (int e = 0; e < kE; ++e) x[e] = 0.0f;
     if (h < G) {
-      const uint16_t* qrow = p.q + (int64_t(seq) * p.num_q_heads + hq0 + h) * D + kE * lane;
-      const bool f16 = p.in_f16 != 0;
-      uint32_t raw[kE / 2];
-      if (kE == 2) {
-        raw[0] = *reinterpret_cast<const uint32_t*>(qrow);
-      } else {
+      // PAIR: column h's q fills its kv-head's half (lanes 16 (h / 4) ..),
+      // the other half stays zero
+      if (!PAIR || (lane >> 4) == (h >> 2)) {
+        const uint16_t* qrow = p.q + (int64_t(seq) * p.num_q_heads + hq0 + h) * kOutD +
+                               kE * (PAIR ? (lane & 15) : lane);
+        const bool f16 = p.in_f16 != 0;
+        uint32_t raw[kE / 2];
+        if (kE == 2) {
+          raw[0] = *reinterpret_cast<const uint32_t*>(qrow);
+        } else {
 #pragma unroll
-        for (int u = 0; u < kE / 2; u += 2) {
-          const uint2 r2 = *reinterpret_cast<const uint2*>(qrow + 2 * u);
-          raw[u] = r2.x;
-          raw[u + 1] = r2.y;
+          for (int u = 0; u < kE / 2; u += 2) {
+            const uint2 r2 = *reinterpret_cast<const uint2*>(qrow + 2 * u);
+            raw[u] = r2.x;
+            raw[u + 1] = r2.y;
+          }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < kE / 2; ++u) {
-        x[2 * u] = in_lo(raw[u], f16);
-        x[2 * u + 1] = in_hi(raw[u], f16);
+        for (int u = 0; u < kE / 2; ++u) {
+          x[2 * u] = in_lo(raw[u], f16);
+          x[2 * u + 1] = in_hi(raw[u], f16);
+        }
       }
       if (p.rotate_k) {
         const int hb = p.block_h;
@@ -506,18 +530,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       v1[t] = pok && (tok0 + g + 8) < L;
       full[t] = pok && tok0 + kStepTok <= L;  // warp-uniform
       constexpr int kKW = DM::kKWords;
-      const uint8_t* krow = st + C::kcode(g) + (D / 8) * c;
+      // (a pair: thread-in-group c reads half c & 1 of kv-head c / 2's row)
+      const uint8_t* krow = PAIR ? st + C::kcode(g, c >> 1) + 16 * (c & 1)
+                                 : st + C::kcode(g) + (D / 8) * c;
       uint32_t kaw[kKW], kbw[kKW];
       if constexpr (kKW == 2) {
         const uint2 ka = *reinterpret_cast<const uint2*>(krow);
-        const uint2 kb = *reinterpret_cast<const uint2*>(krow + 8 * kCodeRow);
+        const uint2 kb = *reinterpret_cast<const uint2*>(krow + 8 * C::kCodeRow);
         kaw[0] = ka.x; kaw[1] = ka.y;
         kbw[0] = kb.x; kbw[1] = kb.y;
       } else {
 #pragma unroll
         for (int u = 0; u < kKW; u += 4) {
           const uint4 ka = *reinterpret_cast<const uint4*>(krow + 4 * u);
-          const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * kCodeRow + 4 * u);
+          const uint4 kb = *reinterpret_cast<const uint4*>(krow + 8 * C::kCodeRow + 4 * u);
           kaw[u] = ka.x; kaw[u + 1] = ka.y; kaw[u + 2] = ka.z; kaw[u + 3] = ka.w;
           kbw[u] = kb.x; kbw[u + 1] = kb.y; kbw[u + 2] = kb.z; kbw[u + 3] = kb.w;
         }
@@ -559,8 +585,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 #pragma unroll
         for (int j = 0; j < 4; ++j) d[j] += __shfl_xor_sync(kFull, d[j], 2);
       }
-      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g));
-      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8));
+      // this lane's head columns 2c, 2c+1 (a pair: of kv-head c / 2)
+      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g, hkc));
+      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8, hkc));
       const float s0 = meta_lo(mk0, BFM), z0 = meta_hi(mk0, BFM);
       const float s1 = meta_lo(mk1, BFM), z1 = meta_hi(mk1, BFM);
       {
@@ -631,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       const float2 x23 = add2(make_float2(sc[t][2], sc[t][3]), nmu);
       const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
       const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g));
-      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8));
+      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g, hkc));
+      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8, hkc));
       float sv0 = meta_lo(mv0, BFM), zv0 = meta_hi(mv0, BFM);
       float sv1 = meta_lo(mv1, BFM), zv1 = meta_hi(mv1, BFM);
       if (!full[t]) {  // rows past the end may hold anything, even inf
@@ -674,11 +701,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       // lane group g's dims of the four token rows: D/16 bytes each, word
       // k/4 of them holding (as byte k mod 4) the codes of dims 2k, 2k + 1
       constexpr int kVW = DM::kVWords;
-      const uint8_t* vrow = vst + C::kcode(0) + (D / 16) * g;
+      // (a pair: lane group g's dims 16g .. are kv-head g / 4's)
+      const uint8_t* vrow = PAIR ? vst + C::kcode(0, g >> 2) + 8 * (g & 3)
+                                 : vst + C::kcode(0) + (D / 16) * g;
       uint32_t rw[4][kVW];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint8_t* src = vrow + (c + 4 * r) * kCodeRow;
+        const uint8_t* src = vrow + (c + 4 * r) * C::kCodeRow;
         if constexpr (kVW == 1) {
           rw[r][0] = *reinterpret_cast<const uint32_t*>(src);
         } else if constexpr (kVW == 2) {
@@ -960,22 +989,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   __syncthreads();
   if (p.rotate_v) smem_fwht<D>(qs, G, p.block_h);
   const float post = p.rotate_v ? p.c_h : 1.0f;
-  for (int idx = tid; idx < G * D; idx += kThreads)
-    p.out[(int64_t(seq) * p.num_q_heads + hq0) * D + idx] = qs[idx] * post;
+  // (a pair: column v's output is its own kv-head's half of the 128 dims)
+  for (int idx = tid; idx < G * kOutD; idx += kThreads) {
+    const int h = idx / kOutD, dd = idx - h * kOutD;
+    const float o = PAIR ? qs[h * D + (h >> 2) * kOutD + dd] : qs[idx];
+    p.out[(int64_t(seq) * p.num_q_heads + hq0) * kOutD + idx] = o * post;
+  }
 }
 
 // Launched with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream drains; it waits for it (griddepcontrol)
 // before reading anything.
-template <int D, int P, bool PACKED, bool APPEND, bool BFM>
+template <int D, int P, bool PACKED, bool APPEND, bool BFM, bool PAIR = false>
 cudaError_t launch_p(const DecodeParams& p, cudaStream_t stream) {
-  using C = Cfg<D, P>;
-  auto kernel = paged_decode_kernel<D, P, PACKED, APPEND, BFM>;
+  using C = Cfg<D, P, PAIR>;
+  auto kernel = paged_decode_kernel<D, P, PACKED, APPEND, BFM, PAIR>;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_splits, p.num_kv_heads, p.num_seqs);
+  cfg.gridDim = dim3(p.num_splits, PAIR ? p.num_kv_heads / 2 : p.num_kv_heads, p.num_seqs);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
@@ -1026,7 +1059,14 @@ cudaError_t SAW_CAT(launch_paged_decode_dims_w, SAW_DECODE_WARPS)(const DecodePa
                                                                   cudaStream_t stream) {
   if (p.append) return cudaErrorInvalidValue;
   switch (p.head_dim) {
-    case 64: return launch_dim<64>(p, stream);
+    case 64:
+      if (p.pair) {  // two kv-heads per CTA, as one head_dim-128 head (16-token pages)
+        if (p.num_seqs == 0) return cudaSuccess;
+        if (p.page_size != 16 || p.group != 4 || p.num_kv_heads % 2) return cudaErrorInvalidValue;
+        return p.meta_bf16 ? launch_p<128, 16, false, false, true, true>(p, stream)
+                           : launch_p<128, 16, false, false, false, true>(p, stream);
+      }
+      return launch_dim<64>(p, stream);
     case 256: return launch_dim<256>(p, stream);
     default: return cudaErrorInvalidValue;
   }

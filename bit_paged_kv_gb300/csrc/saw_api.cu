@@ -140,6 +140,18 @@ int32_t make_plan_bf16(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size
   return SAW_OK;
 }
 
+// Whether the decode runs two head_dim-64 kv-heads per CTA as one
+// head_dim-128 head (paged_decode.cu, PAIR): GQA 4, an even number of
+// kv-heads, 16-token pages, and a grid that keeps at least two CTAs per SM
+// with half as many CTAs (the plan's split count does not change).
+bool decode_pairs(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t page_size, int32_t splits) {
+  if (head_dim != 64 || page_size != 16 || num_kv_heads % 2 || num_q_heads != 4 * num_kv_heads)
+    return false;
+  const int sms = sm_count();
+  return int64_t(num_seqs) * (num_kv_heads / 2) * splits >= 2 * int64_t(sms > 0 ? sms : 148);
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,7 +259,11 @@ size_t saw_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
     return 0;
   if (splits <= 1) return 0;
   const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(splits);
-  return saw::decode_ticket_bytes(num_seqs, num_kv_heads) + rows * size_t(head_dim) * 4 +
+  // kv-head pairs keep 128-float partial rows
+  const int row_dim = decode_pairs(num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, splits)
+                          ? 2 * head_dim
+                          : head_dim;
+  return saw::decode_ticket_bytes(num_seqs, num_kv_heads) + rows * size_t(row_dim) * 4 +
          rows * 2 * 4;
 }
 
@@ -322,6 +338,7 @@ int32_t prepare_decode(saw::DecodeParams& p, const void* q, const void* k_cache,
   p.q_scale = float(scale * 1.4426950408889634);  // log2(e)
   p.in_f16 = (formats & SAW_FMT_F16_INPUT) ? 1 : 0;
   p.meta_bf16 = (formats & SAW_FMT_BF16_META) ? 1 : 0;
+  p.pair = decode_pairs(num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, splits) ? 1 : 0;
   if (need > 0) bind_decode_workspace(p, workspace);
   return SAW_OK;
 }
@@ -331,7 +348,7 @@ void bind_decode_workspace(DecodeParams& p, void* workspace) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.tickets = reinterpret_cast<uint32_t*>(ws);
   p.part_o = reinterpret_cast<float*>(ws + decode_ticket_bytes(p.num_seqs, p.num_kv_heads));
-  p.part_ml = p.part_o + rows * p.head_dim;
+  p.part_ml = p.part_o + rows * (p.pair ? 2 * p.head_dim : p.head_dim);
 }
 
 cudaError_t launch_decode_any(const DecodeParams& p, cudaStream_t stream) {

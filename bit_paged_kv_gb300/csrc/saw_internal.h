@@ -89,6 +89,10 @@ struct DecodeParams {
   int32_t head_dim;             // 128, or 64 / 256
   int32_t in_f16;               // 1: q, k_new and v_new are binary16
   int32_t meta_bf16;            // 1: the caches' (scale, zero) words are bfloat16
+  // 1: head_dim 64, GQA 4: each CTA serves two neighbouring kv-heads as one
+  // head_dim-128 "pair" head with 8 q-head columns (part_o rows are 128
+  // floats wide, the grid has num_kv_heads / 2 rows)
+  int32_t pair;
 };
 
 // One launcher per CTA shape (paged_decode.cu compiled once per shape), and
