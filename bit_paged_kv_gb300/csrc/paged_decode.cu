@@ -85,15 +85,18 @@ struct Dims {
 // A 16-token page is exactly [K chunk | V chunk]; larger pages are copied
 // as 16-row slices of their code and meta regions.
 //
-// PAIR (D = 128 standing for two head_dim-64 kv-heads, 16-token pages):
-// each tensor's part of a stage is the two kv-heads' page chunks back to
-// back, [codes 16 x 32 B | meta 16 words] twice, one copy; dims 0..63 of the
-// pair head are the first kv-head's, 64..127 the second's.  The lanes whose
-// K bytes, V dims or head columns fall in the second half read there.
+// PAIR (D = 128 standing for two head_dim-64 kv-heads, 16-token pages; the
+// code is written for D = 256 over two head_dim-128 kv-heads too, which on
+// GB300 measured slower than one kv-head per CTA): each tensor's part of a
+// stage is the two kv-heads' page chunks back to back, [codes 16 x D/4 B |
+// meta 16 words] twice, one copy; dims 0 .. D/2-1 of the pair head are the
+// first kv-head's, the rest the second's.  The lanes whose K bytes, V dims or
+// head columns fall in the second half read there.
 template <int D, int P, bool PAIR = false>
 struct Cfg {
   using DM = Dims<D>;
-  static_assert(!PAIR || (D == 128 && P == kStepTok), "pairs are two head_dim-64 heads, page 16");
+  static_assert(!PAIR || ((D == 128 || D == 256) && P == kStepTok),
+                "pairs are two head_dim-64 or -128 heads, page 16");
   static constexpr int kCodeRow = PAIR ? D / 4 : DM::kCodeRow;  // code bytes of one row in a chunk
   static constexpr int kStages = DM::kStages;
   static constexpr int kChunk = P * kCodeRow + 4 * P;
@@ -163,10 +166,10 @@ constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 // D: the head dimension.  A thread-in-group c of an MMA quad covers dims
 // [c D/4, (c+1) D/4) of a K row, 32-bit word w of it dims 8w .. 8w+7 of
 // that range; a lane group g covers dims [g D/8, (g+1) D/8) of the output.
-// PAIR: D = 128 stands for two neighbouring head_dim-64 kv-heads of GQA 4
+// PAIR: D stands for two neighbouring kv-heads of head_dim D/2 and GQA 4
 // (Cfg above): q-head column v < 4 is a q-head of the first kv-head, its q
-// zero in dims 64..127, v >= 4 one of the second, zero in dims 0..63; each
-// column's output is its own half of the 128 dims.  The tensor cores do the
+// zero in the second half of the D dims, v >= 4 one of the second, zero in
+// the first half; each column's output is its own half.  The tensor cores do the
 // zero products; every per-tile cost is shared by the two kv-heads.
 template <int D, int P, bool PACKED, bool APPEND, bool BFM, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(const DecodeParams p) {
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       full[t] = pok && tok0 + kStepTok <= L;  // warp-uniform
       constexpr int kKW = DM::kKWords;
       // (a pair: thread-in-group c reads half c & 1 of kv-head c / 2's row)
-      const uint8_t* krow = PAIR ? st + C::kcode(g, c >> 1) + 16 * (c & 1)
+      const uint8_t* krow = PAIR ? st + C::kcode(g, c >> 1) + (D / 8) * (c & 1)
                                  : st + C::kcode(g) + (D / 8) * c;
       uint32_t kaw[kKW], kbw[kKW];
       if constexpr (kKW == 2) {
@@ -701,8 +704,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       // lane group g's dims of the four token rows: D/16 bytes each, word
       // k/4 of them holding (as byte k mod 4) the codes of dims 2k, 2k + 1
       constexpr int kVW = DM::kVWords;
-      // (a pair: lane group g's dims 16g .. are kv-head g / 4's)
-      const uint8_t* vrow = PAIR ? vst + C::kcode(0, g >> 2) + 8 * (g & 3)
+      // (a pair: lane group g's dims g D/8 .. are kv-head g / 4's)
+      const uint8_t* vrow = PAIR ? vst + C::kcode(0, g >> 2) + (D / 16) * (g & 3)
                                  : vst + C::kcode(0) + (D / 16) * g;
       uint32_t rw[4][kVW];
 #pragma unroll

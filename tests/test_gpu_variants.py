@@ -136,19 +136,20 @@ def test_decode_edges(D, h, group, P):
 PAIR_LENS = [0, 1, 15, 16, 17, 33, 100, 511, 700, 1024, 2047, 2500]
 
 
+@pytest.mark.parametrize("D", [64])
 @pytest.mark.parametrize("case", ["one-split", "splits"])
 @pytest.mark.parametrize("rot,h", [((1, 1), 64), ((1, 0), 32), ((0, 0), 64), ((0, 1), 16)])
 @pytest.mark.parametrize("fmt", ["bf16", "f16", "bf16-meta"])
-def test_decode_head_dim_64_kv_head_pairs(case, rot, h, fmt):
-    """head_dim 64 at GQA 4 with many CTAs: each CTA serves two neighbouring
-    kv-heads as one head_dim-128 head (8 q-head columns, each q zero in the
-    other kv-head's half).  80 sequences (one split each) or 40 sequences up
-    to ~12000 tokens (several splits, the merge, 128-float partial rows);
-    lengths 0, 1, page edges and ragged tails; every output against the
-    oracle."""
+def test_decode_kv_head_pairs(D, case, rot, h, fmt):
+    """head_dim 64 at GQA 4 with many CTAs: each CTA serves two
+    neighbouring kv-heads as one head of twice the head_dim (8 q-head
+    columns, each q zero in the other kv-head's half).  80 sequences (one
+    split each) or 40 sequences up to ~12000 tokens (several splits, the
+    merge, partial rows twice as wide); lengths 0, 1, page edges and ragged
+    tails; every output against the oracle."""
     dt = torch.float16 if fmt == "f16" else torch.bfloat16
     meta_bf16 = fmt == "bf16-meta"
-    wl = W.QWEN3_8B_CONCURRENT.variant(head_dim=64, block_h=h, rotate_k=bool(rot[0]),
+    wl = W.QWEN3_8B_CONCURRENT.variant(head_dim=D, block_h=h, rotate_k=bool(rot[0]),
                                        rotate_v=bool(rot[1]), dist="student_t", nu=4)
     if case == "one-split":
         lens_l = (PAIR_LENS * 7)[:80]
@@ -164,19 +165,19 @@ def test_decode_head_dim_64_kv_head_pairs(case, rot, h, fmt):
     Lmax = max(lens_l)
     splits, _ = saw.saw_decode_plan(B, Hkv, P, Lmax, 0)
     if case == "splits":
-        # the pair form is on: its partial rows are 128 floats wide
+        # the pair form is on: its partial rows are 2 D floats wide
         rows = B * Hq * splits
         assert splits > 1
-        assert saw.saw_decode_workspace_bytes(B, Hq, Hkv, 64, P, Lmax, 0) == \
-            (B * Hkv * 8 + 15) // 16 * 16 + rows * 128 * 4 + rows * 2 * 4
+        assert saw.saw_decode_workspace_bytes(B, Hq, Hkv, D, P, Lmax, 0) == \
+            (B * Hkv * 8 + 15) // 16 * 16 + rows * 2 * D * 4 + rows * 2 * 4
     out, st = gpu_decode(q, kc, vc, bt.cuda(), lens.cuda(), Hkv, npages, P, wl.rotate_k,
                          wl.rotate_v, h, meta_bf16=meta_bf16)
     assert st == 0
     ref = oracle_decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, Hkv, npages, P,
                         wl.rotate_k, wl.rotate_v, h, meta_bf16=meta_bf16)
-    got = out.cpu().numpy().reshape(-1, 64)
+    got = out.cpu().numpy().reshape(-1, D)
     assert np.all(np.isfinite(got))
-    err = rel_err(got, ref, f"var-D64-pairs-{case}-rot{rot[0]}{rot[1]}-h{h}-{fmt}")
+    err = rel_err(got, ref, f"var-D{D}-pairs-{case}-rot{rot[0]}{rot[1]}-h{h}-{fmt}")
     assert err <= ATTN_TOL, f"relative error {err:.3e}"
 
 
