@@ -21,18 +21,25 @@
 //    K and V codes and their (scale, zero) words: a whole 16-token page, or
 //    16 rows of a larger page (codes and metadata copied separately).  A warp
 //    consumes its tiles two at a time; the two share one softmax update.
+//  * The loop is bound by instruction issue, so the common case carries no
+//    per-tile bookkeeping: a warp whose (page, kv-head) chunk indices are all
+//    valid and held in shared memory runs its whole tiles in turns of the
+//    ring with constant stage offsets and no checks; the last tiles, the one
+//    holding the new token and any warp with a bad page take a checked step.
 //  * Scores: S = K~ q' on the tensor cores (mma.m16n8k16, binary16 in,
 //    binary32 accumulate), 16 tokens on M, q-heads on N, the head dimension
 //    on K.  K~ are the raw codes, masked in place into binary16 subnormals
 //    (n * 2^-24 or n * 2^-20, exact); q' carries the matching power of two.
 //    The per-token scale and zero are applied afterwards:
-//    t = s*(K~.q') + z*sum(q').
+//    t = s*(K~.q') + z*sum(q').  MMA row j of a tile is token tok_of_row(j),
+//    a permutation that keeps the K-row and V-row reads conflict-free.
 //  * Output: O'^T += V~^T (p*s) on the tensor cores, dims on M, tokens on K,
-//    heads on N, plus sum_j p_j z_j on the CUDA cores.  p*s is moved from the
-//    score fragment to the B-operand layout with four warp shuffles.
+//    heads on N, plus sum_j p_j z_j on the CUDA cores.  p*s goes from the
+//    score fragment to the B-operand layout by two movmatrix transposes.
 //  * Online softmax in base 2 per head; sm_scale*log2(e) scales the binary32
 //    score after the MMA, so an unrotated q enters the MMA exactly; the
-//    accumulators are rescaled only when a running max grows.
+//    accumulators are rescaled only when a running max grows (the lanes
+//    compare their own scores first; the warp reduces only then).
 //  * Splits write (m, l, numerator) partials and take a ticket; the last
 //    split of a (sequence, kv-head) to finish merges them, normalizes and
 //    applies the inverse rotation to V's output.  With one split the CTA
@@ -59,11 +66,21 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Transpose of an 8 x 8 matrix of 16-bit elements held as MMA fragments
+// (lane 4r + q holds row r, columns 2q, 2q + 1).
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// Token of MMA row j (and j + 8) of a 16-token tile: a permutation that keeps
+// the K-row and V-row reads of a warp at the minimum number of shared-memory
+// wavefronts for 32- and 64-byte rows.
+__device__ __forceinline__ constexpr int tok_of_row(int j) { return j ^ (((j >> 1) ^ (j >> 2)) & 1); }
 // dim d of a reduction row sits at d + d / 16: the stores (lane group g
 // writes dims (D/8) g + ..) and the per-dim reads are then free of bank
 // conflicts
 __device__ __forceinline__ int red_col(int d) { return d + (d >> 4); }
-constexpr int kIdCap = 64;                // page ids a warp keeps in shared memory
 constexpr int kStepTok = 16;              // tokens per step (one MMA tile, one softmax update)
 
 // What depends on the head dimension D (64, 128 or 256).
@@ -78,6 +95,7 @@ struct Dims {
   static constexpr int kVWords = D / 64;           // V-row words per lane group
   static constexpr int kKSteps = D / 16;           // k-steps of the score product
   static constexpr bool kFragSmem = D > kHeadDim;  // q' fragments read per k-step from shared memory
+  static constexpr int kIdCap = D <= kHeadDim ? 256 : 64;  // chunk indices a warp keeps in shared memory
 };
 
 // Stage layout for a 16-token step, the same for every page size:
@@ -120,7 +138,7 @@ struct Cfg {
   static constexpr int kOffBars = kRing;
   static constexpr int kOffOk = kOffBars + kWarps * kStages * 8;               // int [W][stages]
   static constexpr int kOffIds = kOffOk + kWarps * kStages * 4;               // int [W][kIdCap]
-  static constexpr int kOffQh = kOffIds + kWarps * kIdCap * 4;                // half [2][D/16 t][32 lanes][4]
+  static constexpr int kOffQh = kOffIds + kWarps * DM::kIdCap * 4;                // half [2][D/16 t][32 lanes][4]
   static constexpr int kOffQsum = kOffQh + 2 * kMaxGroup * D * 2;             // float [2][8]
   static constexpr int kOffFlag = kOffQsum + 2 * kMaxGroup * 4;               // int
   static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (code bytes, meta)
@@ -155,12 +173,12 @@ __device__ void smem_fwht(float* buf, int nvec, int h) {
 constexpr uint32_t kLoNib = 0x000F000Fu;  // bits 0-3 of both halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 
-// PACKED (group <= 4): the MMA's 8 columns carry the hi parts of the (up to)
-// 4 heads in columns 0-3 and the lo parts in columns 4-7, both for q' in the
-// score product and for p*s in the output product; lanes c and c^2 of an
-// MMA quad then hold the two halves of the same heads and are summed with one
-// shuffle.  WIDE (group 5..8): all 8 columns are heads; the score product
-// runs twice (q' hi, then lo) and p*s is one binary16 value.
+// PACKED (group <= 4): the score MMA's 8 columns carry q' of the (up to) 4
+// heads as (hi, lo) pairs, head h in columns 2h, 2h + 1, so thread-in-group c
+// holds both parts of head c and adds them in place: one head per lane.  In
+// the output product head h is column 2h (columns 2h + 1 are zero).  WIDE
+// (group 5..8): all 8 columns are heads, two per lane; the score product
+// runs twice (q' hi, then lo).
 // BFM: the caches' (scale, zero) words are bfloat16 instead of binary16;
 // they are widened to binary32 either way, so only that step differs.
 // D: the head dimension.  A thread-in-group c of an MMA quad covers dims
@@ -202,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const int lane = tid & 31;
   const int g = lane >> 2;  // MMA group id
   const int c = lane & 3;   // thread in group
+  const int sg = tok_of_row(g);  // the token (and sg + 8) of this lane's score rows g, g + 8
   const int hkc = PAIR ? c >> 1 : 0;  // a pair's kv-head of this lane's head columns
   const int G = PAIR ? kMaxGroup : p.group;  // q-head columns of this CTA
   const int hq0 = kvh * G;
@@ -229,41 +248,59 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   }
 
   // ---- this warp's steps: step j covers tokens [p_begin*P + 16j, +16);
-  // warp w takes steps w, w+16, ...
+  // warp w takes steps w, w+W, ...
   const int n_steps = (p_end - p_begin) * C::kStepsPerPage;
   const int n_my = (warp < n_steps) ? (n_steps - warp + kWarps - 1) / kWarps : 0;
+  // this warp's leading steps whose 16 tokens all lie before L
+  const int full_steps = min(n_steps, (L - p_begin * P) / kStepTok);
+  const int n_full = (warp < full_steps) ? (full_steps - warp + kWarps - 1) / kWarps : 0;
   uint8_t* ring = smem + warp * kStages * C::kStage;
   uint64_t* wbars = bars + warp * kStages;
   int32_t* wok = stage_ok + warp * kStages;
   const int32_t* btab = p.block_tables + int64_t(seq) * p.max_blocks;
 
-  // physical page id of this warp's step i (-1: invalid)
-  auto page_id = [&](int i) {
+  // the (page, kv-head) chunk index of this warp's step i (-1: invalid page)
+  auto chunk_id = [&](int i) {
     const int lp = p_begin + (warp + i * kWarps) / C::kStepsPerPage;
-    int id = btab[lp];
+    const int id = btab[lp];
     if (id < 0 || id >= p.num_pages) {
       report(p.dev_status, SAW_ERR_DEVICE_INDEX);
-      id = -1;
+      return -1;
     }
-    return id;
+    return id * p.num_kv_heads + kv0;
   };
-  // the warp's page ids, fetched once instead of one dependent global load
-  // in front of every copy
+  // the warp's chunk indices, fetched once instead of one dependent global
+  // load in front of every copy
+  constexpr int kIdCap = DM::kIdCap;
   int32_t* wids = reinterpret_cast<int32_t*>(smem + C::kOffIds) + warp * kIdCap;
-  for (int e = lane; e < n_my && e < kIdCap; e += 32) wids[e] = page_id(e);
+  bool bad = false;
+  for (int e = lane; e < n_my && e < kIdCap; e += 32) {
+    const int ci = chunk_id(e);
+    wids[e] = ci;
+    bad = bad || ci < 0;
+  }
+  // clean: every chunk index of this warp is in the list and valid, so a
+  // copy needs no checks and every stage holds its page
+  const bool clean = !__any_sync(kFull, bad) && n_my <= kIdCap;
   __syncwarp();
 
-  auto issue = [&](int i) {  // lane 0 only
-    const int s = i % kStages;
+  // lane 0 only; s = i % kStages.  CHECKED: the index may be missing from
+  // the list or invalid (a skipped page: the stage is marked and not filled).
+  auto issue = [&](auto checked, int i, int s) {
     uint8_t* st = ring + s * C::kStage;
-    const int pid = (i < kIdCap) ? wids[i] : page_id(i);
-    wok[s] = (pid >= 0);
-    if (pid < 0) {
-      mbar_arrive(&wbars[s]);
-      return;
+    int ci;
+    if constexpr (decltype(checked)::value) {
+      ci = (i < kIdCap) ? wids[i] : chunk_id(i);
+      wok[s] = (ci >= 0);
+      if (ci < 0) {
+        mbar_arrive(&wbars[s]);
+        return;
+      }
+    } else {
+      ci = wids[i];
     }
     mbar_arrive_expect_tx(&wbars[s], C::kStage);
-    const int64_t off = (int64_t(pid) * p.num_kv_heads + kv0) * C::kChunk;
+    const int64_t off = int64_t(ci) * C::kChunk;
     if (P == 16) {  // the page's chunk (a pair: both kv-heads' chunks), K then V
       bulk_g2s(st, p.k_cache + off, C::kHalf, &wbars[s]);
       bulk_g2s(st + C::kHalf, p.v_cache + off, C::kHalf, &wbars[s]);
@@ -281,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   if (lane == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(&wbars[i], 1);
     mbar_fence_init();
-    for (int i = 0; i < kStages && i < n_my; ++i) issue(i);
+    for (int i = 0; i < kStages && i < n_my; ++i) issue(std::true_type{}, i, i);
   }
   // decode step: the page that receives the new token (position L-1)
   const int new_tok = L - 1;
@@ -341,10 +378,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   // enters the MMA exactly.
   // q' is stored in the B-fragment order of the score MMA: buffer 0 holds,
   // for k-step t and lane (g, c), the four binary16 values of that lane's
-  // two fragment registers (PACKED: column g = hi of head g for g < 4, lo
-  // of head g - 4 otherwise; WIDE: hi of head g); buffer 1 (WIDE) the lo
-  // parts.  Element d of a head, with c = d / (D/4), o = d mod (D/4) and
-  // j = o mod 8, sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group
+  // two fragment registers (PACKED: column g = hi of head g / 2 for even g,
+  // lo for odd g; WIDE: hi of head g); buffer 1 (WIDE) the lo parts.
+  // Element d of a head, with c = d / (D/4), o = d mod (D/4) and j = o mod 8, sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group
   // c, register j & 1, half (j >> 2) & 1: the nibble the K codes put there.
   constexpr int kE = DM::kE;
   if (warp < kMaxGroup) {
@@ -429,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       constexpr int kLo = DM::kKSteps * 32 * 4;  // halves in buffer 0
       if (PACKED) {
         if (h < kMaxGroup / 2) {
-          qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
-          qh[(t * 32 + (h + 4) * 4 + c_) * 4 + w2] = lo;
+          qh[(t * 32 + 2 * h * 4 + c_) * 4 + w2] = hi;
+          qh[(t * 32 + (2 * h + 1) * 4 + c_) * 4 + w2] = lo;
         }
       } else {
         qh[(t * 32 + h * 4 + c_) * 4 + w2] = hi;
@@ -449,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 
   // B fragments of q' for the score MMA (k-step t uses word t/2 of the
   // thread-in-group's share of a token's codes: bytes (0,2) for even t,
-  // (1,3) for odd t).  Column g: PACKED -> hi of head g (g < 4) or lo of
-  // head g - 4; WIDE -> head g.  Kept in registers up to D = 128; read from
+  // (1,3) for odd t).  Column g: PACKED -> hi (even g) or lo (odd g) of
+  // head g / 2; WIDE -> head g.  Kept in registers up to D = 128; read from
   // shared memory per k-step beyond (the output accumulators take the room).
   constexpr int kKS = DM::kKSteps;
   constexpr int kRegKS = DM::kFragSmem ? 1 : kKS;
@@ -470,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       }
     }
   }
-  // this thread's two heads: the MMA gives acc = 2^(S-24) (n . q'), so the
-  // base-2 logit t = sm'*(s (n.q') + z sum(q')) = (sm' 2^(24-S) s) acc +
-  // (sm' sum(q')) z.
-  const int hb = PACKED ? 2 * (c & 1) : 2 * c;
+  // this thread's heads (PACKED: head c, as A; WIDE: heads 2c, 2c + 1): the
+  // MMA gives acc = 2^(S-24) (n . q'), so the base-2 logit
+  // t = sm'*(s (n.q') + z sum(q')) = (sm' 2^(24-S) s) acc + (sm' sum(q')) z.
+  const int hb = PACKED ? c : 2 * c;
   const float qsA = qsum[hb] * p.q_scale, qsB = qsum[hb + 1] * p.q_scale;
   const float skA = qsum[kMaxGroup + hb] * p.q_scale, skB = qsum[kMaxGroup + hb + 1] * p.q_scale;
   const float2 skAB = make_float2(skA, skB), qsAB = make_float2(qsA, qsB);
@@ -485,26 +521,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.0f, 0.0f};
   float z_run[2] = {0.0f, 0.0f};
+  float2 nmu = make_float2(-0.0f, -0.0f);  // minus the running maxes (0 while they are -inf)
   bool failed = false;
   int waited = 0;  // first of this warp's tiles not yet consumed
 
   // One step consumes NT consecutive tiles of this warp (i, i+1, ...): the
   // tiles' score products and PV products are independent, and they share
   // one max reduction and one rescale of the online softmax.
-  auto step = [&](auto ntc, int i) -> bool {
+  // S0 >= 0: i % kStages == S0, known here, so the stage offsets are
+  // constants; and the warp is clean and the tiles are whole and do not hold
+  // the new token, so no tile needs a check.
+  auto step = [&](auto ntc, auto s0c, int i) -> bool {
     constexpr int NT = decltype(ntc)::value;
+    constexpr int S0 = decltype(s0c)::value;
+    constexpr bool kChecks = S0 < 0;
+    auto stage = [&](int t) { return S0 >= 0 ? (S0 + t) % kStages : (i + t) % kStages; };
     waited = i;
     bool ok = true;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
-      ok = mbar_wait_bounded(&wbars[(i + t) % kStages], ((i + t) / kStages) & 1) && ok;
+      ok = mbar_wait_bounded(&wbars[stage(t)], ((i + t) / kStages) & 1) && ok;
     if (!__all_sync(kFull, ok)) return false;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      if (APPEND && i + t == new_i) {
+      if (APPEND && kChecks && i + t == new_i) {
         // replace the copied row of the new token by its freshly quantized one
         const int row = new_local % kStepTok;
-        uint8_t* w = ring + ((i + t) % kStages) * C::kStage;
+        uint8_t* w = ring + stage(t) * C::kStage;
         if (lane < 16) {
           const int tensor = lane >> 3, part = lane & 7;  // 8 x 8 bytes per tensor
           const uint8_t* nr = newrow + tensor * (kCodeRow + 16);
@@ -525,17 +568,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     bool v0[NT], v1[NT], full[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const int s_ = (i + t) % kStages;
+      const int s_ = stage(t);
       const uint8_t* st = ring + s_ * C::kStage;
-      const int tok0 = p_begin * P + (warp + (i + t) * kWarps) * kStepTok;
-      const bool pok = wok[s_] != 0;
-      v0[t] = pok && (tok0 + g) < L;
-      v1[t] = pok && (tok0 + g + 8) < L;
-      full[t] = pok && tok0 + kStepTok <= L;  // warp-uniform
+      full[t] = !kChecks || ((i + t < n_full) && (clean || wok[s_] != 0));  // warp-uniform
       constexpr int kKW = DM::kKWords;
       // (a pair: thread-in-group c reads half c & 1 of kv-head c / 2's row)
-      const uint8_t* krow = PAIR ? st + C::kcode(g, c >> 1) + (D / 8) * (c & 1)
-                                 : st + C::kcode(g) + (D / 8) * c;
+      const uint8_t* krow = PAIR ? st + C::kcode(sg, c >> 1) + (D / 8) * (c & 1)
+                                 : st + C::kcode(sg) + (D / 8) * c;
       uint32_t kaw[kKW], kbw[kKW];
       if constexpr (kKW == 2) {
         const uint2 ka = *reinterpret_cast<const uint2*>(krow);
@@ -584,16 +623,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) d[j] += e2[j];
-      if (PACKED) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) d[j] += __shfl_xor_sync(kFull, d[j], 2);
-      }
-      // this lane's head columns 2c, 2c+1 (a pair: of kv-head c / 2)
-      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g, hkc));
-      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(g + 8, hkc));
+      // the (scale, zero) words of this lane's rows (a pair: of kv-head c / 2)
+      const uint32_t mk0 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(sg, hkc));
+      const uint32_t mk1 = *reinterpret_cast<const uint32_t*>(st + C::kmeta(sg + 8, hkc));
       const float s0 = meta_lo(mk0, BFM), z0 = meta_hi(mk0, BFM);
       const float s1 = meta_lo(mk1, BFM), z1 = meta_hi(mk1, BFM);
-      {
+      if constexpr (PACKED) {
+        // head c of rows g and g + 8: hi part (column 2c) + lo part (2c+1)
+        const float2 hl = add2(make_float2(d[0], d[2]), make_float2(d[1], d[3]));
+        const float2 r = fma2(mul2(make_float2(s0, s1), make_float2(skA, skA)), hl,
+                              mul2(make_float2(z0, z1), make_float2(qsA, qsA)));
+        sc[t][0] = r.x;
+        sc[t][2] = r.y;
+        sc[t][1] = sc[t][3] = 0.0f;
+      } else {
         // heads (A, B) of rows g and g + 8, two per instruction
         const float2 r0 = fma2(mul2(make_float2(s0, s0), skAB), make_float2(d[0], d[1]),
                                mul2(make_float2(z0, z0), qsAB));
@@ -605,6 +648,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         sc[t][3] = r1.y;
       }
       if (!full[t]) {  // the tile holding the end of the sequence, or a bad page
+        const int tok0 = p_begin * P + (warp + (i + t) * kWarps) * kStepTok;
+        const bool pok = clean || wok[s_] != 0;
+        v0[t] = pok && (tok0 + sg) < L;
+        v1[t] = pok && (tok0 + sg + 8) < L;
         sc[t][0] = v0[t] ? sc[t][0] : -INFINITY;
         sc[t][1] = v0[t] ? sc[t][1] : -INFINITY;
         sc[t][2] = v1[t] ? sc[t][2] : -INFINITY;
@@ -612,57 +659,83 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       }
     }
 
-    // ---- online softmax: rescale only when a running max grows
+    // ---- online softmax: rescale only when a running max grows.  A head's
+    // max over the warp exceeds its running max exactly when one lane's
+    // does, so the lanes compare first and reduce only when one grew.
     float mloc0, mloc1;
     if (NT == 2) {
       mloc0 = fmaxf(fmax3(sc[0][0], sc[0][2], sc[1][0]), sc[1][2]);
-      mloc1 = fmaxf(fmax3(sc[0][1], sc[0][3], sc[1][1]), sc[1][3]);
+      mloc1 = PACKED ? -INFINITY : fmaxf(fmax3(sc[0][1], sc[0][3], sc[1][1]), sc[1][3]);
     } else {
       mloc0 = fmaxf(sc[0][0], sc[0][2]);
-      mloc1 = fmaxf(sc[0][1], sc[0][3]);
+      mloc1 = PACKED ? -INFINITY : fmaxf(sc[0][1], sc[0][3]);
     }
+    if (PACKED ? __any_sync(kFull, mloc0 > m_run[0])
+               : __any_sync(kFull, (mloc0 > m_run[0]) || (mloc1 > m_run[1]))) {
+      if constexpr (PACKED) {
 #pragma unroll
-    for (int x = 4; x < 32; x <<= 1) {
-      mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
-      mloc1 = fmaxf(mloc1, __shfl_xor_sync(kFull, mloc1, x));
-    }
-    if (__any_sync(kFull, (mloc0 > m_run[0]) || (mloc1 > m_run[1]))) {
-      const float mn0 = fmaxf(m_run[0], mloc0), mn1 = fmaxf(m_run[1], mloc1);
-      const float al0 = ex2(m_run[0] - ((mn0 == -INFINITY) ? 0.0f : mn0));
-      const float al1 = ex2(m_run[1] - ((mn1 == -INFINITY) ? 0.0f : mn1));
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-      const float2 al = make_float2(al0, al1);  // columns 0, 2 are head A, 1, 3 head B
-      const float2 lz = mul2(make_float2(l_run[0], l_run[1]), al);
-      const float2 zz = mul2(make_float2(z_run[0], z_run[1]), al);
-      l_run[0] = lz.x;
-      l_run[1] = lz.y;
-      z_run[0] = zz.x;
-      z_run[1] = zz.y;
+        for (int x = 4; x < 32; x <<= 1) mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
+        const float mn0 = fmaxf(m_run[0], mloc0);
+        const float mu0 = (mn0 == -INFINITY) ? 0.0f : mn0;
+        const float al0 = ex2(m_run[0] - mu0);
+        m_run[0] = mn0;
+        l_run[0] *= al0;
+        z_run[0] *= al0;
 #pragma unroll
-      for (int k = 0; k < kMT; ++k) {
-        const float2 a01 = mul2(make_float2(acc[k][0], acc[k][1]), al);
-        const float2 a23 = mul2(make_float2(acc[k][2], acc[k][3]), al);
-        acc[k][0] = a01.x;
-        acc[k][1] = a01.y;
-        acc[k][2] = a23.x;
-        acc[k][3] = a23.y;
+        for (int k = 0; k < kMT; ++k) {  // columns 2c + 1 stay zero
+          acc[k][0] *= al0;
+          acc[k][2] *= al0;
+        }
+        nmu.x = -mu0;
+      } else {
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+          mloc0 = fmaxf(mloc0, __shfl_xor_sync(kFull, mloc0, x));
+          mloc1 = fmaxf(mloc1, __shfl_xor_sync(kFull, mloc1, x));
+        }
+        const float mn0 = fmaxf(m_run[0], mloc0), mn1 = fmaxf(m_run[1], mloc1);
+        const float al0 = ex2(m_run[0] - ((mn0 == -INFINITY) ? 0.0f : mn0));
+        const float al1 = ex2(m_run[1] - ((mn1 == -INFINITY) ? 0.0f : mn1));
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        const float2 al = make_float2(al0, al1);  // columns 0, 2 are head A, 1, 3 head B
+        const float2 lz = mul2(make_float2(l_run[0], l_run[1]), al);
+        const float2 zz = mul2(make_float2(z_run[0], z_run[1]), al);
+        l_run[0] = lz.x;
+        l_run[1] = lz.y;
+        z_run[0] = zz.x;
+        z_run[1] = zz.y;
+#pragma unroll
+        for (int k = 0; k < kMT; ++k) {
+          const float2 a01 = mul2(make_float2(acc[k][0], acc[k][1]), al);
+          const float2 a23 = mul2(make_float2(acc[k][2], acc[k][3]), al);
+          acc[k][0] = a01.x;
+          acc[k][1] = a01.y;
+          acc[k][2] = a23.x;
+          acc[k][3] = a23.y;
+        }
+        // x - mu = x + (-mu), exactly
+        nmu = make_float2(-((mn0 == -INFINITY) ? 0.0f : mn0), -((mn1 == -INFINITY) ? 0.0f : mn1));
       }
     }
-    const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
-    const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
-    const float2 nmu = make_float2(-mu0, -mu1);  // x - mu = x + (-mu), exactly
 
     // ---- probabilities, V terms, and the PV products
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const uint8_t* vst = ring + ((i + t) % kStages) * C::kStage + C::kHalf;
-      const float2 x01 = add2(make_float2(sc[t][0], sc[t][1]), nmu);
-      const float2 x23 = add2(make_float2(sc[t][2], sc[t][3]), nmu);
-      const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-      const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g, hkc));
-      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(g + 8, hkc));
+      const uint8_t* vst = ring + stage(t) * C::kStage + C::kHalf;
+      float2 p01, p23;  // PACKED: p01 = (row g, row g + 8) of head c
+      if constexpr (PACKED) {
+        const float2 x = add2(make_float2(sc[t][0], sc[t][2]), make_float2(nmu.x, nmu.x));
+        p01 = make_float2(ex2(x.x), ex2(x.y));
+        p23 = p01;
+      } else {
+        const float2 x01 = add2(make_float2(sc[t][0], sc[t][1]), nmu);
+        const float2 x23 = add2(make_float2(sc[t][2], sc[t][3]), nmu);
+        p01 = make_float2(ex2(x01.x), ex2(x01.y));
+        p23 = make_float2(ex2(x23.x), ex2(x23.y));
+      }
+      const uint32_t mv0 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(sg, hkc));
+      const uint32_t mv1 = *reinterpret_cast<const uint32_t*>(vst + C::kmeta(sg + 8, hkc));
       float sv0 = meta_lo(mv0, BFM), zv0 = meta_hi(mv0, BFM);
       float sv1 = meta_lo(mv1, BFM), zv1 = meta_hi(mv1, BFM);
       if (!full[t]) {  // rows past the end may hold anything, even inf
@@ -671,7 +744,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         sv1 = v1[t] ? sv1 : 0.0f;
         zv1 = v1[t] ? zv1 : 0.0f;
       }
-      {
+      uint32_t b0, b1;
+      if constexpr (PACKED) {
+        l_run[0] = l_run[0] + (p01.x + p01.y);
+        z_run[0] = z_run[0] + fmaf(p01.y, zv1, p01.x * zv0);
+        const float2 ps = mul2(p01, make_float2(sv0, sv1));
+        // the two 8 x 8 blocks (score rows 0-7 and 8-15 by columns 2c: head
+        // c; columns 2c + 1 zero), transposed: B column 2h carries head h
+        b0 = movm_t(pack_half2(ps.x, 0.0f));
+        b1 = movm_t(pack_half2(ps.y, 0.0f));
+      } else {
         const float2 l2 = add2(make_float2(l_run[0], l_run[1]), add2(p01, p23));
         const float2 z2 = add2(make_float2(z_run[0], z_run[1]),
                                fma2(p23, make_float2(zv1, zv1), mul2(p01, make_float2(zv0, zv0))));
@@ -679,27 +761,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         l_run[1] = l2.y;
         z_run[0] = z2.x;
         z_run[1] = z2.y;
+        // (p*s) for this thread's columns over tokens (g, g+8) as binary16
+        const float2 ps01 = mul2(p01, make_float2(sv0, sv0));
+        const float2 ps23 = mul2(p23, make_float2(sv1, sv1));
+        // the two 8 x 8 blocks (score rows 0-7 and 8-15 by head columns),
+        // transposed, are the B fragments of the PV product: k-columns
+        // 2c, 2c+1 (and 2c+8, 2c+9) carry the tokens of score rows 2c, 2c+1
+        b0 = movm_t(pack_half2(ps01.x, ps01.y));
+        b1 = movm_t(pack_half2(ps23.x, ps23.y));
       }
-      // (p*s) for this thread's columns over tokens (g, g+8) as binary16.
-      // PACKED: lanes c >= 2 repeat the heads of lanes c - 2, so output
-      // columns 4-7 duplicate 0-3 and are never read.
-      const float2 ps01 = mul2(p01, make_float2(sv0, sv0));
-      const float2 ps23 = mul2(p23, make_float2(sv1, sv1));
-      const float ps0 = ps01.x, ps1 = ps01.y, ps2 = ps23.x, ps3 = ps23.y;
-      const uint32_t X = pack_half2(ps0, ps2);
-      const uint32_t Y = pack_half2(ps1, ps3);
-      // PV k-columns (2c, 2c+1, 2c+8, 2c+9) carry tokens (c, c+4, c+8, c+12):
-      // any order works when A and B agree, and this one puts the four V
-      // rows a lane group reads 64 bytes apart (2-way bank conflicts, not 4)
-      const int src0 = 4 * c + (g >> 1);
-      const uint32_t xa = __shfl_sync(kFull, X, src0);
-      const uint32_t ya = __shfl_sync(kFull, Y, src0);
-      const uint32_t xb = __shfl_sync(kFull, X, src0 + 16);
-      const uint32_t yb = __shfl_sync(kFull, Y, src0 + 16);
-      const uint32_t va = (g & 1) ? ya : xa;  // tokens (c, c+8)
-      const uint32_t vb = (g & 1) ? yb : xb;  // tokens (c+4, c+12)
-      const uint32_t b0 = prmt(va, vb, 0x5410u);
-      const uint32_t b1 = prmt(va, vb, 0x7632u);
 
       // lane group g's dims of the four token rows: D/16 bytes each, word
       // k/4 of them holding (as byte k mod 4) the codes of dims 2k, 2k + 1
@@ -710,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       uint32_t rw[4][kVW];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint8_t* src = vrow + (c + 4 * r) * C::kCodeRow;
+        const uint8_t* src = vrow + (tok_of_row(2 * c + (r & 1)) + 8 * (r >> 1)) * C::kCodeRow;
         if constexpr (kVW == 1) {
           rw[r][0] = *reinterpret_cast<const uint32_t*>(src);
         } else if constexpr (kVW == 2) {
@@ -747,20 +817,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     if (lane == 0) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
-        if (i + t + kStages < n_my) issue(i + t + kStages);
+        if (i + t + kStages < n_my) {
+          if (!kChecks) {
+            issue(std::false_type{}, i + t + kStages, stage(t));
+          } else if (clean) {
+            issue(std::false_type{}, i + t + kStages, stage(t));
+          } else {
+            issue(std::true_type{}, i + t + kStages, stage(t));
+          }
+        }
     }
     return true;
   };
 
   {
+    using Dyn = std::integral_constant<int, -1>;
     int i = 0;
-    for (; i + 1 < n_my; i += 2) {
-      if (!step(std::integral_constant<int, 2>{}, i)) {
+    if constexpr (kStages == 4) {
+      // whole turns of the ring: two steps with constant stages, up to the
+      // first tile that is not whole or holds the new token
+      const int lim = clean ? min(n_full, new_i >= 0 ? new_i : n_my) : 0;
+      for (; i + 3 < lim; i += 4) {
+        if (!step(std::integral_constant<int, 2>{}, std::integral_constant<int, 0>{}, i) ||
+            !step(std::integral_constant<int, 2>{}, std::integral_constant<int, 2>{}, i + 2)) {
+          failed = true;
+          break;
+        }
+      }
+    }
+    for (; !failed && i + 1 < n_my; i += 2) {
+      if (!step(std::integral_constant<int, 2>{}, Dyn{}, i)) {
         failed = true;
         break;
       }
     }
-    if (!failed && i < n_my && !step(std::integral_constant<int, 1>{}, i)) failed = true;
+    if (!failed && i < n_my && !step(std::integral_constant<int, 1>{}, Dyn{}, i)) failed = true;
   }
 
   if (failed) {
@@ -805,7 +896,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   float* red_z = red_l + kWarps * kMaxGroup;
   float* wgt = red_z + kWarps * kMaxGroup;                            // [16][8]
   float* tot = wgt + kWarps * kMaxGroup;                              // den, zz, M [3][8]
-  if (!PACKED || c < 2) {
+  if constexpr (PACKED) {  // head c: output columns 2c
+    if (g == 0) {
+      red_m[warp * kMaxGroup + c] = m_run[0];
+      red_l[warp * kMaxGroup + c] = l_run[0];
+      red_z[warp * kMaxGroup + c] = z_run[0];
+    }
+    float* base0 = red_acc + (warp * kMaxGroup + c) * kRedStride;
+#pragma unroll
+    for (int k = 0; k < kMT; ++k) {
+      base0[red_col((D / 8) * g + 2 * k)] = acc[k][0];
+      base0[red_col((D / 8) * g + 2 * k + 1)] = acc[k][2];
+    }
+  } else {
     if (g == 0) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
