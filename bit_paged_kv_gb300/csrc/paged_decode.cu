@@ -20,7 +20,8 @@
 //    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds one tile's
 //    K and V codes and their (scale, zero) words: a whole 16-token page, or
 //    16 rows of a larger page (codes and metadata copied separately).  A warp
-//    consumes its tiles two at a time; the two share one softmax update.
+//    consumes its tiles two at a time; the two share one softmax update, and
+//    (four-stage rings) one mbarrier: one wait, one refill arrival.
 //  * The loop is bound by instruction issue, so the common case carries no
 //    per-tile bookkeeping: a warp whose (page, kv-head) chunk indices are all
 //    valid and held in shared memory runs its whole tiles in turns of the
@@ -284,41 +285,64 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const bool clean = !__any_sync(kFull, bad) && n_my <= kIdCap;
   __syncwarp();
 
-  // lane 0 only; s = i % kStages.  CHECKED: the index may be missing from
-  // the list or invalid (a skipped page: the stage is marked and not filled).
-  auto issue = [&](auto checked, int i, int s) {
-    uint8_t* st = ring + s * C::kStage;
-    int ci;
-    if constexpr (decltype(checked)::value) {
-      ci = (i < kIdCap) ? wids[i] : chunk_id(i);
-      wok[s] = (ci >= 0);
-      if (ci < 0) {
-        mbar_arrive(&wbars[s]);
-        return;
+  // With an even ring, stages 2b and 2b + 1 complete on one barrier: a
+  // warp's tiles are consumed and refilled two at a time, so one wait and
+  // one arrival serve both.
+  constexpr bool kPairBars = kStages % 2 == 0;
+  auto bar_of = [&](int s) { return kPairBars ? &wbars[s >> 1] : &wbars[s]; };
+  // lane 0 only: tiles i .. i + n - 1 (n = 2 only with paired barriers) into
+  // stages s = i % kStages, s + 1.  CHECKED: an index may be missing from the
+  // list or invalid (a skipped page: the stage is marked and not filled).
+  auto issue = [&](auto checked, int i, int s, int n) {
+    int ci[2] = {-1, -1};
+    int valid = 0;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u < n) {
+        if constexpr (decltype(checked)::value) {
+          ci[u] = (i + u < kIdCap) ? wids[i + u] : chunk_id(i + u);
+          wok[s + u] = (ci[u] >= 0);
+        } else {
+          ci[u] = wids[i + u];
+        }
+        valid += ci[u] >= 0;
       }
-    } else {
-      ci = wids[i];
     }
-    mbar_arrive_expect_tx(&wbars[s], C::kStage);
-    const int64_t off = int64_t(ci) * C::kChunk;
-    if (P == 16) {  // the page's chunk (a pair: both kv-heads' chunks), K then V
-      bulk_g2s(st, p.k_cache + off, C::kHalf, &wbars[s]);
-      bulk_g2s(st + C::kHalf, p.v_cache + off, C::kHalf, &wbars[s]);
-    } else {
-      const int part = (warp + i * kWarps) % C::kStepsPerPage;
-      const int64_t codes = off + part * (kStepTok * kCodeRow);
-      const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
-      bulk_g2s(st, p.k_cache + codes, kStepTok * kCodeRow, &wbars[s]);
-      bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, &wbars[s]);
-      bulk_g2s(st + C::kHalf, p.v_cache + codes, kStepTok * kCodeRow, &wbars[s]);
-      bulk_g2s(st + C::kHalf + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4, &wbars[s]);
+    uint64_t* bar = bar_of(s);
+    if (valid == 0) {
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_arrive_expect_tx(bar, valid * C::kStage);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u < n && ci[u] >= 0) {
+        uint8_t* st = ring + (s + u) * C::kStage;
+        const int64_t off = int64_t(ci[u]) * C::kChunk;
+        if (P == 16) {  // the page's chunk (a pair: both kv-heads' chunks), K then V
+          bulk_g2s(st, p.k_cache + off, C::kHalf, bar);
+          bulk_g2s(st + C::kHalf, p.v_cache + off, C::kHalf, bar);
+        } else {
+          const int part = (warp + (i + u) * kWarps) % C::kStepsPerPage;
+          const int64_t codes = off + part * (kStepTok * kCodeRow);
+          const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
+          bulk_g2s(st, p.k_cache + codes, kStepTok * kCodeRow, bar);
+          bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, bar);
+          bulk_g2s(st + C::kHalf, p.v_cache + codes, kStepTok * kCodeRow, bar);
+          bulk_g2s(st + C::kHalf + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4, bar);
+        }
+      }
     }
   };
 
   if (lane == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&wbars[i], 1);
+    for (int i = 0; i < (kPairBars ? kStages / 2 : kStages); ++i) mbar_init(&wbars[i], 1);
     mbar_fence_init();
-    for (int i = 0; i < kStages && i < n_my; ++i) issue(std::true_type{}, i, i);
+    if constexpr (kPairBars) {
+      for (int i = 0; i < kStages && i < n_my; i += 2) issue(std::true_type{}, i, i, min(2, n_my - i));
+    } else {
+      for (int i = 0; i < kStages && i < n_my; ++i) issue(std::true_type{}, i, i, 1);
+    }
   }
   // decode step: the page that receives the new token (position L-1)
   const int new_tok = L - 1;
@@ -538,9 +562,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     auto stage = [&](int t) { return S0 >= 0 ? (S0 + t) % kStages : (i + t) % kStages; };
     waited = i;
     bool ok = true;
+    if constexpr (kPairBars) {
+      ok = mbar_wait_bounded(bar_of(stage(0)), (i / kStages) & 1);  // i is even
+    } else {
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
-      ok = mbar_wait_bounded(&wbars[stage(t)], ((i + t) / kStages) & 1) && ok;
+      for (int t = 0; t < NT; ++t)
+        ok = mbar_wait_bounded(bar_of(stage(t)), ((i + t) / kStages) & 1) && ok;
+    }
     if (!__all_sync(kFull, ok)) return false;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -565,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 
     // ---- scores of the NT x 16 tokens
     float sc[NT][4];
-    bool v0[NT], v1[NT], full[NT];
+    bool full[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int s_ = stage(t);
@@ -650,12 +678,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       if (!full[t]) {  // the tile holding the end of the sequence, or a bad page
         const int tok0 = p_begin * P + (warp + (i + t) * kWarps) * kStepTok;
         const bool pok = clean || wok[s_] != 0;
-        v0[t] = pok && (tok0 + sg) < L;
-        v1[t] = pok && (tok0 + sg + 8) < L;
-        sc[t][0] = v0[t] ? sc[t][0] : -INFINITY;
-        sc[t][1] = v0[t] ? sc[t][1] : -INFINITY;
-        sc[t][2] = v1[t] ? sc[t][2] : -INFINITY;
-        sc[t][3] = v1[t] ? sc[t][3] : -INFINITY;
+        const bool v0 = pok && (tok0 + sg) < L;
+        const bool v1 = pok && (tok0 + sg + 8) < L;
+        sc[t][0] = v0 ? sc[t][0] : -INFINITY;
+        sc[t][1] = v0 ? sc[t][1] : -INFINITY;
+        sc[t][2] = v1 ? sc[t][2] : -INFINITY;
+        sc[t][3] = v1 ? sc[t][3] : -INFINITY;
       }
     }
 
@@ -739,10 +767,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
       float sv0 = meta_lo(mv0, BFM), zv0 = meta_hi(mv0, BFM);
       float sv1 = meta_lo(mv1, BFM), zv1 = meta_hi(mv1, BFM);
       if (!full[t]) {  // rows past the end may hold anything, even inf
-        sv0 = v0[t] ? sv0 : 0.0f;
-        zv0 = v0[t] ? zv0 : 0.0f;
-        sv1 = v1[t] ? sv1 : 0.0f;
-        zv1 = v1[t] ? zv1 : 0.0f;
+        // (a valid row's score is never -inf: only the masking above sets it)
+        const bool v0 = sc[t][0] != -INFINITY, v1 = sc[t][2] != -INFINITY;
+        sv0 = v0 ? sv0 : 0.0f;
+        zv0 = v0 ? zv0 : 0.0f;
+        sv1 = v1 ? sv1 : 0.0f;
+        zv1 = v1 ? zv1 : 0.0f;
       }
       uint32_t b0, b1;
       if constexpr (PACKED) {
@@ -815,17 +845,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
 
     __syncwarp();
     if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (i + t + kStages < n_my) {
-          if (!kChecks) {
-            issue(std::false_type{}, i + t + kStages, stage(t));
-          } else if (clean) {
-            issue(std::false_type{}, i + t + kStages, stage(t));
+      if constexpr (kPairBars) {
+        const int nxt = i + kStages;  // the tiles that refill this step's stages
+        const int n = min(NT, n_my - nxt);
+        if (n > 0) {
+          if (!kChecks || clean) {
+            issue(std::false_type{}, nxt, stage(0), n);
           } else {
-            issue(std::true_type{}, i + t + kStages, stage(t));
+            issue(std::true_type{}, nxt, stage(0), n);
           }
         }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (i + t + kStages < n_my) {
+            if (!kChecks || clean) {
+              issue(std::false_type{}, i + t + kStages, stage(t), 1);
+            } else {
+              issue(std::true_type{}, i + t + kStages, stage(t), 1);
+            }
+          }
+        }
+      }
     }
     return true;
   };
@@ -833,32 +874,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   {
     using Dyn = std::integral_constant<int, -1>;
     int i = 0;
+    using I0 = std::integral_constant<int, 0>;
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    // whole turns of the ring with constant stages, up to the first tile that
+    // is not whole or holds the new token: two steps of two tiles (four
+    // stages), or three of one (a three-stage ring, head_dim 256, steps one
+    // tile at a time: its accumulators leave no registers for a second
+    // tile's operands)
+    const int lim = clean ? min(n_full, new_i >= 0 ? new_i : n_my) : 0;
     if constexpr (kStages == 4) {
-      // whole turns of the ring: two steps with constant stages, up to the
-      // first tile that is not whole or holds the new token
-      const int lim = clean ? min(n_full, new_i >= 0 ? new_i : n_my) : 0;
       for (; i + 3 < lim; i += 4) {
-        if (!step(std::integral_constant<int, 2>{}, std::integral_constant<int, 0>{}, i) ||
-            !step(std::integral_constant<int, 2>{}, std::integral_constant<int, 2>{}, i + 2)) {
+        if (!step(I2{}, I0{}, i) || !step(I2{}, I2{}, i + 2)) {
+          failed = true;
+          break;
+        }
+      }
+    } else {
+      static_assert(kStages == 3, "rings of three or four stages");
+      for (; i + 2 < lim; i += 3) {
+        if (!step(I1{}, I0{}, i) || !step(I1{}, I1{}, i + 1) || !step(I1{}, I2{}, i + 2)) {
           failed = true;
           break;
         }
       }
     }
-    for (; !failed && i + 1 < n_my; i += 2) {
-      if (!step(std::integral_constant<int, 2>{}, Dyn{}, i)) {
+    constexpr int kNT = kStages % 2 == 0 ? 2 : 1;
+    for (; !failed && i + kNT - 1 < n_my; i += kNT) {
+      if (!step(std::integral_constant<int, kNT>{}, Dyn{}, i)) {
         failed = true;
         break;
       }
     }
-    if (!failed && i < n_my && !step(std::integral_constant<int, 1>{}, Dyn{}, i)) failed = true;
+    if (kNT == 2 && !failed && i < n_my && !step(I1{}, Dyn{}, i)) failed = true;
   }
 
   if (failed) {
     if (lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
     // let this warp's copies in flight land before the CTA's memory is reused
     for (int i = waited; i < n_my && i < waited + kStages; ++i)
-      (void)mbar_wait_bounded(&wbars[i % kStages], (i / kStages) & 1);
+      (void)mbar_wait_bounded(bar_of(i % kStages), (i / kStages) & 1);
   }
 
   // ---- merge protocol, part 1: with several splits, count this one as
