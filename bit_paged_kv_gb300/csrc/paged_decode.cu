@@ -36,7 +36,9 @@
 //    a permutation that keeps the K-row and V-row reads conflict-free.
 //  * Output: O'^T += V~^T (p*s) on the tensor cores, dims on M, tokens on K,
 //    heads on N, plus sum_j p_j z_j on the CUDA cores.  p*s goes from the
-//    score fragment to the B-operand layout by two movmatrix transposes.
+//    score fragment to the B-operand layout by two movmatrix transposes, and
+//    V~^T from the V rows (read like the K rows) by movmatrix transposes of
+//    their 8 x 8 blocks of code-byte pairs, masked like K.
 //  * Online softmax in base 2 per head; sm_scale*log2(e) scales the binary32
 //    score after the MMA, so an unrotated q enters the MMA exactly; the
 //    accumulators are rescaled only when a running max grows (the lanes
@@ -93,7 +95,6 @@ struct Dims {
   static constexpr int kE = D / 32;                // q and output elements per lane
   static constexpr int kKWords = D / 32;           // K-row words per thread-in-group
   static constexpr int kMT = D / 16;               // 16-dim tiles of the output product
-  static constexpr int kVWords = D / 64;           // V-row words per lane group
   static constexpr int kKSteps = D / 16;           // k-steps of the score product
   static constexpr bool kFragSmem = D > kHeadDim;  // q' fragments read per k-step from shared memory
   static constexpr int kIdCap = D <= kHeadDim ? 256 : 64;  // chunk indices a warp keeps in shared memory
@@ -183,8 +184,9 @@ constexpr uint32_t kHiNib = 0x00F000F0u;  // bits 4-7 of both halves
 // BFM: the caches' (scale, zero) words are bfloat16 instead of binary16;
 // they are widened to binary32 either way, so only that step differs.
 // D: the head dimension.  A thread-in-group c of an MMA quad covers dims
-// [c D/4, (c+1) D/4) of a K row, 32-bit word w of it dims 8w .. 8w+7 of
-// that range; a lane group g covers dims [g D/8, (g+1) D/8) of the output.
+// [c D/4, (c+1) D/4) of a K row (and reads the same bytes of a V row), 32-bit
+// word w of it dims 8w .. 8w+7 of that range; output tile k row g holds dim
+// vdim(g, k) (below).
 // PAIR: D stands for two neighbouring kv-heads of head_dim D/2 and GQA 4
 // (Cfg above): q-head column v < 4 is a q-head of the first kv-head, its q
 // zero in the second half of the D dims, v >= 4 one of the second, zero in
@@ -539,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   const float2 skAB = make_float2(skA, skB), qsAB = make_float2(qsA, qsB);
 
   constexpr int kMT = DM::kMT;
+  // output tile k = 2 db + hh: row g is dim vdim(g, k) (low nibbles), row
+  // g + 8 the next dim (high nibbles): byte hh of byte pair g of block db
+  auto vdim = [](int gg, int k) { return (gg >> 1) * (D / 4) + 8 * (k >> 1) + 4 * (gg & 1) + 2 * (k & 1); };
   float acc[kMT][4];
 #pragma unroll
   for (int i = 0; i < kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -801,45 +806,44 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
         b1 = movm_t(pack_half2(ps23.x, ps23.y));
       }
 
-      // lane group g's dims of the four token rows: D/16 bytes each, word
-      // k/4 of them holding (as byte k mod 4) the codes of dims 2k, 2k + 1
-      constexpr int kVW = DM::kVWords;
-      // (a pair: lane group g's dims g D/8 .. are kv-head g / 4's)
-      const uint8_t* vrow = PAIR ? vst + C::kcode(0, g >> 2) + (D / 16) * (g & 3)
-                                 : vst + C::kcode(0) + (D / 16) * g;
-      uint32_t rw[4][kVW];
+      // V^T operands: the 8 x 8 blocks of 16-bit elements (8 token rows of
+      // the tile by 8 code-byte pairs) are read like the K rows and
+      // transposed by movmatrix; lane (g, c) then holds byte pair g of
+      // tokens 2c, 2c + 1 of the block, which is, masked, the A fragment
+      // over those tokens for the dims of the pair (see vdim below).
+      constexpr int kKW = DM::kKWords;
+      const uint8_t* vrow = PAIR ? vst + C::kcode(sg, c >> 1) + (D / 8) * (c & 1)
+                                 : vst + C::kcode(sg) + (D / 8) * c;
+      uint32_t vaw[kKW], vbw[kKW];
+      if constexpr (kKW == 2) {
+        const uint2 va = *reinterpret_cast<const uint2*>(vrow);
+        const uint2 vb = *reinterpret_cast<const uint2*>(vrow + 8 * C::kCodeRow);
+        vaw[0] = va.x; vaw[1] = va.y;
+        vbw[0] = vb.x; vbw[1] = vb.y;
+      } else {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint8_t* src = vrow + (tok_of_row(2 * c + (r & 1)) + 8 * (r >> 1)) * C::kCodeRow;
-        if constexpr (kVW == 1) {
-          rw[r][0] = *reinterpret_cast<const uint32_t*>(src);
-        } else if constexpr (kVW == 2) {
-          const uint2 v2 = *reinterpret_cast<const uint2*>(src);
-          rw[r][0] = v2.x;
-          rw[r][1] = v2.y;
-        } else {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(src);
-          rw[r][0] = v4.x;
-          rw[r][1] = v4.y;
-          rw[r][2] = v4.z;
-          rw[r][3] = v4.w;
+        for (int u = 0; u < kKW; u += 4) {
+          const uint4 va = *reinterpret_cast<const uint4*>(vrow + 4 * u);
+          const uint4 vb = *reinterpret_cast<const uint4*>(vrow + 8 * C::kCodeRow + 4 * u);
+          vaw[u] = va.x; vaw[u + 1] = va.y; vaw[u + 2] = va.z; vaw[u + 3] = va.w;
+          vbw[u] = vb.x; vbw[u + 1] = vb.y; vbw[u + 2] = vb.z; vbw[u + 3] = vb.w;
         }
       }
 #pragma unroll
-      for (int k = 0; k < kMT; ++k) {
-        const uint32_t w0 = rw[0][k / 4];
-        const uint32_t w1 = rw[1][k / 4];
-        const uint32_t w2 = rw[2][k / 4];
-        const uint32_t w3 = rw[3][k / 4];
-        const uint32_t sel = uint32_t(k & 3) | (uint32_t((k & 3) + 4) << 8);
-        const uint32_t x01 = prmt(w0, w1, sel);
-        const uint32_t x23 = prmt(w2, w3, sel);
-        uint32_t a[4];
-        a[0] = x01 & kLoNib;  // dims of rows g: n * 2^-24
-        a[1] = x01 & kHiNib;  // dims of rows g + 8: n * 2^-20
-        a[2] = x23 & kLoNib;
-        a[3] = x23 & kHiNib;
-        mma_16816(acc[k], a, b0, b1);
+      for (int db = 0; db < kKW; ++db) {
+        const uint32_t ta = movm_t(vaw[db]);  // tokens of score rows 0-7
+        const uint32_t tb = movm_t(vbw[db]);  // rows 8-15
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t x = hh ? (ta >> 8) : ta;
+          const uint32_t y = hh ? (tb >> 8) : tb;
+          uint32_t a[4];
+          a[0] = x & kLoNib;  // dims of rows g: n * 2^-24
+          a[1] = x & kHiNib;  // dims of rows g + 8: n * 2^-20
+          a[2] = y & kLoNib;
+          a[3] = y & kHiNib;
+          mma_16816(acc[2 * db + hh], a, b0, b1);
+        }
       }
     }
 
@@ -960,8 +964,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     float* base0 = red_acc + (warp * kMaxGroup + c) * kRedStride;
 #pragma unroll
     for (int k = 0; k < kMT; ++k) {
-      base0[red_col((D / 8) * g + 2 * k)] = acc[k][0];
-      base0[red_col((D / 8) * g + 2 * k + 1)] = acc[k][2];
+      base0[red_col(vdim(g, k))] = acc[k][0];
+      base0[red_col(vdim(g, k) + 1)] = acc[k][2];
     }
   } else {
     if (g == 0) {
@@ -976,10 +980,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     float* base1 = base0 + kRedStride;
 #pragma unroll
     for (int k = 0; k < kMT; ++k) {
-      base0[red_col((D / 8) * g + 2 * k)] = acc[k][0];
-      base1[red_col((D / 8) * g + 2 * k)] = acc[k][1];
-      base0[red_col((D / 8) * g + 2 * k + 1)] = acc[k][2];
-      base1[red_col((D / 8) * g + 2 * k + 1)] = acc[k][3];
+      base0[red_col(vdim(g, k))] = acc[k][0];
+      base1[red_col(vdim(g, k))] = acc[k][1];
+      base0[red_col(vdim(g, k) + 1)] = acc[k][2];
+      base1[red_col(vdim(g, k) + 1)] = acc[k][3];
     }
   }
   __syncthreads();
