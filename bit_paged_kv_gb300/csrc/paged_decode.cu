@@ -21,7 +21,10 @@
 //    K and V codes and their (scale, zero) words: a whole 16-token page, or
 //    16 rows of a larger page (codes and metadata copied separately).  A warp
 //    consumes its tiles two at a time; the two share one softmax update, and
-//    (four-stage rings) one mbarrier: one wait, one refill arrival.
+//    (four-stage rings) one mbarrier: one wait, one refill arrival.  With a
+//    clean chunk list the whole warp runs the refill on warp-uniform values
+//    and one elected lane arms the barrier and issues the copies; otherwise
+//    lane 0 does it with the checks.
 //  * The loop is bound by instruction issue, so the common case carries no
 //    per-tile bookkeeping: a warp whose (page, kv-head) chunk indices are all
 //    valid and held in shared memory runs its whole tiles in turns of the
@@ -80,6 +83,24 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t a) {
 // the K-row and V-row reads of a warp at the minimum number of shared-memory
 // wavefronts for 32- and 64-byte rows.
 __device__ __forceinline__ constexpr int tok_of_row(int j) { return j ^ (((j >> 1) ^ (j >> 2)) & 1); }
+// Executed by a whole warp with warp-uniform operands: one elected lane
+// arms the mbarrier / issues the bulk copy.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_elect(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // dim d of a reduction row sits at d + d / 16: the stores (lane group g
 // writes dims (D/8) g + ..) and the per-dim reads are then free of bank
 // conflicts
@@ -332,6 +353,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
           bulk_g2s(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, bar);
           bulk_g2s(st + C::kHalf, p.v_cache + codes, kStepTok * kCodeRow, bar);
           bulk_g2s(st + C::kHalf + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4, bar);
+        }
+      }
+    }
+  };
+
+  // the whole warp, clean lists only: tiles i .. i + n - 1 into stages s ..
+  // (the values are the same in every lane, so no lane-0 branch is needed;
+  // one elected lane arms the barrier and issues the copies)
+  auto issue_w = [&](int i, int s, int n) {
+    const uint32_t bar = smem_u32(bar_of(s));
+    mbar_arrive_expect_tx_elect(bar, n * C::kStage);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u < n) {
+        const int ci = __shfl_sync(kFull, wids[i + u], 0);
+        const uint32_t st = smem_u32(ring + (s + u) * C::kStage);
+        const int64_t off = int64_t(ci) * C::kChunk;
+        if (P == 16) {
+          bulk_g2s_elect(st, p.k_cache + off, C::kHalf, bar);
+          bulk_g2s_elect(st + C::kHalf, p.v_cache + off, C::kHalf, bar);
+        } else {
+          const int part = (warp + (i + u) * kWarps) % C::kStepsPerPage;
+          const int64_t codes = off + part * (kStepTok * kCodeRow);
+          const int64_t meta = off + P * kCodeRow + part * (kStepTok * 4);
+          bulk_g2s_elect(st, p.k_cache + codes, kStepTok * kCodeRow, bar);
+          bulk_g2s_elect(st + kStepTok * kCodeRow, p.k_cache + meta, kStepTok * 4, bar);
+          bulk_g2s_elect(st + C::kHalf, p.v_cache + codes, kStepTok * kCodeRow, bar);
+          bulk_g2s_elect(st + C::kHalf + kStepTok * kCodeRow, p.v_cache + meta, kStepTok * 4, bar);
         }
       }
     }
@@ -848,17 +897,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
     }
 
     __syncwarp();
-    if (lane == 0) {
+    if (kPairBars && (!kChecks || clean)) {
+      const int nxt = i + kStages;  // the tiles that refill this step's stages
+      const int n = min(NT, n_my - nxt);
+      if (n > 0) issue_w(nxt, stage(0), n);
+    } else if (lane == 0) {
       if constexpr (kPairBars) {
         const int nxt = i + kStages;  // the tiles that refill this step's stages
         const int n = min(NT, n_my - nxt);
-        if (n > 0) {
-          if (!kChecks || clean) {
-            issue(std::false_type{}, nxt, stage(0), n);
-          } else {
-            issue(std::true_type{}, nxt, stage(0), n);
-          }
-        }
+        if (n > 0) issue(std::true_type{}, nxt, stage(0), n);
       } else {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
