@@ -29,11 +29,16 @@
 //            (s, z) metadata (binary16 or bfloat16) to binary32.
 //      12    producer: 16-key slices (codes and metadata of K and V) through
 //            a 4-stage ring with the bulk-copy engine.
-//      13    MMA: one thread issues S = Q' K^T (M 128, N 64, K 128; q' hi and
-//            lo accumulate into the same scores) and O += P V (M 128, N 128,
-//            K 64) with tcgen05.mma, and signals completion with
-//            tcgen05.commit; the warp also allocates the 256 tensor-memory
-//            columns (S double-buffered at columns 0 and 64, O at 128).
+//      13    MMA: S = Q' K^T (M 128, N 64, K 128; q' hi and lo accumulate
+//            into the same scores) and O += P V (M 128, N 128, K 64) with
+//            tcgen05.mma, completion signalled by tcgen05.commit; the warp
+//            also allocates the 256 tensor-memory columns (S double-buffered
+//            at columns 0 and 64, O at 128).
+//    The producer and MMA warps run converged on warp-uniform values, and one
+//    lane chosen by elect.sync inside the inline PTX issues each copy, MMA,
+//    commit and barrier arrival (instead of a lane-0 branch: the copy and MMA
+//    instructions take uniform registers, and a divergent lane-0 region
+//    converts every operand to them per instruction).
 //  * Operands are unswizzled 8-row x 16-byte core matrices: K-major, except
 //    V, which the P.V product reads MN-major (dims contiguous per key).
 //    Every mbarrier wait is bounded to about a second; the softmax warps,
@@ -102,6 +107,48 @@ constexpr int kSoftBar = 1;
 // 2^e for -126 <= e <= 127, exactly
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
 
+// tcgen05 MMA / commit issued by one elected lane of a converged warp whose
+// operands are warp-uniform (the same lane is elected every time: the MMAs
+// and the commits that track them come from one thread).
+__device__ __forceinline__ void umma_f16_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.u32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// Executed by a whole warp with warp-uniform operands: one elected lane
+// arms the mbarrier / issues the bulk copy.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_elect(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // Byte-permute selectors that build a binary16 pair (x byte m, y byte m) with
 // zero upper bytes from two nibble planes x, y: the zeros replicate the sign
 // bit of a byte below 128 (selector nibble with bit 3 set).
@@ -414,14 +461,19 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
         pid[sl] = id;
         okm |= (id >= 0) << sl;
       }
-      if (lane == 0) {
+      {
+        // the whole warp on warp-uniform values; one elected lane arms the
+        // barrier and issues the copies
         uint8_t* st = smem + kOffRaw + rs * kRawBytes;
-        *reinterpret_cast<int*>(st + kRawOk) = okm;
+        if (lane == 0) *reinterpret_cast<int*>(st + kRawOk) = okm;
+        __syncwarp();
         const uint32_t nbytes = __popc(okm) * (2 * 1024 + 2 * 64);
+        const uint32_t bar = smem_u32(&bars[kRawFull + rs]);
         if (nbytes == 0) {
-          mbar_arrive(&bars[kRawFull + rs]);
+          if (lane == 0) mbar_arrive(&bars[kRawFull + rs]);
         } else {
-          mbar_arrive_expect_tx(&bars[kRawFull + rs], nbytes);
+          mbar_arrive_expect_tx_elect(bar, nbytes);
+          const uint32_t st32 = smem_u32(st);
 #pragma unroll
           for (int sl = 0; sl < 4; ++sl) {
             if (pid[sl] < 0) continue;
@@ -429,10 +481,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
             const int64_t off = (int64_t(pid[sl]) * p.num_kv_heads + kvh) * kChunk;
             const int64_t codes = off + part * 1024;
             const int64_t meta = off + P * (kHeadDim / 2) + part * 64;
-            bulk_g2s(st + sl * 1024, p.k_cache + codes, 1024, &bars[kRawFull + rs]);
-            bulk_g2s(st + kRawV + sl * 1024, p.v_cache + codes, 1024, &bars[kRawFull + rs]);
-            bulk_g2s(st + kRawKM + sl * 64, p.k_cache + meta, 64, &bars[kRawFull + rs]);
-            bulk_g2s(st + kRawVM + sl * 64, p.v_cache + meta, 64, &bars[kRawFull + rs]);
+            bulk_g2s_elect(st32 + sl * 1024, p.k_cache + codes, 1024, bar);
+            bulk_g2s_elect(st32 + kRawV + sl * 1024, p.v_cache + codes, 1024, bar);
+            bulk_g2s_elect(st32 + kRawKM + sl * 64, p.k_cache + meta, 64, bar);
+            bulk_g2s_elect(st32 + kRawVM + sl * 64, p.v_cache + meta, 64, bar);
           }
         }
       }
@@ -445,71 +497,69 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       (void)wait_sleep(&bars[kRawFull + i % kRawStages], (i / kRawStages) & 1);
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    // The whole warp runs the loop on warp-uniform values (every lane polls
+    // the same barriers; lane 0's view decides); one elected lane issues each
+    // MMA and commit, so descriptors and addresses stay uniform.
+    {
       const uint32_t kx0 = smem_u32(smem + kOffKx), vx0 = smem_u32(smem + kOffVx);
       constexpr uint32_t idS = umma_idesc_f16(kBM, kBN);
-      // V is the B operand in MN-major form (keys x dims, dims contiguous):
-      // the same shared-memory layout as the K operand
       constexpr uint32_t idO = umma_idesc_f16(kBM, kHeadDim) | kUmmaBMnMajor;
-      // descriptors built once: a K step only advances the start address
-      // (in 16-byte units, the descriptor's low field): 2 x 1024 bytes of K
-      // operand, 2 x 2048 bytes of V operand
       const uint64_t kxd[2] = {umma_desc(kx0, 1024, 128), umma_desc(kx0 + kKxBytes, 1024, 128)};
-      // MN-major: the next 8 keys (K) are 128 bytes on, the next 8 dims (N)
-      // 1024 bytes on; a K = 16 step advances 256 bytes
       const uint64_t vxd[2] = {umma_desc(vx0, 128, 1024), umma_desc(vx0 + kVxBytes, 128, 1024)};
       constexpr uint64_t kKxStep = (2 * 1024) >> 4, kVxStep = (2 * 128) >> 4;
-      // Both products are issued as soon as their operands are ready,
-      // polling the barriers without blocking or sleeping (a sleep's wake-up
-      // is far coarser than an MMA): S(i+1) needs the K operand of tile i+1,
-      // P.V(i) the softmax of tile i; neither waits for the other.
       int nS = 0, nP = 0;
       bool ok = true;
       long long t_last = clock64();
       while (nP < n_tiles) {
         bool prog = false;
-        if (nS < n_tiles && mbar_test(&bars[kKxFull + (nS & 1)], (nS >> 1) & 1) &&
-            (nS < 2 || mbar_test(&bars[kSEmpty + (nS & 1)], ((nS >> 1) - 1) & 1))) {
+        bool sready = nS < n_tiles && mbar_test(&bars[kKxFull + (nS & 1)], (nS >> 1) & 1) &&
+                      (nS < 2 || mbar_test(&bars[kSEmpty + (nS & 1)], ((nS >> 1) - 1) & 1));
+        sready = __shfl_sync(0xFFFFFFFFu, sready, 0);
+        if (sready) {
           const int b = nS & 1;
           tc_fence_after();
           const uint32_t sd = tmem + uint32_t(kBN * b);
           const uint64_t bd = kxd[b];
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            umma_f16_ta(sd, tmem + kColQh + 8 * ks, bd + ks * kKxStep, idS, ks > 0);
+            umma_f16_ta_elect(sd, tmem + kColQh + 8 * ks, bd + ks * kKxStep, idS, ks > 0);
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            umma_f16_ta(sd, tmem + kColQl + 8 * ks, bd + ks * kKxStep, idS, true);
-          umma_commit(&bars[kSFull + b]);
-          umma_commit(&bars[kKxEmpty + b]);
+            umma_f16_ta_elect(sd, tmem + kColQl + 8 * ks, bd + ks * kKxStep, idS, true);
+          umma_commit_elect(&bars[kSFull + b]);
+          umma_commit_elect(&bars[kKxEmpty + b]);
           ++nS;
           prog = true;
         }
-        if (nP < nS && mbar_test(&bars[kPFull + (nP & 1)], (nP >> 1) & 1) &&
-            mbar_test(&bars[kVxFull + (nP & 1)], (nP >> 1) & 1)) {
+        bool pready = nP < nS && mbar_test(&bars[kPFull + (nP & 1)], (nP >> 1) & 1) &&
+                      mbar_test(&bars[kVxFull + (nP & 1)], (nP >> 1) & 1);
+        pready = __shfl_sync(0xFFFFFFFFu, pready, 0);
+        if (pready) {
           const int bj = nP & 1;
           tc_fence_after();
           const uint64_t bd = vxd[bj];
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            umma_f16_ta(tmem + kColO, tmem + kColP + 32 * bj + 8 * ks, bd + ks * kVxStep, idO,
-                        nP > 0 || ks > 0);
-          umma_commit(&bars[kPvDone + bj]);
+            umma_f16_ta_elect(tmem + kColO, tmem + kColP + 32 * bj + 8 * ks, bd + ks * kVxStep, idO,
+                              nP > 0 || ks > 0);
+          umma_commit_elect(&bars[kPvDone + bj]);
           ++nP;
           prog = true;
         }
         if (prog) {
           t_last = clock64();
-        } else if (clock64() - t_last > kWaitLimitCycles) {
-          ok = false;
-          break;
         } else {
+          const bool late = __shfl_sync(0xFFFFFFFFu, clock64() - t_last > kWaitLimitCycles, 0);
+          if (late) {
+            ok = false;
+            break;
+          }
           __nanosleep(20);  // leave the scheduler's issue slots to the other roles
         }
       }
-      if (!ok) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
+      if (!ok && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
       // every MMA has completed before tensor memory is released
-      umma_commit(&bars[kMmaDone]);
+      umma_commit_elect(&bars[kMmaDone]);
       (void)wait_sleep(&bars[kMmaDone], 0);
     }
     __syncwarp();
@@ -535,23 +585,21 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       }
       if (te == 0) *reinterpret_cast<int*>(mb + kBN * 16) = *reinterpret_cast<const int*>(st + kRawOk);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kMetaFull + b]);
+      mbar_arrive_elect(&bars[kMetaFull + b]);
       // K operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2
       if (i >= 2 && !wait_sleep_all(&bars[kKxEmpty + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
       widen_codes(st, smem + kOffKx + b * kKxBytes, te);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kKxFull + b]);
+      mbar_arrive_elect(&bars[kKxFull + b]);
       // V operand: element (key n, dim k) at (k/8)*1024 + n*16 + (k%8)*2, the
       // K operand's layout (read by the P.V product as MN-major)
       if (i >= 2 && !wait_sleep_all(&bars[kPvDone + b], ((i >> 1) - 1) & 1)) { failed = true; break; }
       widen_codes(st + kRawV, smem + kOffVx + b * kVxBytes, te);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[kVxFull + b]);
-        mbar_arrive(&bars[kRawEmpty + rs]);
-      }
+      mbar_arrive_elect(&bars[kVxFull + b]);
+      mbar_arrive_elect(&bars[kRawEmpty + rs]);
     }
     if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
   } else {
@@ -572,7 +620,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       tmem_ld32(trow + uint32_t(kBN * b + kq), t);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kSEmpty + b]);
+      mbar_arrive_elect(&bars[kSEmpty + b]);
       const float4* msk = reinterpret_cast<const float4*>(smem + kOffMeta + b * kMetaBytes);
       const float4* mzk = msk + kBN / 4;
       const float4* msv = msk + 2 * (kBN / 4);
@@ -708,10 +756,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(const PrefillP
       pz += (za[0] + za[1]) + (za[2] + za[3]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[kPFull + b]);
-        mbar_arrive(&bars[kMetaEmpty + b]);
-      }
+      mbar_arrive_elect(&bars[kPFull + b]);
+      mbar_arrive_elect(&bars[kMetaEmpty + b]);
     }
     if (failed && lane == 0) report(p.dev_status, SAW_ERR_DEVICE_TIMEOUT);
     // ---- epilogue: this half of the output row from tensor memory, code
