@@ -110,6 +110,13 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
       splits = ceil_div(max_pages, pps);
       warps = 8;
     }
+    // Whole turns for every warp: a split of a multiple of `warps` 16-token
+    // tiles gives no warp a tile more than the others (the slowest warp sets
+    // the split's time).  8192 tokens, the long-split bound, is such a
+    // multiple, so the rounding never changes the CTA shape.
+    const int64_t unit = std::max<int64_t>(1, warps / (page_size / 16));
+    pps = ceil_div(pps, unit) * unit;
+    splits = ceil_div(max_pages, pps);
   }
   if (splits > 65535) return SAW_ERR_UNSUPPORTED;
   *splits_out = int32_t(splits);
