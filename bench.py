@@ -1142,7 +1142,7 @@ def run_saw(args):
         "roofline": {
             "bound": "hbm",
             "kernel": "saw_decode_step: paged_decode_kernel<head_dim 128, page 16, wide (GQA 8), "
-                      "append>, 8-warp CTAs, one per (sequence, kv-head) "
+                      "append>, 4-warp CTAs (four per SM), one per (sequence, kv-head) "
                       "(256 new tokens appended, 1.57e6 cached tokens attended per layer)",
             "achieved": achieved,
             "peak": peak,

@@ -23,11 +23,13 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
 # (source, object, extra flags).  The append kernel's bytes are defined by
 # separately rounded binary32 steps; it uses explicit _rn intrinsics and is
 # also compiled with contraction off.  The decode kernel is built once per CTA
-# shape, and once more per shape for head_dim 64 and 256.
+# shape (16, 8 and 4 warps), and once more with 16 and 8 warps for head_dim 64
+# and 256.
 UNITS = [("saw_api.cu", "saw_api.o", []),
          ("quantize_append.cu", "quantize_append.o", ["-fmad=false"]),
          ("paged_decode.cu", "paged_decode_w16.o", ["-DSAW_DECODE_WARPS=16"]),
          ("paged_decode.cu", "paged_decode_w8.o", ["-DSAW_DECODE_WARPS=8"]),
+         ("paged_decode.cu", "paged_decode_w4.o", ["-DSAW_DECODE_WARPS=4"]),
          ("paged_decode.cu", "paged_decode_dims_w16.o",
           ["-DSAW_DECODE_WARPS=16", "-DSAW_DECODE_OTHER_DIMS"]),
          ("paged_decode.cu", "paged_decode_dims_w8.o",

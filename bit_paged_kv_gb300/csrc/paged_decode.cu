@@ -10,9 +10,9 @@
 //
 // Design (sm_103a):
 //  * One CTA per (split of the context, kv-head, sequence): 16 warps, one
-//    CTA per SM, or 8 warps, two CTAs per SM (this file is compiled once per
-//    shape, and once more per shape for head_dim 64 and 256; the host plan
-//    picks the shape).  The whole GQA group of the kv-head is
+//    CTA per SM, 8 warps, two CTAs per SM, or 4 warps, four per SM (this file
+//    is compiled once per shape, and once more for head_dim 64 and 256 with
+//    16 and 8 warps; the host plan picks the shape).  The whole GQA group of the kv-head is
 //    served by the CTA, so each page is read from HBM once, and q is rotated
 //    once per CTA.
 //  * The split is cut into 16-token tiles; warp w of W takes tiles w, w+W, ...
@@ -63,8 +63,8 @@ namespace {
 #define SAW_DECODE_WARPS 16
 #endif
 constexpr int kWarps = SAW_DECODE_WARPS;              // this object's CTA shape
-constexpr int kCtasPerSm = kWarps == 16 ? 1 : 2;      // 128 registers per thread either way
-static_assert(kWarps == 16 || kWarps == 8, "decode CTAs have 16 or 8 warps");
+constexpr int kCtasPerSm = 16 / kWarps;               // 128 registers per thread either way
+static_assert(kWarps == 16 || kWarps == 8 || kWarps == 4, "decode CTAs have 16, 8 or 4 warps");
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -166,7 +166,8 @@ struct Cfg {
   static constexpr int kOffFlag = kOffQsum + 2 * kMaxGroup * 4;               // int
   static constexpr int kOffNew = kOffFlag + 16;  // new token: [K, V] x (code bytes, meta)
   static constexpr int kSmem = kOffNew + 2 * (kCodeRow + 16);
-  static_assert(kSmem <= (kCtasPerSm == 1 ? 227 * 1024 : 113 * 1024), "shared memory per CTA");
+  static_assert(kSmem <= (kCtasPerSm == 1 ? 227 * 1024 : kCtasPerSm == 2 ? 113 * 1024 : 56 * 1024),
+                "shared memory per CTA");
 };
 
 // In-place butterfly over each h-block of nvec vectors of D floats in shared
@@ -458,8 +459,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   // Element d of a head, with c = d / (D/4), o = d mod (D/4) and j = o mod 8, sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group
   // c, register j & 1, half (j >> 2) & 1: the nibble the K codes put there.
   constexpr int kE = DM::kE;
-  if (warp < kMaxGroup) {
-    const int h = warp;
+  for (int h = warp; h < kMaxGroup; h += kWarps) {  // (4-warp CTAs: two heads per warp)
     float x[kE];
 #pragma unroll
     for (int e = 0; e < kE; ++e) x[e] = 0.0f;

@@ -62,7 +62,7 @@ int64_t best_splits(int64_t units, int64_t slots, int64_t max_splits) {
 // The split plan and the CTA shape.  16-warp CTAs (one per SM) serve grids of
 // one wave and long splits; grids of several waves of short splits use 8-warp
 // CTAs, two per SM, so that one CTA's prologue and merge overlap the other's
-// streaming.
+// streaming, or, unsplit with units for four CTAs per SM, 4-warp CTAs.
 int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int32_t max_seq_len,
                   int32_t pages_per_split, int32_t* splits_out,
                   int32_t* pps_out, int32_t* warps_out = nullptr) {
@@ -108,7 +108,11 @@ int32_t make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t page_size, int
       const int64_t s8 = best_splits(units, 2 * sms, max_splits);
       pps = ceil_div(max_pages, s8);
       splits = ceil_div(max_pages, pps);
-      warps = 8;
+      // one split and units for four CTAs per SM: 4-warp CTAs, so that more
+      // CTAs share an SM and one's prologue and epilogue (and, in the fused
+      // step, the next launch's early page copies) overlap the others'
+      // streaming; with splits the 8-warp shape measured faster
+      warps = (splits == 1 && units >= 4 * sms) ? 4 : 8;
     }
     // Whole turns for every warp: a split of a multiple of `warps` 16-token
     // tiles gives no warp a tile more than the others (the slowest warp sets

@@ -99,6 +99,7 @@ struct DecodeParams {
 // per shape for head_dim 64 and 256 (the same source built for those sizes).
 cudaError_t launch_paged_decode_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_w8(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_paged_decode_w4(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_dims_w16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_paged_decode_dims_w8(const DecodeParams& p, cudaStream_t stream);
 // head_dim 64 and 256 append (variants.cu); bulk appends run the tiled
@@ -114,10 +115,12 @@ cudaError_t launch_bf16_append(const uint16_t* k, const uint16_t* v, int64_t k_s
                                int64_t v_stride, const int32_t* slots, int num_tokens, int hkv,
                                uint16_t* kc, uint16_t* vc, int64_t num_slots, int P,
                                int32_t* dev_status, cudaStream_t stream);
+// (head_dim 64 and 256 have no 4-warp build: they take the 8-warp shape)
 inline cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.head_dim != kHeadDim)
-    return p.warps == 8 ? launch_paged_decode_dims_w8(p, stream)
+    return p.warps <= 8 ? launch_paged_decode_dims_w8(p, stream)
                         : launch_paged_decode_dims_w16(p, stream);
+  if (p.warps == 4) return launch_paged_decode_w4(p, stream);
   return p.warps == 8 ? launch_paged_decode_w8(p, stream) : launch_paged_decode_w16(p, stream);
 }
 
