@@ -1039,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   // 16h + w of warps 0-3, reduced over the 16 warps with shuffles inside
   // each half-warp; then one (head, dim) per thread.
   const int nw = min(kWarps, n_steps);  // warps that saw any step
+  static_assert(kMaxGroup * kWarps % 32 == 0, "the weight step's shuffles take whole warps");
   if (tid < kMaxGroup * kWarps) {
     const int h = tid / kWarps, w = tid % kWarps;
     const bool in = h < G && w < nw;
