@@ -157,6 +157,16 @@ def test_plan_and_workspace(L):
     assert s128 > 1 and w128 == (64 * 8 * 8 + 15) // 16 * 16 + 64 * 32 * s128 * (128 + 2) * 4
     with pytest.raises(saw.SawError):
         saw.saw_decode_plan(1, 8, 12, 100, 0)
+    # automatic splits are whole turns of the warps: a multiple of one 16-token
+    # tile per warp of the chosen CTA shape (4, 8 or 16 warps), 16 for the
+    # one-wave batch-1 plan
+    for B, P, L_ in [(1, 16, 32768), (4, 16, 32768), (64, 16, 16384), (8, 64, 131072),
+                     (1, 32, 65536), (256, 16, 8192)]:
+        s, pps = saw.saw_decode_plan(B, 8, P, L_, 0)
+        if s > 1:
+            assert (pps * (P // 16)) % 4 == 0, (B, P, L_, s, pps)
+    s, pps = saw.saw_decode_plan(1, 8, 16, 32768, 0)
+    assert pps % 16 == 0 and s * pps * 16 >= 32768
 
 
 def _step(L, **kw):
