@@ -12,9 +12,9 @@
 //  * One CTA per (split of the context, kv-head, sequence): 16 warps, one
 //    CTA per SM, 8 warps, two CTAs per SM, or 4 warps, four per SM (this file
 //    is compiled once per shape, and once more for head_dim 64 and 256 with
-//    16 and 8 warps; the host plan picks the shape).  The whole GQA group of the kv-head is
-//    served by the CTA, so each page is read from HBM once, and q is rotated
-//    once per CTA.
+//    16 and 8 warps; the host plan picks the shape).  The whole GQA group
+//    of the kv-head is served by the CTA, so each page is read from HBM
+//    once, and q is rotated once per CTA.
 //  * The split is cut into 16-token tiles; warp w of W takes tiles w, w+W, ...
 //    through a private four-stage shared-memory ring filled by the bulk-copy
 //    engine (cp.async.bulk + mbarrier complete_tx).  A stage holds one tile's
@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_kernel(cons
   // for k-step t and lane (g, c), the four binary16 values of that lane's
   // two fragment registers (PACKED: column g = hi of head g / 2 for even g,
   // lo for odd g; WIDE: hi of head g); buffer 1 (WIDE) the lo parts.
-  // Element d of a head, with c = d / (D/4), o = d mod (D/4) and j = o mod 8, sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group
-  // c, register j & 1, half (j >> 2) & 1: the nibble the K codes put there.
+  // Element d of a head, with c = d / (D/4), o = d mod (D/4) and j = o mod 8,
+  // sits at k-step 2 (o / 8) + ((j >> 1) & 1), thread-in-group c, register
+  // j & 1, half (j >> 2) & 1: the nibble the K codes put there.
   constexpr int kE = DM::kE;
   for (int h = warp; h < kMaxGroup; h += kWarps) {  // (4-warp CTAs: two heads per warp)
     float x[kE];
